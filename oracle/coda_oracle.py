@@ -1,0 +1,334 @@
+"""Plain, slow, fp64 CPU oracle for the CODA GEMM+epilogue path.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import, call or run
+this module: only the tests, the package smoke check and the benchmark's CPU
+baseline leg use it.  It shares no code with the CUDA library.
+
+What it computes.  The CODA article (d9bl.com, "CODA：将 Transformer 模块重新
+表达为 GEMM+Epilogue 程序", §3.1 "GEMM+Epilogue 分解") defines the fused op as a
+GEMM  C = alpha*A*B + beta*C_prev  followed by an epilogue  D = f(C)  applied
+elementwise or row by row before the global write.  The agentlenshq.com summary
+("CODA: GEMM-Epilogue FusionによるTransformerトレーニングの最適化", section
+"仕組み") lists the primitive classes f is built from: scaling by a constant or
+a vector, reductions (sum or mean along a dimension), pairwise/elementwise
+transforms (activations), and accumulation into a residual.  The zeli.app page
+("CODA: Wie Transformer-Blöcke als GEMM-Epilogue-Programme neu geschrieben
+werden", comment by augment_me) adds the commuted RMSNorm: the row-wise scale
+of the norm can be pulled past the following projection.
+
+How it computes it.  Every step is a separate pass over a full fp64 tensor, in
+the op-list order, with no intermediate rounding.  In particular the commuted
+RMSNorm is evaluated the *unfused* way: normalise X first, then project (the
+commuted form is only checked against this as a pin).  Inputs are the exact
+bf16 values widened to fp64.  The GEMM uses numpy's fp64 matmul as a library
+step; everything else is written out.
+
+Readings where the pages are silent (each is also listed in the design notes):
+  * GELU is the tanh form; its derivative is the tanh form's exact derivative.
+  * dropout: keep element (row, col) of the [M, N_out] output iff
+    splitmix64(seed, i) < T with i = row*N_out + col, where splitmix64(seed, i)
+    is the i-th output (0-based) of the splitmix64 generator seeded with seed
+    (Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
+    OOPSLA 2014), and T = (uint64) floor(ldexp(1-p, 64)) evaluated in fp64.
+    Kept values are scaled by 1/(1-p) (inverted dropout); p = 0 keeps all.
+  * RMSNorm: r_i = 1/sqrt(mean_k x_ik^2 + eps); gamma scales the K index, so
+    rmsnorm(X) @ W = r (.)_row (X @ (gamma (.)_row W)).
+  * SwiGLU: the GEMM output is [G | U] with G = columns [0, N/2) and
+    U = columns [N/2, N); out = silu(G) * U; ops before SWIGLU act on both
+    halves (column vectors then have N entries), ops after it on N/2 columns.
+  * row reductions run over the columns of the value at the op's position.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# op names (the same names the C header uses, without the CODA_OP_ prefix)
+# ---------------------------------------------------------------------------
+OP_NAMES = (
+    "SCALE", "COL_SCALE", "BIAS", "ROW_SCALE", "RMS_ROWSCALE", "GELU_TANH", "SILU",
+    "SWIGLU", "GELU_TANH_GRAD", "DROPOUT", "RESIDUAL", "STORE_PREACT",
+    "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX",
+)
+
+_U64 = np.uint64
+_MASK64 = (1 << 64) - 1
+
+
+# ---------------------------------------------------------------------------
+# GEMM  (CODA article §3.1: C = alpha * A * B)
+# ---------------------------------------------------------------------------
+def gemm(A: np.ndarray, B: np.ndarray, b_layout: str = "kn") -> np.ndarray:
+    """C[m, n] = sum_k A[m, k] * B(k, n) in fp64.
+
+    b_layout "kn": B is stored [K, N] (row k, column n).
+    b_layout "nk": B is stored [N, K] and the product is A @ B^T (the dgrad
+                   form dY @ W^T with W stored [N, K]).
+    """
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    if b_layout == "kn":
+        return A @ B
+    if b_layout == "nk":
+        return A @ B.T
+    raise ValueError(b_layout)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm, unfused (zeli.app page, augment_me's TLDR on RMSNorm/LayerNorm)
+# ---------------------------------------------------------------------------
+def rms_rstd(X: np.ndarray, eps: float) -> np.ndarray:
+    """r_i = 1 / sqrt(mean_k x_ik^2 + eps), one value per row."""
+    X = np.asarray(X, dtype=np.float64)
+    ms = np.mean(X * X, axis=1)
+    return 1.0 / np.sqrt(ms + eps)
+
+
+def rmsnorm(X: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
+    """Xn[i, k] = r_i * x_ik * gamma_k (the normalised activations, materialised)."""
+    X = np.asarray(X, dtype=np.float64)
+    r = rms_rstd(X, eps)
+    return (r[:, None] * X) * np.asarray(gamma, dtype=np.float64)[None, :]
+
+
+def rmsnorm_project(X, gamma, W, eps, b_layout="kn"):
+    """Normalise-then-project: rmsnorm(X) @ W (the unfused reading)."""
+    return gemm(rmsnorm(X, gamma, eps), W, b_layout)
+
+
+# ---------------------------------------------------------------------------
+# scaling primitives (agentlenshq.com, "仕組み": Scaling by a constant or vector)
+# ---------------------------------------------------------------------------
+def scale(x, alpha):
+    return x * float(alpha)
+
+
+def col_scale(x, v):
+    return x * np.asarray(v, dtype=np.float64)[None, :]
+
+
+def bias(x, v):
+    return x + np.asarray(v, dtype=np.float64)[None, :]
+
+
+def row_scale(x, v):
+    return x * np.asarray(v, dtype=np.float64)[:, None]
+
+
+# ---------------------------------------------------------------------------
+# elementwise transforms (agentlenshq.com, "Pairwise Transformations";
+# CODA article §3.2 DSL example uses gelu)
+# ---------------------------------------------------------------------------
+_SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+_GELU_C = 0.044715
+
+
+def gelu_tanh(x):
+    """0.5 x (1 + tanh( sqrt(2/pi) (x + 0.044715 x^3) ))."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + np.tanh(_SQRT_2_OVER_PI * (x + _GELU_C * x ** 3)))
+
+
+def gelu_tanh_grad(z):
+    """d/dz of gelu_tanh(z), by the product and chain rules:
+    0.5 (1 + t) + 0.5 z (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 z^2),
+    t = tanh(sqrt(2/pi)(z + 0.044715 z^3))."""
+    z = np.asarray(z, dtype=np.float64)
+    t = np.tanh(_SQRT_2_OVER_PI * (z + _GELU_C * z ** 3))
+    dinner = _SQRT_2_OVER_PI * (1.0 + 3.0 * _GELU_C * z * z)
+    return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * dinner
+
+
+def silu(x):
+    """x * sigmoid(x) = x / (1 + exp(-x))."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def swiglu(c):
+    """[G | U] -> silu(G) * U, G = columns [0, N/2), U = columns [N/2, N)."""
+    n = c.shape[1]
+    if n % 2:
+        raise ValueError("SWIGLU needs an even width")
+    h = n // 2
+    return silu(c[:, :h]) * c[:, h:]
+
+
+# ---------------------------------------------------------------------------
+# dropout (CODA article §3.2 DSL example: dropout(output, 0.1))
+# ---------------------------------------------------------------------------
+SPLITMIX_GAMMA = 0x9E3779B97F4A7C15
+SPLITMIX_M1 = 0xBF58476D1CE4E5B9
+SPLITMIX_M2 = 0x94D049BB133111EB
+
+
+def splitmix64(seed: int, idx) -> np.ndarray:
+    """The idx-th (0-based) output of splitmix64 seeded with `seed`.
+
+    splitmix64 advances its state by the odd constant 0x9E3779B97F4A7C15 before
+    each output and returns mix64(state):
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EB
+        z =  z ^ (z >> 31)
+    all modulo 2^64, so output idx is mix64(seed + (idx + 1) * gamma).
+    """
+    idx = np.asarray(idx, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = _U64(seed & _MASK64) + (idx + _U64(1)) * _U64(SPLITMIX_GAMMA)
+        z = (z ^ (z >> _U64(30))) * _U64(SPLITMIX_M1)
+        z = (z ^ (z >> _U64(27))) * _U64(SPLITMIX_M2)
+        z = z ^ (z >> _U64(31))
+    return z
+
+
+def dropout_threshold(p: float) -> int:
+    """T = floor((1-p) * 2^64) evaluated in fp64; None means keep everything."""
+    if not (0.0 <= p < 1.0):
+        raise ValueError("dropout p must be in [0, 1)")
+    if p == 0.0:
+        return None
+    return int(math.ldexp(1.0 - p, 64))
+
+
+def dropout_mask(seed: int, M: int, N: int, p: float, row0: int = 0, rows=None) -> np.ndarray:
+    """keep[m, n] for the rows given (default row0 .. row0+M-1) of an [*, N] output."""
+    T = dropout_threshold(p)
+    if rows is None:
+        rows = np.arange(row0, row0 + M, dtype=np.uint64)
+    rows = np.asarray(rows, dtype=np.uint64)
+    if T is None:
+        return np.ones((rows.size, N), dtype=bool)
+    idx = rows[:, None] * _U64(N) + np.arange(N, dtype=np.uint64)[None, :]
+    return splitmix64(seed, idx) < _U64(T)
+
+
+def dropout(x, p, seed, rows=None):
+    """keep ? x / (1-p) : 0, plus the keep mask."""
+    keep = dropout_mask(seed, x.shape[0], x.shape[1], p, rows=rows)
+    if p == 0.0:
+        return x.copy(), keep
+    return np.where(keep, x / (1.0 - p), 0.0), keep
+
+
+# ---------------------------------------------------------------------------
+# accumulation (CODA article §3.1 beta*C_prev; agentlenshq.com "Accumulation")
+# ---------------------------------------------------------------------------
+def residual(x, R, beta=1.0):
+    return x + float(beta) * np.asarray(R, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# row reductions (agentlenshq.com, "Reductions": sum or mean along a dimension)
+# ---------------------------------------------------------------------------
+def row_sum(x):
+    return np.sum(x, axis=1)
+
+
+def row_mean(x):
+    return np.mean(x, axis=1)
+
+
+def row_sumsq(x):
+    return np.sum(x * x, axis=1)
+
+
+def row_dot(x, aux):
+    return np.sum(x * np.asarray(aux, dtype=np.float64), axis=1)
+
+
+# ---------------------------------------------------------------------------
+# the whole epilogue program, as separate passes in op-list order
+# ---------------------------------------------------------------------------
+def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
+              residual_t=None, z=None, xhat=None, norm_gamma=None, rows=None):
+    """Evaluate D = f(A @ B) for an op list, one unfused pass per op.
+
+    ops: sequence of (name, slot, f0) tuples, names from OP_NAMES.
+    col_vecs / row_vecs: dict slot -> vector (bf16 values widened).
+    residual_t, z, xhat: [M, N_out] aux tensors (or only the sampled rows).
+    norm_gamma: if given, the op list must begin with RMS_ROWSCALE; the GEMM is
+        then evaluated as rmsnorm(A, gamma) @ B (normalise, then project), with
+        B the *unscaled* weight.
+    rows: absolute row indices of the rows of A given (used by dropout's
+        counter and nothing else); default 0..M-1.
+
+    Returns dict with D (fp64), stats {slot: fp64[M]}, keep_count (int64[M] or
+    None), keep (bool mask or None), preact (fp64 or None).
+    """
+    A = np.asarray(A, dtype=np.float64)
+    col_vecs = col_vecs or {}
+    row_vecs = row_vecs or {}
+    M = A.shape[0]
+    if rows is None:
+        rows = np.arange(M)
+    ops = [(o[0], o[1] if len(o) > 1 else 0, o[2] if len(o) > 2 else 0.0) for o in ops]
+
+    start = 0
+    stats = {}
+    if norm_gamma is not None:
+        name, slot, eps = ops[0]
+        if name != "RMS_ROWSCALE":
+            raise ValueError("norm_gamma needs RMS_ROWSCALE as the first op")
+        x = rmsnorm_project(A, norm_gamma, B, eps, b_layout)
+        if slot is not None and slot >= 0:
+            stats[slot] = rms_rstd(A, eps)
+        start = 1
+    else:
+        x = gemm(A, B, b_layout)
+
+    keep_count = None
+    keep = None
+    preact = None
+    for name, slot, f0 in ops[start:]:
+        if name == "SCALE":
+            x = scale(x, f0)
+        elif name == "COL_SCALE":
+            x = col_scale(x, col_vecs[slot])
+        elif name == "BIAS":
+            x = bias(x, col_vecs[slot])
+        elif name == "ROW_SCALE":
+            x = row_scale(x, row_vecs[slot])
+        elif name == "RMS_ROWSCALE":
+            r = rms_rstd(A, f0)
+            x = row_scale(x, r)
+            if slot is not None and slot >= 0:
+                stats[slot] = r
+        elif name == "GELU_TANH":
+            x = gelu_tanh(x)
+        elif name == "SILU":
+            x = silu(x)
+        elif name == "SWIGLU":
+            x = swiglu(x)
+        elif name == "GELU_TANH_GRAD":
+            x = x * gelu_tanh_grad(z)
+        elif name == "DROPOUT":
+            x, keep = dropout(x, f0, seed, rows=rows)
+            keep_count = keep.sum(axis=1).astype(np.int64)
+        elif name == "RESIDUAL":
+            x = residual(x, residual_t, f0)
+        elif name == "STORE_PREACT":
+            preact = x.copy()
+        elif name == "ROW_SUM":
+            stats[slot] = row_sum(x)
+        elif name == "ROW_MEAN":
+            stats[slot] = row_mean(x)
+        elif name == "ROW_SUMSQ":
+            stats[slot] = row_sumsq(x)
+        elif name == "ROW_DOT_AUX":
+            stats[slot] = row_dot(x, xhat)
+        else:
+            raise ValueError(f"unknown op {name}")
+    return dict(D=x, stats=stats, keep_count=keep_count, keep=keep, preact=preact)
+
+
+def to_f64(t) -> np.ndarray:
+    """Widen a tensor (torch bf16/fp32 or numpy) to an fp64 numpy array exactly."""
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            return t.detach().to("cpu", torch.float64).numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.asarray(t, dtype=np.float64)

@@ -1,0 +1,312 @@
+"""Pins for the fp64 oracle: checks against closed forms, brute force, textbook
+identities and published known answers -- never against the oracle itself.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign or index, a transposed operand, a wrong constant) fails it.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import coda_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- GEMM ------
+def _brute_gemm(A, B, layout):
+    M, K = len(A), len(A[0])
+    N = len(B[0]) if layout == "kn" else len(B)
+    C = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = 0.0
+            for k in range(K):
+                b = B[k][j] if layout == "kn" else B[j][k]
+                s += A[i][k] * b
+            C[i][j] = s
+    return np.array(C)
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_gemm_brute_force_8x8x8(layout):
+    A = rng.standard_normal((8, 8))
+    B = rng.standard_normal((8, 8))
+    ref = _brute_gemm(A.tolist(), B.tolist(), layout)
+    np.testing.assert_allclose(O.gemm(A, B, layout), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_gemm_brute_force_rectangular():
+    A = rng.standard_normal((5, 7))
+    B = rng.standard_normal((7, 3))
+    np.testing.assert_allclose(O.gemm(A, B, "kn"), _brute_gemm(A.tolist(), B.tolist(), "kn"), rtol=1e-13)
+    np.testing.assert_allclose(O.gemm(A, B.T.copy(), "nk"), _brute_gemm(A.tolist(), B.tolist(), "kn"),
+                               rtol=1e-13)
+
+
+def test_gemm_identity_and_one_hot():
+    B = rng.standard_normal((6, 9))
+    np.testing.assert_array_equal(O.gemm(np.eye(6), B, "kn"), B)
+    A = np.zeros((4, 6))
+    A[2, 5] = 1.0                      # e_2 e_5^T picks row 5 of B into row 2
+    C = O.gemm(A, B, "kn")
+    np.testing.assert_array_equal(C[2], B[5])
+    assert np.count_nonzero(C[[0, 1, 3]]) == 0
+    # [N,K] layout: C[i, n] = B[n, k]
+    Bnk = rng.standard_normal((9, 6))
+    C = O.gemm(A, Bnk, "nk")
+    np.testing.assert_array_equal(C[2], Bnk[:, 5])
+
+
+def test_gemm_small_integers_exact():
+    A = rng.integers(-8, 9, (33, 64)).astype(np.float64)
+    B = rng.integers(-8, 9, (64, 17)).astype(np.float64)
+    ref = np.zeros((33, 17))
+    for k in range(64):                 # exact integer accumulation
+        ref += np.outer(A[:, k], B[k])
+    np.testing.assert_array_equal(O.gemm(A, B), ref)
+
+
+# ---------------------------------------------------------------- GELU ------
+def _gelu_erf(x):
+    return 0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0)))
+
+
+def test_gelu_closed_forms():
+    assert O.gelu_tanh(0.0) == 0.0
+    x = np.linspace(-6, 6, 1201)
+    # odd part: gelu(x) - gelu(-x) = x exactly, because tanh is odd
+    np.testing.assert_allclose(O.gelu_tanh(x) - O.gelu_tanh(-x), x, atol=1e-14)
+    assert abs(O.gelu_tanh(30.0) - 30.0) < 1e-12
+    assert abs(O.gelu_tanh(-30.0)) < 1e-12
+
+
+def test_gelu_tanh_close_to_exact_erf_gelu():
+    # The tanh form approximates x*Phi(x) to within 4.8e-4 everywhere; a wrong
+    # coefficient (0.04 or 0.05 instead of 0.044715, sqrt(2)/pi, x^2 for x^3)
+    # moves it to >= 2.8e-3.
+    x = np.linspace(-10, 10, 40001)
+    exact = np.array([_gelu_erf(v) for v in x])
+    err = np.abs(O.gelu_tanh(x) - exact).max()
+    assert err < 5e-4, err
+
+
+def test_gelu_grad_matches_finite_difference():
+    z = np.linspace(-7, 7, 1401)
+    h = 1e-5
+    fd = (O.gelu_tanh(z + h) - O.gelu_tanh(z - h)) / (2 * h)
+    np.testing.assert_allclose(O.gelu_tanh_grad(z), fd, atol=1e-9)
+    assert O.gelu_tanh_grad(0.0) == 0.5
+    assert abs(O.gelu_tanh_grad(40.0) - 1.0) < 1e-12
+
+
+# ---------------------------------------------------------------- SiLU ------
+def test_silu_closed_forms():
+    assert O.silu(0.0) == 0.0
+    x = np.linspace(-20, 20, 801)
+    np.testing.assert_allclose(O.silu(x) - O.silu(-x), x, atol=1e-13)
+    # sigmoid(x) = (1 + tanh(x/2)) / 2, an independent closed form
+    np.testing.assert_allclose(O.silu(x), 0.5 * x * (1.0 + np.tanh(0.5 * x)), rtol=1e-13, atol=1e-15)
+    assert abs(O.silu(50.0) - 50.0) < 1e-12
+
+
+def test_swiglu_pairs_halves_not_interleaved():
+    n = 6
+    G = np.arange(1, n + 1, dtype=np.float64)[None, :]
+    U = 10.0 + np.arange(n, dtype=np.float64)[None, :]
+    out = O.swiglu(np.concatenate([G, U], axis=1))
+    expect = np.array([[(j + 1) / (1 + math.exp(-(j + 1))) * (10 + j) for j in range(n)]])
+    np.testing.assert_allclose(out, expect, rtol=1e-14)
+    assert np.count_nonzero(O.swiglu(np.concatenate([G, 0 * U], axis=1))) == 0
+
+
+# ------------------------------------------------------------- RMSNorm ------
+def test_rmsnorm_constant_row():
+    K, c, eps = 64, 3.0, 1e-6
+    X = np.full((2, K), c)
+    X[1] = -c
+    gamma = rng.uniform(0.5, 1.5, K)
+    Xn = O.rmsnorm(X, gamma, eps)
+    f = c / math.sqrt(c * c + eps)
+    np.testing.assert_allclose(Xn[0], gamma * f, rtol=1e-15)
+    np.testing.assert_allclose(Xn[1], -gamma * f, rtol=1e-15)
+
+
+def test_rms_rstd_hand_value():
+    X = np.array([[3.0, 4.0]])          # mean square 12.5
+    assert abs(O.rms_rstd(X, 0.5)[0] - 1.0 / math.sqrt(13.0)) < 1e-16
+    X = np.zeros((1, 10))
+    X[0, 3] = 2.0                        # mean square 0.4
+    assert abs(O.rms_rstd(X, 1e-6)[0] - 1.0 / math.sqrt(0.4 + 1e-6)) < 1e-15
+
+
+def test_commuted_rmsnorm_identity():
+    # zeli.app (augment_me): the row-wise scale of the norm commutes past the
+    # projection: rmsnorm(X) @ W == r (.)_row (X @ (gamma (.)_row W)).
+    X = rng.standard_normal((40, 32))
+    gamma = rng.uniform(0.5, 1.5, 32)
+    W = rng.standard_normal((32, 24))
+    lhs = O.rmsnorm_project(X, gamma, W, 1e-6)
+    r = O.rms_rstd(X, 1e-6)
+    rhs = r[:, None] * (X @ (gamma[:, None] * W))
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------- dropout ------
+def _golden_splitmix():
+    vals = []
+    with open(os.path.join(GOLDEN, "splitmix64_seed0.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                vals.append(int(line, 16))
+    return vals
+
+
+def test_splitmix64_known_answers():
+    expect = _golden_splitmix()
+    got = [int(v) for v in O.splitmix64(0, np.arange(len(expect)))]
+    assert got == expect
+
+
+def test_dropout_threshold_value():
+    # (1 - 0.1) in fp64 times 2^64, truncated: 0.9 is 0x3FECCCCCCCCCCCCD
+    assert O.dropout_threshold(0.1) == 0xE666666666666800
+    assert O.dropout_threshold(0.1) == 16602069666338596864
+    assert O.dropout_threshold(0.5) == 1 << 63
+    assert O.dropout_threshold(0.0) is None
+
+
+def test_dropout_mask_known_answers_and_flat_index():
+    kat = _golden_splitmix()
+    T = O.dropout_threshold(0.1)
+    # the [1,5] output's element i uses stream position i
+    keep = O.dropout_mask(0, 1, 5, 0.1)
+    assert keep[0].tolist() == [v < T for v in kat]
+    # the counter is the row-major flat index of the [M, N] output
+    m, n = 7, 13
+    a = O.dropout_mask(5, m, n, 0.1)
+    b = O.dropout_mask(5, 1, m * n, 0.1).reshape(m, n)
+    np.testing.assert_array_equal(a, b)
+    c = O.dropout_mask(5, 1, n, 0.1, rows=[3])
+    np.testing.assert_array_equal(a[3], c[0])
+
+
+def test_dropout_keep_rate_three_sigma():
+    p = 0.1
+    keep = O.dropout_mask(0, 512, 8192, p)
+    n = keep.size
+    rate = keep.mean()
+    sigma = math.sqrt(p * (1 - p) / n)
+    assert abs(rate - (1 - p)) < 3 * sigma, (rate, sigma)
+    # rows and columns are not correlated with position: per-row rates spread like binomials
+    per_row = keep.mean(axis=1)
+    assert abs(per_row.std() - math.sqrt(p * (1 - p) / 8192)) < 0.25 * math.sqrt(p * (1 - p) / 8192)
+
+
+def test_dropout_scaling_and_identity():
+    x = rng.standard_normal((16, 40))
+    y, keep = O.dropout(x, 0.25, 3)
+    np.testing.assert_array_equal(y[~keep], 0.0)
+    np.testing.assert_allclose(y[keep], x[keep] / 0.75, rtol=1e-15)
+    y0, k0 = O.dropout(x, 0.0, 3)
+    np.testing.assert_array_equal(y0, x)
+    assert k0.all()
+
+
+# ---------------------------------------------------------- reductions ------
+def test_row_reductions_closed_forms():
+    N = 100
+    x = np.tile(np.arange(N, dtype=np.float64), (3, 1))
+    x[1] = 1.0
+    assert O.row_sum(x)[0] == N * (N - 1) / 2
+    assert O.row_sumsq(x)[0] == (N - 1) * N * (2 * N - 1) / 6
+    assert O.row_mean(x)[0] == (N - 1) / 2
+    assert O.row_sum(x)[1] == N and O.row_sumsq(x)[1] == N and O.row_mean(x)[1] == 1.0
+    np.testing.assert_array_equal(O.row_dot(x, np.ones_like(x)), O.row_sum(x))
+
+
+def test_residual_cancels():
+    A = rng.standard_normal((9, 11))
+    B = rng.standard_normal((11, 13))
+    C = A @ B
+    out = O.run_chain(A, B, [("RESIDUAL", 0, 1.0)], residual_t=-C)["D"]
+    assert np.abs(out).max() < 1e-12
+
+
+# --------------------------------------------------------------- chain ------
+def test_chain_zero_gemm_closed_form():
+    # A = 0 makes C = 0, so D = gelu(bias) + residual elementwise
+    M, K, N = 5, 4, 6
+    b = rng.standard_normal(N)
+    R = rng.standard_normal((M, N))
+    out = O.run_chain(np.zeros((M, K)), rng.standard_normal((K, N)),
+                      [("BIAS", 0), ("GELU_TANH",), ("RESIDUAL", 0, 1.0)],
+                      col_vecs={0: b}, residual_t=R)["D"]
+    expect = np.array([[0.5 * v * (1 + math.tanh(math.sqrt(2 / math.pi) * (v + 0.044715 * v ** 3)))
+                        for v in b] for _ in range(M)]) + R
+    np.testing.assert_allclose(out, expect, rtol=1e-14)
+
+
+def test_chain_order_matters_and_alpha_zero():
+    A = rng.standard_normal((3, 4))
+    B = rng.standard_normal((4, 5))
+    b = rng.standard_normal(5)
+    d1 = O.run_chain(A, B, [("SCALE", 0, 2.0), ("BIAS", 0)], col_vecs={0: b})["D"]
+    d2 = O.run_chain(A, B, [("BIAS", 0), ("SCALE", 0, 2.0)], col_vecs={0: b})["D"]
+    np.testing.assert_allclose(d2 - d1, np.tile(b, (3, 1)), rtol=1e-12)
+    d0 = O.run_chain(A, B, [("SCALE", 0, 0.0), ("GELU_TANH",)])["D"]
+    np.testing.assert_array_equal(d0, 0.0)
+
+
+def test_chain_swiglu_then_column_ops_use_half_width():
+    A = rng.standard_normal((4, 8))
+    B = rng.standard_normal((8, 10))
+    b = rng.standard_normal(5)
+    out = O.run_chain(A, B, [("SWIGLU",), ("BIAS", 0), ("ROW_SUM", 1)], col_vecs={0: b})
+    C = A @ B
+    h = C[:, :5] / (1 + np.exp(-C[:, :5])) * C[:, 5:] + b
+    np.testing.assert_allclose(out["D"], h, rtol=1e-13)
+    np.testing.assert_allclose(out["stats"][1], h.sum(axis=1), rtol=1e-13)
+
+
+def test_chain_commuted_norm_reads_unscaled_weight():
+    X = rng.standard_normal((6, 16))
+    gamma = rng.uniform(0.5, 1.5, 16)
+    W = rng.standard_normal((16, 8))
+    out = O.run_chain(X, W, [("RMS_ROWSCALE", 2, 1e-6)], norm_gamma=gamma)
+    r = 1.0 / np.sqrt((X * X).mean(axis=1) + 1e-6)
+    np.testing.assert_allclose(out["stats"][2], r, rtol=1e-14)
+    # against the commuted evaluation with gamma folded into W
+    np.testing.assert_allclose(out["D"], r[:, None] * (X @ (gamma[:, None] * W)), rtol=1e-12)
+
+
+def test_chain_dgrad_form():
+    dY = rng.standard_normal((5, 7))
+    W = rng.standard_normal((9, 7))     # [N, K]
+    Z = rng.standard_normal((5, 9))
+    Xh = rng.standard_normal((5, 9))
+    out = O.run_chain(dY, W, [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)],
+                      b_layout="nk", z=Z, xhat=Xh)
+    h = 1e-6
+    gp = (O.gelu_tanh(Z + h) - O.gelu_tanh(Z - h)) / (2 * h)
+    dX = _brute_gemm(dY.tolist(), W.T.tolist(), "kn") * gp
+    np.testing.assert_allclose(out["D"], dX, rtol=1e-7, atol=1e-8)
+    np.testing.assert_allclose(out["stats"][0], (dX * Xh).sum(axis=1), rtol=1e-7, atol=1e-7)
+    np.testing.assert_allclose(out["stats"][1], dX.sum(axis=1), rtol=1e-7, atol=1e-7)
+
+
+def test_chain_col_row_scale_and_preact_closed_form():
+    # A = I, B = ones makes C = ones, so COL_SCALE then ROW_SCALE gives u_i * v_j,
+    # and the stored pre-activation is that product before the GELU
+    n = 6
+    v = rng.standard_normal(n)
+    u = rng.standard_normal(n)
+    out = O.run_chain(np.eye(n), np.ones((n, n)),
+                      [("COL_SCALE", 1), ("ROW_SCALE", 0), ("STORE_PREACT",), ("SILU",)],
+                      col_vecs={1: v}, row_vecs={0: u})
+    np.testing.assert_allclose(out["preact"], np.outer(u, v), rtol=1e-15)
+    np.testing.assert_allclose(out["D"], O.silu(np.outer(u, v)), rtol=1e-15)
