@@ -1,0 +1,393 @@
+"""Benchmark of the fused GEMM + on-chip epilogue path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|swiglu|dgrad|llama]
+                    [--impl coda|reference]
+
+Default workload: the commuted-RMSNorm projection D = rsqrt(mean(X^2)+1e-6) *
+(X @ (gamma (.) W)), X[4096,2048], W[2048,8192], bf16 in, fp32 accumulate.
+One step = one pass of the fused path over the synthetic batch.  Prints one
+JSON line (rank 0): fused TFLOP/s, the roofline of the fused GEMM kernel, the
+same chain run unfused through the library's own kernels, DRAM bytes fused vs
+unfused, an end-to-end figure through host buffers, clocks, and the fp64
+oracle timed on the host cores as the CPU baseline.
+
+Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
+launching stream, with a 256 MiB device write between steps so every step
+reads its operands from HBM (the inputs are smaller than the 129 MB L2).
+Under torchrun each rank runs an independent replica (the path has no
+cross-GPU exchange); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+_NCORES = len(os.sched_getaffinity(0))
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_NCORES))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 bf16 roofline; DRAM bytes vs unfused"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["coda_gemm_kernel.cuh", "coda_ops.cuh", "coda_ptx.cuh", "coda_internal.h"]
+L2_FLUSH_BYTES = 256 << 20
+
+DESCRIPTIONS = {
+    "rmsproj": "commuted RMSNorm projection D = rsqrt(mean(X^2)+1e-6)*(X@(gamma*W)), X[4096,2048], W[2048,8192]",
+    "swiglu": "SwiGLU up-projection [G|U] = X[8192,4096] @ W[4096,22016], SiLU(G)*U, dropout p=0.1",
+    "dgrad": "dgrad dX = (dY[8192,4096] @ W[16384,4096]^T) * GELU'(Z), rows sum(dX*Xhat), sum(dX)",
+    "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs)",
+}
+DEFAULT_STEPS = {"rmsproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "gemm_epilogue_transformer_tmem_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when the kernel sources changed since that capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"coda_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ timing
+def timed_loop(calls, steps, warmup, flush, stream):
+    """Run `steps` steps; returns (per-call total ms list, total ms).  Every call
+    is bracketed by events on `stream`; the L2 flush runs outside them."""
+    for _ in range(warmup):
+        flush()
+        for c in calls:
+            c()
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+           for _ in range(steps)]
+    for i in range(steps):
+        flush()
+        for j, c in enumerate(calls):
+            evs[i][j][0].record(stream)
+            c()
+            evs[i][j][1].record(stream)
+    torch.cuda.synchronize()
+    per_call = [0.0] * len(calls)
+    for i in range(steps):
+        for j in range(len(calls)):
+            per_call[j] += evs[i][j][0].elapsed_time(evs[i][j][1])
+    return per_call, sum(per_call)
+
+
+def fused_calls(step):
+    return [step.fused]
+
+
+# ------------------------------------------------------------- CPU oracle
+class OracleSample:
+    """The fp64 oracle on a row sample of a workload, inputs generated once.
+    calibrate() picks the row count for about `target_s` seconds per run."""
+
+    def __init__(self, workload: str):
+        from gemm_epilogue_transformer_tmem_gb300 import inputs
+        from oracle import coda_oracle as O
+        self.w, self.I, self.O = workload, inputs, O
+        gen = dict(rmsproj=inputs.make_rmsproj, swiglu=inputs.make_swiglu, dgrad=inputs.make_dgrad,
+                   llama=inputs.make_llama_block)[workload]
+        self.t = {k: O.to_f64(v) for k, v in gen(0).items()}
+        self.Mmax = next(iter(self.t.values())).shape[0] if workload != "llama" else self.t["X"].shape[0]
+        self.rows = 32
+
+    def run(self, rows: int):
+        """Returns (seconds, flops) of the oracle on the first `rows` rows."""
+        I, O, t = self.I, self.O, self.t
+        r = slice(0, rows)
+        t0 = time.perf_counter()
+        if self.w == "rmsproj":
+            O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", 0, I.EPS_RMS)], norm_gamma=t["gamma"])
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "swiglu":
+            O.run_chain(t["X"][r], t["W"], [("SWIGLU",), ("DROPOUT", 0, I.DROPOUT_P)])
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "dgrad":
+            O.run_chain(t["dY"][r], t["W"], [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)],
+                        b_layout="nk", z=t["Z"][r], xhat=t["Xhat"][r])
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        else:
+            eps = I.EPS_RMS
+            X = t["X"][r]
+            O.run_chain(X, t["W_qkv"], [("RMS_ROWSCALE", None, eps)], norm_gamma=t["gamma_attn"])
+            h = O.run_chain(t["attn_out"][r], t["W_o"], [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
+            up = O.run_chain(h, t["W_up"], [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
+                             norm_gamma=t["gamma_mlp"])["D"]
+            O.run_chain(up, t["W_down"], [("RESIDUAL", 0, 1.0)], residual_t=h)
+            d, f = t["W_o"].shape[0], t["W_down"].shape[0]
+            fl = 2 * rows * d * (3 * d + d + 2 * f) + 2 * rows * f * d
+        return time.perf_counter() - t0, fl
+
+    def calibrate(self, target_s: float) -> int:
+        dt, _ = self.run(self.rows)
+        while dt < target_s / 3 and self.rows < self.Mmax:
+            grow = max(2.0, min(16.0, 0.8 * target_s / max(dt, 1e-3)))
+            self.rows = min(self.Mmax, int(self.rows * grow))
+            dt, _ = self.run(self.rows)
+        return self.rows
+
+
+def aggregate_ms(total_ms: float, dist, device) -> float:
+    """Max over ranks of the timed region (each rank ran its own replica)."""
+    if dist is None:
+        return total_ms
+    t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# -------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="rmsproj", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--impl", default="coda", choices=["coda", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
+    warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, steps, warmup, world, rank)
+
+    torch.cuda.set_device(local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    import __graft_entry__ as entry
+    entry.build()
+    from gemm_epilogue_transformer_tmem_gb300 import coda, workloads
+
+    dev = torch.device("cuda", local)
+    step = workloads.BUILDERS[args.workload](dev=dev)
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty((L2_FLUSH_BYTES // 4,), dtype=torch.float32, device=dev)
+    flush = lambda: flush_buf.zero_()  # noqa: E731
+
+    # ---- fused step, device-resident inputs
+    sampler = ClockSampler(local) if rank == 0 else None
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    launches0 = coda.launch_count()
+    per_call, total_ms = timed_loop([step.fused], steps, warmup, flush, stream)
+    launches = coda.launch_count() - launches0 - warmup * step.kernels_per_fused
+    clocks = sampler.stop() if sampler else None
+    st, info = coda.check_device_error()
+    if st != 0:
+        raise RuntimeError(f"device error {st}: {info}")
+    total_ms = aggregate_ms(total_ms, pg, dev)
+    if pg:
+        pg.barrier()
+    ms = total_ms / steps
+    value = world * step.flops / (ms * 1e-3) / 1e12
+
+    # ---- unfused chain through the library's own kernels
+    unfused = None
+    if not args.no_unfused:
+        _, u_total = timed_loop([step.unfused], max(steps // 2, 3), warmup, flush, stream)
+        u_ms = u_total / max(steps // 2, 3)
+        unfused = {"ms_per_step": round(u_ms, 5), "value": round(step.flops / (u_ms * 1e-3) / 1e12, 2),
+                   "unit": UNIT, "kernels_per_step": step.kernels_per_unfused,
+                   "speedup_fused": round(u_ms / ms, 3)}
+
+    # ---- end to end through host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e and rank == 0:
+        hin = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu())
+               for k, v in step.host_inputs.items()}
+        hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in step.host_outputs.items()}
+        e2e_steps = max(steps // 10, 3)
+
+        def e2e_call():
+            for k, v in hin.items():
+                step.host_inputs[k].copy_(v, non_blocking=True)
+            step.fused()
+            for k, v in hout.items():
+                v.copy_(step.host_outputs[k], non_blocking=True)
+
+        _, e_total = timed_loop([e2e_call], e2e_steps, 2, flush, stream)
+        e_ms = e_total / e2e_steps
+        e2e = {"value": round(step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
+               "ms_per_step": round(e_ms, 5),
+               "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hin.values())),
+               "d2h_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hout.values()))}
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    # the fused kernels are timed in short bursts between L2 flushes: burst peak
+    peak = float(peaks["bf16_tflops"])
+    achieved = step.flops / (sum(per_call) / steps * 1e-3) / 1e12
+    traffic = load_traffic(args.workload)
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"bf16 burst, of {peak_src}",
+                "traffic": traffic["bytes_per_launch"] if traffic else None,
+                "algorithmic_bytes": step.fused_bytes}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        osm = OracleSample(args.workload)
+        rows = osm.calibrate(12.0)
+        dt, fl = osm.run(rows)
+        cpu = {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": _NCORES, "kind": "oracle",
+               "sample": f"fp64 oracle on the first {rows} rows of the workload ({dt:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "flops_per_step": step.flops,
+                   "l2": "flushed between steps (256 MiB device write outside the timed events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "weight_prep": "gamma folded into W once per weight version, not in the step"},
+        "roofline": roofline,
+        "dram_bytes": {"fused_algorithmic": step.fused_bytes, "unfused_algorithmic": step.unfused_bytes,
+                       "ncu_fused_per_launch": traffic["bytes_per_launch"] if traffic else None},
+        "unfused": unfused,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def reference_arm(args, steps, warmup, world, rank):
+    """The fp64 oracle timed on the host cores as the reference implementation."""
+    if rank != 0:
+        return
+    osm = OracleSample(args.workload)
+    per_step = max(0.5, min(10.0, 150.0 / (steps + warmup)))
+    rows = osm.calibrate(per_step)
+    vals = []
+    for i in range(warmup + steps):
+        dt, fl = osm.run(rows)
+        if i >= warmup:
+            vals.append((fl / dt / 1e12, dt))
+    value = statistics.median(v for v, _ in vals)
+    ms = statistics.median(dt for _, dt in vals) * 1e3
+    info = (rows,)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "sample": f"first {info[0]} rows per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": _NCORES, "kind": "oracle",
+                         "sample": f"fp64 oracle on the first {info[0]} rows per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,274 @@
+"""ctypes binding of libcoda.so, the GB300 GEMM + on-chip epilogue library.
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  PyTorch provides device memory (torch tensors) and the current CUDA
+stream.  If the library is not built this module raises instead of falling
+back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libcoda.so")
+
+OPCODES = {
+    "SCALE": 0, "COL_SCALE": 1, "BIAS": 2, "ROW_SCALE": 3, "RMS_ROWSCALE": 4, "GELU_TANH": 5,
+    "SILU": 6, "SWIGLU": 7, "GELU_TANH_GRAD": 8, "DROPOUT": 9, "RESIDUAL": 10, "STORE_PREACT": 11,
+    "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15,
+}
+REDUCTIONS = ("ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX")
+MAX_OPS = 16
+NO_SLOT = 0xFFFFFFFF
+B_LAYOUTS = {"kn": 0, "nk": 1}
+STATUS = {0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_UNSUPPORTED", 3: "CODA_ERR_ALIGNMENT",
+          4: "CODA_ERR_CUDA", 5: "CODA_ERR_TIMEOUT", 6: "CODA_ERR_WORKSPACE"}
+
+
+class CodaOp(ctypes.Structure):
+    _fields_ = [("opcode", ctypes.c_uint32), ("slot", ctypes.c_uint32), ("f0", ctypes.c_float),
+                ("f1", ctypes.c_float)]
+
+
+class CodaEpilogue(ctypes.Structure):
+    _fields_ = [("n_ops", ctypes.c_uint32), ("reserved", ctypes.c_uint32), ("seed", ctypes.c_uint64),
+                ("ops", CodaOp * MAX_OPS)]
+
+
+class CodaAux(ctypes.Structure):
+    _fields_ = [("col_vec", ctypes.c_void_p * 4), ("row_vec", ctypes.c_void_p * 2), ("residual", ctypes.c_void_p),
+                ("z", ctypes.c_void_p), ("xhat", ctypes.c_void_p), ("preact_out", ctypes.c_void_p)]
+
+
+class CodaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+_lib = None
+
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SIGS = {
+    "coda_gemm_epilogue": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, ctypes.c_int32, _VP, _VP, _VP, _VP, _VP,
+                                          _VP, ctypes.c_size_t, _VP]),
+    "coda_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _VP, ctypes.POINTER(ctypes.c_size_t)]),
+    "coda_fold_gamma": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
+    "coda_rmsnorm": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP, _VP]),
+    "coda_epilogue_apply": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP]),
+    "coda_check_device_error": (ctypes.c_int, [_VP, _VP]),
+    "coda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "coda_launch_count": (ctypes.c_uint64, []),
+    "coda_set_pipeline_timeout_ns": (None, [ctypes.c_uint64]),
+    "coda_set_max_ctas": (None, [ctypes.c_int32]),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libcoda.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                               "(python -m gemm_epilogue_transformer_tmem_gb300.build)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise CodaError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the CUDA library must live on the GPU")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the CUDA library must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _norm_ops(ops: Sequence) -> list[tuple[str, int, float]]:
+    out = []
+    for o in ops:
+        if isinstance(o, str):
+            o = (o,)
+        name = o[0]
+        slot = o[1] if len(o) > 1 else 0
+        f0 = o[2] if len(o) > 2 else 0.0
+        if slot is None or slot < 0:
+            slot = NO_SLOT
+        out.append((name, int(slot), float(f0)))
+    return out
+
+
+def make_epilogue(ops: Sequence, seed: int = 0) -> CodaEpilogue:
+    """Op list [(name, slot, f0), ...] -> the C descriptor."""
+    ops = _norm_ops(ops)
+    if len(ops) > MAX_OPS:
+        raise ValueError("too many ops")
+    e = CodaEpilogue()
+    e.n_ops = len(ops)
+    e.reserved = 0
+    e.seed = seed & ((1 << 64) - 1)
+    for i, (name, slot, f0) in enumerate(ops):
+        e.ops[i].opcode = OPCODES[name]
+        e.ops[i].slot = slot
+        e.ops[i].f0 = f0
+        e.ops[i].f1 = 0.0
+    return e
+
+
+def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None) -> CodaAux:
+    a = CodaAux()
+    for k, t in (col_vecs or {}).items():
+        a.col_vec[k] = _ptr(t)
+    for k, t in (row_vecs or {}).items():
+        a.row_vec[k] = _ptr(t)
+    a.residual = _ptr(residual)
+    a.z = _ptr(z)
+    a.xhat = _ptr(xhat)
+    a.preact_out = _ptr(preact_out)
+    return a
+
+
+def output_width(N: int, ops: Sequence) -> int:
+    return N // 2 if any(o[0] == "SWIGLU" for o in _norm_ops(ops)) else N
+
+
+def stat_slots(ops: Sequence) -> int:
+    n = 0
+    for name, slot, _ in _norm_ops(ops):
+        if (name in REDUCTIONS or name == "RMS_ROWSCALE") and slot != NO_SLOT:
+            n = max(n, slot + 1)
+    return n
+
+
+def workspace_size(M: int, N: int, K: int, ops: Sequence = ()) -> int:
+    n = ctypes.c_size_t(0)
+    e = make_epilogue(ops)
+    _check(lib().coda_workspace_size(M, N, K, ctypes.byref(e), ctypes.byref(n)), "coda_workspace_size")
+    return n.value
+
+
+@dataclass
+class Result:
+    D: torch.Tensor
+    row_stats: Optional[torch.Tensor]
+    keep_count: Optional[torch.Tensor]
+
+
+def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_layout: str = "kn", seed: int = 0,
+                  col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None,
+                  out: Optional[torch.Tensor] = None, row_stats: Optional[torch.Tensor] = None,
+                  keep_count: Optional[torch.Tensor] = None, want_keep_count: bool = True,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> Result:
+    """D = f(A @ B) through coda_gemm_epilogue; allocates missing outputs with torch."""
+    M, K = A.shape
+    N = B.shape[1] if b_layout == "kn" else B.shape[0]
+    n_out = output_width(N, ops)
+    dev = A.device
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=dev)
+    ns = stat_slots(ops)
+    if row_stats is None and ns > 0:
+        row_stats = torch.empty((ns, M), dtype=torch.float32, device=dev)
+    has_dropout = any(o[0] == "DROPOUT" for o in _norm_ops(ops))
+    if keep_count is None and has_dropout and want_keep_count:
+        keep_count = torch.empty((M,), dtype=torch.int32, device=dev)
+    wbytes = workspace_size(M, N, K, ops)
+    if workspace is None and wbytes > 0:
+        workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
+    e = make_epilogue(ops, seed)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(e), ctypes.byref(a),
+                                  _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
+                                  workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(st, "coda_gemm_epilogue")
+    return Result(out, row_stats, keep_count)
+
+
+def fold_gamma(W: torch.Tensor, gamma: torch.Tensor, b_layout: str = "kn", out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """bf16(gamma (.)_row W): gamma scales W's K index (rows for [K,N], columns for [N,K])."""
+    if b_layout == "kn":
+        K, N = W.shape
+    else:
+        N, K = W.shape
+    if out is None:
+        out = torch.empty_like(W)
+    _check(lib().coda_fold_gamma(_ptr(W), _ptr(gamma), _ptr(out), K, N, B_LAYOUTS[b_layout], _stream(stream)),
+           "coda_fold_gamma")
+    return out
+
+
+def rmsnorm(X: torch.Tensor, gamma: torch.Tensor, eps: float, out: Optional[torch.Tensor] = None,
+            rstd: Optional[torch.Tensor] = None, stream=None):
+    M, K = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    if rstd is None:
+        rstd = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(lib().coda_rmsnorm(_ptr(X), _ptr(gamma), M, K, eps, _ptr(out), _ptr(rstd), _stream(stream)),
+           "coda_rmsnorm")
+    return out, rstd
+
+
+def epilogue_apply(C: torch.Tensor, ops: Sequence, *, seed: int = 0, col_vecs=None, row_vecs=None, residual=None,
+                   z=None, xhat=None, preact_out=None, out: Optional[torch.Tensor] = None,
+                   row_stats: Optional[torch.Tensor] = None, keep_count: Optional[torch.Tensor] = None,
+                   stream=None) -> Result:
+    """The unfused form: the op list applied to a bf16 tensor C already in memory."""
+    M, N = C.shape
+    n_out = output_width(N, ops)
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=C.device)
+    ns = stat_slots(ops)
+    if row_stats is None and ns > 0:
+        row_stats = torch.empty((ns, M), dtype=torch.float32, device=C.device)
+    if keep_count is None and any(o[0] == "DROPOUT" for o in _norm_ops(ops)):
+        keep_count = torch.empty((M,), dtype=torch.int32, device=C.device)
+    e = make_epilogue(ops, seed)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    _check(lib().coda_epilogue_apply(_ptr(C), M, N, ctypes.byref(e), ctypes.byref(a), _ptr(out), _ptr(row_stats),
+                                     _ptr(keep_count), _stream(stream)), "coda_epilogue_apply")
+    return Result(out, row_stats, keep_count)
+
+
+def check_device_error(stream=None) -> tuple[int, list[int]]:
+    info = (ctypes.c_uint32 * 4)()
+    st = lib().coda_check_device_error(_stream(stream), info)
+    return st, list(info)
+
+
+def launch_count() -> int:
+    return int(lib().coda_launch_count())
+
+
+def set_pipeline_timeout_ns(ns: int) -> None:
+    lib().coda_set_pipeline_timeout_ns(ns)
+
+
+def set_max_ctas(n: int) -> None:
+    lib().coda_set_max_ctas(n)

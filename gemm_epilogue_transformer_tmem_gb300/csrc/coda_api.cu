@@ -1,0 +1,497 @@
+// Host side of the C ABI declared in include/coda.h: argument and op-list
+// validation, compilation of the op list into the kernels' program, TMA tensor
+// map encoding, launch on the caller's stream, and the device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "coda_internal.h"
+#include "coda_launch.h"
+
+namespace coda {
+
+// first device-side failure: code, block, role, tile (see coda_check_device_error)
+__device__ uint32_t g_coda_err[4];
+
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_max_ctas{0};
+
+constexpr int kMaxDevices = 64;
+struct DevInfo {
+  bool init;
+  int sms;
+  int max_smem;
+  uint32_t* err;
+};
+DevInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+coda_status device_info(DevInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CODA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return CODA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return CODA_ERR_CUDA;
+    // the kernels are compiled for sm_103a only
+    if (major != 10 || minor != 3) return CODA_ERR_UNSUPPORTED;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_coda_err) != cudaSuccess) return CODA_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    d.init = true;
+  }
+  out = d;
+  return CODA_OK;
+}
+
+coda_status encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? CODA_OK : CODA_ERR_CUDA;
+}
+
+// bf16 2-D row-major tensor [outer, inner] with box [box_outer, box_inner]
+coda_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                     uint32_t box_outer, CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_CUDA;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// The op list after validation, in the form the kernels read.
+struct Compiled {
+  EpiProgram prog;
+  bool glu = false;
+  int n_aux = 0;
+  const void* aux_ptr[kMaxAux] = {nullptr, nullptr, nullptr};
+  bool has_rms = false;
+  int rms_slot = -1;
+  float rms_eps = 0.0f;
+  bool needs_row_stats = false;
+  int max_stat_slot = -1;
+};
+
+coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int64_t N, int64_t K, bool fused,
+                             Compiled& c) {
+  std::memset(&c.prog, 0, sizeof(c.prog));
+  c.prog.glu_pos = -1;
+  const uint32_t n_ops = epi ? epi->n_ops : 0u;
+  if (n_ops > CODA_MAX_OPS) return CODA_ERR_INVALID_ARG;
+  if (epi && epi->reserved != 0) return CODA_ERR_INVALID_ARG;
+  c.prog.n_ops = static_cast<int32_t>(n_ops);
+  c.prog.seed = epi ? epi->seed : 0ull;
+  static const coda_aux kNoAux = {};
+  const coda_aux& ax = aux ? *aux : kNoAux;
+
+  // pass 1: the SWIGLU position
+  for (uint32_t o = 0; o < n_ops; ++o)
+    if (epi->ops[o].opcode == CODA_OP_SWIGLU) {
+      if (c.prog.glu_pos >= 0) return CODA_ERR_INVALID_ARG;
+      c.prog.glu_pos = static_cast<int32_t>(o);
+    }
+  c.glu = c.prog.glu_pos >= 0;
+  if (c.glu && (N % 16) != 0) return CODA_ERR_INVALID_ARG;
+  const int64_t n_out = c.glu ? N / 2 : N;
+
+  int aux_index[kMaxAux] = {-1, -1, -1};
+  auto use_aux = [&](int kind, const void* ptr) -> int {
+    if (aux_index[kind] < 0) {
+      aux_index[kind] = c.n_aux;
+      c.aux_ptr[c.n_aux] = ptr;
+      ++c.n_aux;
+    }
+    return aux_index[kind];
+  };
+  bool seen_preact = false;
+  for (uint32_t o = 0; o < n_ops; ++o) {
+    const coda_op& op = epi->ops[o];
+    DevOp& d = c.prog.ops[o];
+    d.code = op.opcode;
+    d.slot = op.slot;
+    d.f0 = op.f0;
+    d.f1 = 0.0f;
+    d.u = 0;
+    d.red = -1;
+    d.aux = -1;
+    if (op.f1 != 0.0f || !std::isfinite(op.f0)) return CODA_ERR_INVALID_ARG;
+    const bool after_glu = !c.glu || static_cast<int32_t>(o) > c.prog.glu_pos;
+    switch (op.opcode) {
+      case CODA_OP_SCALE:
+      case CODA_OP_GELU_TANH:
+      case CODA_OP_SILU:
+      case CODA_OP_SWIGLU:
+        break;
+      case CODA_OP_COL_SCALE:
+      case CODA_OP_BIAS:
+        if (op.slot >= CODA_MAX_COL_VECS || ax.col_vec[op.slot] == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.col_vec[op.slot])) return CODA_ERR_ALIGNMENT;
+        c.prog.col_vec[op.slot] = static_cast<const uint16_t*>(ax.col_vec[op.slot]);
+        break;
+      case CODA_OP_ROW_SCALE:
+        if (op.slot >= CODA_MAX_ROW_VECS || ax.row_vec[op.slot] == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned4(ax.row_vec[op.slot])) return CODA_ERR_ALIGNMENT;
+        c.prog.row_vec[op.slot] = ax.row_vec[op.slot];
+        break;
+      case CODA_OP_RMS_ROWSCALE:
+        if (!fused) return CODA_ERR_UNSUPPORTED;
+        if (c.has_rms || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
+        if (op.slot != CODA_NO_SLOT) {
+          if (op.slot >= CODA_MAX_STAT_SLOTS) return CODA_ERR_INVALID_ARG;
+          c.rms_slot = static_cast<int>(op.slot);
+          c.needs_row_stats = true;
+          if (c.rms_slot > c.max_stat_slot) c.max_stat_slot = c.rms_slot;
+        }
+        c.has_rms = true;
+        c.rms_eps = op.f0;
+        break;
+      case CODA_OP_GELU_TANH_GRAD:
+        if (!after_glu || ax.z == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.z)) return CODA_ERR_ALIGNMENT;
+        d.aux = use_aux(AUX_Z, ax.z);
+        break;
+      case CODA_OP_DROPOUT: {
+        if (!after_glu || c.prog.has_dropout) return CODA_ERR_INVALID_ARG;
+        if (!(op.f0 >= 0.0f && op.f0 < 1.0f)) return CODA_ERR_INVALID_ARG;
+        c.prog.has_dropout = 1;
+        const double keep = 1.0 - static_cast<double>(op.f0);
+        // T = floor((1-p) * 2^64) in fp64; p == 0 keeps everything (flagged by f0 == 0)
+        d.u = (op.f0 == 0.0f) ? ~0ull : static_cast<uint64_t>(std::ldexp(keep, 64));
+        d.f1 = static_cast<float>(1.0 / keep);
+        break;
+      }
+      case CODA_OP_RESIDUAL:
+        if (!after_glu || ax.residual == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.residual)) return CODA_ERR_ALIGNMENT;
+        d.aux = use_aux(AUX_RESIDUAL, ax.residual);
+        break;
+      case CODA_OP_STORE_PREACT:
+        if (seen_preact || ax.preact_out == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.preact_out)) return CODA_ERR_ALIGNMENT;
+        seen_preact = true;
+        c.prog.preact = static_cast<uint16_t*>(ax.preact_out);
+        c.prog.preact_width = static_cast<int32_t>(after_glu ? n_out : N);
+        break;
+      case CODA_OP_ROW_SUM:
+      case CODA_OP_ROW_MEAN:
+      case CODA_OP_ROW_SUMSQ:
+      case CODA_OP_ROW_DOT_AUX:
+        if (!after_glu || op.slot >= CODA_MAX_STAT_SLOTS) return CODA_ERR_INVALID_ARG;
+        if (c.prog.n_red >= CODA_MAX_REDUCTIONS) return CODA_ERR_INVALID_ARG;
+        if (op.opcode == CODA_OP_ROW_DOT_AUX) {
+          if (ax.xhat == nullptr) return CODA_ERR_INVALID_ARG;
+          if (!aligned16(ax.xhat)) return CODA_ERR_ALIGNMENT;
+          d.aux = use_aux(AUX_XHAT, ax.xhat);
+        }
+        d.red = c.prog.n_red;
+        c.prog.red.slot[c.prog.n_red] = static_cast<int32_t>(op.slot);
+        c.prog.red.is_mean[c.prog.n_red] = op.opcode == CODA_OP_ROW_MEAN ? 1 : 0;
+        ++c.prog.n_red;
+        c.needs_row_stats = true;
+        if (static_cast<int>(op.slot) > c.max_stat_slot) c.max_stat_slot = static_cast<int>(op.slot);
+        break;
+      default:
+        return CODA_ERR_INVALID_ARG;
+    }
+  }
+  return CODA_OK;
+}
+
+struct Geometry {
+  int64_t n_out;
+  int out_cols;
+  int num_m_tiles, num_n_tiles, num_kb;
+  int64_t num_tiles;
+};
+
+Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu) {
+  Geometry g{};
+  g.n_out = glu ? N / 2 : N;
+  g.out_cols = glu ? BN / 2 : BN;
+  g.num_m_tiles = static_cast<int>((M + BM - 1) / BM);
+  g.num_n_tiles = static_cast<int>((g.n_out + g.out_cols - 1) / g.out_cols);
+  g.num_kb = static_cast<int>((K + BK - 1) / BK);
+  g.num_tiles = static_cast<int64_t>(g.num_m_tiles) * g.num_n_tiles;
+  return g;
+}
+
+size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
+  size_t b = static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * static_cast<size_t>(M) * sizeof(float);
+  if (c.prog.has_dropout) b += static_cast<size_t>(g.num_n_tiles) * static_cast<size_t>(M) * sizeof(uint32_t);
+  return b;
+}
+
+coda_status check_dims(int64_t M, int64_t N, int64_t K) {
+  const int64_t lim = (int64_t{1} << 31) - 1;
+  if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return CODA_ERR_INVALID_ARG;
+  if ((N % 8) != 0 || (K % 8) != 0) return CODA_ERR_INVALID_ARG;
+  return CODA_OK;
+}
+
+coda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CODA_OK : CODA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace coda
+
+using namespace coda;
+
+extern "C" {
+
+coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi, size_t* bytes) {
+  if (bytes == nullptr) return CODA_ERR_INVALID_ARG;
+  *bytes = 0;
+  coda_status s = check_dims(M, N, K);
+  if (s != CODA_OK) return s;
+  // sizes only: validate the op list without its aux tensors being present
+  Compiled c;
+  coda_aux dummy{};
+  static const uint16_t kAligned[8] __attribute__((aligned(16))) = {};
+  for (int i = 0; i < CODA_MAX_COL_VECS; ++i) dummy.col_vec[i] = kAligned;
+  for (int i = 0; i < CODA_MAX_ROW_VECS; ++i) dummy.row_vec[i] = reinterpret_cast<const float*>(kAligned);
+  dummy.residual = dummy.z = dummy.xhat = kAligned;
+  dummy.preact_out = const_cast<uint16_t*>(kAligned);
+  s = compile_epilogue(epi, &dummy, N, K, true, c);
+  if (s != CODA_OK) return s;
+  *bytes = workspace_bytes_for(M, geometry(M, N, K, c.glu), c);
+  return CODA_OK;
+}
+
+coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int32_t b_layout,
+                               const coda_epilogue* epi, const coda_aux* aux, void* D, float* row_stats,
+                               uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream) {
+  coda_status s = check_dims(M, N, K);
+  if (s != CODA_OK) return s;
+  if (b_layout != CODA_B_KN && b_layout != CODA_B_NK) return CODA_ERR_INVALID_ARG;
+  Compiled c;
+  s = compile_epilogue(epi, aux, N, K, true, c);
+  if (s != CODA_OK) return s;
+  if (M == 0 || N == 0) return CODA_OK;
+  if (D == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return CODA_ERR_ALIGNMENT;
+  if (c.needs_row_stats && row_stats == nullptr) return CODA_ERR_INVALID_ARG;
+  if (row_stats && !aligned4(row_stats)) return CODA_ERR_ALIGNMENT;
+  if (row_keep_count && !aligned4(row_keep_count)) return CODA_ERR_ALIGNMENT;
+  const Geometry g = geometry(M, N, K, c.glu);
+  if (g.num_tiles > (int64_t{1} << 31) - 1) return CODA_ERR_UNSUPPORTED;
+  const size_t ws_need = workspace_bytes_for(M, g, c);
+  if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
+  if (workspace && !aligned16(workspace)) return CODA_ERR_ALIGNMENT;
+
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  s = encoder();
+  if (s != CODA_OK) return s;
+
+  CUtensorMap maps[6];
+  std::memset(maps, 0, sizeof(maps));
+  s = make_map(&maps[2], D, static_cast<uint64_t>(g.n_out), static_cast<uint64_t>(M), kChunk, 32,
+               CU_TENSOR_MAP_SWIZZLE_64B);
+  if (s != CODA_OK) return s;
+  if (K > 0) {
+    s = make_map(&maps[0], A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), BK, BM,
+                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != CODA_OK) return s;
+    if (b_layout == CODA_B_KN)
+      s = make_map(&maps[1], B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, BK,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      s = make_map(&maps[1], B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), BK, BN / 2,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != CODA_OK) return s;
+  } else {
+    maps[0] = maps[2];
+    maps[1] = maps[2];
+  }
+  for (int k = 0; k < 3; ++k) {
+    if (k < c.n_aux) {
+      s = make_map(&maps[3 + k], c.aux_ptr[k], static_cast<uint64_t>(g.n_out), static_cast<uint64_t>(M), kChunk,
+                   32, CU_TENSOR_MAP_SWIZZLE_64B);
+      if (s != CODA_OK) return s;
+    } else {
+      maps[3 + k] = maps[2];
+    }
+  }
+
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = static_cast<int32_t>(M);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.N_out = static_cast<int32_t>(g.n_out);
+  p.half = c.glu ? static_cast<int32_t>(N / 2) : 0;
+  p.num_m_tiles = g.num_m_tiles;
+  p.num_n_tiles = g.num_n_tiles;
+  p.num_tiles = static_cast<int32_t>(g.num_tiles);
+  p.num_kb = g.num_kb;
+  p.n_aux = c.n_aux;
+  p.rms_slot = c.rms_slot;
+  p.rms_eps = c.rms_eps;
+  p.inv_K = K > 0 ? static_cast<float>(1.0 / static_cast<double>(K)) : 0.0f;
+  p.timeout_ns = g_timeout_ns.load();
+  p.row_stats = row_stats;
+  if (ws_need > 0) {
+    p.ws_red = static_cast<float*>(workspace);
+    if (c.prog.has_dropout && row_keep_count != nullptr)
+      p.ws_keep = reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) +
+                                              static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * M);
+  }
+  p.epi_warp_bytes = static_cast<uint32_t>(2 * kBoxBytes + c.n_aux * 2 * kBoxBytes);
+  const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * p.epi_warp_bytes;
+  const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
+  const size_t fixed = 1024 + epi_bytes + ctl_bytes;
+  if (static_cast<size_t>(dev.max_smem) < fixed + 2 * kStageBytes) return CODA_ERR_UNSUPPORTED;
+  int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) / kStageBytes);
+  if (stages > kMaxStages) stages = kMaxStages;
+  p.stages = stages;
+  p.smem_epi_off = static_cast<uint32_t>(stages * kStageBytes);
+  p.smem_ctl_off = static_cast<uint32_t>(stages * kStageBytes + epi_bytes);
+  p.err = dev.err;
+  p.prog = c.prog;
+  const size_t smem = fixed + static_cast<size_t>(stages) * kStageBytes;
+
+  int grid = dev.sms;
+  const int cap = g_max_ctas.load();
+  if (cap > 0 && cap < grid) grid = cap;
+  if (g.num_tiles < grid) grid = static_cast<int>(g.num_tiles);
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool mn = b_layout == CODA_B_KN;
+  cudaError_t e = c.glu ? launch_gemm_glu(mn, c.has_rms, maps, p, grid, smem, st)
+                        : launch_gemm_plain(mn, c.has_rms, maps, p, grid, smem, st);
+  if (e != cudaSuccess) return CODA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  const bool need_keep = c.prog.has_dropout && row_keep_count != nullptr;
+  if (c.prog.n_red > 0 || need_keep) {
+    e = launch_finalize(p.ws_red, p.ws_keep, p.M, g.num_n_tiles, c.prog.n_red, c.prog.red,
+                        static_cast<float>(1.0 / static_cast<double>(g.n_out)), row_stats,
+                        need_keep ? row_keep_count : nullptr, st);
+    if (e != cudaSuccess) return CODA_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
+  return CODA_OK;
+}
+
+coda_status coda_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, int32_t b_layout,
+                            void* stream) {
+  coda_status s = check_dims(0, N, K);
+  if (s != CODA_OK) return s;
+  if (b_layout != CODA_B_KN && b_layout != CODA_B_NK) return CODA_ERR_INVALID_ARG;
+  if (K == 0 || N == 0) return CODA_OK;
+  if (!W || !gamma || !W_out) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(gamma) || !aligned16(W_out)) return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e =
+      launch_fold_gamma(W, gamma, W_out, K, N, b_layout == CODA_B_KN, dev.sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps, void* Xn_out,
+                         float* rstd_out, void* stream) {
+  coda_status s = check_dims(M, 8, K);
+  if (s != CODA_OK) return s;
+  if (!std::isfinite(eps) || eps < 0.0f || K == 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  if (!X || !gamma || !Xn_out) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(gamma) || !aligned16(Xn_out) || (rstd_out && !aligned4(rstd_out)))
+    return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e = launch_rmsnorm(X, gamma, M, K, eps, Xn_out, rstd_out, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_epilogue_apply(const void* C, int64_t M, int64_t N, const coda_epilogue* epi, const coda_aux* aux,
+                                void* D, float* row_stats, uint32_t* row_keep_count, void* stream) {
+  coda_status s = check_dims(M, N, 8);
+  if (s != CODA_OK) return s;
+  Compiled c;
+  s = compile_epilogue(epi, aux, N, 8, false, c);
+  if (s != CODA_OK) return s;
+  if (M == 0 || N == 0) return CODA_OK;
+  if (!C || !D) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(C) || !aligned16(D)) return CODA_ERR_ALIGNMENT;
+  if (c.needs_row_stats && row_stats == nullptr) return CODA_ERR_INVALID_ARG;
+  if ((row_stats && !aligned4(row_stats)) || (row_keep_count && !aligned4(row_keep_count)))
+    return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const int64_t n_out = c.glu ? N / 2 : N;
+  const cudaError_t e = launch_epilogue_apply(C, D, M, static_cast<int>(N), static_cast<int>(n_out),
+                                              c.glu ? static_cast<int>(N / 2) : 0, c.aux_ptr, row_stats,
+                                              c.prog.has_dropout ? row_keep_count : nullptr, c.prog,
+                                              static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_check_device_error(void* stream, uint32_t* info) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CODA_ERR_CUDA;
+  DevInfo dev;
+  coda_status s = device_info(dev);
+  if (s != CODA_OK) return s;
+  uint32_t h[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, dev.err, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return CODA_ERR_CUDA;
+  if (info) std::memcpy(info, h, sizeof(h));
+  if (h[0] == 0) return CODA_OK;
+  const uint32_t z[4] = {0, 0, 0, 0};
+  if (cudaMemcpy(dev.err, z, sizeof(z), cudaMemcpyHostToDevice) != cudaSuccess) return CODA_ERR_CUDA;
+  return static_cast<coda_status>(h[0]);
+}
+
+const char* coda_status_string(coda_status status) {
+  switch (status) {
+    case CODA_OK: return "CODA_OK";
+    case CODA_ERR_INVALID_ARG: return "CODA_ERR_INVALID_ARG";
+    case CODA_ERR_UNSUPPORTED: return "CODA_ERR_UNSUPPORTED";
+    case CODA_ERR_ALIGNMENT: return "CODA_ERR_ALIGNMENT";
+    case CODA_ERR_CUDA: return "CODA_ERR_CUDA";
+    case CODA_ERR_TIMEOUT: return "CODA_ERR_TIMEOUT";
+    case CODA_ERR_WORKSPACE: return "CODA_ERR_WORKSPACE";
+    default: return "CODA_ERR_UNKNOWN";
+  }
+}
+
+uint64_t coda_launch_count(void) { return g_launches.load(); }
+
+void coda_set_pipeline_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1000000000ull : ns); }
+
+void coda_set_max_ctas(int32_t n) { g_max_ctas.store(n < 0 ? 0 : n); }
+
+}  // extern "C"

@@ -1,0 +1,429 @@
+// The fused GEMM + on-chip epilogue kernel for sm_103a.
+//
+// CODA article (d9bl.com, §3.1 and Fig. 1): the GEMM produces the output tile
+// and the epilogue f is applied to it before the single global write of D.
+// agentlenshq.com ("仕組み"): the GEMM mainloop is fixed, the epilogue is built
+// from composable primitives.  zeli.app (augment_me): the RMSNorm row scale is
+// gathered as per-row partial sums over the K tiles and applied after the
+// projection.
+//
+// GB300 design: one persistent CTA per SM, warp-specialised:
+//   warp 0      TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles into a
+//               ring of 128-byte-swizzled shared-memory stages
+//   warp 1      MMA issuer: tcgen05.mma (M=128, N=256, K=16) into one of two
+//               fp32 accumulators in tensor memory (2 x 256 columns)
+//   warp 2      allocates / frees the 512 tensor-memory columns
+//   warps 4-7   epilogue: tcgen05.ld drains the accumulator one 32-column chunk
+//               at a time (thread = row), runs the op list, packs bf16 (RNE)
+//               into swizzled staging and TMA-stores it; aux tiles (residual,
+//               Z, Xhat) arrive by TMA one chunk ahead.  While they work on
+//               tile i, the MMA warp already fills the other accumulator.
+//   warps 8-11  (commuted RMSNorm only) read every A stage from shared memory
+//               and accumulate sum_k x^2 for their row, then r = rsqrt(s/K+eps)
+// Every mbarrier wait is bounded: on expiry the kernel records a timeout in the
+// device error word, lets in-flight copies land, frees tensor memory and exits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "coda_internal.h"
+#include "coda_ops.cuh"
+#include "coda_ptx.cuh"
+
+namespace coda {
+
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t role, uint32_t tile) {
+  if (atomicCAS(err, 0u, static_cast<uint32_t>(CODA_ERR_TIMEOUT)) == 0u) {
+    err[1] = blockIdx.x;
+    err[2] = role;
+    err[3] = tile;
+  }
+}
+
+static __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
+                                       uint64_t timeout_ns, uint32_t* err, uint32_t role, uint32_t tile) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((it & 15u) == 0u && globaltimer_ns() - t0 > timeout_ns) {
+      record_error(err, role, tile);
+      *abort_flag = 1u;
+      return false;
+    }
+  }
+}
+
+// bounded wait used only on the abort path; ignores the abort flag
+static __device__ __noinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+struct Waiter {
+  Ctl* ctl;
+  uint64_t timeout;
+  uint32_t* err;
+  uint32_t role;
+  __device__ __forceinline__ bool operator()(uint64_t* bar, uint32_t parity, uint32_t tile) const {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, &ctl->abort_flag, timeout, err, role, tile);
+  }
+};
+
+// Aux values of one 32-row x 32-column box staged with the 64-byte swizzle:
+// 16-byte chunk c of row r sits at r*64 + ((c ^ ((r >> 1) & 3)) * 16).
+struct SmemAux {
+  const uint8_t* base;   // staging buffer of aux tensor 0 for the current chunk
+  int r;                 // row inside the box (the lane)
+  __device__ __forceinline__ void load(int k, float (&out)[32]) const {
+    const uint8_t* rowp = base + k * (2 * kBoxBytes) + r * 64;
+    const int sw = (r >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 q = *reinterpret_cast<const uint4*>(rowp + ((c ^ sw) << 4));
+      unpack8(q, out + 8 * c);
+    }
+  }
+};
+
+template <bool kGLU, bool kBMN, bool kRowStats>
+__global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
+    coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                              const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
+                              const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
+                              const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + p.smem_ctl_off);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + p.stages * kStageABytes;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1 + (kRowStats ? 128 : 0));
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&ctl->tfull[a], 1);
+      mbar_init(&ctl->tempty[a], 128);
+      mbar_init(&ctl->rsfull[a], 128);
+      mbar_init(&ctl->rsempty[a], 128);
+    }
+    for (int q = 0; q < kEpiWarps; ++q)
+      for (int b = 0; b < 2; ++b) mbar_init(&ctl->auxfull[q][b], 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort_flag = 0u;
+    fence_mbar_init();
+    if (p.num_kb > 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+    tma_prefetch_desc(&tmD);
+  }
+  if (warp == 2) {
+    tmem_alloc(&ctl->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && p.num_kb > 0) {
+      const Waiter W{ctl, p.timeout_ns, p.err, ROLE_PRODUCER};
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const int m_tile = tile % p.num_m_tiles;
+        const int n_tile = tile / p.num_m_tiles;
+        const int m0 = m_tile * BM;
+        const int nb0 = kGLU ? n_tile * (BN / 2) : n_tile * BN;
+        const int nb1 = kGLU ? p.half + n_tile * (BN / 2) : nb0 + BN / 2;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!W(&ctl->empty[stage], phase ^ 1u, tile)) {
+            ok = false;
+            break;
+          }
+          uint64_t* fb = &ctl->full[stage];
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          armed |= 1u << stage;
+          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          const int k0 = kb * BK;
+          uint8_t* a_dst = sA + stage * kStageABytes;
+          uint8_t* b_dst = sB + stage * kStageBBytes;
+          tma_load_2d(a_dst, &tmA, fb, k0, m0);
+          if (kBMN) {
+            tma_load_2d(b_dst, &tmB, fb, nb0, k0);
+            tma_load_2d(b_dst + 8192, &tmB, fb, nb0 + 64, k0);
+            tma_load_2d(b_dst + 16384, &tmB, fb, nb1, k0);
+            tma_load_2d(b_dst + 24576, &tmB, fb, nb1 + 64, k0);
+          } else {
+            tma_load_2d(b_dst, &tmB, fb, k0, nb0);
+            tma_load_2d(b_dst + 16384, &tmB, fb, k0, nb1);
+          }
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < p.stages; ++s)
+          if (armed & (1u << s)) wait_drain(&ctl->full[s], (armed_phase >> s) & 1u, 2000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
+      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, kBMN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!W(&ctl->tempty[acc], acc_phase ^ 1u, tile)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + acc * kAccCols;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!W(&ctl->full[stage], phase, tile)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kStageBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k) {
+            const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
+                                     : make_smem_desc(b_addr + k * 32, 16, 1024);
+            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl->empty[stage]);
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&ctl->tfull[acc]);
+      }
+      // no MMA may still write tensor memory when it is freed
+      mma_commit(&ctl->drain);
+      wait_drain(&ctl->drain, 0u, 2000000ull);
+    }
+  } else if (warp >= 4 && warp < 4 + kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp - 4;
+    const Waiter W{ctl, p.timeout_ns, p.err, ROLE_EPILOGUE};
+    constexpr int kOutCols = kGLU ? BN / 2 : BN;
+    uint8_t* wbase = smem + p.smem_epi_off + q * p.epi_warp_bytes;
+    uint8_t* out_stage = wbase;
+    uint8_t* aux_stage = wbase + 2 * kBoxBytes;
+    const int n_aux = p.n_aux;
+    const int r_in_tile = q * 32 + lane;
+    uint32_t aux_phase = 0;   // bit b: parity of the next completion of buffer b
+    uint32_t aux_armed = 0;   // bit b: buffer b has a load that was not waited for
+    int abuf = 0;
+    int sbuf = 0;
+    int local = 0;
+    bool ok = true;
+
+    auto issue_aux = [&](int b, int col, int row0) {
+      __syncwarp();
+      if (lane == 0) {
+        uint64_t* bar = &ctl->auxfull[q][b];
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_aux * kBoxBytes));
+        tma_load_2d(aux_stage + (0 * 2 + b) * kBoxBytes, &tmX0, bar, col, row0);
+        if (n_aux > 1) tma_load_2d(aux_stage + (1 * 2 + b) * kBoxBytes, &tmX1, bar, col, row0);
+        if (n_aux > 2) tma_load_2d(aux_stage + (2 * 2 + b) * kBoxBytes, &tmX2, bar, col, row0);
+      }
+      aux_armed |= 1u << b;
+    };
+
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+      const int m_tile = tile % p.num_m_tiles;
+      const int n_tile = tile / p.num_m_tiles;
+      const int m0 = m_tile * BM;
+      const int row = m0 + r_in_tile;
+      const bool row_ok = row < p.M;
+      const int col_base = n_tile * kOutCols;
+      int nch = (p.N_out - col_base + kChunk - 1) / kChunk;
+      if (nch > kOutCols / kChunk) nch = kOutCols / kChunk;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      if (n_aux > 0) issue_aux(abuf, col_base, m0 + q * 32);
+
+      bool okw = W(&ctl->tfull[acc], acc_phase, tile);
+      if (!__all_sync(0xFFFFFFFFu, okw)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      float r_rms = 1.0f;
+      if (kRowStats) {
+        okw = W(&ctl->rsfull[acc], acc_phase, tile);
+        if (!__all_sync(0xFFFFFFFFu, okw)) {
+          ok = false;
+          break;
+        }
+        r_rms = ctl->rs[acc][r_in_tile];
+        mbar_arrive(&ctl->rsempty[acc]);
+      }
+
+      float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+      uint32_t keep = 0;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      for (int c = 0; c < nch; ++c) {
+        const int col = col_base + c * kChunk;
+        if (n_aux > 0) {
+          if (c + 1 < nch) issue_aux(abuf ^ 1, col + kChunk, m0 + q * 32);
+          okw = W(&ctl->auxfull[q][abuf], (aux_phase >> abuf) & 1u, tile);
+          if (!__all_sync(0xFFFFFFFFu, okw)) {
+            ok = false;
+            break;
+          }
+          aux_phase ^= 1u << abuf;
+          aux_armed &= ~(1u << abuf);
+        }
+        float v[32], u[32];
+        if (p.num_kb > 0) {
+          tmem_ld32(t_row + c * kChunk, v);
+          if (kGLU) tmem_ld32(t_row + BN / 2 + c * kChunk, u);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = 0.0f;
+            u[j] = 0.0f;
+          }
+        }
+        if (c == nch - 1) {
+          tc_fence_before_sync();
+          mbar_arrive(&ctl->tempty[acc]);
+        }
+        int nvalid = p.N_out - col;
+        if (nvalid > kChunk) nvalid = kChunk;
+        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms};
+        const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
+        run_ops<32, kGLU>(p.prog, v, u, rc, ax, red, keep);
+
+        // stage bf16 row chunk (64-byte swizzle) and TMA-store the 32x32 box
+        uint8_t* ob = out_stage + sbuf * kBoxBytes;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        {
+          uint8_t* rowp = ob + lane * 64;
+          const int sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = pack8(v + 8 * cc);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmD, ob, col, m0 + q * 32);
+          bulk_commit_group();
+        }
+        sbuf ^= 1;
+        if (n_aux > 0) abuf ^= 1;
+      }
+      if (!ok) break;
+      if (row_ok) {
+        const size_t Ms = static_cast<size_t>(p.M);
+#pragma unroll
+        for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
+          if (r < p.prog.n_red)
+            p.ws_red[(static_cast<size_t>(r) * p.num_n_tiles + n_tile) * Ms + row] = red[r];
+        if (p.ws_keep != nullptr) p.ws_keep[static_cast<size_t>(n_tile) * Ms + row] = keep;
+        if (kRowStats && p.rms_slot >= 0 && n_tile == 0)
+          p.row_stats[static_cast<size_t>(p.rms_slot) * Ms + row] = r_rms;
+      }
+    }
+    if (lane == 0) {
+      bulk_wait_group<0>();
+      if (!ok) {
+        for (int b = 0; b < 2; ++b)
+          if (aux_armed & (1u << b)) wait_drain(&ctl->auxfull[q][b], (aux_phase >> b) & 1u, 2000000ull);
+      }
+    }
+    __syncwarp();
+  } else if (kRowStats && warp >= 8) {
+    // ------------------------------------ row statistics (commuted RMSNorm)
+    const int q = warp - 8;
+    const int r = q * 32 + lane;
+    const Waiter W{ctl, p.timeout_ns, p.err, ROLE_ROWSTATS};
+    int stage = 0;
+    uint32_t phase = 0;
+    int local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+      float s = 0.0f;
+      for (int kb = 0; kb < p.num_kb; ++kb) {
+        const bool okw = W(&ctl->full[stage], phase, tile);
+        if (!__all_sync(0xFFFFFFFFu, okw)) {
+          ok = false;
+          break;
+        }
+        // row r of the 128B-swizzled A stage: its eight 16-byte chunks in an
+        // order that spreads the warp over all banks (the sum ignores order)
+        const uint8_t* arow = sA + stage * kStageABytes + r * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 w = *reinterpret_cast<const uint4*>(arow + ((j ^ (r & 7)) << 4));
+          float x[8];
+          unpack8(w, x);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = fmaf(x[e], x[e], s);
+        }
+        mbar_arrive(&ctl->empty[stage]);
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const bool okw = W(&ctl->rsempty[acc], acc_phase ^ 1u, tile);
+      if (!__all_sync(0xFFFFFFFFu, okw)) break;
+      ctl->rs[acc][r] = rsqrtf(fmaf(s, p.inv_K, p.rms_eps));
+      mbar_arrive(&ctl->rsfull[acc]);
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool kGLU, bool kBMN, bool kRowStats>
+cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

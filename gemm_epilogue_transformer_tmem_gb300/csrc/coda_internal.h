@@ -1,0 +1,104 @@
+// Internal definitions shared by the host API and the kernels of the CODA
+// GEMM+epilogue library (not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/coda.h"
+
+namespace coda {
+
+// Tile shape of the fused kernel: one 128-row x 256-column fp32 accumulator per
+// tcgen05 MMA chain (M=128, N=256, K=16 instructions), K staged 64 bf16 at a time
+// (one 128-byte swizzle atom per row).
+constexpr int BM = 128;
+constexpr int BN = 256;            // MMA N: columns of B per tile (G|U halves for SwiGLU)
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int kAccCols = 256;      // TMEM columns per accumulator buffer
+constexpr int kTmemCols = 512;     // two accumulator buffers
+constexpr int kEpiWarps = 4;
+constexpr int kChunk = 32;         // epilogue columns per TMEM load / TMA store box
+constexpr int kStageABytes = BM * BK * 2;          // 16 KB
+constexpr int kStageBBytes = BN * BK * 2;          // 32 KB
+constexpr int kStageBytes = kStageABytes + kStageBBytes;
+constexpr int kBoxBytes = 32 * kChunk * 2;         // 32 rows x 32 bf16 = 2 KB
+constexpr int kMaxStages = 8;
+constexpr int kMaxAux = 3;                         // residual, z, xhat
+
+// aux tensor kinds (index into the aux tensor-map array)
+enum AuxKind : int { AUX_RESIDUAL = 0, AUX_Z = 1, AUX_XHAT = 2 };
+
+// One compiled epilogue op.  `red` is the reduction register (0..3) for the
+// reduction ops; `u` carries the dropout threshold; f1 the dropout scale.
+struct DevOp {
+  uint32_t code;
+  uint32_t slot;
+  float f0;
+  float f1;
+  uint64_t u;
+  int32_t red;
+  int32_t aux;      // staging index of the aux tensor this op reads, or -1
+};
+
+struct RedInfo {
+  int32_t slot[CODA_MAX_REDUCTIONS];
+  int32_t is_mean[CODA_MAX_REDUCTIONS];
+};
+
+struct EpiProgram {
+  int32_t n_ops;
+  int32_t glu_pos;         // index of the SWIGLU op, -1 if none
+  int32_t n_red;
+  int32_t has_dropout;
+  uint64_t seed;
+  DevOp ops[CODA_MAX_OPS];
+  RedInfo red;
+  const uint16_t* col_vec[CODA_MAX_COL_VECS];
+  const float* row_vec[CODA_MAX_ROW_VECS];
+  uint16_t* preact;
+  int32_t preact_width;
+  int32_t pad;
+};
+
+struct GemmParams {
+  int32_t M, N, K;
+  int32_t N_out;           // output width (N/2 with SWIGLU)
+  int32_t half;            // N/2 with SWIGLU, else 0
+  int32_t num_m_tiles, num_n_tiles, num_tiles, num_kb, stages;
+  int32_t n_aux;           // aux tensors staged by TMA
+  int32_t rms_slot;        // row-stat slot for r_i, -1 if none
+  float rms_eps;
+  float inv_K;
+  uint64_t timeout_ns;
+  float* row_stats;
+  float* ws_red;           // [n_red][num_n_tiles][M]
+  uint32_t* ws_keep;       // [num_n_tiles][M]
+  uint32_t smem_epi_off;   // offset of the epilogue staging region
+  uint32_t smem_ctl_off;   // offset of the control block
+  uint32_t epi_warp_bytes; // staging bytes per epilogue warp
+  uint32_t* err;           // device error word (4 x u32)
+  EpiProgram prog;
+};
+
+// Shared-memory control block of the fused kernel (mbarriers, tensor-memory
+// base address, abort flag, commuted-RMSNorm row scales for both accumulators).
+struct Ctl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t rsfull[2];
+  uint64_t rsempty[2];
+  uint64_t auxfull[kEpiWarps][2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+  float rs[2][BM];
+};
+
+// device error word layout: [0] code, [1] block, [2] role, [3] tile
+enum ErrRole : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_ROWSTATS = 4 };
+
+}  // namespace coda

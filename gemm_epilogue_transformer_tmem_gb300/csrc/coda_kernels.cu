@@ -1,0 +1,220 @@
+// Small kernels around the fused GEMM: the deterministic finish of the
+// cross-tile row reductions, the gamma fold of the commuted RMSNorm, and the
+// unfused memory-bound kernels (RMSNorm, epilogue applied to a stored C) that
+// the fused kernel replaces.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "coda_internal.h"
+#include "coda_launch.h"
+#include "coda_ops.cuh"
+
+namespace coda {
+
+// ---------------------------------------------------------------- finalize
+// row_stats[slot][i] = sum over column tiles of the partials, in tile order
+// (deterministic), divided by the row width for ROW_MEAN; keep counts likewise.
+__global__ void finalize_rows_kernel(const float* __restrict__ ws_red, const uint32_t* __restrict__ ws_keep,
+                                     int M, int num_n_tiles, int n_red, RedInfo info, float inv_width,
+                                     float* __restrict__ row_stats, uint32_t* __restrict__ keep_count) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= M) return;
+  const size_t Ms = static_cast<size_t>(M);
+  for (int r = 0; r < n_red; ++r) {
+    float s = 0.0f;
+    const float* src = ws_red + static_cast<size_t>(r) * num_n_tiles * Ms + row;
+    for (int t = 0; t < num_n_tiles; ++t) s += src[static_cast<size_t>(t) * Ms];
+    if (info.is_mean[r]) s *= inv_width;
+    row_stats[static_cast<size_t>(info.slot[r]) * Ms + row] = s;
+  }
+  if (keep_count != nullptr) {
+    uint32_t k = 0;
+    for (int t = 0; t < num_n_tiles; ++t) k += ws_keep[static_cast<size_t>(t) * Ms + row];
+    keep_count[row] = k;
+  }
+}
+
+cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
+                            const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
+                            cudaStream_t st) {
+  const int threads = 256;
+  const int blocks = (M + threads - 1) / threads;
+  finalize_rows_kernel<<<blocks, threads, 0, st>>>(ws_red, ws_keep, M, num_n_tiles, n_red, info, inv_width,
+                                                   row_stats, keep_count);
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------- gamma fold
+// W_out[k,n] = bf16(gamma[k] * W[k,n]) ([K,N] layout) or W_out[n,k] = bf16(gamma[k]
+// * W[n,k]) ([N,K] layout); 8 elements (16 bytes) per thread, grid-stride.
+template <bool kKN>
+__global__ void fold_gamma_kernel(const uint16_t* __restrict__ W, const uint16_t* __restrict__ gamma,
+                                  uint16_t* __restrict__ W_out, int64_t K, int64_t N) {
+  const int64_t total8 = (K * N) >> 3;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t e = i << 3;
+    const uint4 q = __ldg(reinterpret_cast<const uint4*>(W) + i);
+    float w[8], o[8];
+    unpack8(q, w);
+    if (kKN) {
+      const int64_t k = e / N;   // N % 8 == 0: the 8 elements share a row k
+      const float g = __uint_as_float(static_cast<uint32_t>(__ldg(gamma + k)) << 16);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = w[j] * g;
+    } else {
+      const int64_t k0 = e % K;  // K % 8 == 0: columns k0 .. k0+7 of one row n
+      float g[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + k0)), g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] = w[j] * g[j];
+    }
+    reinterpret_cast<uint4*>(W_out)[i] = pack8(o);
+  }
+}
+
+cudaError_t launch_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, bool kn,
+                              int num_sms, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t total8 = (K * N) >> 3;
+  int64_t blocks = (total8 + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (kn)
+    fold_gamma_kernel<true><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(gamma), static_cast<uint16_t*>(W_out), K, N);
+  else
+    fold_gamma_kernel<false><<<static_cast<int>(blocks), threads, 0, st>>>(
+        static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(gamma), static_cast<uint16_t*>(W_out), K, N);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- unfused RMSNorm
+// One warp per row: sum of squares in fp32, r = rsqrt(ss/K + eps), then
+// Xn = bf16(r * x * gamma).  K % 8 == 0.
+__global__ void rmsnorm_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ gamma, int64_t M,
+                               int64_t K, float eps, uint16_t* __restrict__ Xn, float* __restrict__ rstd) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + row * K);
+  const int64_t n8 = K >> 3;
+  float ss = 0.0f;
+  for (int64_t i = lane; i < n8; i += 32) {
+    float x[8];
+    unpack8(__ldg(xr + i), x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const float r = rsqrtf(ss / static_cast<float>(K) + eps);
+  if (lane == 0 && rstd != nullptr) rstd[row] = r;
+  uint4* yr = reinterpret_cast<uint4*>(Xn + row * K);
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  for (int64_t i = lane; i < n8; i += 32) {
+    float x[8], g[8], y[8];
+    unpack8(__ldg(xr + i), x);
+    unpack8(__ldg(gr + i), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = r * x[j] * g[j];
+    yr[i] = pack8(y);
+  }
+}
+
+cudaError_t launch_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps, void* Xn,
+                           float* rstd, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t blocks = (M + 7) / 8;
+  rmsnorm_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint16_t*>(X), static_cast<const uint16_t*>(gamma), M, K, eps, static_cast<uint16_t*>(Xn),
+      rstd);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------- unfused epilogue application
+// Aux values for 8 consecutive columns straight from global memory.
+struct GmemAux {
+  const uint16_t* const* ptr;   // aux tensors by staging index
+  size_t off;                   // element offset of (row, col)
+  __device__ __forceinline__ void load(int k, float (&out)[8]) const {
+    unpack8(__ldg(reinterpret_cast<const uint4*>(ptr[k] + off)), out);
+  }
+};
+
+struct ApplyParams {
+  int64_t M;
+  int32_t N;       // input width
+  int32_t N_out;   // output width
+  int32_t half;    // SwiGLU: U offset in the input
+  const uint16_t* aux[kMaxAux];
+  float* row_stats;
+  uint32_t* keep_count;
+  EpiProgram prog;
+};
+
+// One warp per row; each lane handles 8 consecutive columns per step (16-byte
+// loads and stores), row reductions finished by warp shuffles.
+template <bool kGLU>
+__global__ void epilogue_apply_kernel(const uint16_t* __restrict__ C, uint16_t* __restrict__ D,
+                                      const __grid_constant__ ApplyParams ap) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= ap.M) return;
+  float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+  uint32_t keep = 0;
+  const uint16_t* crow = C + row * ap.N;
+  uint16_t* drow = D + row * ap.N_out;
+  for (int col = lane * 8; col < ap.N_out; col += 256) {
+    float v[8], u[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(crow + col)), v);
+    if (kGLU) unpack8(__ldg(reinterpret_cast<const uint4*>(crow + ap.half + col)), u);
+    const RowCtx rc{static_cast<int>(row), true, col, 8, ap.half, ap.N_out, static_cast<int>(ap.M), 1.0f};
+    const GmemAux ax{ap.aux, static_cast<size_t>(row) * ap.N_out + col};
+    run_ops<8, kGLU>(ap.prog, v, u, rc, ax, red, keep);
+    *reinterpret_cast<uint4*>(drow + col) = pack8(v);
+  }
+  for (int r = 0; r < ap.prog.n_red; ++r) {
+    float s = red[0];
+    if (r == 1) s = red[1];
+    if (r == 2) s = red[2];
+    if (r == 3) s = red[3];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    if (lane == 0) {
+      if (ap.prog.red.is_mean[r]) s /= static_cast<float>(ap.N_out);
+      ap.row_stats[static_cast<size_t>(ap.prog.red.slot[r]) * ap.M + row] = s;
+    }
+  }
+  if (ap.keep_count != nullptr) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) keep += __shfl_xor_sync(0xFFFFFFFFu, keep, o);
+    if (lane == 0) ap.keep_count[row] = keep;
+  }
+}
+
+cudaError_t launch_epilogue_apply(const void* C, void* D, int64_t M, int N, int N_out, int half,
+                                  const void* const* aux, float* row_stats, uint32_t* keep_count,
+                                  const EpiProgram& prog, cudaStream_t st) {
+  ApplyParams ap{};
+  ap.M = M;
+  ap.N = N;
+  ap.N_out = N_out;
+  ap.half = half;
+  for (int k = 0; k < kMaxAux; ++k) ap.aux[k] = static_cast<const uint16_t*>(aux[k]);
+  ap.row_stats = row_stats;
+  ap.keep_count = keep_count;
+  ap.prog = prog;
+  const int threads = 256;
+  const int64_t blocks = (M + 7) / 8;
+  if (prog.glu_pos >= 0)
+    epilogue_apply_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+        static_cast<const uint16_t*>(C), static_cast<uint16_t*>(D), ap);
+  else
+    epilogue_apply_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+        static_cast<const uint16_t*>(C), static_cast<uint16_t*>(D), ap);
+  return cudaGetLastError();
+}
+
+}  // namespace coda

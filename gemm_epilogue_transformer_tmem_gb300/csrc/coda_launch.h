@@ -1,0 +1,28 @@
+// Host-side launchers of the library's kernels (internal).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "coda_internal.h"
+
+namespace coda {
+
+// fused GEMM + epilogue; maps = {A, B, D, aux0, aux1, aux2}
+cudaError_t launch_gemm_glu(bool b_mn_major, bool row_stats, const CUtensorMap* maps, const GemmParams& p,
+                            int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_plain(bool b_mn_major, bool row_stats, const CUtensorMap* maps, const GemmParams& p,
+                              int grid, size_t smem, cudaStream_t st);
+
+cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
+                            const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
+                            cudaStream_t st);
+cudaError_t launch_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, bool kn,
+                              int num_sms, cudaStream_t st);
+cudaError_t launch_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps, void* Xn,
+                           float* rstd, cudaStream_t st);
+cudaError_t launch_epilogue_apply(const void* C, void* D, int64_t M, int N, int N_out, int half,
+                                  const void* const* aux, float* row_stats, uint32_t* keep_count,
+                                  const EpiProgram& prog, cudaStream_t st);
+
+}  // namespace coda

@@ -1,0 +1,269 @@
+// Device-side epilogue op interpreter.
+//
+// The CODA article (d9bl.com, §3.1) applies an epilogue f elementwise or row by
+// row to the GEMM output tile before it is written; agentlenshq.com ("仕組み")
+// builds f from scaling, reduction, elementwise-transform and accumulation
+// primitives.  Here f is an op list run in order on NE consecutive fp32 values
+// of one output row held in registers.  With SwiGLU the thread also holds the U
+// values paired with its G values; ops before the SWIGLU op act on both.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "coda_internal.h"
+
+namespace coda {
+
+constexpr float kSqrt2OverPi = 0.7978845608028654f;
+constexpr float kGeluC = 0.044715f;
+constexpr uint64_t kSplitmixGamma = 0x9E3779B97F4A7C15ull;
+
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float inner = kSqrt2OverPi * fmaf(kGeluC * x * x, x, x);
+  return 0.5f * x * (1.0f + tanhf(inner));
+}
+
+// derivative of gelu_tanh_f: product rule on 0.5 x (1 + tanh(u(x)))
+__device__ __forceinline__ float gelu_tanh_grad_f(float z) {
+  const float z2 = z * z;
+  const float t = tanhf(kSqrt2OverPi * fmaf(kGeluC * z2, z, z));
+  const float du = kSqrt2OverPi * fmaf(3.0f * kGeluC, z2, 1.0f);
+  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * du;
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
+
+// splitmix64 output function (Steele, Lea & Flood, OOPSLA 2014)
+__device__ __forceinline__ uint64_t splitmix_mix(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 q, float* out) {
+  out[0] = bf16_lo(q.x); out[1] = bf16_hi(q.x);
+  out[2] = bf16_lo(q.y); out[3] = bf16_hi(q.y);
+  out[4] = bf16_lo(q.z); out[5] = bf16_hi(q.z);
+  out[6] = bf16_lo(q.w); out[7] = bf16_hi(q.w);
+}
+
+// round-to-nearest-even pack of two floats into a bf16x2 word
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* v) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  return q;
+}
+
+// NE values of a bf16 vector starting at `col`; entries at or past `width` read 0.
+template <int NE>
+__device__ __forceinline__ void load_colvec(const uint16_t* vec, int col, int width, float (&out)[NE]) {
+  if (col + NE <= width) {
+#pragma unroll
+    for (int i = 0; i < NE / 8; ++i) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(vec + col) + i);
+      unpack8(q, out + 8 * i);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NE; ++j)
+      out[j] = (col + j < width) ? __uint_as_float(static_cast<uint32_t>(__ldg(vec + col + j)) << 16) : 0.0f;
+  }
+}
+
+template <int NE>
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, int col, int width, const float (&v)[NE]) {
+  if (col + NE <= width) {
+#pragma unroll
+    for (int i = 0; i < NE / 8; ++i) reinterpret_cast<uint4*>(dst + col)[i] = pack8(v + 8 * i);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NE; ++j)
+      if (col + j < width) {
+        const __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+        dst[col + j] = *reinterpret_cast<const uint16_t*>(&h);
+      }
+  }
+}
+
+__device__ __forceinline__ void add_red(float (&red)[CODA_MAX_REDUCTIONS], int idx, float s) {
+  if (idx == 0) red[0] += s;
+  else if (idx == 1) red[1] += s;
+  else if (idx == 2) red[2] += s;
+  else red[3] += s;
+}
+
+// Where the row values of one output row live for this run of NE columns.
+struct RowCtx {
+  int row;          // absolute output row
+  bool row_ok;      // row < M
+  int col;          // first output column of the run
+  int nvalid;       // columns of the run that are < N_out (0..NE)
+  int half;         // SwiGLU: column offset of U in the GEMM output (N/2)
+  int n_out;        // output width
+  int M;
+  float r_rms;      // commuted-RMSNorm row scale of this row
+};
+
+// Run the op list on v (and, before SWIGLU, on u).  `aux.load(k, out)` fills
+// NE values of aux tensor k for this run.
+template <int NE, bool kGLU, class Aux>
+__device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], float (&u)[NE], const RowCtx& c,
+                                        const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS], uint32_t& keep_cnt) {
+  const int n_ops = P.n_ops;
+  for (int o = 0; o < n_ops; ++o) {
+    const DevOp op = P.ops[o];
+    const bool pre = kGLU && (o < P.glu_pos);
+    switch (op.code) {
+      case CODA_OP_SCALE: {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] *= op.f0;
+        if (pre) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] *= op.f0;
+        }
+        break;
+      }
+      case CODA_OP_COL_SCALE:
+      case CODA_OP_BIAS: {
+        const uint16_t* vec = P.col_vec[op.slot];
+        float cv[NE];
+        load_colvec<NE>(vec, c.col, c.n_out, cv);
+        const bool is_bias = op.code == CODA_OP_BIAS;
+        if (is_bias) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) v[j] += cv[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) v[j] *= cv[j];
+        }
+        if (pre) {
+          load_colvec<NE>(vec + c.half, c.col, c.n_out, cv);
+          if (is_bias) {
+#pragma unroll
+            for (int j = 0; j < NE; ++j) u[j] += cv[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < NE; ++j) u[j] *= cv[j];
+          }
+        }
+        break;
+      }
+      case CODA_OP_ROW_SCALE:
+      case CODA_OP_RMS_ROWSCALE: {
+        const float s = (op.code == CODA_OP_RMS_ROWSCALE) ? c.r_rms
+                        : (c.row_ok ? __ldg(P.row_vec[op.slot] + c.row) : 0.0f);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] *= s;
+        if (pre) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] *= s;
+        }
+        break;
+      }
+      case CODA_OP_GELU_TANH: {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = gelu_tanh_f(v[j]);
+        if (pre) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] = gelu_tanh_f(u[j]);
+        }
+        break;
+      }
+      case CODA_OP_SILU: {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]);
+        if (pre) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] = silu_f(u[j]);
+        }
+        break;
+      }
+      case CODA_OP_SWIGLU: {
+        if (kGLU) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]) * u[j];
+        }
+        break;
+      }
+      case CODA_OP_GELU_TANH_GRAD: {
+        float z[NE];
+        aux.load(op.aux, z);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] *= gelu_tanh_grad_f(z[j]);
+        break;
+      }
+      case CODA_OP_DROPOUT: {
+        // element (row, col + j) is output n = row*N_out + col + j of the stream
+        const uint64_t n0 = static_cast<uint64_t>(c.row) * static_cast<uint64_t>(c.n_out) +
+                            static_cast<uint64_t>(c.col);
+        uint64_t state = P.seed + (n0 + 1ull) * kSplitmixGamma;
+        const bool keep_all = op.f0 == 0.0f;
+        uint32_t kc = 0;
+#pragma unroll
+        for (int j = 0; j < NE; ++j) {
+          const bool keep = keep_all || (splitmix_mix(state) < op.u);
+          state += kSplitmixGamma;
+          v[j] = keep ? v[j] * op.f1 : 0.0f;
+          kc += (keep && j < c.nvalid) ? 1u : 0u;
+        }
+        keep_cnt += kc;
+        break;
+      }
+      case CODA_OP_RESIDUAL: {
+        float r[NE];
+        aux.load(op.aux, r);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = fmaf(op.f0, r[j], v[j]);
+        break;
+      }
+      case CODA_OP_STORE_PREACT: {
+        if (c.row_ok) {
+          uint16_t* base = P.preact + static_cast<size_t>(c.row) * static_cast<size_t>(P.preact_width);
+          store_row_bf16<NE>(base, c.col, c.n_out, v);
+          if (pre) store_row_bf16<NE>(base + c.half, c.col, c.n_out, u);
+        }
+        break;
+      }
+      case CODA_OP_ROW_SUM:
+      case CODA_OP_ROW_MEAN: {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] : 0.0f;
+        add_red(red, op.red, s);
+        break;
+      }
+      case CODA_OP_ROW_SUMSQ: {
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * v[j] : 0.0f;
+        add_red(red, op.red, s);
+        break;
+      }
+      case CODA_OP_ROW_DOT_AUX: {
+        float x[NE];
+        aux.load(op.aux, x);
+        float s = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * x[j] : 0.0f;
+        add_red(red, op.red, s);
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+}  // namespace coda

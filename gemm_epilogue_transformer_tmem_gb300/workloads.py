@@ -1,0 +1,200 @@
+"""The GEMM+epilogue workloads as library calls: the fused step, the same chain
+unfused (the library's own GEMM with no epilogue, then one separate
+memory-bound kernel per step), and their algorithmic DRAM bytes.
+
+Shapes and distributions come from `inputs`; every call here goes through the
+C ABI (coda.py).  The commuted-RMSNorm weights are folded once (gamma (.)_row W)
+when a step is built: the fold is weight preparation, like a layout change of
+a static weight, and it is timed separately, not inside the step.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Callable, Optional
+
+import torch
+
+from . import coda, inputs
+
+BF16 = 2
+F32 = 4
+
+
+@dataclass
+class Step:
+    name: str
+    flops: int
+    fused_bytes: int          # algorithmic DRAM bytes of the fused step
+    unfused_bytes: int        # algorithmic DRAM bytes of the unfused chain
+    fused: Callable[[], None]
+    unfused: Callable[[], None]
+    host_inputs: dict = field(default_factory=dict)    # name -> device tensor fed per step in e2e mode
+    host_outputs: dict = field(default_factory=dict)   # name -> device tensor read back per step
+    kernels_per_fused: int = 1
+    kernels_per_unfused: int = 1
+    prep: Optional[Callable[[], None]] = None           # weight preparation (gamma fold)
+    outputs: dict = field(default_factory=dict)
+
+
+def _ws(M, N, K, ops, dev):
+    n = coda.workspace_size(M, N, K, ops)
+    return torch.empty((max(n, 16),), dtype=torch.uint8, device=dev), n
+
+
+def build_rmsproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
+    """D = rsqrt(mean(X^2)+eps) * (X @ (gamma (.) W)), commuted, with r_i written out."""
+    t = t or inputs.make_rmsproj(seed, M, K, N)
+    X, g, W = (t[k].to(dev) for k in ("X", "gamma", "W"))
+    Wf = torch.empty_like(W)
+    prep = lambda: coda.fold_gamma(W, g, "kn", out=Wf)   # noqa: E731
+    prep()
+    ops = [("RMS_ROWSCALE", 0, inputs.EPS_RMS)]
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rs = torch.empty((1, M), dtype=torch.float32, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    Xn = torch.empty_like(X)
+    rstd = torch.empty((M,), dtype=torch.float32, device=dev)
+    Du = torch.empty_like(D)
+
+    def fused():
+        coda.gemm_epilogue(X, Wf, ops, out=D, row_stats=rs, workspace=ws)
+
+    def unfused():
+        coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn, rstd=rstd)
+        coda.gemm_epilogue(Xn, W, [], out=Du)
+
+    fb = M * K * BF16 + K * N * BF16 + M * N * BF16 + M * F32
+    ub = (M * K * BF16 + K * BF16 + M * K * BF16 + M * F32) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
+    return Step("rmsproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
+                host_outputs=dict(D=D, r=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
+                outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn))
+
+
+def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
+    """out = dropout(silu(G) * U, p), [G|U] = X @ W."""
+    t = t or inputs.make_swiglu(seed, M, K, N_out)
+    X, W = t["X"].to(dev), t["W"].to(dev)
+    N = 2 * N_out
+    ops = [("SWIGLU",), ("DROPOUT", 0, inputs.DROPOUT_P)]
+    D = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
+    kc = torch.empty((M,), dtype=torch.int32, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    H = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
+    Du = torch.empty_like(D)
+    kcu = torch.empty_like(kc)
+
+    def fused():
+        coda.gemm_epilogue(X, W, ops, seed=inputs.DROPOUT_SEED, out=D, keep_count=kc, workspace=ws)
+
+    def unfused():
+        coda.gemm_epilogue(X, W, [], out=C)
+        coda.epilogue_apply(C, [("SWIGLU",)], out=H)
+        coda.epilogue_apply(H, [("DROPOUT", 0, inputs.DROPOUT_P)], seed=inputs.DROPOUT_SEED, out=Du, keep_count=kcu)
+
+    fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16 + M * 4
+    ub = (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16 + (2 * M * N_out * BF16 + M * 4)
+    return Step("swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
+                kernels_per_fused=2, kernels_per_unfused=3, outputs=dict(D=D, keep=kc, D_unfused=Du))
+
+
+def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
+    """dX = (dY @ W^T) * GELU'(Z), sum_j dX*Xhat and sum_j dX per row."""
+    t = t or inputs.make_dgrad(seed, M, K, N)
+    dY, W, Z, Xh = (t[k].to(dev) for k in ("dY", "W", "Z", "Xhat"))
+    ops = [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)]
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rs = torch.empty((2, M), dtype=torch.float32, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Du = torch.empty_like(D)
+    rsu = torch.empty_like(rs)
+    Dz = torch.empty_like(D)
+
+    def fused():
+        coda.gemm_epilogue(dY, W, ops, b_layout="nk", z=Z, xhat=Xh, out=D, row_stats=rs, workspace=ws)
+
+    def unfused():
+        coda.gemm_epilogue(dY, W, [], b_layout="nk", out=C)
+        coda.epilogue_apply(C, [("GELU_TANH_GRAD",)], z=Z, out=Du)
+        coda.epilogue_apply(Du, [("ROW_DOT_AUX", 0), ("ROW_SUM", 1)], xhat=Xh, out=Dz, row_stats=rsu)
+
+    fb = (M * K + N * K + 3 * M * N) * BF16 + 2 * M * F32
+    ub = (M * K + N * K + M * N) * BF16 + 3 * M * N * BF16 + (2 * M * N * BF16 + 2 * M * F32)
+    return Step("dgrad", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
+                host_outputs=dict(D=D, stats=rs), kernels_per_fused=2, kernels_per_unfused=3,
+                outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu))
+
+
+def llama_block_forward(t: dict, prepared: Optional[dict] = None, out: Optional[dict] = None) -> dict:
+    """LLaMA-like non-attention block on device tensors, four fused calls:
+      qkv = rmsnorm(X; g_attn) @ W_qkv                 (commuted RMSNorm)
+      h   = attn_out @ W_o + X                          (residual)
+      up  = silu(G) * U, [G|U] = rmsnorm(h; g_mlp) @ W_up   (commuted RMSNorm + SwiGLU)
+      y   = up @ W_down + h                             (residual)
+    attn_out stands in for the attention output (attention is not part of this path)."""
+    eps = inputs.EPS_RMS
+    if prepared is None:
+        prepared = dict(W_qkv=coda.fold_gamma(t["W_qkv"], t["gamma_attn"], "kn"),
+                        W_up=coda.fold_gamma(t["W_up"], t["gamma_mlp"], "kn"))
+    out = out or {}
+    qkv = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_ROWSCALE", None, eps)], out=out.get("qkv")).D
+    h = coda.gemm_epilogue(t["attn_out"], t["W_o"], [("RESIDUAL", 0, 1.0)], residual=t["X"], out=out.get("h")).D
+    up = coda.gemm_epilogue(h, prepared["W_up"], [("RMS_ROWSCALE", None, eps), ("SWIGLU",)], out=out.get("up")).D
+    y = coda.gemm_epilogue(up, t["W_down"], [("RESIDUAL", 0, 1.0)], residual=h, out=out.get("y")).D
+    return dict(qkv=qkv, h=h, up=up, y=y)
+
+
+def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> Step:
+    t = t or inputs.make_llama_block(seed, tokens, d, ffn)
+    t = {k: v.to(dev) for k, v in t.items()}
+    prepared = {}
+
+    def prep():
+        prepared["W_qkv"] = coda.fold_gamma(t["W_qkv"], t["gamma_attn"], "kn", out=prepared.get("W_qkv"))
+        prepared["W_up"] = coda.fold_gamma(t["W_up"], t["gamma_mlp"], "kn", out=prepared.get("W_up"))
+
+    prep()
+    T = tokens
+    out = dict(qkv=torch.empty((T, 3 * d), dtype=torch.bfloat16, device=dev),
+               h=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+               up=torch.empty((T, ffn), dtype=torch.bfloat16, device=dev),
+               y=torch.empty((T, d), dtype=torch.bfloat16, device=dev))
+    un = dict(xn=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+              qkv=torch.empty((T, 3 * d), dtype=torch.bfloat16, device=dev),
+              c_o=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+              h=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+              hn=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+              c_up=torch.empty((T, 2 * ffn), dtype=torch.bfloat16, device=dev),
+              up=torch.empty((T, ffn), dtype=torch.bfloat16, device=dev),
+              c_down=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+              y=torch.empty((T, d), dtype=torch.bfloat16, device=dev))
+
+    def fused():
+        llama_block_forward(t, prepared, out)
+
+    def unfused():
+        eps = inputs.EPS_RMS
+        coda.rmsnorm(t["X"], t["gamma_attn"], eps, out=un["xn"])
+        coda.gemm_epilogue(un["xn"], t["W_qkv"], [], out=un["qkv"])
+        coda.gemm_epilogue(t["attn_out"], t["W_o"], [], out=un["c_o"])
+        coda.epilogue_apply(un["c_o"], [("RESIDUAL", 0, 1.0)], residual=t["X"], out=un["h"])
+        coda.rmsnorm(un["h"], t["gamma_mlp"], eps, out=un["hn"])
+        coda.gemm_epilogue(un["hn"], t["W_up"], [], out=un["c_up"])
+        coda.epilogue_apply(un["c_up"], [("SWIGLU",)], out=un["up"])
+        coda.gemm_epilogue(un["up"], t["W_down"], [], out=un["c_down"])
+        coda.epilogue_apply(un["c_down"], [("RESIDUAL", 0, 1.0)], residual=un["h"], out=un["y"])
+
+    flops = 2 * T * d * (3 * d) + 2 * T * d * d + 2 * T * d * (2 * ffn) + 2 * T * ffn * d
+    act = T * d * BF16
+    fb = (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (2 * act + d * d * BF16 + act) + \
+         (act + d * 2 * ffn * BF16 + T * ffn * BF16) + (T * ffn * BF16 + ffn * d * BF16 + 2 * act)
+    ub = (2 * act) + (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (act + d * d * BF16 + act) + 3 * act + \
+         (2 * act) + (act + d * 2 * ffn * BF16 + T * 2 * ffn * BF16) + (T * 2 * ffn * BF16 + T * ffn * BF16) + \
+         (T * ffn * BF16 + ffn * d * BF16 + act) + 3 * act
+    return Step("llama", flops, fb, ub, fused, unfused, host_inputs=dict(X=t["X"], attn_out=t["attn_out"]),
+                host_outputs=dict(y=out["y"], qkv=out["qkv"]), kernels_per_fused=4, kernels_per_unfused=9,
+                prep=prep, outputs=out)
+
+
+BUILDERS = dict(rmsproj=build_rmsproj, swiglu=build_swiglu, dgrad=build_dgrad, llama=build_llama)

@@ -1,0 +1,254 @@
+/*
+ * coda.h -- C ABI of the GB300 (sm_103a) GEMM + on-chip epilogue library.
+ *
+ * The operation.  The CODA article (d9bl.com, "CODA：将 Transformer 模块重新
+ * 表达为 GEMM+Epilogue 程序", §3.1 "GEMM+Epilogue 分解", Fig. 1 and Fig. 4)
+ * writes the fused kernel as a GEMM  C = alpha*A*B + beta*C_prev  followed by an
+ * epilogue  D = f(C)  that is applied elementwise or row by row while the output
+ * tile is still on chip, before the single global write of D.  The
+ * agentlenshq.com summary ("CODA: GEMM-Epilogue FusionによるTransformer
+ * トレーニングの最適化", section "仕組み") keeps the GEMM mainloop fixed and
+ * builds f from a small set of composable primitives: scaling (by a constant or
+ * a vector), reductions (sum or mean along a dimension), pairwise/elementwise
+ * transforms (activations) and accumulation (residual).  The zeli.app page
+ * ("CODA: Wie Transformer-Blöcke als GEMM-Epilogue-Programme neu geschrieben
+ * werden", augment_me's comment) adds the commuted RMSNorm: the norm's row
+ * scale r_i is pulled past the projection,
+ *     rmsnorm(X) @ W  ==  r (.)_row ( X @ (gamma (.)_row W) ),
+ * with r_i = 1/sqrt(mean_k x_ik^2 + eps) gathered over the K tiles of X.
+ *
+ * Here f is an op list (coda_epilogue) interpreted on the fp32 accumulator tile
+ * after it is drained from tensor memory; the pages' DSL and compiler are not
+ * reproduced.  alpha is the SCALE op; beta*C_prev is the RESIDUAL op.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps no reference after the call returns and allocates no device memory.
+ *   - Matrices are dense row-major with the row stride equal to the row width.
+ *   - A, B, D, residual, Z, Xhat, column vectors, gamma and the pre-activation
+ *     output are bf16 (stored as 16-bit words); row vectors, row statistics and
+ *     the accumulator are fp32; keep counts are uint32.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous: they validate, enqueue and return.  A returned CODA_OK means
+ *     the work was enqueued, not that it finished.
+ *   - Argument, alignment and op-list checks happen on the host before anything
+ *     is enqueued; on failure nothing is enqueued and no output is touched.
+ *   - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *     recorded in a per-device error word and reported by
+ *     coda_check_device_error().  Kernels never trap.
+ *   - No function prints, throws or aborts.  Functions are thread-safe except
+ *     that concurrent launches on one device share the device error word.
+ */
+#ifndef CODA_H
+#define CODA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CODA_API __attribute__((visibility("default")))
+#else
+#define CODA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CODA_OK = 0,
+  CODA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad op list         */
+  CODA_ERR_UNSUPPORTED = 2,   /* valid request this build cannot run         */
+  CODA_ERR_ALIGNMENT = 3,     /* pointer or row stride not 16-byte aligned   */
+  CODA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed           */
+  CODA_ERR_TIMEOUT = 5,       /* a device-side wait exceeded its time limit  */
+  CODA_ERR_WORKSPACE = 6      /* workspace missing or too small              */
+} coda_status;
+
+/* Storage of the B operand. */
+typedef enum {
+  CODA_B_KN = 0,   /* B is [K, N] row-major: C = A @ B   (weights as x @ W)    */
+  CODA_B_NK = 1    /* B is [N, K] row-major: C = A @ B^T (dgrad dY @ W^T, or an
+                      nn.Linear weight stored [out, in])                        */
+} coda_b_layout;
+
+/*
+ * Epilogue opcodes.  Ops run in list order on the fp32 value x of each output
+ * element (row i, column j).  "width" is the current row width: N before a
+ * SWIGLU op, N/2 after it (N_out = N/2 when the list has SWIGLU, else N).
+ *
+ * Scaling (agentlenshq.com "Scaling"; alpha of CODA §3.1):
+ *   SCALE          x *= f0
+ *   COL_SCALE      x *= colvec[slot][j]         (bf16 vector of `width` entries)
+ *   BIAS           x += colvec[slot][j]         (bf16 vector of `width` entries)
+ *   ROW_SCALE      x *= rowvec[slot][i]         (fp32 vector of M entries)
+ *   RMS_ROWSCALE   x *= r_i, r_i = 1/sqrt(sum_k A[i,k]^2 / K + f0) gathered from
+ *                  the A tiles the mainloop streams (commuted RMSNorm, zeli.app);
+ *                  f0 = eps.  If slot != CODA_NO_SLOT, r_i is also written to
+ *                  row_stats[slot*M + i].  With B = bf16(gamma (.)_row W) (see
+ *                  coda_fold_gamma) the result is rmsnorm(A; gamma) @ W.
+ * Elementwise transforms (agentlenshq.com "Pairwise Transformations"):
+ *   GELU_TANH      x = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
+ *   SILU           x = x / (1 + exp(-x))
+ *   SWIGLU         pairs output column j < N/2 (G) with column j + N/2 (U):
+ *                  x_j = silu(G_j) * U_j; width becomes N/2.  At most once.
+ *   GELU_TANH_GRAD x *= GELU_TANH'(z[i,j])      (z: bf16 [M, N_out], aux.z)
+ *   DROPOUT        f0 = p in [0,1).  keep iff splitmix64(seed, i*N_out + j) < T,
+ *                  T = floor(ldexp(1-p, 64)) in fp64; kept x *= 1/(1-p), dropped
+ *                  x = 0.  splitmix64(seed, n) is output n (0-based) of the
+ *                  splitmix64 generator seeded with `seed` (Steele, Lea & Flood,
+ *                  OOPSLA 2014).  At most once.  Per-row keep counts go to
+ *                  row_keep_count when it is non-NULL.
+ * Accumulation (agentlenshq.com "Accumulation"; beta*C_prev of CODA §3.1):
+ *   RESIDUAL       x += f0 * residual[i,j]      (bf16 [M, N_out], aux.residual)
+ *   STORE_PREACT   writes bf16(x) to aux.preact_out[i, j] ([M, width]); at most once
+ * Reductions over the row's `width` columns (agentlenshq.com "Reductions"):
+ *   ROW_SUM        row_stats[slot*M + i] = sum_j x
+ *   ROW_MEAN       row_stats[slot*M + i] = sum_j x / width
+ *   ROW_SUMSQ      row_stats[slot*M + i] = sum_j x^2
+ *   ROW_DOT_AUX    row_stats[slot*M + i] = sum_j x * xhat[i,j]  (aux.xhat [M,N_out])
+ *
+ * Ops that read an [M, N_out] aux tensor, reductions and DROPOUT must come
+ * after SWIGLU when the list has one.  At most CODA_MAX_REDUCTIONS reductions.
+ */
+typedef enum {
+  CODA_OP_SCALE = 0,
+  CODA_OP_COL_SCALE = 1,
+  CODA_OP_BIAS = 2,
+  CODA_OP_ROW_SCALE = 3,
+  CODA_OP_RMS_ROWSCALE = 4,
+  CODA_OP_GELU_TANH = 5,
+  CODA_OP_SILU = 6,
+  CODA_OP_SWIGLU = 7,
+  CODA_OP_GELU_TANH_GRAD = 8,
+  CODA_OP_DROPOUT = 9,
+  CODA_OP_RESIDUAL = 10,
+  CODA_OP_STORE_PREACT = 11,
+  CODA_OP_ROW_SUM = 12,
+  CODA_OP_ROW_MEAN = 13,
+  CODA_OP_ROW_SUMSQ = 14,
+  CODA_OP_ROW_DOT_AUX = 15,
+  CODA_OP_COUNT_ = 16
+} coda_opcode;
+
+#define CODA_MAX_OPS 16
+#define CODA_MAX_COL_VECS 4
+#define CODA_MAX_ROW_VECS 2
+#define CODA_MAX_STAT_SLOTS 8
+#define CODA_MAX_REDUCTIONS 4
+#define CODA_NO_SLOT 0xFFFFFFFFu
+
+typedef struct {
+  uint32_t opcode;   /* coda_opcode                                   */
+  uint32_t slot;     /* vector slot or row-stat slot, per opcode      */
+  float f0;          /* scalar parameter, per opcode                  */
+  float f1;          /* reserved, must be 0                           */
+} coda_op;
+
+typedef struct {
+  uint32_t n_ops;                 /* 0 .. CODA_MAX_OPS; 0 = plain GEMM      */
+  uint32_t reserved;              /* must be 0                              */
+  uint64_t seed;                  /* dropout seed                           */
+  coda_op ops[CODA_MAX_OPS];
+} coda_epilogue;
+
+typedef struct {
+  const void* col_vec[CODA_MAX_COL_VECS];  /* bf16 [width at the op]        */
+  const float* row_vec[CODA_MAX_ROW_VECS]; /* fp32 [M]                      */
+  const void* residual;                    /* bf16 [M, N_out]               */
+  const void* z;                           /* bf16 [M, N_out]               */
+  const void* xhat;                        /* bf16 [M, N_out]               */
+  void* preact_out;                        /* bf16 [M, width at the op]     */
+} coda_aux;
+
+/*
+ * coda_gemm_epilogue -- D = f(A @ B) in one persistent kernel on the calling
+ * stream: TMA-staged bf16 operands, tcgen05 MMA into fp32 tensor memory, the
+ * op list applied to the drained tile, bf16 (round-to-nearest-even) TMA store.
+ * Row reductions and keep counts are finished by a second small kernel.
+ *
+ *   A        bf16 [M, K]
+ *   B        bf16 [K, N] (CODA_B_KN) or [N, K] (CODA_B_NK)
+ *   M, N, K  M >= 0, N >= 0, K >= 0, each < 2^31.  N and K must be multiples of
+ *            8 (16-byte rows); with SWIGLU, N must be a multiple of 16.  M == 0
+ *            or N == 0 enqueues nothing.  K == 0 means C = 0.
+ *   epi      op list (may be NULL: plain GEMM)
+ *   aux      aux tensors the op list names (may be NULL if it names none)
+ *   D        bf16 [M, N_out] output
+ *   row_stats fp32 [CODA_MAX_STAT_SLOTS or fewer][M], slot-major; required if
+ *            the list has a reduction or an RMS_ROWSCALE with a slot
+ *   row_keep_count uint32 [M] or NULL
+ *   workspace / workspace_bytes: device scratch of at least
+ *            coda_workspace_size() bytes (may be NULL when that size is 0);
+ *            the call overwrites it; it must not be shared by calls that can
+ *            run at the same time.
+ * All pointers must be 16-byte aligned.  Returns CODA_OK once enqueued.
+ */
+CODA_API coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                               int32_t b_layout, const coda_epilogue* epi, const coda_aux* aux,
+                               void* D, float* row_stats, uint32_t* row_keep_count,
+                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* Scratch bytes coda_gemm_epilogue needs for these sizes and this op list
+ * (row-reduction and keep-count partials, one per 128/256-column tile). */
+CODA_API coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi,
+                                size_t* bytes);
+
+/*
+ * coda_fold_gamma -- W_out = bf16(gamma[k] * W[k, n]) for the commuted RMSNorm
+ * (zeli.app, augment_me: gamma is folded into the projection weight so that only
+ * the row scale r_i remains for the epilogue).  W and W_out have the layout
+ * `b_layout` ([K,N] or [N,K]); gamma is bf16 [K].  W_out may equal W.
+ */
+CODA_API coda_status coda_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N,
+                            int32_t b_layout, void* stream);
+
+/*
+ * coda_rmsnorm -- the unfused normalisation pass: Xn[i,k] = bf16(r_i x_ik gamma_k),
+ * r_i = 1/sqrt(mean_k x_ik^2 + eps); rstd_out (fp32 [M]) may be NULL.  This is the
+ * separate memory-bound kernel that the commuted form removes; it exists so the
+ * unfused chain can be run and measured with the library's own kernels.
+ */
+CODA_API coda_status coda_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps,
+                         void* Xn_out, float* rstd_out, void* stream);
+
+/*
+ * coda_epilogue_apply -- the same op list applied by a separate memory-bound
+ * kernel to a bf16 tensor C [M, N] already in global memory (the unfused form:
+ * one read of C, one write of D).  RMS_ROWSCALE is not available here (it needs
+ * the GEMM's A operand).  Reductions are finished inside this kernel, so it
+ * needs no workspace.
+ */
+CODA_API coda_status coda_epilogue_apply(const void* C, int64_t M, int64_t N, const coda_epilogue* epi,
+                                const coda_aux* aux, void* D, float* row_stats,
+                                uint32_t* row_keep_count, void* stream);
+
+/*
+ * coda_check_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns CODA_ERR_TIMEOUT if a kernel gave up on
+ * a pipeline wait since the last check (its outputs are then undefined),
+ * CODA_ERR_CUDA if the synchronisation failed, else CODA_OK.  If `info` is
+ * non-NULL it receives 4 words: code, block, role, tile of the first failure.
+ */
+CODA_API coda_status coda_check_device_error(void* stream, uint32_t* info);
+
+/* Human-readable name of a status code (static string). */
+CODA_API const char* coda_status_string(coda_status status);
+
+/* Number of kernels this library has enqueued in this process (all devices). */
+CODA_API uint64_t coda_launch_count(void);
+
+/*
+ * Tuning knobs, for measurement.  coda_set_pipeline_timeout_ns sets how long a
+ * device-side pipeline wait may spin before the kernel records CODA_ERR_TIMEOUT
+ * and exits (default 1e9 ns; 0 restores the default).  coda_set_max_ctas caps
+ * the persistent grid (0 = one CTA per SM).
+ */
+CODA_API void coda_set_pipeline_timeout_ns(uint64_t ns);
+CODA_API void coda_set_max_ctas(int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CODA_H */

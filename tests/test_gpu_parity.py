@@ -1,0 +1,394 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 oracle.
+
+Tolerance (bf16 inputs, fp32 accumulation, bf16 output):
+    |gpu - ref| <= 1e-2 + 1e-2 |ref| elementwise, and
+    ||gpu - ref||_F / ||ref||_F <= 5e-3.
+Integer results (dropout mask, keep counts) and exact-arithmetic cases
+(small-integer GEMMs whose sums are exact in fp32 and bf16) are bit-exact.
+Full-size workloads are compared on sampled rows (first, last, tile edges and
+random rows), which the oracle evaluates row by row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__ as entry
+from gemm_epilogue_transformer_tmem_gb300 import coda, inputs
+from oracle import coda_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+FRO = 5e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    entry.build()
+    coda.lib()
+    yield
+    st, info = coda.check_device_error()
+    assert st == 0, f"device error word set: {info}"
+
+
+def cu(t):
+    return t.to("cuda")
+
+
+def f64(t):
+    return O.to_f64(t)
+
+
+def assert_close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    err = np.abs(got - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} elements out of tolerance, worst at {i}: "
+                             f"gpu {got[i]!r} ref {ref[i]!r}")
+    nref = np.linalg.norm(ref)
+    if nref > 0:
+        fro = np.linalg.norm(got - ref) / nref
+        assert fro <= FRO, f"{what}: relative Frobenius error {fro:.3e}"
+
+
+def sync_ok():
+    torch.cuda.synchronize()
+    st, info = coda.check_device_error()
+    assert st == 0, f"device error {st}: {info}"
+
+
+def rand(shape, seed, std=1.0):
+    return inputs.randn_bf16(shape, std, seed)
+
+
+# --------------------------------------------------------------- plain GEMM
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_small_integer_gemm_bit_exact(layout):
+    # |values| <= 2 and K = 64: every partial sum is an integer below 2^8, so
+    # fp32 accumulation and the bf16 store are exact
+    M, K, N = 200, 64, 264
+    A = inputs.small_int_bf16((M, K), 2, 1)
+    B = inputs.small_int_bf16((K, N) if layout == "kn" else (N, K), 2, 2)
+    r = coda.gemm_epilogue(cu(A), cu(B), [], b_layout=layout)
+    sync_ok()
+    ref = O.gemm(f64(A), f64(B), layout)
+    np.testing.assert_array_equal(f64(r.D), ref)
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,K,N", [(128, 64, 256), (1, 8, 8), (300, 200, 264), (257, 1000, 520),
+                                   (129, 4096, 264), (640, 136, 1032)])
+def test_plain_gemm(layout, M, K, N):
+    A = rand((M, K), 10 + M)
+    B = rand((K, N) if layout == "kn" else (N, K), 20 + N, 1.0 / math.sqrt(K))
+    r = coda.gemm_epilogue(cu(A), cu(B), [], b_layout=layout)
+    sync_ok()
+    assert_close(f64(r.D), O.gemm(f64(A), f64(B), layout), f"gemm {layout} {M}x{K}x{N}")
+
+
+def test_k_zero_is_empty_sum():
+    M, N = 70, 40
+    b = rand((N,), 5)
+    ops = [("BIAS", 0), ("GELU_TANH",)]
+    A = torch.empty((M, 0), dtype=torch.bfloat16, device="cuda")
+    B = torch.empty((0, N), dtype=torch.bfloat16, device="cuda")
+    r = coda.gemm_epilogue(A, B, ops, col_vecs={0: cu(b)})
+    sync_ok()
+    ref = O.run_chain(np.zeros((M, 0)), np.zeros((0, N)), ops, col_vecs={0: f64(b)})["D"]
+    assert_close(f64(r.D), ref, "K = 0")
+
+
+def test_pr1_bias_gelu_residual():
+    t = inputs.make_pr1(seed=0)
+    ops = [("BIAS", 0), ("GELU_TANH",), ("RESIDUAL", 0, 1.0)]
+    r = coda.gemm_epilogue(cu(t["X"]), cu(t["W"]), ops, col_vecs={0: cu(t["bias"])}, residual=cu(t["residual"]))
+    sync_ok()
+    ref = O.run_chain(f64(t["X"]), f64(t["W"]), ops, col_vecs={0: f64(t["bias"])}, residual_t=f64(t["residual"]))
+    assert_close(f64(r.D), ref["D"], "pr1")
+
+
+# ------------------------------------------------------------ each op alone
+M_R, K_R, N_R = 300, 192, 264     # ragged in M (not /128), N (not /256, not /32) and K (not /64)
+
+OP_CASES = {
+    "scale": [("SCALE", 0, 0.5)],
+    "col_scale": [("COL_SCALE", 1)],
+    "bias": [("BIAS", 0)],
+    "row_scale": [("ROW_SCALE", 0)],
+    "gelu": [("GELU_TANH",)],
+    "silu": [("SILU",)],
+    "gelu_grad": [("GELU_TANH_GRAD",)],
+    "residual": [("RESIDUAL", 0, 0.75)],
+    "preact_gelu": [("STORE_PREACT",), ("GELU_TANH",)],
+    "reductions": [("ROW_SUM", 0), ("ROW_MEAN", 1), ("ROW_SUMSQ", 2), ("ROW_DOT_AUX", 3)],
+    "swiglu": [("SWIGLU",)],
+    "bias_swiglu_bias_sum": [("BIAS", 0), ("SWIGLU",), ("BIAS", 1), ("ROW_SUM", 0)],
+    "scale_preact_swiglu": [("SCALE", 0, 2.0), ("STORE_PREACT",), ("SWIGLU",), ("ROW_SUMSQ", 1)],
+    "chain": [("SCALE", 0, 1.5), ("BIAS", 0), ("GELU_TANH",), ("COL_SCALE", 1), ("RESIDUAL", 0, 1.0),
+              ("ROW_MEAN", 2)],
+}
+
+
+def _op_case_tensors(ops, layout, seed):
+    glu = any(o[0] == "SWIGLU" for o in ops)
+    N = 2 * N_R if glu else N_R
+    n_out = N // 2 if glu else N
+    A = rand((M_R, K_R), seed)
+    B = rand((K_R, N) if layout == "kn" else (N, K_R), seed + 1, 1.0 / math.sqrt(K_R))
+    # column vectors: before SWIGLU they span N columns, after it N/2
+    pos = [i for i, o in enumerate(ops) if o[0] == "SWIGLU"]
+    gpos = pos[0] if pos else len(ops)
+    widths = {}
+    for i, o in enumerate(ops):
+        if o[0] in ("COL_SCALE", "BIAS"):
+            widths[o[1]] = N if i < gpos else n_out
+    col = {s: rand((w,), seed + 10 + s) for s, w in widths.items()}
+    row = {0: torch.rand((M_R,), generator=torch.Generator().manual_seed(seed + 20)) + 0.5}
+    aux = dict(residual=rand((M_R, n_out), seed + 30), z=rand((M_R, n_out), seed + 31),
+               xhat=rand((M_R, n_out), seed + 32))
+    return A, B, N, n_out, col, row, aux
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("case", sorted(OP_CASES))
+def test_op(case, layout):
+    ops = OP_CASES[case]
+    A, B, N, n_out, col, row, aux = _op_case_tensors(ops, layout, 100 + len(case))
+    preact = None
+    if any(o[0] == "STORE_PREACT" for o in ops):
+        i = [o[0] for o in ops].index("STORE_PREACT")
+        g = [o[0] for o in ops].index("SWIGLU") if any(o[0] == "SWIGLU" for o in ops) else len(ops)
+        preact = torch.full((M_R, N if i < g else n_out), float("nan"), dtype=torch.bfloat16, device="cuda")
+    r = coda.gemm_epilogue(cu(A), cu(B), ops, b_layout=layout, col_vecs={k: cu(v) for k, v in col.items()},
+                           row_vecs={0: cu(row[0])}, residual=cu(aux["residual"]), z=cu(aux["z"]),
+                           xhat=cu(aux["xhat"]), preact_out=preact)
+    sync_ok()
+    ref = O.run_chain(f64(A), f64(B), ops, b_layout=layout, col_vecs={k: f64(v) for k, v in col.items()},
+                      row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
+                      xhat=f64(aux["xhat"]))
+    assert_close(f64(r.D), ref["D"], case)
+    for slot, v in ref["stats"].items():
+        assert_close(f64(r.row_stats[slot]), v, f"{case} stat {slot}")
+    if preact is not None:
+        assert_close(f64(preact), ref["preact"], f"{case} preact")
+
+
+# ------------------------------------------------------------------ dropout
+@pytest.mark.parametrize("seed", [0, 12345])
+@pytest.mark.parametrize("glu", [False, True])
+def test_dropout_mask_bit_exact(glu, seed):
+    # pre-dropout value = bias[j] != 0 exactly (SCALE 0 kills the GEMM), so the
+    # mask is read off D without ambiguity
+    M, K = 333, 64
+    n_out = 264
+    N = 2 * n_out if glu else n_out
+    A = rand((M, K), 7)
+    B = rand((K, N), 8)
+    b = rand((N,), 9)
+    b = torch.where(b == 0, torch.ones_like(b), b)
+    ops = [("SCALE", 0, 0.0), ("BIAS", 0)]
+    if glu:
+        # silu(bias_G) * bias_U: pick bias so that both halves are nonzero
+        ops += [("SWIGLU",)]
+    ops += [("DROPOUT", 0, 0.1)]
+    r = coda.gemm_epilogue(cu(A), cu(B), ops, seed=seed, col_vecs={0: cu(b)})
+    sync_ok()
+    ref = O.run_chain(f64(A), f64(B), ops, seed=seed, col_vecs={0: f64(b)})
+    nonzero = ref["D"] != 0
+    keep_gpu = f64(r.D) != 0
+    np.testing.assert_array_equal(keep_gpu[nonzero | ~ref["keep"]], ref["keep"][nonzero | ~ref["keep"]])
+    np.testing.assert_array_equal(r.keep_count.cpu().numpy().astype(np.int64), ref["keep_count"])
+    assert_close(f64(r.D), ref["D"], "dropout values")
+
+
+def test_dropout_p_zero_keeps_all():
+    M, K, N = 130, 64, 256
+    A = rand((M, K), 1)
+    B = rand((K, N), 2, 0.125)
+    r = coda.gemm_epilogue(cu(A), cu(B), [("DROPOUT", 0, 0.0)], seed=99)
+    r0 = coda.gemm_epilogue(cu(A), cu(B), [])
+    sync_ok()
+    assert torch.equal(r.D, r0.D)
+    assert (r.keep_count.cpu() == N).all()
+
+
+# ----------------------------------------------------------- commuted norm
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_fold_gamma_bit_exact(layout):
+    K, N = 200, 264
+    W = rand((K, N) if layout == "kn" else (N, K), 3)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 4)
+    got = coda.fold_gamma(cu(W), cu(g), layout)
+    sync_ok()
+    gw = f64(g)[:, None] * f64(W) if layout == "kn" else f64(W) * f64(g)[None, :]
+    # the product of two bf16 values is exact in fp64; one RNE rounding to bf16
+    expect = torch.from_numpy(gw).to(torch.bfloat16)
+    assert torch.equal(got.cpu(), expect)
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,K,N", [(300, 192, 264), (128, 2048, 512)])
+def test_commuted_rmsnorm(layout, M, K, N):
+    X = rand((M, K), 41)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 42)
+    W = rand((K, N) if layout == "kn" else (N, K), 43, 1.0 / math.sqrt(K))
+    Wf = coda.fold_gamma(cu(W), cu(g), layout)
+    ops = [("RMS_ROWSCALE", 1, 1e-6)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops, b_layout=layout)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, b_layout=layout, norm_gamma=f64(g))
+    assert_close(f64(r.D), ref["D"], "commuted rmsnorm")
+    assert_close(f64(r.row_stats[1]), ref["stats"][1], "rms row scale")
+
+
+def test_commuted_rmsnorm_then_swiglu():
+    # r_i applies to both halves before the nonlinearity: silu(r G) * (r U)
+    M, K, n_out = 200, 256, 136
+    X = rand((M, K), 51)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 52)
+    W = rand((K, 2 * n_out), 53, 1.0 / math.sqrt(K))
+    Wf = coda.fold_gamma(cu(W), cu(g), "kn")
+    ops = [("RMS_ROWSCALE", 0, 1e-6), ("SWIGLU",), ("ROW_SUM", 1)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g))
+    assert_close(f64(r.D), ref["D"], "rms -> swiglu")
+    assert_close(f64(r.row_stats[0]), ref["stats"][0], "rms r")
+    assert_close(f64(r.row_stats[1]), ref["stats"][1], "row sum")
+
+
+# --------------------------------------------------------------------- dgrad
+def test_dgrad_small():
+    M, K, N = 300, 128, 520
+    dY = rand((M, K), 61)
+    W = rand((N, K), 62, 1.0 / math.sqrt(K))
+    Z = rand((M, N), 63)
+    Xh = rand((M, N), 64)
+    ops = [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)]
+    r = coda.gemm_epilogue(cu(dY), cu(W), ops, b_layout="nk", z=cu(Z), xhat=cu(Xh))
+    sync_ok()
+    ref = O.run_chain(f64(dY), f64(W), ops, b_layout="nk", z=f64(Z), xhat=f64(Xh))
+    assert_close(f64(r.D), ref["D"], "dgrad dX")
+    assert_close(f64(r.row_stats[0]), ref["stats"][0], "sum dX*Xhat")
+    assert_close(f64(r.row_stats[1]), ref["stats"][1], "sum dX")
+
+
+# --------------------------------------------------------- unfused kernels
+def test_unfused_rmsnorm():
+    M, K = 300, 520
+    X = rand((M, K), 71)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 72)
+    xn, rstd = coda.rmsnorm(cu(X), cu(g), 1e-6)
+    sync_ok()
+    assert_close(f64(xn), O.rmsnorm(f64(X), f64(g), 1e-6), "rmsnorm")
+    assert_close(f64(rstd), O.rms_rstd(f64(X), 1e-6), "rstd")
+
+
+@pytest.mark.parametrize("case", ["chain", "swiglu", "reductions", "gelu_grad", "bias_swiglu_bias_sum"])
+def test_unfused_epilogue_apply(case):
+    ops = OP_CASES[case]
+    A, B, N, n_out, col, row, aux = _op_case_tensors(ops, "kn", 300)
+    C = rand((M_R, N), 301)
+    r = coda.epilogue_apply(cu(C), ops, col_vecs={k: cu(v) for k, v in col.items()}, row_vecs={0: cu(row[0])},
+                            residual=cu(aux["residual"]), z=cu(aux["z"]), xhat=cu(aux["xhat"]))
+    sync_ok()
+    # C = C @ I exactly, so the oracle chain on (C, I) is the epilogue alone
+    ref = O.run_chain(f64(C), np.eye(N), ops, col_vecs={k: f64(v) for k, v in col.items()},
+                      row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
+                      xhat=f64(aux["xhat"]))
+    assert_close(f64(r.D), ref["D"], f"apply {case}")
+    for slot, v in ref["stats"].items():
+        assert_close(f64(r.row_stats[slot]), v, f"apply {case} stat {slot}")
+
+
+def test_unfused_dropout_matches_fused_mask():
+    M, N = 257, 264
+    C = rand((M, N), 81)
+    r = coda.epilogue_apply(cu(C), [("DROPOUT", 0, 0.1)], seed=7)
+    sync_ok()
+    ref = O.run_chain(f64(C), np.eye(N), [("DROPOUT", 0, 0.1)], seed=7)
+    np.testing.assert_array_equal(r.keep_count.cpu().numpy().astype(np.int64), ref["keep_count"])
+    assert_close(f64(r.D), ref["D"], "unfused dropout")
+
+
+# ------------------------------------------------- full-size, sampled rows
+def _sampled(M, seed):
+    return inputs.sample_rows(M, 40, seed)
+
+
+def test_full_rmsproj_sampled():
+    w = inputs.WORKLOADS["rmsproj"]
+    t = inputs.make_rmsproj()
+    Wf = coda.fold_gamma(cu(t["W"]), cu(t["gamma"]), "kn")
+    ops = [("RMS_ROWSCALE", 0, inputs.EPS_RMS)]
+    r = coda.gemm_epilogue(cu(t["X"]), Wf, ops)
+    sync_ok()
+    rows = _sampled(w.M, 1)
+    ref = O.run_chain(f64(t["X"][rows]), f64(t["W"]), ops, norm_gamma=f64(t["gamma"]))
+    assert_close(f64(r.D[rows]), ref["D"], "rmsproj")
+    assert_close(f64(r.row_stats[0][rows]), ref["stats"][0], "rmsproj r")
+
+
+def test_full_swiglu_dropout_sampled():
+    w = inputs.WORKLOADS["swiglu"]
+    t = inputs.make_swiglu()
+    ops = [("SWIGLU",), ("DROPOUT", 0, inputs.DROPOUT_P)]
+    r = coda.gemm_epilogue(cu(t["X"]), cu(t["W"]), ops, seed=inputs.DROPOUT_SEED)
+    sync_ok()
+    rows = _sampled(w.M, 2)
+    ref = O.run_chain(f64(t["X"][rows]), f64(t["W"]), ops, seed=inputs.DROPOUT_SEED, rows=rows)
+    assert_close(f64(r.D[rows]), ref["D"], "swiglu+dropout")
+    kc = r.keep_count.cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(kc[rows], ref["keep_count"])
+    # keep rate over the whole 8192 x 11008 output within 1-p +- 3 sigma
+    n = w.M * (w.N // 2)
+    p = inputs.DROPOUT_P
+    rate = kc.sum() / n
+    assert abs(rate - (1 - p)) < 3 * math.sqrt(p * (1 - p) / n), rate
+
+
+def test_full_dgrad_sampled():
+    w = inputs.WORKLOADS["dgrad"]
+    t = inputs.make_dgrad()
+    ops = [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)]
+    r = coda.gemm_epilogue(cu(t["dY"]), cu(t["W"]), ops, b_layout="nk", z=cu(t["Z"]), xhat=cu(t["Xhat"]))
+    sync_ok()
+    rows = _sampled(w.M, 3)
+    ref = O.run_chain(f64(t["dY"][rows]), f64(t["W"]), ops, b_layout="nk", z=f64(t["Z"][rows]),
+                      xhat=f64(t["Xhat"][rows]))
+    assert_close(f64(r.D[rows]), ref["D"], "dgrad")
+    assert_close(f64(r.row_stats[0][rows]), ref["stats"][0], "dgrad sum dX*Xhat")
+    assert_close(f64(r.row_stats[1][rows]), ref["stats"][1], "dgrad sum dX")
+
+
+def test_full_llama_block_chain_sampled():
+    from gemm_epilogue_transformer_tmem_gb300 import workloads
+    t = inputs.make_llama_block()
+    out = workloads.llama_block_forward({k: cu(v) for k, v in t.items()})
+    sync_ok()
+    rows = _sampled(inputs.LLAMA_BLOCK["tokens"], 4)
+    ref = workloads_oracle_llama(t, rows)
+    for name in ("qkv", "h", "y"):
+        assert_close(f64(out[name][rows]), ref[name], f"llama {name}")
+
+
+def workloads_oracle_llama(t, rows):
+    """The block evaluated by the oracle on the given rows, unfused, in fp64."""
+    eps = inputs.EPS_RMS
+    X = f64(t["X"][rows])
+    qkv = O.run_chain(X, f64(t["W_qkv"]), [("RMS_ROWSCALE", None, eps)], norm_gamma=f64(t["gamma_attn"]))["D"]
+    h = O.run_chain(f64(t["attn_out"][rows]), f64(t["W_o"]), [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
+    up = O.run_chain(h, f64(t["W_up"]), [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
+                     norm_gamma=f64(t["gamma_mlp"]))["D"]
+    y = O.run_chain(up, f64(t["W_down"]), [("RESIDUAL", 0, 1.0)], residual_t=h)["D"]
+    return dict(qkv=qkv, h=h, y=y)

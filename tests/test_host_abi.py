@@ -1,0 +1,153 @@
+"""CPU-side checks of the C ABI: the library builds, loads and exports every
+symbol include/coda.h declares; struct layouts match; host validation rejects
+bad arguments before anything reaches a device.  No kernel runs here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+from gemm_epilogue_transformer_tmem_gb300 import coda
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "coda.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN, CUDA, TIMEOUT, WORKSPACE = range(7)
+
+
+@pytest.fixture(scope="module")
+def L():
+    entry.build()
+    return coda.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"CODA_API\s+[\w\s\*]+?\b(coda_\w+)\s*\(", src)
+
+
+def test_header_declares_entry_points():
+    names = _declared()
+    for n in ["coda_gemm_epilogue", "coda_workspace_size", "coda_fold_gamma", "coda_rmsnorm",
+              "coda_epilogue_apply", "coda_check_device_error", "coda_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_struct_layouts():
+    assert ctypes.sizeof(coda.CodaOp) == 16
+    assert ctypes.sizeof(coda.CodaEpilogue) == 16 + 16 * 16
+    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4)
+
+
+def test_opcode_values_match_header():
+    src = open(HEADER).read()
+    for name, val in coda.OPCODES.items():
+        m = re.search(r"CODA_OP_%s\s*=\s*(\d+)" % name, src)
+        assert m and int(m.group(1)) == val, name
+
+
+def test_status_strings(L):
+    for code, name in coda.STATUS.items():
+        assert L.coda_status_string(code).decode() == name
+
+
+def _ws(L, M, N, K, ops):
+    e = coda.make_epilogue(ops)
+    n = ctypes.c_size_t(123)
+    st = L.coda_workspace_size(M, N, K, ctypes.byref(e), ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size_closed_form(L):
+    # one fp32 partial per (reduction, 256-column tile, row); 128-column tiles with SWIGLU
+    assert _ws(L, 1000, 1024, 64, []) == (OK, 0)
+    assert _ws(L, 1000, 1024, 64, [("ROW_SUM", 0)]) == (OK, 4 * 4 * 1000)
+    assert _ws(L, 1000, 1032, 64, [("ROW_SUM", 0), ("ROW_SUMSQ", 1)]) == (OK, 2 * 5 * 4 * 1000)
+    assert _ws(L, 8, 2 * 264, 64, [("SWIGLU",), ("DROPOUT", 0, 0.1)]) == (OK, 3 * 8 * 4)
+    assert _ws(L, 8, 64, 64, [("RMS_ROWSCALE", 0, 1e-6)]) == (OK, 0)
+
+
+@pytest.mark.parametrize("ops,why", [
+    ([("ROW_SUM", 9)], "stat slot out of range"),
+    ([("SWIGLU",), ("SWIGLU",)], "two SWIGLU"),
+    ([("DROPOUT", 0, 1.0)], "p = 1"),
+    ([("DROPOUT", 0, -0.1)], "p < 0"),
+    ([("DROPOUT", 0, 0.1), ("DROPOUT", 0, 0.1)], "two dropouts"),
+    ([("ROW_SUM", 0)] * 5, "five reductions"),
+    ([("RESIDUAL", 0, 1.0), ("SWIGLU",)], "residual before SWIGLU"),
+    ([("SCALE", 0, float("nan"))], "nan parameter"),
+])
+def test_invalid_op_lists(L, ops, why):
+    st, _ = _ws(L, 64, 64, 64, ops)
+    assert st == INVALID, why
+
+
+def test_unknown_opcode(L):
+    e = coda.make_epilogue([("SCALE", 0, 1.0)])
+    e.ops[0].opcode = 77
+    n = ctypes.c_size_t(0)
+    assert L.coda_workspace_size(8, 8, 8, ctypes.byref(e), ctypes.byref(n)) == INVALID
+    e.ops[0].opcode = 0
+    e.reserved = 1
+    assert L.coda_workspace_size(8, 8, 8, ctypes.byref(e), ctypes.byref(n)) == INVALID
+
+
+def test_dims_validation(L):
+    assert _ws(L, 64, 60, 64, [])[0] == INVALID        # N % 8
+    assert _ws(L, 64, 64, 60, [])[0] == INVALID        # K % 8
+    assert _ws(L, -1, 64, 64, [])[0] == INVALID
+    assert _ws(L, 64, 2 * 12, 64, [("SWIGLU",)])[0] == INVALID   # N % 16 with SWIGLU
+    assert _ws(L, 64, 64, 0, [("RMS_ROWSCALE", 0, 1e-6)])[0] == INVALID
+
+
+def _gemm(L, A, B, M, N, K, ops=(), aux=None, D=0x1000, stats=None, ws=None, ws_bytes=0, layout=0):
+    e = coda.make_epilogue(ops)
+    a = aux if aux is not None else coda.CodaAux()
+    return L.coda_gemm_epilogue(A, B, M, N, K, layout, ctypes.byref(e), ctypes.byref(a), D, stats, None, ws,
+                                ws_bytes, None)
+
+
+def test_gemm_validation_before_device(L):
+    # every one of these fails in host validation, before any CUDA call
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=2) == INVALID
+    assert _gemm(L, 0x1008, 0x2000, 64, 64, 64) == ALIGN
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, D=0x1004) == ALIGN
+    assert _gemm(L, None, 0x2000, 64, 64, 64) == INVALID
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, D=None) == INVALID
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, ops=[("BIAS", 0)]) == INVALID          # no bias vector
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, ops=[("ROW_SUM", 0)]) == INVALID       # no row_stats
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, ops=[("ROW_SUM", 0)], stats=0x3000) == WORKSPACE
+    aux = coda.CodaAux()
+    aux.residual = 0x4004
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, ops=[("RESIDUAL", 0, 1.0)], aux=aux) == ALIGN
+
+
+def test_empty_problems_enqueue_nothing(L):
+    # M == 0 or N == 0: nothing to compute, nothing touched, no device needed
+    before = L.coda_launch_count()
+    assert _gemm(L, 0x1000, 0x2000, 0, 64, 64) == OK
+    assert _gemm(L, 0x1000, 0x2000, 64, 0, 64) == OK
+    assert L.coda_launch_count() == before
+
+
+def test_other_entry_points_validate(L):
+    assert L.coda_fold_gamma(0x1000, 0x2000, 0x3000, 64, 64, 5, None) == INVALID
+    assert L.coda_fold_gamma(0x1000, 0x2004, 0x3000, 64, 64, 0, None) == ALIGN
+    assert L.coda_rmsnorm(0x1000, 0x2000, 64, 60, 1e-6, 0x3000, None, None) == INVALID
+    assert L.coda_rmsnorm(0x1000, 0x2000, 64, 64, -1.0, 0x3000, None, None) == INVALID
+    e = coda.make_epilogue([("RMS_ROWSCALE", 0, 1e-6)])
+    a = coda.CodaAux()
+    assert L.coda_epilogue_apply(0x1000, 64, 64, ctypes.byref(e), ctypes.byref(a), 0x2000, 0x3000, None,
+                                 None) == UNSUPPORTED
+
+
+def test_binding_helpers():
+    assert coda.output_width(22016, [("SWIGLU",), ("DROPOUT", 0, 0.1)]) == 11008
+    assert coda.stat_slots([("RMS_ROWSCALE", 2, 1e-6), ("ROW_SUM", 0)]) == 3
+    assert coda.stat_slots([("RMS_ROWSCALE", None, 1e-6)]) == 0
