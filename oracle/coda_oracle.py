@@ -254,8 +254,10 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
     rows: absolute row indices of the rows of A given (used by dropout's
         counter and nothing else); default 0..M-1.
 
-    Returns dict with D (fp64), stats {slot: fp64[M]}, keep_count (int64[M] or
-    None), keep (bool mask or None), preact (fp64 or None).
+    Returns dict with D (fp64), stats {slot: fp64[M]}, stat_scale {slot: fp64[M]}
+    (the L2 norm of each row reduction's summands: the scale of its rounding
+    error when the summands carry independent relative errors), keep_count
+    (int64[M] or None), keep (bool mask or None), preact (fp64 or None).
     """
     A = np.asarray(A, dtype=np.float64)
     col_vecs = col_vecs or {}
@@ -281,6 +283,7 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
     keep_count = None
     keep = None
     preact = None
+    stat_scale = {}
     for name, slot, f0 in ops[start:]:
         if name == "SCALE":
             x = scale(x, f0)
@@ -312,15 +315,29 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
             preact = x.copy()
         elif name == "ROW_SUM":
             stats[slot] = row_sum(x)
+            stat_scale[slot] = np.sqrt(row_sumsq(x))
         elif name == "ROW_MEAN":
             stats[slot] = row_mean(x)
+            stat_scale[slot] = np.sqrt(row_sumsq(x)) / x.shape[1]
         elif name == "ROW_SUMSQ":
             stats[slot] = row_sumsq(x)
+            stat_scale[slot] = np.sqrt(row_sumsq(x * x))
         elif name == "ROW_DOT_AUX":
             stats[slot] = row_dot(x, xhat)
+            stat_scale[slot] = np.sqrt(row_sumsq(x * np.asarray(xhat, dtype=np.float64)))
         else:
             raise ValueError(f"unknown op {name}")
-    return dict(D=x, stats=stats, keep_count=keep_count, keep=keep, preact=preact)
+    return dict(D=x, stats=stats, stat_scale=stat_scale, keep_count=keep_count, keep=keep, preact=preact)
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (8 significant bits), ties to
+    even: the rounding every library call applies to its bf16 outputs.  Used
+    where a workload chains calls, so the oracle rounds the outputs of its calls
+    the same way.  (Normal range only; no overflow or subnormal handling.)"""
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)                    # x = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
 
 
 def to_f64(t) -> np.ndarray:

@@ -61,6 +61,28 @@ def assert_close(got, ref, what=""):
         assert fro <= FRO, f"{what}: relative Frobenius error {fro:.3e}"
 
 
+def assert_stat_close(got, ref, scale, what=""):
+    """Row reductions: each summand carries the elementwise error of the output
+    (relative 1e-2 at most), and independent errors add in quadrature, so the
+    bound is 1e-2 + 1e-2 * max(|ref|, ||summands||_2) (scale = the L2 norm)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    bound = ATOL + RTOL * np.maximum(np.abs(ref), scale)
+    err = np.abs(got - ref)
+    if (err > bound).any():
+        i = int(np.argmax(err - bound))
+        raise AssertionError(f"{what}: {(err > bound).sum()} rows out of tolerance, worst row {i}: "
+                             f"gpu {got[i]!r} ref {ref[i]!r} bound {bound[i]!r}")
+
+
+def check_stats(r, ref, what):
+    for slot, v in ref["stats"].items():
+        if slot in ref["stat_scale"]:
+            assert_stat_close(f64(r.row_stats[slot]), v, ref["stat_scale"][slot], f"{what} stat {slot}")
+        else:
+            assert_close(f64(r.row_stats[slot]), v, f"{what} stat {slot}")
+
+
 def sync_ok():
     torch.cuda.synchronize()
     st, info = coda.check_device_error()
@@ -177,8 +199,7 @@ def test_op(case, layout):
                       row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
                       xhat=f64(aux["xhat"]))
     assert_close(f64(r.D), ref["D"], case)
-    for slot, v in ref["stats"].items():
-        assert_close(f64(r.row_stats[slot]), v, f"{case} stat {slot}")
+    check_stats(r, ref, case)
     if preact is not None:
         assert_close(f64(preact), ref["preact"], f"{case} preact")
 
@@ -251,11 +272,18 @@ def test_commuted_rmsnorm(layout, M, K, N):
     assert_close(f64(r.row_stats[1]), ref["stats"][1], "rms row scale")
 
 
-def test_commuted_rmsnorm_then_swiglu():
-    # r_i applies to both halves before the nonlinearity: silu(r G) * (r U)
+@pytest.mark.parametrize("exact_gamma", [False, True])
+def test_commuted_rmsnorm_then_swiglu(exact_gamma):
+    # r_i applies to both halves before the nonlinearity: silu(r G) * (r U).
+    # With gamma in {1/2, 1, 2} the fold gamma*W is exact in bf16, so the GPU
+    # and the oracle see the same weights and the row sum gets the strict bound.
     M, K, n_out = 200, 256, 136
     X = rand((M, K), 51)
-    g = inputs.uniform_bf16((K,), 0.5, 1.5, 52)
+    if exact_gamma:
+        g = torch.tensor([0.5, 1.0, 2.0])[torch.randint(0, 3, (K,), generator=torch.Generator().manual_seed(5))]
+        g = g.to(torch.bfloat16)
+    else:
+        g = inputs.uniform_bf16((K,), 0.5, 1.5, 52)
     W = rand((K, 2 * n_out), 53, 1.0 / math.sqrt(K))
     Wf = coda.fold_gamma(cu(W), cu(g), "kn")
     ops = [("RMS_ROWSCALE", 0, 1e-6), ("SWIGLU",), ("ROW_SUM", 1)]
@@ -264,7 +292,10 @@ def test_commuted_rmsnorm_then_swiglu():
     ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g))
     assert_close(f64(r.D), ref["D"], "rms -> swiglu")
     assert_close(f64(r.row_stats[0]), ref["stats"][0], "rms r")
-    assert_close(f64(r.row_stats[1]), ref["stats"][1], "row sum")
+    if exact_gamma:
+        assert_close(f64(r.row_stats[1]), ref["stats"][1], "row sum (exact fold)")
+    else:
+        check_stats(r, ref, "rms -> swiglu")
 
 
 # --------------------------------------------------------------------- dgrad
@@ -279,8 +310,7 @@ def test_dgrad_small():
     sync_ok()
     ref = O.run_chain(f64(dY), f64(W), ops, b_layout="nk", z=f64(Z), xhat=f64(Xh))
     assert_close(f64(r.D), ref["D"], "dgrad dX")
-    assert_close(f64(r.row_stats[0]), ref["stats"][0], "sum dX*Xhat")
-    assert_close(f64(r.row_stats[1]), ref["stats"][1], "sum dX")
+    check_stats(r, ref, "dgrad")
 
 
 # --------------------------------------------------------- unfused kernels
@@ -307,8 +337,7 @@ def test_unfused_epilogue_apply(case):
                       row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
                       xhat=f64(aux["xhat"]))
     assert_close(f64(r.D), ref["D"], f"apply {case}")
-    for slot, v in ref["stats"].items():
-        assert_close(f64(r.row_stats[slot]), v, f"apply {case} stat {slot}")
+    check_stats(r, ref, f"apply {case}")
 
 
 def test_unfused_dropout_matches_fused_mask():
@@ -367,8 +396,9 @@ def test_full_dgrad_sampled():
     ref = O.run_chain(f64(t["dY"][rows]), f64(t["W"]), ops, b_layout="nk", z=f64(t["Z"][rows]),
                       xhat=f64(t["Xhat"][rows]))
     assert_close(f64(r.D[rows]), ref["D"], "dgrad")
-    assert_close(f64(r.row_stats[0][rows]), ref["stats"][0], "dgrad sum dX*Xhat")
-    assert_close(f64(r.row_stats[1][rows]), ref["stats"][1], "dgrad sum dX")
+    for slot in (0, 1):
+        assert_stat_close(f64(r.row_stats[slot][rows]), ref["stats"][slot], ref["stat_scale"][slot],
+                          f"dgrad stat {slot}")
 
 
 def test_full_llama_block_chain_sampled():
@@ -378,17 +408,20 @@ def test_full_llama_block_chain_sampled():
     sync_ok()
     rows = _sampled(inputs.LLAMA_BLOCK["tokens"], 4)
     ref = workloads_oracle_llama(t, rows)
-    for name in ("qkv", "h", "y"):
+    for name in ("qkv", "h", "up", "y"):
         assert_close(f64(out[name][rows]), ref[name], f"llama {name}")
 
 
 def workloads_oracle_llama(t, rows):
-    """The block evaluated by the oracle on the given rows, unfused, in fp64."""
+    """The block evaluated by the oracle on the given rows, unfused, in fp64.
+    Each of the four calls returns bf16, so the oracle rounds each call's
+    output to bf16 before the next call reads it."""
     eps = inputs.EPS_RMS
+    R = O.round_bf16
     X = f64(t["X"][rows])
     qkv = O.run_chain(X, f64(t["W_qkv"]), [("RMS_ROWSCALE", None, eps)], norm_gamma=f64(t["gamma_attn"]))["D"]
     h = O.run_chain(f64(t["attn_out"][rows]), f64(t["W_o"]), [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
-    up = O.run_chain(h, f64(t["W_up"]), [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
+    up = O.run_chain(R(h), f64(t["W_up"]), [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
                      norm_gamma=f64(t["gamma_mlp"]))["D"]
-    y = O.run_chain(up, f64(t["W_down"]), [("RESIDUAL", 0, 1.0)], residual_t=h)["D"]
-    return dict(qkv=qkv, h=h, y=y)
+    y = O.run_chain(R(up), f64(t["W_down"]), [("RESIDUAL", 0, 1.0)], residual_t=R(h))["D"]
+    return dict(qkv=qkv, h=h, up=up, y=y)

@@ -310,3 +310,18 @@ def test_chain_col_row_scale_and_preact_closed_form():
                       col_vecs={1: v}, row_vecs={0: u})
     np.testing.assert_allclose(out["preact"], np.outer(u, v), rtol=1e-15)
     np.testing.assert_allclose(out["D"], O.silu(np.outer(u, v)), rtol=1e-15)
+
+
+def test_round_bf16_against_bit_patterns():
+    import torch
+    # bf16 keeps the top 16 bits of an fp32 word; values already on the bf16
+    # grid are unchanged, midpoints go to the even neighbour
+    assert O.round_bf16(1.0) == 1.0
+    assert O.round_bf16(1.0 + 2 ** -8) == 1.0                  # midpoint, even below
+    assert O.round_bf16(1.0 + 3 * 2 ** -8) == 1.0 + 2 ** -6    # midpoint, even above
+    assert O.round_bf16(1.0 + 2 ** -8 + 2 ** -20) == 1.0 + 2 ** -7
+    assert O.round_bf16(-3.0) == -3.0
+    # fp32 inputs: a single rounding, so torch's fp32 -> bf16 conversion agrees exactly
+    x = np.random.default_rng(7).standard_normal(20000).astype(np.float32)
+    expect = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), expect)
