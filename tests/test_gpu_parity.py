@@ -407,21 +407,36 @@ def test_full_llama_block_chain_sampled():
     out = workloads.llama_block_forward({k: cu(v) for k, v in t.items()})
     sync_ok()
     rows = _sampled(inputs.LLAMA_BLOCK["tokens"], 4)
-    ref = workloads_oracle_llama(t, rows)
+    ref = workloads_oracle_llama(t, rows, prepared=True)
     for name in ("qkv", "h", "up", "y"):
         assert_close(f64(out[name][rows]), ref[name], f"llama {name}")
+    # against the unprepared block (gamma applied in fp64, no bf16 weight
+    # preparation): the whole-block deviation stays within the Frobenius bound
+    ref0 = workloads_oracle_llama(t, rows, prepared=False)
+    y = f64(out["y"][rows])
+    assert np.linalg.norm(y - ref0["y"]) / np.linalg.norm(ref0["y"]) <= FRO
 
 
-def workloads_oracle_llama(t, rows):
+def workloads_oracle_llama(t, rows, prepared):
     """The block evaluated by the oracle on the given rows, unfused, in fp64.
-    Each of the four calls returns bf16, so the oracle rounds each call's
-    output to bf16 before the next call reads it."""
+    Each of the four calls returns bf16, so the oracle rounds each call's output
+    to bf16 before the next call reads it.  With prepared=True the norm weights
+    are the prepared ones, bf16(gamma (.)_row W) -- the block's documented weight
+    preparation, rounded by the oracle itself -- and the norm is applied with
+    unit gamma; with prepared=False gamma is applied in fp64 to the activations."""
     eps = inputs.EPS_RMS
     R = O.round_bf16
     X = f64(t["X"][rows])
-    qkv = O.run_chain(X, f64(t["W_qkv"]), [("RMS_ROWSCALE", None, eps)], norm_gamma=f64(t["gamma_attn"]))["D"]
+
+    def norm_proj(A, W, g, extra):
+        W, g = f64(W), f64(g)
+        if prepared:
+            return O.run_chain(A, R(g[:, None] * W), [("RMS_ROWSCALE", None, eps)] + extra,
+                               norm_gamma=np.ones_like(g))["D"]
+        return O.run_chain(A, W, [("RMS_ROWSCALE", None, eps)] + extra, norm_gamma=g)["D"]
+
+    qkv = norm_proj(X, t["W_qkv"], t["gamma_attn"], [])
     h = O.run_chain(f64(t["attn_out"][rows]), f64(t["W_o"]), [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
-    up = O.run_chain(R(h), f64(t["W_up"]), [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
-                     norm_gamma=f64(t["gamma_mlp"]))["D"]
+    up = norm_proj(R(h), t["W_up"], t["gamma_mlp"], [("SWIGLU",)])
     y = O.run_chain(R(up), f64(t["W_down"]), [("RESIDUAL", 0, 1.0)], residual_t=R(h))["D"]
     return dict(qkv=qkv, h=h, up=up, y=y)
