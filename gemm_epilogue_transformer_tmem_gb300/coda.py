@@ -58,6 +58,8 @@ _I64 = ctypes.c_int64
 _SIGS = {
     "coda_gemm_epilogue": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, ctypes.c_int32, _VP, _VP, _VP, _VP, _VP,
                                           _VP, ctypes.c_size_t, _VP]),
+    "coda_gemm_epilogue_noalloc": (ctypes.c_int, [_VP, _VP, _I64, _I64, _I64, ctypes.c_int32, _VP, _VP, _VP, _VP,
+                                                  _VP, _VP]),
     "coda_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _VP, ctypes.POINTER(ctypes.c_size_t)]),
     "coda_fold_gamma": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
     "coda_rmsnorm": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP, _VP]),
@@ -207,6 +209,25 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
                                   workspace.numel() if workspace is not None else 0, _stream(stream))
     _check(st, "coda_gemm_epilogue")
     return Result(out, row_stats, keep_count)
+
+
+def gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence, *, out: torch.Tensor,
+                          row_stats: Optional[torch.Tensor] = None, keep_count: Optional[torch.Tensor] = None,
+                          b_layout: str = "kn", seed: int = 0, col_vecs=None, row_vecs=None, residual=None, z=None,
+                          xhat=None, preact_out=None, stream=None) -> Result:
+    """coda_gemm_epilogue_noalloc: the caller passes every output; the library's
+    fixed scratch buffer replaces the workspace, so nothing is allocated here."""
+    M, K = A.shape
+    N = B.shape[1] if b_layout == "kn" else B.shape[0]
+    e = make_epilogue(ops, seed)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    _check(lib().coda_gemm_epilogue_noalloc(_ptr(A), _ptr(B), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(e),
+                                            ctypes.byref(a), _ptr(out), _ptr(row_stats), _ptr(keep_count),
+                                            _stream(stream)), "coda_gemm_epilogue_noalloc")
+    return Result(out, row_stats, keep_count)
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def fold_gamma(W: torch.Tensor, gamma: torch.Tensor, b_layout: str = "kn", out: Optional[torch.Tensor] = None,

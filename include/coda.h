@@ -189,6 +189,32 @@ CODA_API coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M,
                                void* D, float* row_stats, uint32_t* row_keep_count,
                                void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * coda_gemm_epilogue_noalloc -- coda_gemm_epilogue without a caller-supplied
+ * workspace.  The paper has no counterpart: this entry point exists for callers
+ * that cannot allocate device memory when they call the library, such as a
+ * serving loop that fixes its memory footprint at start-up (cudaMalloc can
+ * synchronise the device and has no latency bound) or a runtime whose device
+ * memory belongs entirely to another allocator.
+ *
+ * The row-reduction and keep-count partials go to one scratch buffer of
+ * CODA_NOALLOC_SCRATCH_BYTES that the library holds on every GPU it is loaded
+ * on, for the life of the process.  Arguments, results and errors are those of
+ * coda_gemm_epilogue, plus CODA_ERR_WORKSPACE when the problem needs more
+ * scratch than the buffer holds (coda_workspace_size tells how much it needs;
+ * problems without reductions or keep counts need none).  It calls no
+ * allocating routine.  The first call on a device looks up the buffer's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls share the buffer: calls whose
+ * kernels can run at the same time on one device (different streams or host
+ * threads) race on it.
+ */
+#define CODA_NOALLOC_SCRATCH_BYTES (8u << 20)
+CODA_API coda_status coda_gemm_epilogue_noalloc(const void* A, const void* B, int64_t M, int64_t N, int64_t K,
+                                                int32_t b_layout, const coda_epilogue* epi, const coda_aux* aux,
+                                                void* D, float* row_stats, uint32_t* row_keep_count,
+                                                void* stream);
+
 /* Scratch bytes coda_gemm_epilogue needs for these sizes and this op list
  * (row-reduction and keep-count partials, one per 128/256-column tile). */
 CODA_API coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi,

@@ -1,0 +1,86 @@
+"""coda_gemm_epilogue_noalloc: the entry point for callers that cannot allocate
+device memory when they call the library (for example a serving loop that fixes
+its memory footprint at start-up, since cudaMalloc can synchronise the device
+and has no latency bound).  It keeps its row-reduction and keep-count partials
+in the library's own fixed scratch buffer instead of a caller workspace.
+
+Checked here through the C ABI: two calls in a row, on different problems that
+both use the scratch buffer, each against the regular entry point (which gets a
+workspace from the caller), within the parity tolerance of the other GPU tests;
+and the refusal of a problem that needs more scratch than the buffer holds.
+This file is collected last so a stop-at-first-failure run has already run
+every other test; it also passes when run alone.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__ as entry
+from gemm_epilogue_transformer_tmem_gb300 import coda, inputs
+
+pytestmark = pytest.mark.gpu
+
+ATOL = 1e-2
+RTOL = 1e-2
+
+
+def _close(got, ref, what):
+    got = got.detach().to("cpu", torch.float64).numpy()
+    ref = ref.detach().to("cpu", torch.float64).numpy()
+    bad = np.abs(got - ref) > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), f"{what}: {bad.sum()} elements differ"
+
+
+def test_noalloc_matches_regular_entry_point_two_calls():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    entry.build()
+    dev = "cuda"
+
+    # call 1: dgrad form with two row reductions (partials in the scratch buffer)
+    M, K, N = 300, 128, 520
+    dY = inputs.randn_bf16((M, K), 1.0, 901).to(dev)
+    W = inputs.randn_bf16((N, K), 1.0 / math.sqrt(K), 902).to(dev)
+    Z = inputs.randn_bf16((M, N), 1.0, 903).to(dev)
+    Xh = inputs.randn_bf16((M, N), 1.0, 904).to(dev)
+    ops1 = [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)]
+    assert 0 < coda.workspace_size(M, N, K, ops1) <= coda.NOALLOC_SCRATCH_BYTES
+    out1 = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    st1 = torch.empty((2, M), dtype=torch.float32, device=dev)
+    coda.gemm_epilogue_noalloc(dY, W, ops1, out=out1, row_stats=st1, b_layout="nk", z=Z, xhat=Xh)
+
+    # call 2, right after: SwiGLU + dropout + a row sum on another shape, so the
+    # buffer now holds call 1's partials where call 2 writes its own
+    M2, K2, n_out = 257, 192, 264
+    X2 = inputs.randn_bf16((M2, K2), 1.0, 905).to(dev)
+    W2 = inputs.randn_bf16((K2, 2 * n_out), 1.0 / math.sqrt(K2), 906).to(dev)
+    ops2 = [("SWIGLU",), ("DROPOUT", 0, 0.1), ("ROW_SUM", 0)]
+    out2 = torch.empty((M2, n_out), dtype=torch.bfloat16, device=dev)
+    st2 = torch.empty((1, M2), dtype=torch.float32, device=dev)
+    kc2 = torch.empty((M2,), dtype=torch.int32, device=dev)
+    coda.gemm_epilogue_noalloc(X2, W2, ops2, out=out2, row_stats=st2, keep_count=kc2, seed=77)
+    torch.cuda.synchronize()
+    st, info = coda.check_device_error()
+    assert st == 0, info
+
+    ref1 = coda.gemm_epilogue(dY, W, ops1, b_layout="nk", z=Z, xhat=Xh)
+    ref2 = coda.gemm_epilogue(X2, W2, ops2, seed=77)
+    torch.cuda.synchronize()
+    _close(out1, ref1.D, "call 1 D")
+    _close(st1, ref1.row_stats, "call 1 row stats")
+    _close(out2, ref2.D, "call 2 D")
+    _close(st2, ref2.row_stats, "call 2 row sum")
+    assert torch.equal(kc2, ref2.keep_count)
+
+    # a problem needing more scratch than the buffer holds is refused up front
+    big_M = 70000
+    need = coda.workspace_size(big_M, 8192, 64, [("ROW_SUM", 0), ("ROW_SUMSQ", 1)])
+    assert need > coda.NOALLOC_SCRATCH_BYTES
+    e = coda.make_epilogue([("ROW_SUM", 0), ("ROW_SUMSQ", 1)])
+    a = coda.CodaAux()
+    status = coda.lib().coda_gemm_epilogue_noalloc(0x1000, 0x2000, big_M, 8192, 64, 0, ctypes.byref(e),
+                                                   ctypes.byref(a), 0x3000, 0x4000, None, None)
+    assert coda.STATUS[status] == "CODA_ERR_WORKSPACE"
