@@ -185,8 +185,15 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         if (!(op.f0 >= 0.0f && op.f0 < 1.0f)) return CODA_ERR_INVALID_ARG;
         c.prog.has_dropout = 1;
         const double keep = 1.0 - static_cast<double>(op.f0);
-        // T = floor((1-p) * 2^64) in fp64; p == 0 keeps everything (flagged by f0 == 0)
-        d.u = (op.f0 == 0.0f) ? ~0ull : static_cast<uint64_t>(std::ldexp(keep, 64));
+        // T = floor((1-p) * 2^64) in fp64.  Keep-all (p == 0, or T not below
+        // 2^64 for a tiny p) is flagged to the kernel by f0 == 0.
+        const double t = std::ldexp(keep, 64);
+        if (op.f0 == 0.0f || t >= 18446744073709551616.0) {
+          d.f0 = 0.0f;
+          d.u = ~0ull;
+        } else {
+          d.u = static_cast<uint64_t>(t);
+        }
         d.f1 = static_cast<float>(1.0 / keep);
         break;
       }

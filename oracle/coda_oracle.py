@@ -184,12 +184,16 @@ def splitmix64(seed: int, idx) -> np.ndarray:
 
 
 def dropout_threshold(p: float) -> int:
-    """T = floor((1-p) * 2^64) evaluated in fp64; None means keep everything."""
+    """T = floor((1-p) * 2^64) evaluated in fp64; None means keep everything
+    (p = 0, or p so small that (1-p) * 2^64 is not below 2^64)."""
     if not (0.0 <= p < 1.0):
         raise ValueError("dropout p must be in [0, 1)")
     if p == 0.0:
         return None
-    return int(math.ldexp(1.0 - p, 64))
+    t = math.ldexp(1.0 - p, 64)
+    if t >= 2.0 ** 64:
+        return None
+    return int(t)
 
 
 def dropout_mask(seed: int, M: int, N: int, p: float, row0: int = 0, rows=None) -> np.ndarray:
@@ -245,7 +249,8 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
               residual_t=None, z=None, xhat=None, norm_gamma=None, rows=None):
     """Evaluate D = f(A @ B) for an op list, one unfused pass per op.
 
-    ops: sequence of (name, slot, f0) tuples, names from OP_NAMES.
+    ops: sequence of (name, slot, f0) tuples, names from OP_NAMES; f0 is taken
+        as the float32 the op list carries (widened exactly to fp64).
     col_vecs / row_vecs: dict slot -> vector (bf16 values widened).
     residual_t, z, xhat: [M, N_out] aux tensors (or only the sampled rows).
     norm_gamma: if given, the op list must begin with RMS_ROWSCALE; the GEMM is
@@ -265,7 +270,8 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
     M = A.shape[0]
     if rows is None:
         rows = np.arange(M)
-    ops = [(o[0], o[1] if len(o) > 1 else 0, o[2] if len(o) > 2 else 0.0) for o in ops]
+    # op parameters are float32 in the op list; use exactly those values
+    ops = [(o[0], o[1] if len(o) > 1 else 0, float(np.float32(o[2])) if len(o) > 2 else 0.0) for o in ops]
 
     start = 0
     stats = {}

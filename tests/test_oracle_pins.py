@@ -325,3 +325,16 @@ def test_round_bf16_against_bit_patterns():
     x = np.random.default_rng(7).standard_normal(20000).astype(np.float32)
     expect = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
     np.testing.assert_array_equal(O.round_bf16(x.astype(np.float64)), expect)
+
+
+def test_dropout_threshold_float32_parameter():
+    # op-list parameters are float32: p = float32(0.1) widens exactly to fp64,
+    # 1 - p is exact in fp64, and the threshold is floor((1 - p) * 2^64)
+    from fractions import Fraction
+    p32 = float(np.float32(0.1))
+    assert O.dropout_threshold(p32) == int((1 - Fraction(p32)) * 2 ** 64)
+    assert O.dropout_threshold(p32) != O.dropout_threshold(0.1)
+    assert O.dropout_threshold(1e-30) is None          # (1-p) * 2^64 rounds to 2^64: keep all
+    out = O.run_chain(np.eye(3), np.ones((3, 3)), [("DROPOUT", 0, 0.1)], seed=1)
+    keep = O.dropout_mask(1, 3, 3, p32)
+    np.testing.assert_array_equal(out["keep"], keep)
