@@ -69,6 +69,7 @@ _SIGS = {
     "coda_launch_count": (ctypes.c_uint64, []),
     "coda_set_pipeline_timeout_ns": (None, [ctypes.c_uint64]),
     "coda_set_max_ctas": (None, [ctypes.c_int32]),
+    "coda_set_cta_pair": (None, [ctypes.c_int32]),
 }
 
 
@@ -293,3 +294,11 @@ def set_pipeline_timeout_ns(ns: int) -> None:
 
 def set_max_ctas(n: int) -> None:
     lib().coda_set_max_ctas(n)
+
+
+PAIR_MODES = {"auto": 0, "single": 1, "pair": 2}
+
+
+def set_cta_pair(mode: str) -> None:
+    """'auto' (CTA pairs when M > 128), 'single' (one-CTA kernel) or 'pair' (CTA pairs)."""
+    lib().coda_set_cta_pair(PAIR_MODES[mode])

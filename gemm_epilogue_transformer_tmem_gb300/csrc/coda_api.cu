@@ -23,6 +23,7 @@ namespace {
 std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_max_ctas{0};
+std::atomic<int> g_pair_mode{0};   // 0 auto, 1 single CTAs only, 2 CTA pairs whenever K > 0
 
 constexpr int kMaxDevices = 64;
 struct DevInfo {
@@ -241,20 +242,25 @@ struct Geometry {
   int64_t num_tiles;
 };
 
-Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu) {
+// tile_m: rows per tile (128 for one CTA, 256 for a CTA pair)
+Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu, int tile_m = BM) {
   Geometry g{};
   g.n_out = glu ? N / 2 : N;
   g.out_cols = glu ? BN / 2 : BN;
-  g.num_m_tiles = static_cast<int>((M + BM - 1) / BM);
+  g.num_m_tiles = static_cast<int>((M + tile_m - 1) / tile_m);
   g.num_n_tiles = static_cast<int>((g.n_out + g.out_cols - 1) / g.out_cols);
   g.num_kb = static_cast<int>((K + BK - 1) / BK);
   g.num_tiles = static_cast<int64_t>(g.num_m_tiles) * g.num_n_tiles;
   return g;
 }
 
+// Workspace layout: row-reduction partials [n_red][column tiles][M] fp32, then
+// keep-count partials [column tiles][M] u32, then the commuted-norm row scales
+// [M] fp32 (written by the pre-pass kernel for CTA-pair tiles).
 size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
   size_t b = static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * static_cast<size_t>(M) * sizeof(float);
   if (c.prog.has_dropout) b += static_cast<size_t>(g.num_n_tiles) * static_cast<size_t>(M) * sizeof(uint32_t);
+  if (c.has_rms) b += static_cast<size_t>(M) * sizeof(float);
   return b;
 }
 
@@ -308,7 +314,10 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   if (c.needs_row_stats && row_stats == nullptr) return CODA_ERR_INVALID_ARG;
   if (row_stats && !aligned4(row_stats)) return CODA_ERR_ALIGNMENT;
   if (row_keep_count && !aligned4(row_keep_count)) return CODA_ERR_ALIGNMENT;
-  const Geometry g = geometry(M, N, K, c.glu);
+  // CTA pairs (cta_group::2, 256-row tiles) once there are at least two row blocks
+  const int pair_mode = g_pair_mode.load();
+  const bool pair = K > 0 && (pair_mode == 2 || (pair_mode == 0 && M > BM));
+  const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM);
   if (g.num_tiles > (int64_t{1} << 31) - 1) return CODA_ERR_UNSUPPORTED;
   const size_t ws_need = workspace_bytes_for(M, g, c);
   if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
@@ -367,35 +376,58 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   p.inv_K = K > 0 ? static_cast<float>(1.0 / static_cast<double>(K)) : 0.0f;
   p.timeout_ns = g_timeout_ns.load();
   p.row_stats = row_stats;
+  float* rms_ws = nullptr;
   if (ws_need > 0) {
     p.ws_red = static_cast<float*>(workspace);
-    if (c.prog.has_dropout && row_keep_count != nullptr)
-      p.ws_keep = reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) +
-                                              static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * M);
+    uint32_t* keep_ws = reinterpret_cast<uint32_t*>(static_cast<float*>(workspace) +
+                                                    static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * M);
+    if (c.prog.has_dropout && row_keep_count != nullptr) p.ws_keep = keep_ws;
+    rms_ws = reinterpret_cast<float*>(keep_ws + (c.prog.has_dropout ? static_cast<size_t>(g.num_n_tiles) * M : 0));
   }
   p.epi_warp_bytes = static_cast<uint32_t>(2 * kBoxBytes + c.n_aux * 2 * kBoxBytes);
   const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * p.epi_warp_bytes;
   const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
   const size_t fixed = 1024 + epi_bytes + ctl_bytes;
-  if (static_cast<size_t>(dev.max_smem) < fixed + 2 * kStageBytes) return CODA_ERR_UNSUPPORTED;
-  int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) / kStageBytes);
+  const size_t stage_bytes = pair ? kPairStageBytes : kStageBytes;
+  if (static_cast<size_t>(dev.max_smem) < fixed + 2 * stage_bytes) return CODA_ERR_UNSUPPORTED;
+  int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
   p.stages = stages;
-  p.smem_epi_off = static_cast<uint32_t>(stages * kStageBytes);
-  p.smem_ctl_off = static_cast<uint32_t>(stages * kStageBytes + epi_bytes);
+  p.smem_epi_off = static_cast<uint32_t>(stages * stage_bytes);
+  p.smem_ctl_off = static_cast<uint32_t>(stages * stage_bytes + epi_bytes);
   p.err = dev.err;
   p.prog = c.prog;
-  const size_t smem = fixed + static_cast<size_t>(stages) * kStageBytes;
-
-  int grid = dev.sms;
-  const int cap = g_max_ctas.load();
-  if (cap > 0 && cap < grid) grid = cap;
-  if (g.num_tiles < grid) grid = static_cast<int>(g.num_tiles);
+  const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool mn = b_layout == CODA_B_KN;
-  cudaError_t e = c.glu ? launch_gemm_glu(mn, c.has_rms, maps, p, grid, smem, st)
-                        : launch_gemm_plain(mn, c.has_rms, maps, p, grid, smem, st);
+  const int cap = g_max_ctas.load();
+  int grid = dev.sms;
+  if (cap > 0 && cap < grid) grid = cap;
+  cudaError_t e;
+  // CTA pairs take the commuted-norm row scales from a pre-pass kernel (their A
+  // halves signal the pair leader's barrier, so no row-statistics warps)
+  const bool rowstat_warps = c.has_rms && !pair;
+  if (pair && c.has_rms) {
+    e = launch_rms_rowscale(A, M, K, p.inv_K, c.rms_eps, rms_ws,
+                            c.rms_slot >= 0 ? row_stats + static_cast<size_t>(c.rms_slot) * M : nullptr, dev.sms, st);
+    if (e != cudaSuccess) return CODA_ERR_CUDA;
+    g_launches.fetch_add(1);
+    p.rms_vec = rms_ws;
+  }
+  if (pair) {
+    int pairs = 0;
+    e = c.glu ? max_pairs_glu(mn, rowstat_warps, smem, &pairs) : max_pairs_plain(mn, rowstat_warps, smem, &pairs);
+    if (e != cudaSuccess) return CODA_ERR_CUDA;
+    if (pairs < 1) return CODA_ERR_UNSUPPORTED;
+    if (pairs > grid / 2) pairs = grid / 2 > 0 ? grid / 2 : 1;
+    if (g.num_tiles < pairs) pairs = static_cast<int>(g.num_tiles);
+    grid = 2 * pairs;
+  } else if (g.num_tiles < grid) {
+    grid = static_cast<int>(g.num_tiles);
+  }
+  e = c.glu ? launch_gemm_glu(mn, rowstat_warps, pair, maps, p, grid, smem, st)
+            : launch_gemm_plain(mn, rowstat_warps, pair, maps, p, grid, smem, st);
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
   const bool need_keep = c.prog.has_dropout && row_keep_count != nullptr;
@@ -500,5 +532,7 @@ uint64_t coda_launch_count(void) { return g_launches.load(); }
 void coda_set_pipeline_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 1000000000ull : ns); }
 
 void coda_set_max_ctas(int32_t n) { g_max_ctas.store(n < 0 ? 0 : n); }
+
+void coda_set_cta_pair(int32_t mode) { g_pair_mode.store(mode < 0 || mode > 2 ? 0 : mode); }
 
 }  // extern "C"

@@ -7,7 +7,9 @@
 // gathered as per-row partial sums over the K tiles and applied after the
 // projection.
 //
-// GB300 design: one persistent CTA per SM, warp-specialised:
+// GB300 design: one persistent CTA per SM, or a cluster of two CTAs sharing a
+// tcgen05 cta_group::2 MMA on a 256-row tile (each CTA stages half of B);
+// warp-specialised:
 //   warp 0      TMA producer: A [128 x 64] and B [256 x 64] bf16 tiles into a
 //               ring of 128-byte-swizzled shared-memory stages
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=256, K=16) into one of two
@@ -18,8 +20,10 @@
 //               into swizzled staging and TMA-stores it; aux tiles (residual,
 //               Z, Xhat) arrive by TMA one chunk ahead.  While they work on
 //               tile i, the MMA warp already fills the other accumulator.
-//   warps 8-11  (commuted RMSNorm only) read every A stage from shared memory
-//               and accumulate sum_k x^2 for their row, then r = rsqrt(s/K+eps)
+//   warps 8-11  (commuted RMSNorm, single CTA) read every A stage from shared
+//               memory and accumulate sum_k x^2 for their row, then
+//               r = rsqrt(s/K+eps).  A CTA pair takes r from a pre-pass kernel
+//               that overlaps the pair's mainloop (programmatic dependent launch).
 // Every mbarrier wait is bounded: on expiry the kernel records a timeout in the
 // device error word, lets in-flight copies land, frees tensor memory and exits.
 #pragma once
@@ -75,6 +79,18 @@ struct Waiter {
   }
 };
 
+// Warp-wide wait: lane 0 alone polls the barrier (32 lanes spinning on one
+// mbarrier serialise in shared memory and steal bandwidth from the MMA's
+// operand reads), then the outcome is broadcast and __syncwarp orders the other
+// lanes' subsequent reads after lane 0's acquire.
+__device__ __forceinline__ bool warp_wait(const Waiter& W, uint64_t* bar, uint32_t parity, uint32_t tile, int lane) {
+  int ok = 1;
+  if (lane == 0) ok = W(bar, parity, tile) ? 1 : 0;
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
 // Aux values of one 32-row x 32-column box staged with the 64-byte swizzle:
 // 16-byte chunk c of row r sits at r*64 + ((c ^ ((r >> 1) & 3)) * 16).
 struct SmemAux {
@@ -91,12 +107,19 @@ struct SmemAux {
   }
 };
 
-template <bool kGLU, bool kBMN, bool kRowStats>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair>
 __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
                               const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
                               const __grid_constant__ GemmParams p) {
+  // Per-CTA tile geometry.  A CTA pair shares one 256-row tile: rank r of the
+  // pair owns rows r*128 .. r*128+127 of it and stages half of B.
+  constexpr int kTileM = kPair ? 2 * BM : BM;
+  constexpr int kStageB = kPair ? kPairStageBBytes : kStageBBytes;
+  // bytes the leader's full barrier expects per stage (both CTAs' loads for a pair)
+  constexpr uint32_t kExpectTx = kPair ? 2u * kPairStageBytes : static_cast<uint32_t>(kStageBytes);
+
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -105,15 +128,20 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   uint8_t* sB = smem + p.stages * kStageABytes;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0u;
+  const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&ctl->full[s], 1);
-      mbar_init(&ctl->empty[s], 1 + (kRowStats ? 128 : 0));
+      // a stage is free once the MMA commit and the four row-statistics warps arrived
+      mbar_init(&ctl->empty[s], 1 + (kRowStats ? 4 : 0));
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], 128);
+      mbar_init(&ctl->tempty[a], kPair ? 256 : 128);
       mbar_init(&ctl->rsfull[a], 128);
       mbar_init(&ctl->rsempty[a], 128);
     }
@@ -129,11 +157,17 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     tma_prefetch_desc(&tmD);
   }
   if (warp == 2) {
-    tmem_alloc(&ctl->tmem_base, kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(&ctl->tmem_base, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&ctl->tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
 
@@ -145,33 +179,55 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step) {
         const int m_tile = tile % p.num_m_tiles;
         const int n_tile = tile / p.num_m_tiles;
-        const int m0 = m_tile * BM;
-        const int nb0 = kGLU ? n_tile * (BN / 2) : n_tile * BN;
-        const int nb1 = kGLU ? p.half + n_tile * (BN / 2) : nb0 + BN / 2;
+        const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
+        // B columns (N index) of this tile held by this CTA: for SwiGLU the G
+        // half and the U half of the same output columns
+        int nb0, nb1;
+        if constexpr (kPair) {
+          nb0 = kGLU ? (rank == 0u ? n_tile * (BN / 2) : p.half + n_tile * (BN / 2))
+                     : n_tile * BN + static_cast<int>(rank) * (BN / 2);
+          nb1 = nb0;
+        } else {
+          nb0 = kGLU ? n_tile * (BN / 2) : n_tile * BN;
+          nb1 = kGLU ? p.half + n_tile * (BN / 2) : nb0 + BN / 2;
+        }
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!W(&ctl->empty[stage], phase ^ 1u, tile)) {
             ok = false;
             break;
           }
           uint64_t* fb = &ctl->full[stage];
-          mbar_arrive_expect_tx(fb, kStageBytes);
-          armed |= 1u << stage;
-          armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          if (leader) {
+            mbar_arrive_expect_tx(fb, kExpectTx);
+            armed |= 1u << stage;
+            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          }
           const int k0 = kb * BK;
           uint8_t* a_dst = sA + stage * kStageABytes;
-          uint8_t* b_dst = sB + stage * kStageBBytes;
-          tma_load_2d(a_dst, &tmA, fb, k0, m0);
-          if (kBMN) {
-            tma_load_2d(b_dst, &tmB, fb, nb0, k0);
-            tma_load_2d(b_dst + 8192, &tmB, fb, nb0 + 64, k0);
-            tma_load_2d(b_dst + 16384, &tmB, fb, nb1, k0);
-            tma_load_2d(b_dst + 24576, &tmB, fb, nb1 + 64, k0);
+          uint8_t* b_dst = sB + stage * kStageB;
+          if constexpr (kPair) {
+            const uint32_t fbc = mapa_shared(smem_u32(fb), 0u);   // the leader's barrier
+            tma_load_2d_pair(a_dst, &tmA, fbc, k0, m0);
+            if (kBMN) {
+              tma_load_2d_pair(b_dst, &tmB, fbc, nb0, k0);
+              tma_load_2d_pair(b_dst + 8192, &tmB, fbc, nb0 + 64, k0);
+            } else {
+              tma_load_2d_pair(b_dst, &tmB, fbc, k0, nb0);
+            }
           } else {
-            tma_load_2d(b_dst, &tmB, fb, k0, nb0);
-            tma_load_2d(b_dst + 16384, &tmB, fb, k0, nb1);
+            tma_load_2d(a_dst, &tmA, fb, k0, m0);
+            if (kBMN) {
+              tma_load_2d(b_dst, &tmB, fb, nb0, k0);
+              tma_load_2d(b_dst + 8192, &tmB, fb, nb0 + 64, k0);
+              tma_load_2d(b_dst + 16384, &tmB, fb, nb1, k0);
+              tma_load_2d(b_dst + 24576, &tmB, fb, nb1 + 64, k0);
+            } else {
+              tma_load_2d(b_dst, &tmB, fb, k0, nb0);
+              tma_load_2d(b_dst + 16384, &tmB, fb, k0, nb1);
+            }
           }
           if (++stage == p.stages) {
             stage = 0;
@@ -180,20 +236,26 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         }
       }
       if (!ok) {
+        // give copies already issued a bounded time to land before the CTA exits
         for (int s = 0; s < p.stages; ++s)
           if (armed & (1u << s)) wait_drain(&ctl->full[s], (armed_phase >> s) & 1u, 2000000ull);
+        if (kPair) {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
-      constexpr uint32_t idesc = make_idesc_bf16(BM, BN, kBMN);
+      constexpr uint32_t idesc = make_idesc_bf16(kTileM, BN, kBMN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!W(&ctl->tempty[acc], acc_phase ^ 1u, tile)) {
@@ -209,25 +271,37 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kStageBBytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kStageB);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, 1024);
             const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
                                      : make_smem_desc(b_addr + k * 32, 16, 1024);
-            mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            if constexpr (kPair)
+              mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            else
+              mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
-          mma_commit(&ctl->empty[stage]);
+          if constexpr (kPair)
+            mma_commit_pair_mc(&ctl->empty[stage], 0x3);
+          else
+            mma_commit(&ctl->empty[stage]);
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&ctl->tfull[acc]);
+        if constexpr (kPair)
+          mma_commit_pair_mc(&ctl->tfull[acc], 0x3);
+        else
+          mma_commit(&ctl->tfull[acc]);
       }
       // no MMA may still write tensor memory when it is freed
-      mma_commit(&ctl->drain);
+      if constexpr (kPair)
+        mma_commit_pair(&ctl->drain);
+      else
+        mma_commit(&ctl->drain);
       wait_drain(&ctl->drain, 0u, 2000000ull);
     }
   } else if (warp >= 4 && warp < 4 + kEpiWarps) {
@@ -259,10 +333,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       aux_armed |= 1u << b;
     };
 
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = tile0; tile < p.num_tiles; tile += tile_step, ++local) {
       const int m_tile = tile % p.num_m_tiles;
       const int n_tile = tile / p.num_m_tiles;
-      const int m0 = m_tile * BM;
+      const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
       const int row = m0 + r_in_tile;
       const bool row_ok = row < p.M;
       const int col_base = n_tile * kOutCols;
@@ -272,21 +346,26 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       const uint32_t acc_phase = (local >> 1) & 1;
       if (n_aux > 0) issue_aux(abuf, col_base, m0 + q * 32);
 
-      bool okw = W(&ctl->tfull[acc], acc_phase, tile);
-      if (!__all_sync(0xFFFFFFFFu, okw)) {
+      bool okw = warp_wait(W, &ctl->tfull[acc], acc_phase, tile, lane);
+      if (!okw) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
       float r_rms = 1.0f;
       if (kRowStats) {
-        okw = W(&ctl->rsfull[acc], acc_phase, tile);
-        if (!__all_sync(0xFFFFFFFFu, okw)) {
+        okw = warp_wait(W, &ctl->rsfull[acc], acc_phase, tile, lane);
+        if (!okw) {
           ok = false;
           break;
         }
         r_rms = ctl->rs[acc][r_in_tile];
         mbar_arrive(&ctl->rsempty[acc]);
+      } else if (p.rms_vec != nullptr) {
+        // row scales from the pre-pass kernel, which may still have been running
+        // when this grid started: wait for it before the first read
+        if (local == 0) griddep_wait();
+        r_rms = row_ok ? p.rms_vec[row] : 1.0f;
       }
 
       float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -296,8 +375,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         const int col = col_base + c * kChunk;
         if (n_aux > 0) {
           if (c + 1 < nch) issue_aux(abuf ^ 1, col + kChunk, m0 + q * 32);
-          okw = W(&ctl->auxfull[q][abuf], (aux_phase >> abuf) & 1u, tile);
-          if (!__all_sync(0xFFFFFFFFu, okw)) {
+          okw = warp_wait(W, &ctl->auxfull[q][abuf], (aux_phase >> abuf) & 1u, tile, lane);
+          if (!okw) {
             ok = false;
             break;
           }
@@ -316,8 +395,12 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           }
         }
         if (c == nch - 1) {
+          // accumulator drained: release it to the MMA warp (the leader's barrier)
           tc_fence_before_sync();
-          mbar_arrive(&ctl->tempty[acc]);
+          if constexpr (kPair)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0u));
+          else
+            mbar_arrive(&ctl->tempty[acc]);
         }
         int nvalid = p.N_out - col;
         if (nvalid > kChunk) nvalid = kChunk;
@@ -367,6 +450,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     __syncwarp();
   } else if (kRowStats && warp >= 8) {
     // ------------------------------------ row statistics (commuted RMSNorm)
+    // Each A stage is read alongside the MMA as soon as it is in shared memory;
+    // one arrival per warp frees the stage.  (CTA pairs get their row scales
+    // from a pre-pass kernel instead: there the A halves signal the leader's
+    // barrier, not their own CTA's.)
     const int q = warp - 8;
     const int r = q * 32 + lane;
     const Waiter W{ctl, p.timeout_ns, p.err, ROLE_ROWSTATS};
@@ -374,11 +461,11 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     uint32_t phase = 0;
     int local = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step, ++local) {
       float s = 0.0f;
       for (int kb = 0; kb < p.num_kb; ++kb) {
-        const bool okw = W(&ctl->full[stage], phase, tile);
-        if (!__all_sync(0xFFFFFFFFu, okw)) {
+        const bool okw = warp_wait(W, &ctl->full[stage], phase, tile, lane);
+        if (!okw) {
           ok = false;
           break;
         }
@@ -393,7 +480,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
 #pragma unroll
           for (int e = 0; e < 8; ++e) s = fmaf(x[e], x[e], s);
         }
-        mbar_arrive(&ctl->empty[stage]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->empty[stage]);
         if (++stage == p.stages) {
           stage = 0;
           phase ^= 1u;
@@ -402,8 +490,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       if (!ok) break;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      const bool okw = W(&ctl->rsempty[acc], acc_phase ^ 1u, tile);
-      if (!__all_sync(0xFFFFFFFFu, okw)) break;
+      const bool okw = warp_wait(W, &ctl->rsempty[acc], acc_phase ^ 1u, tile, lane);
+      if (!okw) break;
       ctl->rs[acc][r] = rsqrtf(fmaf(s, p.inv_K, p.rms_eps));
       mbar_arrive(&ctl->rsfull[acc]);
     }
@@ -411,19 +499,62 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // neither CTA leaves while its peer may still signal it
   if (warp == 2) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <bool kGLU, bool kBMN, bool kRowStats>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair>
 cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
-  return cudaGetLastError();
+  if constexpr (!kPair) {
+    kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return cudaGetLastError();
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kRowStats ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    // after a row-scale pre-pass: start the mainloop early, the epilogue waits
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.rms_vec != nullptr ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+  }
+}
+
+// Largest number of CTA pairs of this kernel that can be resident at once.
+template <bool kGLU, bool kBMN, bool kRowStats>
+cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kRowStats ? 384 : 256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(pairs, kern, &cfg);
 }
 
 }  // namespace coda

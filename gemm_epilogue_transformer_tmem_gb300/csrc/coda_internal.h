@@ -23,6 +23,10 @@ constexpr int kChunk = 32;         // epilogue columns per TMEM load / TMA store
 constexpr int kStageABytes = BM * BK * 2;          // 16 KB
 constexpr int kStageBBytes = BN * BK * 2;          // 32 KB
 constexpr int kStageBytes = kStageABytes + kStageBBytes;
+// CTA pair (cta_group::2): a 256 x 256 tile; each CTA stages its 128 rows of A
+// and half (128 columns) of B
+constexpr int kPairStageBBytes = (BN / 2) * BK * 2;  // 16 KB
+constexpr int kPairStageBytes = kStageABytes + kPairStageBBytes;
 constexpr int kBoxBytes = 32 * kChunk * 2;         // 32 rows x 32 bf16 = 2 KB
 constexpr int kMaxStages = 8;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
@@ -79,6 +83,7 @@ struct GemmParams {
   uint32_t smem_ctl_off;   // offset of the control block
   uint32_t epi_warp_bytes; // staging bytes per epilogue warp
   uint32_t* err;           // device error word (4 x u32)
+  const float* rms_vec;    // commuted RMSNorm row scales from the pre-pass kernel, or null
   EpiProgram prog;
 };
 

@@ -8,6 +8,7 @@
 #include "coda_internal.h"
 #include "coda_launch.h"
 #include "coda_ops.cuh"
+#include "coda_ptx.cuh"
 
 namespace coda {
 
@@ -41,6 +42,70 @@ cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M,
   const int blocks = (M + threads - 1) / threads;
   finalize_rows_kernel<<<blocks, threads, 0, st>>>(ws_red, ws_keep, M, num_n_tiles, n_red, info, inv_width,
                                                    row_stats, keep_count);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- commuted-norm row scales
+// r_i = rsqrt(sum_k a_ik^2 / K + eps) for every row of A: the row-statistics
+// side path for CTA-pair tiles, run just before the GEMM (a warp per row,
+// grid-stride).  For a small A it runs as one 4-warp block per SM, so that the
+// GEMM's CTA fits beside it and starts its mainloop while this finishes
+// (programmatic dependent launch; only the GEMM's epilogue waits for it).  For
+// a large A, whose pass would outlast the GEMM's first tiles, it runs as a full
+// grid at full memory bandwidth instead.  K % 8 == 0.
+__global__ void __launch_bounds__(256) rms_rowscale_kernel(const uint16_t* __restrict__ A, int64_t M, int64_t K,
+                                                           float inv_K, float eps, float* __restrict__ r,
+                                                           float* __restrict__ r_copy) {
+  griddep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t n8 = K >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); row < M;
+       row += stride) {
+    const uint4* ar = reinterpret_cast<const uint4*>(A + row * K);
+    float ss = 0.0f;
+    int64_t i = lane;
+    for (; i + 224 < n8; i += 256) {   // eight independent 16-byte loads in flight per lane
+      uint4 q[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) q[u] = __ldg(ar + i + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        float x[8];
+        unpack8(q[u], x);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+      }
+    }
+    for (; i < n8; i += 32) {
+      float x[8];
+      unpack8(__ldg(ar + i), x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if (lane == 0) {
+      const float v = rsqrtf(fmaf(ss, inv_K, eps));
+      r[row] = v;
+      if (r_copy != nullptr) r_copy[row] = v;
+    }
+  }
+}
+
+cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, float* r, float* r_copy,
+                                int num_sms, cudaStream_t st) {
+  // keep the SM configured for maximum shared memory so the GEMM's CTA can
+  // start beside this kernel's blocks instead of waiting for the SM to drain
+  cudaError_t e = cudaFuncSetAttribute(rms_rowscale_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  const bool overlap = M * K * 2 <= (int64_t{48} << 20);
+  const int threads = overlap ? 128 : 256;
+  int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
+  if (overlap && blocks > num_sms) blocks = num_sms;
+  rms_rowscale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(static_cast<const uint16_t*>(A), M, K,
+                                                                          inv_K, eps, r, r_copy);
   return cudaGetLastError();
 }
 

@@ -9,14 +9,20 @@
 namespace coda {
 
 // fused GEMM + epilogue; maps = {A, B, D, aux0, aux1, aux2}
-cudaError_t launch_gemm_glu(bool b_mn_major, bool row_stats, const CUtensorMap* maps, const GemmParams& p,
+// pair: cta_group::2 on clusters of two CTAs (grid counts CTAs and is even)
+cudaError_t launch_gemm_glu(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps, const GemmParams& p,
                             int grid, size_t smem, cudaStream_t st);
-cudaError_t launch_gemm_plain(bool b_mn_major, bool row_stats, const CUtensorMap* maps, const GemmParams& p,
-                              int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_plain(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                              const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+// how many CTA pairs of the pair kernel fit on the device at once
+cudaError_t max_pairs_glu(bool b_mn_major, bool row_stats, size_t smem, int* pairs);
+cudaError_t max_pairs_plain(bool b_mn_major, bool row_stats, size_t smem, int* pairs);
 
 cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
                             const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
                             cudaStream_t st);
+cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, float* r, float* r_copy,
+                                int num_sms, cudaStream_t st);
 cudaError_t launch_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, bool kn,
                               int num_sms, cudaStream_t st);
 cudaError_t launch_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps, void* Xn,

@@ -268,10 +268,14 @@ CODA_API uint64_t coda_launch_count(void);
  * Tuning knobs, for measurement.  coda_set_pipeline_timeout_ns sets how long a
  * device-side pipeline wait may spin before the kernel records CODA_ERR_TIMEOUT
  * and exits (default 1e9 ns; 0 restores the default).  coda_set_max_ctas caps
- * the persistent grid (0 = one CTA per SM).
+ * the persistent grid (0 = one CTA per SM).  coda_set_cta_pair selects between
+ * the single-CTA kernel and the CTA-pair kernel.
  */
 CODA_API void coda_set_pipeline_timeout_ns(uint64_t ns);
 CODA_API void coda_set_max_ctas(int32_t n);
+/* 0 (default): CTA pairs (tcgen05 cta_group::2 on 256-row tiles, two SMs per
+ * tile) when M > 128; 1: single-CTA 128-row tiles only; 2: CTA pairs whenever K > 0. */
+CODA_API void coda_set_cta_pair(int32_t mode);
 
 #ifdef __cplusplus
 }

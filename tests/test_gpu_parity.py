@@ -36,6 +36,15 @@ def _built():
     assert st == 0, f"device error word set: {info}"
 
 
+@pytest.fixture(params=["single", "pair"])
+def mode(request):
+    """Run a test on the single-CTA kernel (128-row tiles) and on the CTA-pair
+    kernel (tcgen05 cta_group::2, 256-row tiles)."""
+    coda.set_cta_pair(request.param)
+    yield request.param
+    coda.set_cta_pair("auto")
+
+
 def cu(t):
     return t.to("cuda")
 
@@ -95,7 +104,7 @@ def rand(shape, seed, std=1.0):
 
 # --------------------------------------------------------------- plain GEMM
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-def test_small_integer_gemm_bit_exact(layout):
+def test_small_integer_gemm_bit_exact(layout, mode):
     # |values| <= 2 and K = 64: every partial sum is an integer below 2^8, so
     # fp32 accumulation and the bf16 store are exact
     M, K, N = 200, 64, 264
@@ -110,7 +119,7 @@ def test_small_integer_gemm_bit_exact(layout):
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,K,N", [(128, 64, 256), (1, 8, 8), (300, 200, 264), (257, 1000, 520),
                                    (129, 4096, 264), (640, 136, 1032)])
-def test_plain_gemm(layout, M, K, N):
+def test_plain_gemm(layout, M, K, N, mode):
     A = rand((M, K), 10 + M)
     B = rand((K, N) if layout == "kn" else (N, K), 20 + N, 1.0 / math.sqrt(K))
     r = coda.gemm_epilogue(cu(A), cu(B), [], b_layout=layout)
@@ -130,7 +139,7 @@ def test_k_zero_is_empty_sum():
     assert_close(f64(r.D), ref, "K = 0")
 
 
-def test_pr1_bias_gelu_residual():
+def test_pr1_bias_gelu_residual(mode):
     t = inputs.make_pr1(seed=0)
     ops = [("BIAS", 0), ("GELU_TANH",), ("RESIDUAL", 0, 1.0)]
     r = coda.gemm_epilogue(cu(t["X"]), cu(t["W"]), ops, col_vecs={0: cu(t["bias"])}, residual=cu(t["residual"]))
@@ -183,7 +192,7 @@ def _op_case_tensors(ops, layout, seed):
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("case", sorted(OP_CASES))
-def test_op(case, layout):
+def test_op(case, layout, mode):
     ops = OP_CASES[case]
     A, B, N, n_out, col, row, aux = _op_case_tensors(ops, layout, 100 + len(case))
     preact = None
@@ -207,7 +216,7 @@ def test_op(case, layout):
 # ------------------------------------------------------------------ dropout
 @pytest.mark.parametrize("seed", [0, 12345])
 @pytest.mark.parametrize("glu", [False, True])
-def test_dropout_mask_bit_exact(glu, seed):
+def test_dropout_mask_bit_exact(glu, seed, mode):
     # pre-dropout value = bias[j] != 0 exactly (SCALE 0 kills the GEMM), so the
     # mask is read off D without ambiguity
     M, K = 333, 64
@@ -232,7 +241,7 @@ def test_dropout_mask_bit_exact(glu, seed):
     assert_close(f64(r.D), ref["D"], "dropout values")
 
 
-def test_dropout_p_zero_keeps_all():
+def test_dropout_p_zero_keeps_all(mode):
     M, K, N = 130, 64, 256
     A = rand((M, K), 1)
     B = rand((K, N), 2, 0.125)
@@ -259,7 +268,7 @@ def test_fold_gamma_bit_exact(layout):
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("M,K,N", [(300, 192, 264), (128, 2048, 512)])
-def test_commuted_rmsnorm(layout, M, K, N):
+def test_commuted_rmsnorm(layout, M, K, N, mode):
     X = rand((M, K), 41)
     g = inputs.uniform_bf16((K,), 0.5, 1.5, 42)
     W = rand((K, N) if layout == "kn" else (N, K), 43, 1.0 / math.sqrt(K))
@@ -273,7 +282,7 @@ def test_commuted_rmsnorm(layout, M, K, N):
 
 
 @pytest.mark.parametrize("exact_gamma", [False, True])
-def test_commuted_rmsnorm_then_swiglu(exact_gamma):
+def test_commuted_rmsnorm_then_swiglu(exact_gamma, mode):
     # r_i applies to both halves before the nonlinearity: silu(r G) * (r U).
     # With gamma in {1/2, 1, 2} the fold gamma*W is exact in bf16, so the GPU
     # and the oracle see the same weights and the row sum gets the strict bound.
@@ -299,7 +308,7 @@ def test_commuted_rmsnorm_then_swiglu(exact_gamma):
 
 
 # --------------------------------------------------------------------- dgrad
-def test_dgrad_small():
+def test_dgrad_small(mode):
     M, K, N = 300, 128, 520
     dY = rand((M, K), 61)
     W = rand((N, K), 62, 1.0 / math.sqrt(K))

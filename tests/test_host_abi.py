@@ -65,12 +65,14 @@ def _ws(L, M, N, K, ops):
 
 
 def test_workspace_size_closed_form(L):
-    # one fp32 partial per (reduction, 256-column tile, row); 128-column tiles with SWIGLU
+    # one fp32 partial per (reduction, 256-column tile, row); 128-column tiles with SWIGLU;
+    # one fp32 row scale per row with RMS_ROWSCALE
     assert _ws(L, 1000, 1024, 64, []) == (OK, 0)
     assert _ws(L, 1000, 1024, 64, [("ROW_SUM", 0)]) == (OK, 4 * 4 * 1000)
     assert _ws(L, 1000, 1032, 64, [("ROW_SUM", 0), ("ROW_SUMSQ", 1)]) == (OK, 2 * 5 * 4 * 1000)
     assert _ws(L, 8, 2 * 264, 64, [("SWIGLU",), ("DROPOUT", 0, 0.1)]) == (OK, 3 * 8 * 4)
-    assert _ws(L, 8, 64, 64, [("RMS_ROWSCALE", 0, 1e-6)]) == (OK, 0)
+    assert _ws(L, 8, 64, 64, [("RMS_ROWSCALE", 0, 1e-6)]) == (OK, 8 * 4)       # row scales [M]
+    assert _ws(L, 8, 64, 64, [("RMS_ROWSCALE", 0, 1e-6), ("ROW_SUM", 1)]) == (OK, 8 * 4 + 8 * 4)
 
 
 @pytest.mark.parametrize("ops,why", [
