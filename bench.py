@@ -137,14 +137,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timing
-def timed_loop(calls, steps, warmup, flush, stream):
-    """Run `steps` steps; returns (per-call total ms list, total ms).  Every call
-    is bracketed by events on `stream`; the L2 flush runs outside them."""
+def timed_loop(calls, steps, warmup, flush, stream, counter=None):
+    """Run `steps` steps; returns (per-call total ms list, total ms, kernels the
+    library launched during the timed steps per `counter`, or None).  Every
+    call is bracketed by events on `stream`; the L2 flush runs outside them."""
     for _ in range(warmup):
         flush()
         for c in calls:
             c()
     torch.cuda.synchronize()
+    count0 = counter() if counter else None
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
            for _ in range(steps)]
     for i in range(steps):
@@ -154,11 +156,12 @@ def timed_loop(calls, steps, warmup, flush, stream):
             c()
             evs[i][j][1].record(stream)
     torch.cuda.synchronize()
+    launched = (counter() - count0) if counter else None
     per_call = [0.0] * len(calls)
     for i in range(steps):
         for j in range(len(calls)):
             per_call[j] += evs[i][j][0].elapsed_time(evs[i][j][1])
-    return per_call, sum(per_call)
+    return per_call, sum(per_call), launched
 
 
 def fused_calls(step):
@@ -272,9 +275,7 @@ def main():
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    launches0 = coda.launch_count()
-    per_call, total_ms = timed_loop([step.fused], steps, warmup, flush, stream)
-    launches = coda.launch_count() - launches0 - warmup * step.kernels_per_fused
+    per_call, total_ms, launches = timed_loop([step.fused], steps, warmup, flush, stream, coda.launch_count)
     clocks = sampler.stop() if sampler else None
     st, info = coda.check_device_error()
     if st != 0:
@@ -288,10 +289,11 @@ def main():
     # ---- unfused chain through the library's own kernels
     unfused = None
     if not args.no_unfused:
-        _, u_total = timed_loop([step.unfused], max(steps // 2, 3), warmup, flush, stream)
-        u_ms = u_total / max(steps // 2, 3)
+        u_steps = max(steps // 2, 3)
+        _, u_total, u_launched = timed_loop([step.unfused], u_steps, warmup, flush, stream, coda.launch_count)
+        u_ms = u_total / u_steps
         unfused = {"ms_per_step": round(u_ms, 5), "value": round(step.flops / (u_ms * 1e-3) / 1e12, 2),
-                   "unit": UNIT, "kernels_per_step": step.kernels_per_unfused,
+                   "unit": UNIT, "kernels_per_step": u_launched / u_steps,
                    "speedup_fused": round(u_ms / ms, 3)}
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
@@ -309,7 +311,7 @@ def main():
             for k, v in hout.items():
                 v.copy_(step.host_outputs[k], non_blocking=True)
 
-        _, e_total = timed_loop([e2e_call], e2e_steps, 2, flush, stream)
+        _, e_total, _ = timed_loop([e2e_call], e2e_steps, 3, flush, stream)
         e_ms = e_total / e2e_steps
         e2e = {"value": round(step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e_ms, 5),

@@ -367,6 +367,14 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   p.N_out = static_cast<int32_t>(g.n_out);
   p.half = c.glu ? static_cast<int32_t>(N / 2) : 0;
   p.num_m_tiles = g.num_m_tiles;
+  {
+    // rasterization group: about 48 MB of A rows kept hot in the 129 MB L2
+    const int64_t block_bytes = static_cast<int64_t>(pair ? 2 * BM : BM) * (K > 0 ? K : 1) * 2;
+    int64_t gm = (int64_t{48} << 20) / block_bytes;
+    if (gm < 1) gm = 1;
+    if (gm > g.num_m_tiles) gm = g.num_m_tiles;
+    p.group_m = static_cast<int32_t>(gm);
+  }
   p.num_n_tiles = g.num_n_tiles;
   p.num_tiles = static_cast<int32_t>(g.num_tiles);
   p.num_kb = g.num_kb;

@@ -79,6 +79,20 @@ struct Waiter {
   }
 };
 
+// Tile order: groups of `group_m` row blocks; within a group the row block
+// varies fastest, then the column block.  The CTAs working at any moment share
+// a few row blocks of A and a few column blocks of B, so A is read from DRAM
+// once and B once per group, instead of A once per column block.
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& m_tile, int& n_tile) {
+  const int group_tiles = p.group_m * p.num_n_tiles;
+  const int g = tile / group_tiles;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.group_m, p.num_m_tiles - first_m);
+  const int local = tile - g * group_tiles;
+  m_tile = first_m + local % gm;
+  n_tile = local / gm;
+}
+
 // Warp-wide wait: lane 0 alone polls the barrier (32 lanes spinning on one
 // mbarrier serialise in shared memory and steal bandwidth from the MMA's
 // operand reads), then the outcome is broadcast and __syncwarp orders the other
@@ -180,8 +194,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       uint32_t armed = 0, armed_phase = 0;
       bool ok = true;
       for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step) {
-        const int m_tile = tile % p.num_m_tiles;
-        const int n_tile = tile / p.num_m_tiles;
+        int m_tile, n_tile;
+        tile_coords(tile, p, m_tile, n_tile);
         const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
         // B columns (N index) of this tile held by this CTA: for SwiGLU the G
         // half and the U half of the same output columns
@@ -334,8 +348,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     };
 
     for (int tile = tile0; tile < p.num_tiles; tile += tile_step, ++local) {
-      const int m_tile = tile % p.num_m_tiles;
-      const int n_tile = tile / p.num_m_tiles;
+      int m_tile, n_tile;
+      tile_coords(tile, p, m_tile, n_tile);
       const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
       const int row = m0 + r_in_tile;
       const bool row_ok = row < p.M;

@@ -71,6 +71,7 @@ struct GemmParams {
   int32_t N_out;           // output width (N/2 with SWIGLU)
   int32_t half;            // N/2 with SWIGLU, else 0
   int32_t num_m_tiles, num_n_tiles, num_tiles, num_kb, stages;
+  int32_t group_m;         // row blocks per rasterization group (see tile_coords)
   int32_t n_aux;           // aux tensors staged by TMA
   int32_t rms_slot;        // row-stat slot for r_i, -1 if none
   float rms_eps;

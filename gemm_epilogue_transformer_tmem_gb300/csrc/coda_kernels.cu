@@ -47,12 +47,11 @@ cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M,
 
 // ------------------------------------------------- commuted-norm row scales
 // r_i = rsqrt(sum_k a_ik^2 / K + eps) for every row of A: the row-statistics
-// side path for CTA-pair tiles, run just before the GEMM (a warp per row,
-// grid-stride).  For a small A it runs as one 4-warp block per SM, so that the
-// GEMM's CTA fits beside it and starts its mainloop while this finishes
-// (programmatic dependent launch; only the GEMM's epilogue waits for it).  For
-// a large A, whose pass would outlast the GEMM's first tiles, it runs as a full
-// grid at full memory bandwidth instead.  K % 8 == 0.
+// side path for CTA-pair tiles, run just before the GEMM as a full grid at
+// memory bandwidth (a warp per row, eight 16-byte loads in flight per lane).
+// The GEMM is launched as its programmatic dependent, so its launch overlaps
+// this kernel's tail and only its epilogue waits for the row scales.
+// K % 8 == 0.
 __global__ void __launch_bounds__(256) rms_rowscale_kernel(const uint16_t* __restrict__ A, int64_t M, int64_t K,
                                                            float inv_K, float eps, float* __restrict__ r,
                                                            float* __restrict__ r_copy) {
@@ -95,15 +94,9 @@ __global__ void __launch_bounds__(256) rms_rowscale_kernel(const uint16_t* __res
 
 cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, float* r, float* r_copy,
                                 int num_sms, cudaStream_t st) {
-  // keep the SM configured for maximum shared memory so the GEMM's CTA can
-  // start beside this kernel's blocks instead of waiting for the SM to drain
-  cudaError_t e = cudaFuncSetAttribute(rms_rowscale_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
-  if (e != cudaSuccess) return e;
-  const bool overlap = M * K * 2 <= (int64_t{48} << 20);
-  const int threads = overlap ? 128 : 256;
-  int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
-  if (overlap && blocks > num_sms) blocks = num_sms;
+  (void)num_sms;
+  const int threads = 256;
+  const int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
   rms_rowscale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(static_cast<const uint16_t*>(A), M, K,
                                                                           inv_K, eps, r, r_copy);
   return cudaGetLastError();
