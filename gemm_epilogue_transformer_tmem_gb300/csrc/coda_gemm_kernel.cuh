@@ -335,14 +335,17 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     int local = 0;
     bool ok = true;
 
+    // aux tiles and D are touched once: mark them first to leave L2, so the
+    // A and B tiles that other CTAs reuse stay resident
+    const uint64_t stream_policy = policy_evict_first();
     auto issue_aux = [&](int b, int col, int row0) {
       __syncwarp();
       if (lane == 0) {
         uint64_t* bar = &ctl->auxfull[q][b];
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_aux * kBoxBytes));
-        tma_load_2d(aux_stage + (0 * 2 + b) * kBoxBytes, &tmX0, bar, col, row0);
-        if (n_aux > 1) tma_load_2d(aux_stage + (1 * 2 + b) * kBoxBytes, &tmX1, bar, col, row0);
-        if (n_aux > 2) tma_load_2d(aux_stage + (2 * 2 + b) * kBoxBytes, &tmX2, bar, col, row0);
+        tma_load_2d_hint(aux_stage + (0 * 2 + b) * kBoxBytes, &tmX0, bar, col, row0, stream_policy);
+        if (n_aux > 1) tma_load_2d_hint(aux_stage + (1 * 2 + b) * kBoxBytes, &tmX1, bar, col, row0, stream_policy);
+        if (n_aux > 2) tma_load_2d_hint(aux_stage + (2 * 2 + b) * kBoxBytes, &tmX2, bar, col, row0, stream_policy);
       }
       aux_armed |= 1u << b;
     };
@@ -436,7 +439,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmD, ob, col, m0 + q * 32);
+          tma_store_2d_hint(&tmD, ob, col, m0 + q * 32, stream_policy);
           bulk_commit_group();
         }
         sbuf ^= 1;
