@@ -1,6 +1,6 @@
 """Benchmark of the fused GEMM + on-chip epilogue path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|swiglu|dgrad|llama]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|dgrad|llama|skinny]
                     [--impl coda|reference]
 
 Default workload: the commuted-RMSNorm projection D = rsqrt(mean(X^2)+1e-6) *
@@ -47,11 +47,14 @@ L2_FLUSH_BYTES = 256 << 20
 
 DESCRIPTIONS = {
     "rmsproj": "commuted RMSNorm projection D = rsqrt(mean(X^2)+1e-6)*(X@(gamma*W)), X[4096,2048], W[2048,8192]",
+    "lnproj": "commuted LayerNorm projection D = r*(X@(gamma*W) - mu*colsum(gamma*W)) + beta@W, X[4096,2048], "
+              "W[2048,8192]",
     "swiglu": "SwiGLU up-projection [G|U] = X[8192,4096] @ W[4096,22016], SiLU(G)*U, dropout p=0.1",
     "dgrad": "dgrad dX = (dY[8192,4096] @ W[16384,4096]^T) * GELU'(Z), rows sum(dX*Xhat), sum(dX)",
+    "skinny": "decode-sized MLP up-projection: rmsnorm(X[128,4096]) @ W[4096,22016] (commuted), SiLU(G)*U",
     "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs)",
 }
-DEFAULT_STEPS = {"rmsproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60}
+DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000}
 
 
 def kernel_hash() -> str:
@@ -177,8 +180,8 @@ class OracleSample:
         from gemm_epilogue_transformer_tmem_gb300 import inputs
         from oracle import coda_oracle as O
         self.w, self.I, self.O = workload, inputs, O
-        gen = dict(rmsproj=inputs.make_rmsproj, swiglu=inputs.make_swiglu, dgrad=inputs.make_dgrad,
-                   llama=inputs.make_llama_block)[workload]
+        gen = dict(rmsproj=inputs.make_rmsproj, lnproj=inputs.make_lnproj, swiglu=inputs.make_swiglu,
+                   dgrad=inputs.make_dgrad, llama=inputs.make_llama_block, skinny=inputs.make_skinny)[workload]
         self.t = {k: O.to_f64(v) for k, v in gen(0).items()}
         self.Mmax = next(iter(self.t.values())).shape[0] if workload != "llama" else self.t["X"].shape[0]
         self.rows = 32
@@ -190,6 +193,14 @@ class OracleSample:
         t0 = time.perf_counter()
         if self.w == "rmsproj":
             O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", 0, I.EPS_RMS)], norm_gamma=t["gamma"])
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "lnproj":
+            O.run_chain(t["X"][r], t["W"], [("LN_ROWSCALE", 0, I.EPS_LN)], norm_gamma=t["gamma"],
+                        norm_beta=t["beta"])
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "skinny":
+            O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", None, I.EPS_RMS), ("SWIGLU",)],
+                        norm_gamma=t["gamma"])
             fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
         elif self.w == "swiglu":
             O.run_chain(t["X"][r], t["W"], [("SWIGLU",), ("DROPOUT", 0, I.DROPOUT_P)])
@@ -343,14 +354,21 @@ def main():
         return
 
     peaks, peak_src = load_peaks()
-    # the fused kernels are timed in short bursts between L2 flushes: burst peak
-    peak = float(peaks["bf16_tflops"])
-    achieved = step.flops / (sum(per_call) / steps * 1e-3) / 1e12
+    call_s = sum(per_call) / steps * 1e-3
     traffic = load_traffic(args.workload)
-    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "peak_source": f"bf16 burst, of {peak_src}",
-                "traffic": traffic["bytes_per_launch"] if traffic else None,
-                "algorithmic_bytes": step.fused_bytes}
+    if step.bound == "hbm":
+        # the weight stream bounds the step: algorithmic bytes against the measured copy bandwidth
+        peak = float(peaks["hbm_gbs"])
+        achieved = step.fused_bytes / call_s / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(achieved / peak, 4), "peak_source": f"HBM copy, of {peak_src}"}
+    else:
+        # the fused kernels are timed in short bursts between L2 flushes: burst peak
+        peak = float(peaks["bf16_tflops"])
+        achieved = step.flops / call_s / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                    "frac": round(achieved / peak, 4), "peak_source": f"bf16 burst, of {peak_src}"}
+    roofline.update(traffic=traffic["bytes_per_launch"] if traffic else None, algorithmic_bytes=step.fused_bytes)
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:

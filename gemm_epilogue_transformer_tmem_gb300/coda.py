@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(HERE, "libcoda.so")
 OPCODES = {
     "SCALE": 0, "COL_SCALE": 1, "BIAS": 2, "ROW_SCALE": 3, "RMS_ROWSCALE": 4, "GELU_TANH": 5,
     "SILU": 6, "SWIGLU": 7, "GELU_TANH_GRAD": 8, "DROPOUT": 9, "RESIDUAL": 10, "STORE_PREACT": 11,
-    "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15,
+    "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15, "GELU_ERF": 16, "GELU_ERF_GRAD": 17,
+    "LN_ROWSCALE": 18,
 }
 REDUCTIONS = ("ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX")
 MAX_OPS = 16
@@ -42,7 +43,8 @@ class CodaEpilogue(ctypes.Structure):
 
 class CodaAux(ctypes.Structure):
     _fields_ = [("col_vec", ctypes.c_void_p * 4), ("row_vec", ctypes.c_void_p * 2), ("residual", ctypes.c_void_p),
-                ("z", ctypes.c_void_p), ("xhat", ctypes.c_void_p), ("preact_out", ctypes.c_void_p)]
+                ("z", ctypes.c_void_p), ("xhat", ctypes.c_void_p), ("preact_out", ctypes.c_void_p),
+                ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p)]
 
 
 class CodaError(RuntimeError):
@@ -63,6 +65,8 @@ _SIGS = {
     "coda_workspace_size": (ctypes.c_int, [_I64, _I64, _I64, _VP, ctypes.POINTER(ctypes.c_size_t)]),
     "coda_fold_gamma": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
     "coda_rmsnorm": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP, _VP]),
+    "coda_fold_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
+    "coda_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP]),
     "coda_epilogue_apply": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "coda_check_device_error": (ctypes.c_int, [_VP, _VP]),
     "coda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -143,8 +147,11 @@ def make_epilogue(ops: Sequence, seed: int = 0) -> CodaEpilogue:
     return e
 
 
-def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None) -> CodaAux:
+def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None, ln_colsum=None,
+             ln_bias=None) -> CodaAux:
     a = CodaAux()
+    a.ln_colsum = _ptr(ln_colsum)
+    a.ln_bias = _ptr(ln_bias)
     for k, t in (col_vecs or {}).items():
         a.col_vec[k] = _ptr(t)
     for k, t in (row_vecs or {}).items():
@@ -165,6 +172,8 @@ def stat_slots(ops: Sequence) -> int:
     for name, slot, _ in _norm_ops(ops):
         if (name in REDUCTIONS or name == "RMS_ROWSCALE") and slot != NO_SLOT:
             n = max(n, slot + 1)
+        if name == "LN_ROWSCALE" and slot != NO_SLOT:
+            n = max(n, slot + 2)        # r_i and mu_i
     return n
 
 
@@ -184,6 +193,7 @@ class Result:
 
 def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_layout: str = "kn", seed: int = 0,
                   col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None,
+                  ln_colsum=None, ln_bias=None,
                   out: Optional[torch.Tensor] = None, row_stats: Optional[torch.Tensor] = None,
                   keep_count: Optional[torch.Tensor] = None, want_keep_count: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None) -> Result:
@@ -204,7 +214,7 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
     if workspace is None and wbytes > 0:
         workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
     e = make_epilogue(ops, seed)
-    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias)
     st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(e), ctypes.byref(a),
                                   _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
                                   workspace.numel() if workspace is not None else 0, _stream(stream))
@@ -215,13 +225,13 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
 def gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence, *, out: torch.Tensor,
                           row_stats: Optional[torch.Tensor] = None, keep_count: Optional[torch.Tensor] = None,
                           b_layout: str = "kn", seed: int = 0, col_vecs=None, row_vecs=None, residual=None, z=None,
-                          xhat=None, preact_out=None, stream=None) -> Result:
+                          xhat=None, preact_out=None, ln_colsum=None, ln_bias=None, stream=None) -> Result:
     """coda_gemm_epilogue_noalloc: the caller passes every output; the library's
     fixed scratch buffer replaces the workspace, so nothing is allocated here."""
     M, K = A.shape
     N = B.shape[1] if b_layout == "kn" else B.shape[0]
     e = make_epilogue(ops, seed)
-    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias)
     _check(lib().coda_gemm_epilogue_noalloc(_ptr(A), _ptr(B), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(e),
                                             ctypes.byref(a), _ptr(out), _ptr(row_stats), _ptr(keep_count),
                                             _stream(stream)), "coda_gemm_epilogue_noalloc")
@@ -242,6 +252,31 @@ def fold_gamma(W: torch.Tensor, gamma: torch.Tensor, b_layout: str = "kn", out: 
         out = torch.empty_like(W)
     _check(lib().coda_fold_gamma(_ptr(W), _ptr(gamma), _ptr(out), K, N, B_LAYOUTS[b_layout], _stream(stream)),
            "coda_fold_gamma")
+    return out
+
+
+def fold_layernorm(W: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor] = None, b_layout: str = "kn",
+                   stream=None):
+    """Commuted-LayerNorm weights: (bf16(gamma (.)_row W), colsum of it (fp32), beta^T W (fp32))."""
+    if b_layout == "kn":
+        K, N = W.shape
+    else:
+        N, K = W.shape
+    W_out = torch.empty_like(W)
+    c = torch.empty((N,), dtype=torch.float32, device=W.device)
+    b = torch.empty((N,), dtype=torch.float32, device=W.device)
+    _check(lib().coda_fold_layernorm(_ptr(W), _ptr(gamma), _ptr(beta), _ptr(W_out), _ptr(c), _ptr(b), K, N,
+                                     B_LAYOUTS[b_layout], _stream(stream)), "coda_fold_layernorm")
+    return W_out, c, b
+
+
+def layernorm(X: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor], eps: float,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    M, K = X.shape
+    if out is None:
+        out = torch.empty_like(X)
+    _check(lib().coda_layernorm(_ptr(X), _ptr(gamma), _ptr(beta), M, K, eps, _ptr(out), _stream(stream)),
+           "coda_layernorm")
     return out
 
 

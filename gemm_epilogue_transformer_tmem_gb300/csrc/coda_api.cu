@@ -96,7 +96,8 @@ struct Compiled {
   bool glu = false;
   int n_aux = 0;
   const void* aux_ptr[kMaxAux] = {nullptr, nullptr, nullptr};
-  bool has_rms = false;
+  bool has_rms = false;   // RMS_ROWSCALE or LN_ROWSCALE (row statistics of A)
+  bool is_ln = false;     // ... and it is LN_ROWSCALE
   int rms_slot = -1;
   float rms_eps = 0.0f;
   bool needs_row_stats = false;
@@ -150,6 +151,7 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
     switch (op.opcode) {
       case CODA_OP_SCALE:
       case CODA_OP_GELU_TANH:
+      case CODA_OP_GELU_ERF:
       case CODA_OP_SILU:
       case CODA_OP_SWIGLU:
         break;
@@ -176,7 +178,26 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         c.has_rms = true;
         c.rms_eps = op.f0;
         break;
+      case CODA_OP_LN_ROWSCALE:
+        if (!fused) return CODA_ERR_UNSUPPORTED;
+        if (c.has_rms || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
+        if (ax.ln_colsum == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.ln_colsum) || (ax.ln_bias != nullptr && !aligned16(ax.ln_bias))) return CODA_ERR_ALIGNMENT;
+        if (op.slot != CODA_NO_SLOT) {
+          // r_i to row_stats[slot], mu_i to row_stats[slot + 1]
+          if (op.slot + 1 >= CODA_MAX_STAT_SLOTS) return CODA_ERR_INVALID_ARG;
+          c.rms_slot = static_cast<int>(op.slot);
+          c.needs_row_stats = true;
+          if (c.rms_slot + 1 > c.max_stat_slot) c.max_stat_slot = c.rms_slot + 1;
+        }
+        c.has_rms = true;
+        c.is_ln = true;
+        c.rms_eps = op.f0;
+        c.prog.ln_colsum = ax.ln_colsum;
+        c.prog.ln_bias = ax.ln_bias;
+        break;
       case CODA_OP_GELU_TANH_GRAD:
+      case CODA_OP_GELU_ERF_GRAD:
         if (!after_glu || ax.z == nullptr) return CODA_ERR_INVALID_ARG;
         if (!aligned16(ax.z)) return CODA_ERR_ALIGNMENT;
         d.aux = use_aux(AUX_Z, ax.z);
@@ -260,7 +281,7 @@ Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu, int tile_m = BM) {
 size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
   size_t b = static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * static_cast<size_t>(M) * sizeof(float);
   if (c.prog.has_dropout) b += static_cast<size_t>(g.num_n_tiles) * static_cast<size_t>(M) * sizeof(uint32_t);
-  if (c.has_rms) b += static_cast<size_t>(M) * sizeof(float);
+  if (c.has_rms) b += static_cast<size_t>(M) * sizeof(float) * (c.is_ln ? 2 : 1);   // r [M] (+ mu [M])
   return b;
 }
 
@@ -293,6 +314,7 @@ coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epil
   for (int i = 0; i < CODA_MAX_ROW_VECS; ++i) dummy.row_vec[i] = reinterpret_cast<const float*>(kAligned);
   dummy.residual = dummy.z = dummy.xhat = kAligned;
   dummy.preact_out = const_cast<uint16_t*>(kAligned);
+  dummy.ln_colsum = dummy.ln_bias = reinterpret_cast<const float*>(kAligned);
   s = compile_epilogue(epi, &dummy, N, K, true, c);
   if (s != CODA_OK) return s;
   *bytes = workspace_bytes_for(M, geometry(M, N, K, c.glu), c);
@@ -380,6 +402,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   p.num_kb = g.num_kb;
   p.n_aux = c.n_aux;
   p.rms_slot = c.rms_slot;
+  p.norm_ln = c.is_ln ? 1 : 0;
   p.rms_eps = c.rms_eps;
   p.inv_K = K > 0 ? static_cast<float>(1.0 / static_cast<double>(K)) : 0.0f;
   p.timeout_ns = g_timeout_ns.load();
@@ -417,8 +440,12 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   // halves signal the pair leader's barrier, so no row-statistics warps)
   const bool rowstat_warps = c.has_rms && !pair;
   if (pair && c.has_rms) {
-    e = launch_rms_rowscale(A, M, K, p.inv_K, c.rms_eps, rms_ws,
-                            c.rms_slot >= 0 ? row_stats + static_cast<size_t>(c.rms_slot) * M : nullptr, dev.sms, st);
+    float* mu_ws = c.is_ln ? rms_ws + M : nullptr;
+    e = launch_rms_rowscale(A, M, K, p.inv_K, c.rms_eps, c.is_ln, rms_ws,
+                            c.rms_slot >= 0 ? row_stats + static_cast<size_t>(c.rms_slot) * M : nullptr, mu_ws,
+                            (c.is_ln && c.rms_slot >= 0) ? row_stats + static_cast<size_t>(c.rms_slot + 1) * M : nullptr,
+                            st);
+    p.mu_vec = mu_ws;
     if (e != cudaSuccess) return CODA_ERR_CUDA;
     g_launches.fetch_add(1);
     p.rms_vec = rms_ws;
@@ -462,6 +489,46 @@ coda_status coda_fold_gamma(const void* W, const void* gamma, void* W_out, int64
   if (s != CODA_OK) return s;
   const cudaError_t e =
       launch_fold_gamma(W, gamma, W_out, K, N, b_layout == CODA_B_KN, dev.sms, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_fold_layernorm(const void* W, const void* gamma, const void* beta, void* W_out, float* colsum_out,
+                                float* bias_out, int64_t K, int64_t N, int32_t b_layout, void* stream) {
+  coda_status s = check_dims(0, N, K);
+  if (s != CODA_OK) return s;
+  if (b_layout != CODA_B_KN && b_layout != CODA_B_NK) return CODA_ERR_INVALID_ARG;
+  if (K == 0 || N == 0) return CODA_OK;
+  if (!W || !gamma || !W_out || !colsum_out || !bias_out || W_out == W) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(gamma) || !aligned16(W_out) || (beta && !aligned16(beta)) ||
+      !aligned4(colsum_out) || !aligned4(bias_out))
+    return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool kn = b_layout == CODA_B_KN;
+  cudaError_t e = launch_fold_gamma(W, gamma, W_out, K, N, kn, dev.sms, st);
+  if (e != cudaSuccess) return CODA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  e = launch_ln_colsum(W_out, W, beta, K, N, kn, colsum_out, bias_out, st);
+  if (e != cudaSuccess) return CODA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return CODA_OK;
+}
+
+coda_status coda_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K, float eps,
+                           void* Xn_out, void* stream) {
+  coda_status s = check_dims(M, 8, K);
+  if (s != CODA_OK) return s;
+  if (!std::isfinite(eps) || eps < 0.0f || K == 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0) return CODA_OK;
+  if (!X || !gamma || !Xn_out) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(gamma) || !aligned16(Xn_out) || (beta && !aligned16(beta))) return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e = launch_layernorm(X, gamma, beta, M, K, eps, Xn_out, static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) g_launches.fetch_add(1);
   return from_cuda(e);
 }

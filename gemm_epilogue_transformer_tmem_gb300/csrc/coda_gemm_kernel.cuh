@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         break;
       }
       tc_fence_after_sync();
-      float r_rms = 1.0f;
+      float r_rms = 1.0f, mu = 0.0f;
       if (kRowStats) {
         okw = warp_wait(W, &ctl->rsfull[acc], acc_phase, tile, lane);
         if (!okw) {
@@ -377,12 +377,14 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           break;
         }
         r_rms = ctl->rs[acc][r_in_tile];
+        mu = ctl->rmu[acc][r_in_tile];
         mbar_arrive(&ctl->rsempty[acc]);
       } else if (p.rms_vec != nullptr) {
-        // row scales from the pre-pass kernel, which may still have been running
-        // when this grid started: wait for it before the first read
+        // row statistics from the pre-pass kernel, which may still have been
+        // running when this grid started: wait for it before the first read
         if (local == 0) griddep_wait();
         r_rms = row_ok ? p.rms_vec[row] : 1.0f;
+        if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
       }
 
       float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         }
         int nvalid = p.N_out - col;
         if (nvalid > kChunk) nvalid = kChunk;
-        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms};
+        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
         const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
         run_ops<32, kGLU>(p.prog, v, u, rc, ax, red, keep);
 
@@ -453,8 +455,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           if (r < p.prog.n_red)
             p.ws_red[(static_cast<size_t>(r) * p.num_n_tiles + n_tile) * Ms + row] = red[r];
         if (p.ws_keep != nullptr) p.ws_keep[static_cast<size_t>(n_tile) * Ms + row] = keep;
-        if (kRowStats && p.rms_slot >= 0 && n_tile == 0)
+        if (kRowStats && p.rms_slot >= 0 && n_tile == 0) {
           p.row_stats[static_cast<size_t>(p.rms_slot) * Ms + row] = r_rms;
+          if (p.norm_ln) p.row_stats[static_cast<size_t>(p.rms_slot + 1) * Ms + row] = mu;
+        }
       }
     }
     if (lane == 0) {
@@ -466,7 +470,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     }
     __syncwarp();
   } else if (kRowStats && warp >= 8) {
-    // ------------------------------------ row statistics (commuted RMSNorm)
+    // ------------------- row statistics (commuted RMSNorm / LayerNorm)
     // Each A stage is read alongside the MMA as soon as it is in shared memory;
     // one arrival per warp frees the stage.  (CTA pairs get their row scales
     // from a pre-pass kernel instead: there the A halves signal the leader's
@@ -479,7 +483,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     int local = 0;
     bool ok = true;
     for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step, ++local) {
-      float s = 0.0f;
+      // LayerNorm sums are taken about the row's first element (shifted data),
+      // so the variance cancels only as far as the row's spread; RMSNorm
+      // needs the raw sum of squares (shift 0)
+      float s = 0.0f, s1 = 0.0f, shift = 0.0f;
       for (int kb = 0; kb < p.num_kb; ++kb) {
         const bool okw = warp_wait(W, &ctl->full[stage], phase, tile, lane);
         if (!okw) {
@@ -489,13 +496,19 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         // row r of the 128B-swizzled A stage: its eight 16-byte chunks in an
         // order that spreads the warp over all banks (the sum ignores order)
         const uint8_t* arow = sA + stage * kStageABytes + r * 128;
+        if (kb == 0 && p.norm_ln)   // logical chunk 0 sits at physical chunk (r & 7)
+          shift = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(arow + ((r & 7) << 4))) << 16);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint4 w = *reinterpret_cast<const uint4*>(arow + ((j ^ (r & 7)) << 4));
           float x[8];
           unpack8(w, x);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) s = fmaf(x[e], x[e], s);
+          for (int e = 0; e < 8; ++e) {
+            const float d = x[e] - shift;
+            s = fmaf(d, d, s);
+            s1 += d;
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl->empty[stage]);
@@ -509,7 +522,16 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       const uint32_t acc_phase = (local >> 1) & 1;
       const bool okw = warp_wait(W, &ctl->rsempty[acc], acc_phase ^ 1u, tile, lane);
       if (!okw) break;
-      ctl->rs[acc][r] = rsqrtf(fmaf(s, p.inv_K, p.rms_eps));
+      if (p.norm_ln) {
+        // LayerNorm: mean = shift + mean(d), variance = mean(d^2) - mean(d)^2
+        const float m = s1 * p.inv_K;
+        const float var = fmaxf(fmaf(s, p.inv_K, -m * m), 0.0f);
+        ctl->rmu[acc][r] = shift + m;
+        ctl->rs[acc][r] = rsqrtf(var + p.rms_eps);
+      } else {
+        ctl->rmu[acc][r] = 0.0f;
+        ctl->rs[acc][r] = rsqrtf(fmaf(s, p.inv_K, p.rms_eps));
+      }
       mbar_arrive(&ctl->rsfull[acc]);
     }
   }

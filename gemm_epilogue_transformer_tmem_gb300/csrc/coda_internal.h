@@ -64,6 +64,8 @@ struct EpiProgram {
   uint16_t* preact;
   int32_t preact_width;
   int32_t pad;
+  const float* ln_colsum;  // LN_ROWSCALE: c (fp32 [width])
+  const float* ln_bias;    // LN_ROWSCALE: b (fp32 [width]) or null
 };
 
 struct GemmParams {
@@ -84,7 +86,10 @@ struct GemmParams {
   uint32_t smem_ctl_off;   // offset of the control block
   uint32_t epi_warp_bytes; // staging bytes per epilogue warp
   uint32_t* err;           // device error word (4 x u32)
-  const float* rms_vec;    // commuted RMSNorm row scales from the pre-pass kernel, or null
+  const float* rms_vec;    // commuted-norm row scales r from the pre-pass kernel, or null
+  const float* mu_vec;     // commuted LayerNorm row means from the pre-pass kernel, or null
+  int32_t norm_ln;         // the row statistics are LayerNorm's (mean and centred variance)
+  int32_t pad2;
   EpiProgram prog;
 };
 
@@ -102,6 +107,7 @@ struct Ctl {
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];
+  float rmu[2][BM];        // commuted LayerNorm: row means for both accumulators
 };
 
 // device error word layout: [0] code, [1] block, [2] role, [3] tile

@@ -46,15 +46,94 @@ cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M,
 }
 
 // ------------------------------------------------- commuted-norm row scales
-// r_i = rsqrt(sum_k a_ik^2 / K + eps) for every row of A: the row-statistics
-// side path for CTA-pair tiles, run just before the GEMM as a full grid at
-// memory bandwidth (a warp per row, eight 16-byte loads in flight per lane).
-// The GEMM is launched as its programmatic dependent, so its launch overlaps
-// this kernel's tail and only its epilogue waits for the row scales.
+// Row statistics of A for the commuted norms: the side path for CTA-pair tiles,
+// run just before the GEMM as a full grid at memory bandwidth (a warp per row,
+// eight 16-byte loads in flight per lane).  The GEMM is launched as its
+// programmatic dependent, so its launch overlaps this kernel's tail and only
+// its epilogue waits for the statistics.
+//   RMSNorm:   r_i = rsqrt(sum_k a_ik^2 / K + eps)
+//   LayerNorm: mu_i = sum_k a_ik / K,  r_i = rsqrt(sum_k (a_ik - mu_i)^2 / K + eps),
+//              in one pass over data shifted by the row's first element
+//              (the shifted-data variance of Chan, Golub & LeVeque, 1983):
+//              with d = a - a_i0, var = sum d^2 / K - (sum d / K)^2, which
+//              cancels only as far as the row's spread, not its mean.
 // K % 8 == 0.
+__device__ __forceinline__ float warp_row_sum(const uint4* ar, int64_t n8, int lane, float shift, bool squares) {
+  float acc = 0.0f;
+  int64_t i = lane;
+  for (; i + 224 < n8; i += 256) {
+    uint4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = __ldg(ar + i + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float x[8];
+      unpack8(q[u], x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = x[j] - shift;
+        acc = squares ? fmaf(d, d, acc) : acc + d;
+      }
+    }
+  }
+  for (; i < n8; i += 32) {
+    float x[8];
+    unpack8(__ldg(ar + i), x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float d = x[j] - shift;
+      acc = squares ? fmaf(d, d, acc) : acc + d;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
+}
+
+// sum_k (a_k - shift) and sum_k (a_k - shift)^2 over one row, reduced over the warp
+__device__ __forceinline__ void warp_row_moments(const uint4* ar, int64_t n8, int lane, float shift, float& s1,
+                                                 float& s2) {
+  float a1 = 0.0f, a2 = 0.0f;
+  int64_t i = lane;
+  for (; i + 224 < n8; i += 256) {
+    uint4 q[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) q[u] = __ldg(ar + i + 32 * u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float x[8];
+      unpack8(q[u], x);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = x[j] - shift;
+        a1 += d;
+        a2 = fmaf(d, d, a2);
+      }
+    }
+  }
+  for (; i < n8; i += 32) {
+    float x[8];
+    unpack8(__ldg(ar + i), x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float d = x[j] - shift;
+      a1 += d;
+      a2 = fmaf(d, d, a2);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a1 += __shfl_xor_sync(0xFFFFFFFFu, a1, o);
+    a2 += __shfl_xor_sync(0xFFFFFFFFu, a2, o);
+  }
+  s1 = a1;
+  s2 = a2;
+}
+
 __global__ void __launch_bounds__(256) rms_rowscale_kernel(const uint16_t* __restrict__ A, int64_t M, int64_t K,
-                                                           float inv_K, float eps, float* __restrict__ r,
-                                                           float* __restrict__ r_copy) {
+                                                           float inv_K, float eps, int layernorm,
+                                                           float* __restrict__ r, float* __restrict__ r_copy,
+                                                           float* __restrict__ mu, float* __restrict__ mu_copy) {
   griddep_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t n8 = K >> 3;
@@ -62,43 +141,148 @@ __global__ void __launch_bounds__(256) rms_rowscale_kernel(const uint16_t* __res
   for (int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); row < M;
        row += stride) {
     const uint4* ar = reinterpret_cast<const uint4*>(A + row * K);
-    float ss = 0.0f;
-    int64_t i = lane;
-    for (; i + 224 < n8; i += 256) {   // eight independent 16-byte loads in flight per lane
-      uint4 q[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) q[u] = __ldg(ar + i + 32 * u);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        float x[8];
-        unpack8(q[u], x);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
-      }
+    float m = 0.0f, ss;
+    if (layernorm) {
+      const float shift = __uint_as_float(static_cast<uint32_t>(__ldg(A + row * K)) << 16);
+      float s1, s2;
+      warp_row_moments(ar, n8, lane, shift, s1, s2);
+      const float d = s1 * inv_K;
+      m = shift + d;
+      ss = fmaxf(s2 - s1 * d, 0.0f);   // sum (a - mu)^2
+    } else {
+      ss = warp_row_sum(ar, n8, lane, 0.0f, true);
     }
-    for (; i < n8; i += 32) {
-      float x[8];
-      unpack8(__ldg(ar + i), x);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
     if (lane == 0) {
       const float v = rsqrtf(fmaf(ss, inv_K, eps));
       r[row] = v;
       if (r_copy != nullptr) r_copy[row] = v;
+      if (layernorm) {
+        mu[row] = m;
+        if (mu_copy != nullptr) mu_copy[row] = m;
+      }
     }
   }
 }
 
-cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, float* r, float* r_copy,
-                                int num_sms, cudaStream_t st) {
-  (void)num_sms;
+cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, bool layernorm, float* r,
+                                float* r_copy, float* mu, float* mu_copy, cudaStream_t st) {
   const int threads = 256;
   const int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
-  rms_rowscale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(static_cast<const uint16_t*>(A), M, K,
-                                                                          inv_K, eps, r, r_copy);
+  rms_rowscale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint16_t*>(A), M, K, inv_K, eps, layernorm ? 1 : 0, r, r_copy, mu, mu_copy);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ LayerNorm fold
+// c_n = sum_k W'[k,n] over the folded bf16 weight, b_n = sum_k beta_k W[k,n]
+// (fp32).  [K,N] layout: a thread per column n, coalesced along n.  [N,K]
+// layout: a warp per row n.
+__global__ void ln_colsum_kn_kernel(const uint16_t* __restrict__ Wf, const uint16_t* __restrict__ W,
+                                    const uint16_t* __restrict__ beta, int64_t K, int64_t N, float* __restrict__ c,
+                                    float* __restrict__ b) {
+  const int64_t n = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (n >= N) return;
+  float sc = 0.0f, sb = 0.0f;
+  for (int64_t k = 0; k < K; ++k) {
+    sc += __uint_as_float(static_cast<uint32_t>(__ldg(Wf + k * N + n)) << 16);
+    if (beta != nullptr)
+      sb = fmaf(__uint_as_float(static_cast<uint32_t>(__ldg(beta + k)) << 16),
+                __uint_as_float(static_cast<uint32_t>(__ldg(W + k * N + n)) << 16), sb);
+  }
+  c[n] = sc;
+  b[n] = sb;
+}
+
+__global__ void ln_colsum_nk_kernel(const uint16_t* __restrict__ Wf, const uint16_t* __restrict__ W,
+                                    const uint16_t* __restrict__ beta, int64_t K, int64_t N, float* __restrict__ c,
+                                    float* __restrict__ b) {
+  const int64_t n = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (n >= N) return;
+  const uint4* wf = reinterpret_cast<const uint4*>(Wf + n * K);
+  const uint4* w = reinterpret_cast<const uint4*>(W + n * K);
+  const uint4* bt = reinterpret_cast<const uint4*>(beta);
+  float sc = 0.0f, sb = 0.0f;
+  for (int64_t i = lane; i < (K >> 3); i += 32) {
+    float x[8];
+    unpack8(__ldg(wf + i), x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc += x[j];
+    if (beta != nullptr) {
+      float y[8], g[8];
+      unpack8(__ldg(w + i), y);
+      unpack8(__ldg(bt + i), g);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sb = fmaf(g[j], y[j], sb);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sc += __shfl_xor_sync(0xFFFFFFFFu, sc, o);
+    sb += __shfl_xor_sync(0xFFFFFFFFu, sb, o);
+  }
+  if (lane == 0) {
+    c[n] = sc;
+    b[n] = sb;
+  }
+}
+
+cudaError_t launch_ln_colsum(const void* W_folded, const void* W, const void* beta, int64_t K, int64_t N, bool kn,
+                             float* c, float* b, cudaStream_t st) {
+  if (kn) {
+    const int threads = 256;
+    ln_colsum_kn_kernel<<<static_cast<unsigned>((N + threads - 1) / threads), threads, 0, st>>>(
+        static_cast<const uint16_t*>(W_folded), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(beta),
+        K, N, c, b);
+  } else {
+    const int threads = 256;
+    ln_colsum_nk_kernel<<<static_cast<unsigned>((N + 7) / 8), threads, 0, st>>>(
+        static_cast<const uint16_t*>(W_folded), static_cast<const uint16_t*>(W), static_cast<const uint16_t*>(beta),
+        K, N, c, b);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- unfused LayerNorm
+// One warp per row: mean, centred variance (two passes), then
+// Xn = bf16(gamma * (x - mu) * r + beta).  K % 8 == 0.
+__global__ void layernorm_kernel(const uint16_t* __restrict__ X, const uint16_t* __restrict__ gamma,
+                                 const uint16_t* __restrict__ beta, int64_t M, int64_t K, float eps,
+                                 uint16_t* __restrict__ Xn) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + row * K);
+  const int64_t n8 = K >> 3;
+  const float inv_K = 1.0f / static_cast<float>(K);
+  const float m = warp_row_sum(xr, n8, lane, 0.0f, false) * inv_K;
+  const float r = rsqrtf(fmaf(warp_row_sum(xr, n8, lane, m, true), inv_K, eps));
+  uint4* yr = reinterpret_cast<uint4*>(Xn + row * K);
+  const uint4* gr = reinterpret_cast<const uint4*>(gamma);
+  const uint4* br = reinterpret_cast<const uint4*>(beta);
+  for (int64_t i = lane; i < n8; i += 32) {
+    float x[8], g[8], bb[8], y[8];
+    unpack8(__ldg(xr + i), x);
+    unpack8(__ldg(gr + i), g);
+    if (beta != nullptr) {
+      unpack8(__ldg(br + i), bb);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bb[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) y[j] = fmaf(g[j] * (x[j] - m), r, bb[j]);
+    yr[i] = pack8(y);
+  }
+}
+
+cudaError_t launch_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K, float eps,
+                             void* Xn, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t blocks = (M + 7) / 8;
+  layernorm_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint16_t*>(X), static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta), M, K,
+      eps, static_cast<uint16_t*>(Xn));
   return cudaGetLastError();
 }
 

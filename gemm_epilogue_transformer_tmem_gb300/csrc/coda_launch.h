@@ -21,8 +21,12 @@ cudaError_t max_pairs_plain(bool b_mn_major, bool row_stats, size_t smem, int* p
 cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
                             const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
                             cudaStream_t st);
-cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, float* r, float* r_copy,
-                                int num_sms, cudaStream_t st);
+cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K, float eps, bool layernorm, float* r,
+                                float* r_copy, float* mu, float* mu_copy, cudaStream_t st);
+cudaError_t launch_ln_colsum(const void* W_folded, const void* W, const void* beta, int64_t K, int64_t N, bool kn,
+                             float* c, float* b, cudaStream_t st);
+cudaError_t launch_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K, float eps,
+                             void* Xn, cudaStream_t st);
 cudaError_t launch_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, bool kn,
                               int num_sms, cudaStream_t st);
 cudaError_t launch_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t K, float eps, void* Xn,

@@ -34,6 +34,16 @@ __device__ __forceinline__ float gelu_tanh_grad_f(float z) {
 
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
+// exact GELU: x * Phi(x), Phi the standard normal distribution function
+__device__ __forceinline__ float gelu_erf_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
+
+// its derivative: Phi(z) + z * phi(z)
+__device__ __forceinline__ float gelu_erf_grad_f(float z) {
+  const float cdf = 0.5f * (1.0f + erff(z * 0.70710678118654752f));
+  const float pdf = 0.39894228040143268f * expf(-0.5f * z * z);
+  return fmaf(z, pdf, cdf);
+}
+
 // splitmix64 output function (Steele, Lea & Flood, OOPSLA 2014)
 __device__ __forceinline__ uint64_t splitmix_mix(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
@@ -82,6 +92,27 @@ __device__ __forceinline__ void load_colvec(const uint16_t* vec, int col, int wi
   }
 }
 
+// NE values of an fp32 vector starting at `col` (0 past `width` or for a null vector).
+template <int NE>
+__device__ __forceinline__ void load_colvec_f32(const float* vec, int col, int width, float (&out)[NE]) {
+  if (vec == nullptr) {
+#pragma unroll
+    for (int j = 0; j < NE; ++j) out[j] = 0.0f;
+  } else if (col + NE <= width) {
+#pragma unroll
+    for (int i = 0; i < NE / 4; ++i) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(vec + col) + i);
+      out[4 * i] = q.x;
+      out[4 * i + 1] = q.y;
+      out[4 * i + 2] = q.z;
+      out[4 * i + 3] = q.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < NE; ++j) out[j] = (col + j < width) ? __ldg(vec + col + j) : 0.0f;
+  }
+}
+
 template <int NE>
 __device__ __forceinline__ void store_row_bf16(uint16_t* dst, int col, int width, const float (&v)[NE]) {
   if (col + NE <= width) {
@@ -113,7 +144,8 @@ struct RowCtx {
   int half;         // SwiGLU: column offset of U in the GEMM output (N/2)
   int n_out;        // output width
   int M;
-  float r_rms;      // commuted-RMSNorm row scale of this row
+  float r_rms;      // commuted-norm row scale of this row
+  float mu;         // commuted-LayerNorm row mean of this row
 };
 
 // Run the op list on v (and, before SWIGLU, on u).  `aux.load(k, out)` fills
@@ -172,6 +204,21 @@ __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], flo
         }
         break;
       }
+      case CODA_OP_LN_ROWSCALE: {
+        // r (x - mu c_j) + b_j
+        float cv[NE], bv[NE];
+        load_colvec_f32<NE>(P.ln_colsum, c.col, c.n_out, cv);
+        load_colvec_f32<NE>(P.ln_bias, c.col, c.n_out, bv);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], v[j]), bv[j]);
+        if (pre) {
+          load_colvec_f32<NE>(P.ln_colsum ? P.ln_colsum + c.half : nullptr, c.col, c.n_out, cv);
+          load_colvec_f32<NE>(P.ln_bias ? P.ln_bias + c.half : nullptr, c.col, c.n_out, bv);
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], u[j]), bv[j]);
+        }
+        break;
+      }
       case CODA_OP_GELU_TANH: {
 #pragma unroll
         for (int j = 0; j < NE; ++j) v[j] = gelu_tanh_f(v[j]);
@@ -179,6 +226,22 @@ __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], flo
 #pragma unroll
           for (int j = 0; j < NE; ++j) u[j] = gelu_tanh_f(u[j]);
         }
+        break;
+      }
+      case CODA_OP_GELU_ERF: {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = gelu_erf_f(v[j]);
+        if (pre) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] = gelu_erf_f(u[j]);
+        }
+        break;
+      }
+      case CODA_OP_GELU_ERF_GRAD: {
+        float z[NE];
+        aux.load(op.aux, z);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] *= gelu_erf_grad_f(z[j]);
         break;
       }
       case CODA_OP_SILU: {

@@ -18,6 +18,14 @@ workload descriptions:
            Xn[8192,4096] ~ N(0,1), W ~ N(0, var 1/4096)
   dgrad    dX = (dY @ W^T) * GELU'(Z) and per-row sum(dX*Xhat), dY[8192,4096],
            W[16384,4096], Z and Xhat [8192,16384], all N(0,1)
+  lnproj   commuted LayerNorm projection (the GPT-2 / BERT normalisation),
+           the rmsproj shapes: X[4096,2048] ~ N(0,1) plus a per-row offset
+           ~ N(0.5, 0.5^2), gamma ~ U(0.5,1.5), beta ~ N(0, 0.1^2),
+           W[2048,8192] ~ N(0, var 1/2048)
+  skinny   the LLaMA block's MLP up-projection at 128 tokens (a decode-sized
+           batch): commuted RMSNorm -> SwiGLU, X[128,4096] ~ N(0,1),
+           gamma ~ U(0.5,1.5), W[4096,2*11008] ~ N(0, std 0.02).  180 MB of
+           weights against 23 GFLOP: bound by HBM, not by the tensor cores
   llama    LLaMA-7B-like non-attention block at 16384 tokens, d=4096,
            ffn=11008, weights N(0, std 0.02), gammas U(0.5,1.5)
 
@@ -58,17 +66,23 @@ WORKLOADS = {
     "rmsproj": Workload("rmsproj", 4096, 2048, 8192, "kn",
                         "commuted RMSNorm projection D = rsqrt(mean(X^2)+1e-6) * (X @ (gamma*W)); "
                         "X[4096,2048], W[2048,8192]"),
+    "lnproj": Workload("lnproj", 4096, 2048, 8192, "kn",
+                       "commuted LayerNorm projection D = r (X @ (gamma*W) - mu colsum(gamma*W)) + beta@W; "
+                       "X[4096,2048], W[2048,8192]"),
     "swiglu": Workload("swiglu", 8192, 4096, 2 * 11008, "kn",
                        "SwiGLU up-projection [G|U] = Xn @ W[4096,2*11008], SiLU(G)*U, dropout p=0.1"),
     "dgrad": Workload("dgrad", 8192, 4096, 16384, "nk",
                       "dgrad dX = (dY @ W^T) * GELU'(Z) + per-row sum(dX*Xhat), sum(dX); "
                       "dY[8192,4096], W[16384,4096]"),
+    "skinny": Workload("skinny", 128, 4096, 2 * 11008, "kn",
+                       "decode-sized MLP up-projection: rmsnorm(X[128,4096]) @ W[4096,2*11008], SiLU(G)*U"),
 }
 
 # LLaMA-7B-like non-attention block at 16384 tokens (four GEMM+epilogue calls)
 LLAMA_BLOCK = dict(tokens=16384, d=4096, ffn=11008)
 
 EPS_RMS = 1e-6
+EPS_LN = 1e-5
 DROPOUT_P = 0.1
 DROPOUT_SEED = 0
 
@@ -119,6 +133,25 @@ def make_rmsproj(seed: int = 0, M: int = 4096, K: int = 2048, N: int = 8192) -> 
         X=randn_bf16((M, K), 1.0, seed + 11),
         gamma=uniform_bf16((K,), 0.5, 1.5, seed + 12),
         W=randn_bf16((K, N), 1.0 / math.sqrt(2048.0), seed + 13),
+    )
+
+
+def make_lnproj(seed: int = 0, M: int = 4096, K: int = 2048, N: int = 8192) -> dict:
+    X = torch.randn(M, K, generator=_gen(seed + 51), dtype=torch.float32)
+    X += 0.5 + 0.5 * torch.randn(M, 1, generator=_gen(seed + 52), dtype=torch.float32)
+    return dict(
+        X=X.to(torch.bfloat16),
+        gamma=uniform_bf16((K,), 0.5, 1.5, seed + 53),
+        beta=randn_bf16((K,), 0.1, seed + 54),
+        W=randn_bf16((K, N), 1.0 / math.sqrt(2048.0), seed + 55),
+    )
+
+
+def make_skinny(seed: int = 0, M: int = 128, K: int = 4096, N_out: int = 11008) -> dict:
+    return dict(
+        X=randn_bf16((M, K), 1.0, seed + 61),
+        gamma=uniform_bf16((K,), 0.5, 1.5, seed + 62),
+        W=randn_bf16((K, 2 * N_out), 0.02, seed + 63),
     )
 
 

@@ -30,6 +30,7 @@ class Step:
     unfused: Callable[[], None]
     host_inputs: dict = field(default_factory=dict)    # name -> device tensor fed per step in e2e mode
     host_outputs: dict = field(default_factory=dict)   # name -> device tensor read back per step
+    bound: str = "tensor"     # what bounds the fused kernel: "tensor" or "hbm"
     kernels_per_fused: int = 1
     kernels_per_unfused: int = 1
     prep: Optional[Callable[[], None]] = None           # weight preparation (gamma fold)
@@ -70,6 +71,40 @@ def build_rmsproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
                 outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn))
 
 
+def build_lnproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
+    """D = r (X @ Wf - mu colsum(Wf)) + beta@W, Wf = gamma (.) W: commuted LayerNorm
+    projection, with r_i and mu_i written out.  The fold (Wf, its column sums
+    and beta@W) is weight preparation."""
+    t = t or inputs.make_lnproj(seed, M, K, N)
+    X, g, beta, W = (t[k].to(dev) for k in ("X", "gamma", "beta", "W"))
+    prepared = {}
+
+    def prep():
+        prepared["Wf"], prepared["c"], prepared["b"] = coda.fold_layernorm(W, g, beta, "kn")
+
+    prep()
+    ops = [("LN_ROWSCALE", 0, inputs.EPS_LN)]
+    D = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    rs = torch.empty((2, M), dtype=torch.float32, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    Xn = torch.empty_like(X)
+    Du = torch.empty_like(D)
+
+    def fused():
+        coda.gemm_epilogue(X, prepared["Wf"], ops, ln_colsum=prepared["c"], ln_bias=prepared["b"], out=D,
+                           row_stats=rs, workspace=ws)
+
+    def unfused():
+        coda.layernorm(X, g, beta, inputs.EPS_LN, out=Xn)
+        coda.gemm_epilogue(Xn, W, [], out=Du)
+
+    fb = M * K * BF16 + K * N * BF16 + 2 * N * F32 + M * N * BF16 + 2 * M * F32
+    ub = (M * K * BF16 + 2 * K * BF16 + M * K * BF16) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
+    return Step("lnproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
+                host_outputs=dict(D=D, stats=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
+                outputs=dict(D=D, stats=rs, D_unfused=Du, Xn=Xn))
+
+
 def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
     """out = dropout(silu(G) * U, p), [G|U] = X @ W."""
     t = t or inputs.make_swiglu(seed, M, K, N_out)
@@ -96,6 +131,38 @@ def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Ste
     ub = (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16 + (2 * M * N_out * BF16 + M * 4)
     return Step("swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
                 kernels_per_fused=2, kernels_per_unfused=3, outputs=dict(D=D, keep=kc, D_unfused=Du))
+
+
+def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step:
+    """up = silu(r G) * (r U), [G|U] = X @ (gamma (.) W): commuted RMSNorm into the
+    SwiGLU up-projection at a decode-sized batch.  The 180 MB weight stream
+    bounds it, so its roofline is HBM bandwidth."""
+    t = t or inputs.make_skinny(seed, M, K, N_out)
+    X, g, W = (t[k].to(dev) for k in ("X", "gamma", "W"))
+    N = 2 * N_out
+    Wf = torch.empty_like(W)
+    prep = lambda: coda.fold_gamma(W, g, "kn", out=Wf)   # noqa: E731
+    prep()
+    ops = [("RMS_ROWSCALE", None, inputs.EPS_RMS), ("SWIGLU",)]
+    D = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    Xn = torch.empty_like(X)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Du = torch.empty_like(D)
+
+    def fused():
+        coda.gemm_epilogue(X, Wf, ops, out=D, workspace=ws)
+
+    def unfused():
+        coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn)
+        coda.gemm_epilogue(Xn, W, [], out=C)
+        coda.epilogue_apply(C, [("SWIGLU",)], out=Du)
+
+    fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16
+    ub = (2 * M * K * BF16 + K * BF16) + (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16
+    return Step("skinny", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
+                bound="hbm", kernels_per_fused=1, kernels_per_unfused=3, prep=prep,
+                outputs=dict(D=D, D_unfused=Du))
 
 
 def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
@@ -197,4 +264,5 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
                 prep=prep, outputs=out)
 
 
-BUILDERS = dict(rmsproj=build_rmsproj, swiglu=build_swiglu, dgrad=build_dgrad, llama=build_llama)
+BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,
+                llama=build_llama, skinny=build_skinny)

@@ -87,12 +87,22 @@ typedef enum {
  *                  f0 = eps.  If slot != CODA_NO_SLOT, r_i is also written to
  *                  row_stats[slot*M + i].  With B = bf16(gamma (.)_row W) (see
  *                  coda_fold_gamma) the result is rmsnorm(A; gamma) @ W.
+ *   LN_ROWSCALE    commuted LayerNorm: x = r_i * (x - mu_i * c_j) + b_j, with
+ *                  mu_i = mean_k A[i,k], r_i = 1/sqrt(mean_k (A[i,k]-mu_i)^2 + f0)
+ *                  gathered from A like RMS_ROWSCALE (f0 = eps), c = aux.ln_colsum
+ *                  and b = aux.ln_bias (fp32 vectors of `width` entries, b may be
+ *                  NULL).  With B, c and b from coda_fold_layernorm the result is
+ *                  layernorm(A; gamma, beta) @ W.  At most one RMS_ROWSCALE or
+ *                  LN_ROWSCALE per list.
  * Elementwise transforms (agentlenshq.com "Pairwise Transformations"):
  *   GELU_TANH      x = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
  *   SILU           x = x / (1 + exp(-x))
  *   SWIGLU         pairs output column j < N/2 (G) with column j + N/2 (U):
  *                  x_j = silu(G_j) * U_j; width becomes N/2.  At most once.
  *   GELU_TANH_GRAD x *= GELU_TANH'(z[i,j])      (z: bf16 [M, N_out], aux.z)
+ *   GELU_ERF       x = x * Phi(x) = 0.5 x (1 + erf(x / sqrt(2)))   (exact GELU)
+ *   GELU_ERF_GRAD  x *= Phi(z) + z phi(z), phi the standard normal density
+ *                  (z: bf16 [M, N_out], aux.z)
  *   DROPOUT        f0 = p in [0,1).  keep iff splitmix64(seed, i*N_out + j) < T,
  *                  T = floor(ldexp(1-p, 64)) in fp64; kept x *= 1/(1-p), dropped
  *                  x = 0.  splitmix64(seed, n) is output n (0-based) of the
@@ -128,7 +138,10 @@ typedef enum {
   CODA_OP_ROW_MEAN = 13,
   CODA_OP_ROW_SUMSQ = 14,
   CODA_OP_ROW_DOT_AUX = 15,
-  CODA_OP_COUNT_ = 16
+  CODA_OP_GELU_ERF = 16,
+  CODA_OP_GELU_ERF_GRAD = 17,
+  CODA_OP_LN_ROWSCALE = 18,
+  CODA_OP_COUNT_ = 19
 } coda_opcode;
 
 #define CODA_MAX_OPS 16
@@ -159,6 +172,8 @@ typedef struct {
   const void* z;                           /* bf16 [M, N_out]               */
   const void* xhat;                        /* bf16 [M, N_out]               */
   void* preact_out;                        /* bf16 [M, width at the op]     */
+  const float* ln_colsum;                  /* fp32 [width], LN_ROWSCALE     */
+  const float* ln_bias;                    /* fp32 [width], LN_ROWSCALE     */
 } coda_aux;
 
 /*
@@ -230,6 +245,22 @@ CODA_API coda_status coda_fold_gamma(const void* W, const void* gamma, void* W_o
                             int32_t b_layout, void* stream);
 
 /*
+ * coda_fold_layernorm -- weights for the commuted LayerNorm (LN_ROWSCALE): the
+ * zeli.app comment (augment_me) names LayerNorm beside RMSNorm as a norm whose
+ * row-wise factors commute past the projection:
+ *     layernorm(X) @ W = r (.)_row ( X @ W' - mu (x) c ) + b,
+ *     W' = gamma (.)_row W,  c_j = sum_k W'[k,j],  b_j = sum_k beta_k W[k,j].
+ * Writes W_out = bf16(gamma[k] * W[k,n]) (layout `b_layout`), colsum_out =
+ * column sums of the bf16 W_out in fp32 (so the identity holds exactly for the
+ * folded weight) and bias_out = beta^T W in fp32 (NULL beta: zeros).  gamma and
+ * beta are bf16 [K]; colsum_out and bias_out are fp32 [N].  W_out must not
+ * alias W.
+ */
+CODA_API coda_status coda_fold_layernorm(const void* W, const void* gamma, const void* beta, void* W_out,
+                                         float* colsum_out, float* bias_out, int64_t K, int64_t N,
+                                         int32_t b_layout, void* stream);
+
+/*
  * coda_rmsnorm -- the unfused normalisation pass: Xn[i,k] = bf16(r_i x_ik gamma_k),
  * r_i = 1/sqrt(mean_k x_ik^2 + eps); rstd_out (fp32 [M]) may be NULL.  This is the
  * separate memory-bound kernel that the commuted form removes; it exists so the
@@ -239,10 +270,18 @@ CODA_API coda_status coda_rmsnorm(const void* X, const void* gamma, int64_t M, i
                          void* Xn_out, float* rstd_out, void* stream);
 
 /*
+ * coda_layernorm -- the unfused LayerNorm pass: Xn[i,k] = bf16(gamma_k (x_ik - mu_i)
+ * r_i + beta_k), mu_i = mean_k x_ik, r_i = 1/sqrt(mean_k (x_ik - mu_i)^2 + eps);
+ * beta may be NULL.  The memory-bound kernel the commuted form removes.
+ */
+CODA_API coda_status coda_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K,
+                                    float eps, void* Xn_out, void* stream);
+
+/*
  * coda_epilogue_apply -- the same op list applied by a separate memory-bound
  * kernel to a bf16 tensor C [M, N] already in global memory (the unfused form:
- * one read of C, one write of D).  RMS_ROWSCALE is not available here (it needs
- * the GEMM's A operand).  Reductions are finished inside this kernel, so it
+ * one read of C, one write of D).  RMS_ROWSCALE and LN_ROWSCALE are not
+ * available here (they need the GEMM's A operand).  Reductions are finished inside this kernel, so it
  * needs no workspace.
  */
 CODA_API coda_status coda_epilogue_apply(const void* C, int64_t M, int64_t N, const coda_epilogue* epi,

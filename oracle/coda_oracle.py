@@ -25,6 +25,7 @@ step; everything else is written out.
 
 Readings where the pages are silent (each is also listed in the design notes):
   * GELU is the tanh form; its derivative is the tanh form's exact derivative.
+    The exact form x * Phi(x) (GELU_ERF) and its derivative are separate ops.
   * dropout: keep element (row, col) of the [M, N_out] output iff
     splitmix64(seed, i) < T with i = row*N_out + col, where splitmix64(seed, i)
     is the i-th output (0-based) of the splitmix64 generator seeded with seed
@@ -33,6 +34,8 @@ Readings where the pages are silent (each is also listed in the design notes):
     Kept values are scaled by 1/(1-p) (inverted dropout); p = 0 keeps all.
   * RMSNorm: r_i = 1/sqrt(mean_k x_ik^2 + eps); gamma scales the K index, so
     rmsnorm(X) @ W = r (.)_row (X @ (gamma (.)_row W)).
+  * LayerNorm: mu_i = mean_k x_ik, r_i = 1/sqrt(mean_k (x_ik - mu_i)^2 + eps)
+    (the biased variance); layernorm(X) = gamma (.) (x - mu) r + beta.
   * SwiGLU: the GEMM output is [G | U] with G = columns [0, N/2) and
     U = columns [N/2, N); out = silu(G) * U; ops before SWIGLU act on both
     halves (column vectors then have N entries), ops after it on N/2 columns.
@@ -50,7 +53,7 @@ import numpy as np
 OP_NAMES = (
     "SCALE", "COL_SCALE", "BIAS", "ROW_SCALE", "RMS_ROWSCALE", "GELU_TANH", "SILU",
     "SWIGLU", "GELU_TANH_GRAD", "DROPOUT", "RESIDUAL", "STORE_PREACT",
-    "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX",
+    "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX", "GELU_ERF", "GELU_ERF_GRAD", "LN_ROWSCALE",
 )
 
 _U64 = np.uint64
@@ -98,6 +101,29 @@ def rmsnorm_project(X, gamma, W, eps, b_layout="kn"):
     return gemm(rmsnorm(X, gamma, eps), W, b_layout)
 
 
+def ln_stats(X: np.ndarray, eps: float):
+    """mu_i = mean_k x_ik and r_i = 1 / sqrt(mean_k (x_ik - mu_i)^2 + eps)."""
+    X = np.asarray(X, dtype=np.float64)
+    mu = np.mean(X, axis=1)
+    var = np.mean((X - mu[:, None]) ** 2, axis=1)
+    return mu, 1.0 / np.sqrt(var + eps)
+
+
+def layernorm(X, gamma, beta, eps):
+    """Xn[i, k] = gamma_k (x_ik - mu_i) r_i + beta_k (beta None: 0)."""
+    X = np.asarray(X, dtype=np.float64)
+    mu, r = ln_stats(X, eps)
+    out = (X - mu[:, None]) * r[:, None] * np.asarray(gamma, dtype=np.float64)[None, :]
+    if beta is not None:
+        out = out + np.asarray(beta, dtype=np.float64)[None, :]
+    return out
+
+
+def layernorm_project(X, gamma, beta, W, eps, b_layout="kn"):
+    """Normalise-then-project: layernorm(X) @ W (the unfused reading)."""
+    return gemm(layernorm(X, gamma, beta, eps), W, b_layout)
+
+
 # ---------------------------------------------------------------------------
 # scaling primitives (agentlenshq.com, "仕組み": Scaling by a constant or vector)
 # ---------------------------------------------------------------------------
@@ -139,6 +165,21 @@ def gelu_tanh_grad(z):
     t = np.tanh(_SQRT_2_OVER_PI * (z + _GELU_C * z ** 3))
     dinner = _SQRT_2_OVER_PI * (1.0 + 3.0 * _GELU_C * z * z)
     return 0.5 * (1.0 + t) + 0.5 * z * (1.0 - t * t) * dinner
+
+
+_erf = np.vectorize(math.erf, otypes=[np.float64])
+
+
+def gelu_erf(x):
+    """The exact GELU: x * Phi(x) = 0.5 x (1 + erf(x / sqrt(2)))."""
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + _erf(x / math.sqrt(2.0)))
+
+
+def gelu_erf_grad(z):
+    """d/dz [z Phi(z)] = Phi(z) + z phi(z), phi(z) = exp(-z^2/2) / sqrt(2 pi)."""
+    z = np.asarray(z, dtype=np.float64)
+    return 0.5 * (1.0 + _erf(z / math.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
 
 
 def silu(x):
@@ -246,16 +287,20 @@ def row_dot(x, aux):
 # the whole epilogue program, as separate passes in op-list order
 # ---------------------------------------------------------------------------
 def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
-              residual_t=None, z=None, xhat=None, norm_gamma=None, rows=None):
+              residual_t=None, z=None, xhat=None, norm_gamma=None, norm_beta=None, ln_colsum=None,
+              ln_bias=None, rows=None):
     """Evaluate D = f(A @ B) for an op list, one unfused pass per op.
 
     ops: sequence of (name, slot, f0) tuples, names from OP_NAMES; f0 is taken
         as the float32 the op list carries (widened exactly to fp64).
     col_vecs / row_vecs: dict slot -> vector (bf16 values widened).
     residual_t, z, xhat: [M, N_out] aux tensors (or only the sampled rows).
-    norm_gamma: if given, the op list must begin with RMS_ROWSCALE; the GEMM is
-        then evaluated as rmsnorm(A, gamma) @ B (normalise, then project), with
-        B the *unscaled* weight.
+    norm_gamma: if given, the op list must begin with RMS_ROWSCALE or
+        LN_ROWSCALE; the GEMM is then evaluated as rmsnorm(A; gamma) @ B or
+        layernorm(A; gamma, norm_beta) @ B (normalise, then project), with B the
+        *unscaled* weight.
+    ln_colsum / ln_bias: the c and b vectors of an LN_ROWSCALE evaluated as
+        written (x = r (x - mu c) + b) when the norm is not given unfused.
     rows: absolute row indices of the rows of A given (used by dropout's
         counter and nothing else); default 0..M-1.
 
@@ -277,11 +322,18 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
     stats = {}
     if norm_gamma is not None:
         name, slot, eps = ops[0]
-        if name != "RMS_ROWSCALE":
-            raise ValueError("norm_gamma needs RMS_ROWSCALE as the first op")
-        x = rmsnorm_project(A, norm_gamma, B, eps, b_layout)
-        if slot is not None and slot >= 0:
-            stats[slot] = rms_rstd(A, eps)
+        if name == "RMS_ROWSCALE":
+            x = rmsnorm_project(A, norm_gamma, B, eps, b_layout)
+            if slot is not None and slot >= 0:
+                stats[slot] = rms_rstd(A, eps)
+        elif name == "LN_ROWSCALE":
+            x = layernorm_project(A, norm_gamma, norm_beta, B, eps, b_layout)
+            if slot is not None and slot >= 0:
+                mu, r = ln_stats(A, eps)
+                stats[slot] = r
+                stats[slot + 1] = mu
+        else:
+            raise ValueError("norm_gamma needs RMS_ROWSCALE or LN_ROWSCALE as the first op")
         start = 1
     else:
         x = gemm(A, B, b_layout)
@@ -304,10 +356,24 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
             x = row_scale(x, r)
             if slot is not None and slot >= 0:
                 stats[slot] = r
+        elif name == "LN_ROWSCALE":
+            mu, r = ln_stats(A, f0)
+            c = np.asarray(ln_colsum, dtype=np.float64)
+            b = np.zeros_like(c) if ln_bias is None else np.asarray(ln_bias, dtype=np.float64)
+            if x.shape[1] != c.shape[0]:
+                raise ValueError("LN_ROWSCALE vectors must match the width")
+            x = r[:, None] * (x - mu[:, None] * c[None, :]) + b[None, :]
+            if slot is not None and slot >= 0:
+                stats[slot] = r
+                stats[slot + 1] = mu
         elif name == "GELU_TANH":
             x = gelu_tanh(x)
         elif name == "SILU":
             x = silu(x)
+        elif name == "GELU_ERF":
+            x = gelu_erf(x)
+        elif name == "GELU_ERF_GRAD":
+            x = x * gelu_erf_grad(z)
         elif name == "SWIGLU":
             x = swiglu(x)
         elif name == "GELU_TANH_GRAD":

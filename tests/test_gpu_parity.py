@@ -159,6 +159,9 @@ OP_CASES = {
     "gelu": [("GELU_TANH",)],
     "silu": [("SILU",)],
     "gelu_grad": [("GELU_TANH_GRAD",)],
+    "gelu_erf": [("GELU_ERF",)],
+    "gelu_erf_grad": [("GELU_ERF_GRAD",)],
+    "bias_gelu_erf_swiglu": [("BIAS", 0), ("GELU_ERF",), ("SWIGLU",)],
     "residual": [("RESIDUAL", 0, 0.75)],
     "preact_gelu": [("STORE_PREACT",), ("GELU_TANH",)],
     "reductions": [("ROW_SUM", 0), ("ROW_MEAN", 1), ("ROW_SUMSQ", 2), ("ROW_DOT_AUX", 3)],
@@ -307,6 +310,107 @@ def test_commuted_rmsnorm_then_swiglu(exact_gamma, mode):
         check_stats(r, ref, "rms -> swiglu")
 
 
+# ------------------------------------------------------ commuted LayerNorm
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("with_beta", [True, False])
+def test_fold_layernorm(layout, with_beta):
+    K, N = 200, 264
+    W = rand((K, N) if layout == "kn" else (N, K), 81, 1.0 / math.sqrt(K))
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 82)
+    beta = rand((K,), 83, 0.3) if with_beta else None
+    Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta) if with_beta else None, layout)
+    sync_ok()
+    # the folded weights are the RMS fold's (one RNE rounding of an exact product)
+    assert torch.equal(Wf.cpu(), coda.fold_gamma(cu(W), cu(g), layout).cpu())
+    Wkn = f64(W) if layout == "kn" else f64(W).T
+    Wf_kn = f64(Wf) if layout == "kn" else f64(Wf).T
+    # c = the column sums of the weights the GEMM actually multiplies (the bf16
+    # fold), so X@Wf - mu c is (X - mu)@Wf up to fp32 summation error
+    c_ref = Wf_kn.sum(axis=0)
+    c_tol = 1e-5 * np.abs(Wf_kn).sum(axis=0) + 1e-6
+    assert (np.abs(f64(c) - c_ref) <= c_tol).all()
+    b_ref = f64(beta) @ Wkn if with_beta else np.zeros(N)
+    b_tol = 1e-5 * (np.abs(f64(beta)) @ np.abs(Wkn) if with_beta else np.zeros(N)) + 1e-6
+    assert (np.abs(f64(b) - b_ref) <= b_tol).all()
+
+
+def _ln_problem(M, K, N, layout, seed, mean=0.5):
+    # nonzero row means (a common offset plus a per-row shift), so the mu c term matters
+    X = inputs.randn_bf16((M, K), 1.0, seed)
+    shift = inputs.randn_bf16((M, 1), 0.5, seed + 1)
+    X = (X.float() + mean + shift.float()).to(torch.bfloat16)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, seed + 2)
+    beta = rand((K,), seed + 3, 0.3)
+    W = rand((K, N) if layout == "kn" else (N, K), seed + 4, 1.0 / math.sqrt(K))
+    return X, g, beta, W
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("M,K,N", [(300, 192, 264), (128, 2048, 512), (520, 512, 136)])
+def test_commuted_layernorm(layout, M, K, N, mode):
+    X, g, beta, W = _ln_problem(M, K, N, layout, 91)
+    Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta), layout)
+    ops = [("LN_ROWSCALE", 1, 1e-5)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops, b_layout=layout, ln_colsum=c, ln_bias=b)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, b_layout=layout, norm_gamma=f64(g), norm_beta=f64(beta))
+    assert_close(f64(r.D), ref["D"], "commuted layernorm")
+    assert_close(f64(r.row_stats[1]), ref["stats"][1], "ln r")
+    # mu is a mean of bf16 values: fp32 summation error only
+    mu = f64(r.row_stats[2])
+    assert (np.abs(mu - ref["stats"][2]) <= 1e-5 * (1 + np.abs(ref["stats"][2]))).all()
+
+
+def test_commuted_layernorm_large_mean(mode):
+    # rows with mean 30 and spread 1: the variance must come from the spread,
+    # not from the difference of two large second moments
+    M, K, N = 260, 1024, 264
+    X, g, beta, W = _ln_problem(M, K, N, "kn", 141, mean=30.0)
+    Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta), "kn")
+    ops = [("LN_ROWSCALE", 0, 1e-5)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops, ln_colsum=c, ln_bias=b)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g), norm_beta=f64(beta))
+    assert_close(f64(r.D), ref["D"], "layernorm, mean 30")
+    assert_close(f64(r.row_stats[0]), ref["stats"][0], "ln r, mean 30")
+    mu = f64(r.row_stats[1])
+    assert (np.abs(mu - ref["stats"][1]) <= 1e-5 * (1 + np.abs(ref["stats"][1]))).all()
+
+
+def test_commuted_layernorm_no_beta_no_slot(mode):
+    M, K, N = 260, 320, 200
+    X, g, _, W = _ln_problem(M, K, N, "kn", 101, mean=-1.0)
+    Wf, c, b = coda.fold_layernorm(cu(W), cu(g), None, "kn")
+    ops = [("LN_ROWSCALE", -1, 1e-5), ("GELU_ERF",)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops, ln_colsum=c)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g))
+    assert_close(f64(r.D), ref["D"], "ln (no beta) -> erf gelu")
+
+
+def test_commuted_layernorm_then_swiglu(mode):
+    # r and mu apply to both halves before the nonlinearity, each half with its
+    # own column sums and bias
+    M, K, n_out = 200, 256, 136
+    X, g, beta, W = _ln_problem(M, K, 2 * n_out, "kn", 111)
+    Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta), "kn")
+    ops = [("LN_ROWSCALE", 0, 1e-5), ("SWIGLU",), ("ROW_SUM", 2)]
+    r = coda.gemm_epilogue(cu(X), Wf, ops, ln_colsum=c, ln_bias=b)
+    sync_ok()
+    ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g), norm_beta=f64(beta))
+    assert_close(f64(r.D), ref["D"], "ln -> swiglu")
+    assert_close(f64(r.row_stats[0]), ref["stats"][0], "ln r")
+    check_stats(r, {"stats": {2: ref["stats"][2]}, "stat_scale": ref["stat_scale"]}, "ln -> swiglu")
+
+
+def test_layernorm_rowscale_rejected_unfused_and_without_colsum():
+    C = cu(rand((64, 64), 121))
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        coda.epilogue_apply(C, [("LN_ROWSCALE", -1, 1e-5)])
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):
+        coda.gemm_epilogue(C, C, [("LN_ROWSCALE", -1, 1e-5)])
+
+
 # --------------------------------------------------------------------- dgrad
 def test_dgrad_small(mode):
     M, K, N = 300, 128, 520
@@ -331,6 +435,15 @@ def test_unfused_rmsnorm():
     sync_ok()
     assert_close(f64(xn), O.rmsnorm(f64(X), f64(g), 1e-6), "rmsnorm")
     assert_close(f64(rstd), O.rms_rstd(f64(X), 1e-6), "rstd")
+
+
+@pytest.mark.parametrize("with_beta", [True, False])
+def test_unfused_layernorm(with_beta):
+    M, K = 300, 520
+    X, g, beta, _ = _ln_problem(M, K, 8, "kn", 131)
+    xn = coda.layernorm(cu(X), cu(g), cu(beta) if with_beta else None, 1e-5)
+    sync_ok()
+    assert_close(f64(xn), O.layernorm(f64(X), f64(g), f64(beta) if with_beta else None, 1e-5), "layernorm")
 
 
 @pytest.mark.parametrize("case", ["chain", "swiglu", "reductions", "gelu_grad", "bias_swiglu_bias_sum"])
@@ -375,6 +488,20 @@ def test_full_rmsproj_sampled():
     ref = O.run_chain(f64(t["X"][rows]), f64(t["W"]), ops, norm_gamma=f64(t["gamma"]))
     assert_close(f64(r.D[rows]), ref["D"], "rmsproj")
     assert_close(f64(r.row_stats[0][rows]), ref["stats"][0], "rmsproj r")
+
+
+def test_full_lnproj_sampled():
+    w = inputs.WORKLOADS["lnproj"]
+    t = inputs.make_lnproj()
+    Wf, c, b = coda.fold_layernorm(cu(t["W"]), cu(t["gamma"]), cu(t["beta"]), "kn")
+    ops = [("LN_ROWSCALE", 0, inputs.EPS_LN)]
+    r = coda.gemm_epilogue(cu(t["X"]), Wf, ops, ln_colsum=c, ln_bias=b)
+    sync_ok()
+    rows = _sampled(w.M, 2)
+    ref = O.run_chain(f64(t["X"][rows]), f64(t["W"]), ops, norm_gamma=f64(t["gamma"]), norm_beta=f64(t["beta"]))
+    assert_close(f64(r.D[rows]), ref["D"], "lnproj")
+    assert_close(f64(r.row_stats[0][rows]), ref["stats"][0], "lnproj r")
+    assert_close(f64(r.row_stats[1][rows]), ref["stats"][1], "lnproj mu")
 
 
 def test_full_swiglu_dropout_sampled():

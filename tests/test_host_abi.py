@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_struct_layouts():
     assert ctypes.sizeof(coda.CodaOp) == 16
     assert ctypes.sizeof(coda.CodaEpilogue) == 16 + 16 * 16
-    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4)
+    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4 + 2)
 
 
 def test_opcode_values_match_header():
@@ -153,3 +153,10 @@ def test_binding_helpers():
     assert coda.output_width(22016, [("SWIGLU",), ("DROPOUT", 0, 0.1)]) == 11008
     assert coda.stat_slots([("RMS_ROWSCALE", 2, 1e-6), ("ROW_SUM", 0)]) == 3
     assert coda.stat_slots([("RMS_ROWSCALE", None, 1e-6)]) == 0
+
+
+def test_workspace_size_for_layernorm_op_list():
+    # sizing needs no aux tensors: r_i and mu_i per row for the commuted LayerNorm
+    M, N, K = 300, 264, 192
+    assert coda.workspace_size(M, N, K, [("LN_ROWSCALE", 0, 1e-5)]) == 2 * M * 4
+    assert coda.workspace_size(M, N, K, [("LN_ROWSCALE", -1, 1e-5), ("ROW_SUM", 2)]) >= 2 * M * 4

@@ -338,3 +338,58 @@ def test_dropout_threshold_float32_parameter():
     out = O.run_chain(np.eye(3), np.ones((3, 3)), [("DROPOUT", 0, 0.1)], seed=1)
     keep = O.dropout_mask(1, 3, 3, p32)
     np.testing.assert_array_equal(out["keep"], keep)
+
+
+def test_gelu_erf_textbook_values():
+    # x * Phi(x) at points where the standard normal distribution function has
+    # well-known values: Phi(1) = 0.8413447460685429, Phi(2) = 0.9772498680518208
+    assert O.gelu_erf(0.0) == 0.0
+    assert abs(O.gelu_erf(1.0) - 0.8413447460685429) < 1e-15
+    assert abs(O.gelu_erf(-1.0) + (1 - 0.8413447460685429)) < 1e-15
+    assert abs(O.gelu_erf(2.0) - 2 * 0.9772498680518208) < 1e-15
+    x = np.linspace(-6, 6, 601)
+    np.testing.assert_allclose(O.gelu_erf(x) - O.gelu_erf(-x), x, atol=1e-14)   # erf is odd
+    # and the tanh approximation stays within its known 5e-4 of it
+    assert np.abs(O.gelu_erf(x) - O.gelu_tanh(x)).max() < 5e-4
+
+
+def test_gelu_erf_grad():
+    z = np.linspace(-7, 7, 1401)
+    h = 1e-5
+    fd = (O.gelu_erf(z + h) - O.gelu_erf(z - h)) / (2 * h)
+    np.testing.assert_allclose(O.gelu_erf_grad(z), fd, atol=1e-9)
+    assert O.gelu_erf_grad(0.0) == 0.5
+    # phi(1) = 0.24197072451914337: Phi(1) + phi(1)
+    assert abs(O.gelu_erf_grad(1.0) - (0.8413447460685429 + 0.24197072451914337)) < 1e-15
+
+
+def test_layernorm_hand_values_and_constant_row():
+    X = np.array([[1.0, 2.0, 3.0, 4.0]])          # mean 2.5, biased variance 1.25
+    mu, r = O.ln_stats(X, 0.0)
+    assert mu[0] == 2.5 and abs(r[0] - 1.0 / math.sqrt(1.25)) < 1e-15
+    np.testing.assert_allclose(O.layernorm(X, np.ones(4), None, 0.0)[0],
+                               (np.array([1, 2, 3, 4]) - 2.5) / math.sqrt(1.25), rtol=1e-14)
+    # a constant row normalises to beta
+    K = 32
+    g = rng.uniform(0.5, 1.5, K)
+    b = rng.standard_normal(K)
+    np.testing.assert_allclose(O.layernorm(np.full((1, K), 7.0), g, b, 1e-5)[0], b, rtol=1e-14, atol=1e-14)
+
+
+def test_commuted_layernorm_identity():
+    # layernorm(X) @ W == r (.)_row (X @ W' - mu (x) colsum(W')) + beta^T W, W' = gamma (.)_row W
+    X = rng.standard_normal((30, 48)) + 0.7
+    g = rng.uniform(0.5, 1.5, 48)
+    b = rng.standard_normal(48)
+    W = rng.standard_normal((48, 20))
+    eps = float(np.float32(1e-5))           # the op list carries eps as float32
+    lhs = O.layernorm_project(X, g, b, W, eps)
+    Wf = g[:, None] * W
+    mu, r = O.ln_stats(X, eps)
+    rhs = r[:, None] * (X @ Wf - mu[:, None] * Wf.sum(axis=0)[None, :]) + (b @ W)[None, :]
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-11, atol=1e-11)
+    # and the chain's written-out form of LN_ROWSCALE gives the same
+    out = O.run_chain(X, Wf, [("LN_ROWSCALE", 0, 1e-5)], ln_colsum=Wf.sum(axis=0), ln_bias=b @ W)
+    np.testing.assert_allclose(out["D"], lhs, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(out["stats"][0], r, rtol=1e-14)
+    np.testing.assert_allclose(out["stats"][1], mu, rtol=1e-14)
