@@ -12,8 +12,8 @@ unfused, an end-to-end figure through host buffers, clocks, and the fp64
 oracle timed on the host cores as the CPU baseline.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
-launching stream, with a 256 MiB device write between steps so every step
-reads its operands from HBM (the inputs are smaller than the 129 MB L2).
+launching stream, with a 256 MiB device write and a 256 MiB read between steps
+so every step reads its operands from HBM and starts with no dirty L2 lines.
 Under torchrun each rank runs an independent replica (the path has no
 cross-GPU exchange); the time is the max over ranks.
 """
@@ -269,6 +269,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--split-k", default="auto", choices=["auto", "off", "force"],
+                    help="split over K for single-CTA problems (library knob; default auto)")
     args = ap.parse_args()
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
     warmup = max(args.warmup, 3)
@@ -290,12 +292,22 @@ def main():
     import __graft_entry__ as entry
     entry.build()
     from gemm_epilogue_transformer_tmem_gb300 import coda, workloads
+    coda.set_split_k(args.split_k)
 
     dev = torch.device("cuda", local)
     step = workloads.BUILDERS[args.workload](dev=dev)
     stream = torch.cuda.current_stream()
+    # L2 flush between steps: write a buffer larger than L2, then read another
+    # one, so the timed step starts with a cold L2 that holds no dirty lines
+    # (a write alone leaves ~126 MB to be written back during the next step,
+    # which takes HBM bandwidth from it)
     flush_buf = torch.empty((L2_FLUSH_BYTES // 4,), dtype=torch.float32, device=dev)
-    flush = lambda: flush_buf.zero_()  # noqa: E731
+    flush_rd = torch.ones((L2_FLUSH_BYTES // 4,), dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.zero_()
+        torch.sum(flush_rd, dim=0, out=flush_out)
 
     # ---- fused step, device-resident inputs
     sampler = ClockSampler(local) if rank == 0 else None
@@ -307,6 +319,7 @@ def main():
         time.sleep(0.3)
     per_call, total_ms, launches = timed_loop([step.fused], steps, warmup, flush, stream, coda.launch_count)
     clocks = sampler.stop() if sampler else None
+    plan = coda.last_plan()      # how the step's last GEMM call ran
     st, info = coda.check_device_error()
     if st != 0:
         raise RuntimeError(f"device error {st}: {info}")
@@ -383,9 +396,11 @@ def main():
         "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "flops_per_step": step.flops,
-                   "l2": "flushed between steps (256 MiB device write outside the timed events)",
+                   "l2": "flushed between steps outside the timed events: a 256 MiB device write, then a "
+                         "256 MiB read, so no dirty lines are written back inside the timed region",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "weight_prep": "gamma folded into W once per weight version, not in the step"},
+                   "weight_prep": "gamma folded into W once per weight version, not in the step",
+                   "plan_of_last_gemm": plan},
         "roofline": roofline,
         "dram_bytes": {"fused_algorithmic": step.fused_bytes, "unfused_algorithmic": step.unfused_bytes,
                        "ncu_fused_per_launch": traffic["bytes_per_launch"] if traffic else None},

@@ -47,6 +47,12 @@ class CodaAux(ctypes.Structure):
                 ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p)]
 
 
+class CodaPlan(ctypes.Structure):
+    _fields_ = [("pair", ctypes.c_int32), ("split", ctypes.c_int32), ("grid", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64), ("prepass", ctypes.c_int32),
+                ("sequence", ctypes.c_int32)]
+
+
 class CodaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -74,6 +80,9 @@ _SIGS = {
     "coda_set_pipeline_timeout_ns": (None, [ctypes.c_uint64]),
     "coda_set_max_ctas": (None, [ctypes.c_int32]),
     "coda_set_cta_pair": (None, [ctypes.c_int32]),
+    "coda_set_split_k": (None, [ctypes.c_int32]),
+    "coda_last_plan": (None, [_VP]),
+    "coda_set_fixed_sequences": (None, [ctypes.c_int32]),
 }
 
 
@@ -337,3 +346,23 @@ PAIR_MODES = {"auto": 0, "single": 1, "pair": 2}
 def set_cta_pair(mode: str) -> None:
     """'auto' (CTA pairs when M > 128), 'single' (one-CTA kernel) or 'pair' (CTA pairs)."""
     lib().coda_set_cta_pair(PAIR_MODES[mode])
+
+
+SPLIT_MODES = {"auto": 0, "off": 1, "force": 2}
+
+
+def last_plan() -> dict:
+    """How this thread's last gemm_epilogue call ran (kernel, split, grid, ...)."""
+    pl = CodaPlan()
+    lib().coda_last_plan(ctypes.byref(pl))
+    return {k: getattr(pl, k) for k, _ in CodaPlan._fields_}
+
+
+def set_fixed_sequences(enable: bool) -> None:
+    """Use the kernels built for fixed op sequences (default) or always interpret."""
+    lib().coda_set_fixed_sequences(1 if enable else 0)
+
+
+def set_split_k(mode: str) -> None:
+    """'auto' (split K over idle SMs for eligible problems), 'off' or 'force'."""
+    lib().coda_set_split_k(SPLIT_MODES[mode])

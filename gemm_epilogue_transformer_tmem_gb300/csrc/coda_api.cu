@@ -12,6 +12,7 @@
 
 #include "coda_internal.h"
 #include "coda_launch.h"
+#include "coda_sequences.h"
 
 namespace coda {
 
@@ -24,6 +25,9 @@ std::atomic<uint64_t> g_launches{0};
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_max_ctas{0};
 std::atomic<int> g_pair_mode{0};   // 0 auto, 1 single CTAs only, 2 CTA pairs whenever K > 0
+std::atomic<int> g_split_mode{0};  // 0 auto, 1 never split over K, 2 split whenever eligible
+std::atomic<int> g_fixed_seqs{1};  // 1: use the fixed op sequences, 0: always the interpreter
+thread_local coda_plan g_last_plan{};
 
 constexpr int kMaxDevices = 64;
 struct DevInfo {
@@ -285,6 +289,69 @@ size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
   return b;
 }
 
+// CTA pairs once there are two row blocks (mode 0), always (2) or never (1)
+bool use_pair(int64_t M, int64_t K) {
+  const int mode = g_pair_mode.load();
+  return K > 0 && (mode == 2 || (mode == 0 && M > BM));
+}
+
+// Whether a single-CTA problem may split its K range over several CTAs
+// (stream-K).  Automatic: at most 128 tiles of 128 rows and at least 16
+// k-blocks (K >= 1024) -- problems that leave SMs idle and have a long K to
+// share; the decision to split also needs idle SMs on the device.  Forced:
+// any problem with two k-blocks or more.  Independent of the device, so that
+// coda_workspace_size is too.
+bool split_eligible(const Geometry& g, bool pair) {
+  const int mode = g_split_mode.load();
+  if (pair || mode == 1 || g.num_kb < 2) return false;
+  if (mode == 2) return g.num_tiles <= 4096;
+  return g.num_kb >= 16 && g.num_tiles <= 128;
+}
+
+// Split-K part of the workspace, after the rest rounded up to 256 bytes:
+// partial accumulators [tiles][kSplitSegs][BN x BM] fp32, then a u32 arrival
+// counter per tile.
+// The fixed op sequence whose opcodes are exactly this list's, or SEQ_INTERP.
+int match_sequence(const coda_epilogue* epi, bool glu) {
+  if (!g_fixed_seqs.load()) return SEQ_INTERP;
+  const uint32_t n = epi ? epi->n_ops : 0u;
+  for (const SeqDef& d : kSeqDefs) {
+    if (d.glu != glu || static_cast<uint32_t>(d.n) != n) continue;
+    bool same = true;
+    for (uint32_t o = 0; o < n && same; ++o) same = epi->ops[o].opcode == d.codes[o];
+    if (same) return d.id;
+  }
+  return SEQ_INTERP;
+}
+
+cudaError_t launch_gemm_seq(int seq, bool glu, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                            const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
+  switch (seq) {
+    case SEQ_RMS:
+    case SEQ_LN:
+      return launch_gemm_norm(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_RMS_SWIGLU:
+      return launch_gemm_norm_glu(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_NONE:
+    case SEQ_RESIDUAL:
+    case SEQ_BIAS_GELU_RESIDUAL:
+      return launch_gemm_fwd(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_SWIGLU:
+    case SEQ_SWIGLU_DROPOUT:
+      return launch_gemm_fwd_glu(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_DGRAD:
+      return launch_gemm_bwd(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    default:
+      return launch_gemm_interp(glu, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+  }
+}
+
+size_t split_base(size_t b) { return (b + 255) & ~size_t(255); }
+size_t split_bytes(const Geometry& g) {
+  return static_cast<size_t>(g.num_tiles) * kSplitSegs * kPartFloats * sizeof(float) +
+         static_cast<size_t>(g.num_tiles) * sizeof(uint32_t);
+}
+
 coda_status check_dims(int64_t M, int64_t N, int64_t K) {
   const int64_t lim = (int64_t{1} << 31) - 1;
   if (M < 0 || N < 0 || K < 0 || M > lim || N > lim || K > lim) return CODA_ERR_INVALID_ARG;
@@ -297,11 +364,9 @@ coda_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CODA_OK : CODA_
 }  // namespace
 }  // namespace coda
 
-using namespace coda;
-
-extern "C" {
-
-coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi, size_t* bytes) {
+namespace coda {
+coda_status workspace_need(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi, bool with_split,
+                           size_t* bytes) {
   if (bytes == nullptr) return CODA_ERR_INVALID_ARG;
   *bytes = 0;
   coda_status s = check_dims(M, N, K);
@@ -317,8 +382,21 @@ coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epil
   dummy.ln_colsum = dummy.ln_bias = reinterpret_cast<const float*>(kAligned);
   s = compile_epilogue(epi, &dummy, N, K, true, c);
   if (s != CODA_OK) return s;
-  *bytes = workspace_bytes_for(M, geometry(M, N, K, c.glu), c);
+  const bool pair = use_pair(M, K);
+  const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM);
+  const size_t base = workspace_bytes_for(M, g, c);
+  *bytes = (with_split && split_eligible(g, pair)) ? split_base(base) + split_bytes(g) : base;
   return CODA_OK;
+}
+}  // namespace coda
+
+using namespace coda;
+
+extern "C" {
+
+
+coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi, size_t* bytes) {
+  return workspace_need(M, N, K, epi, true, bytes);
 }
 
 coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int32_t b_layout,
@@ -337,12 +415,13 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   if (row_stats && !aligned4(row_stats)) return CODA_ERR_ALIGNMENT;
   if (row_keep_count && !aligned4(row_keep_count)) return CODA_ERR_ALIGNMENT;
   // CTA pairs (cta_group::2, 256-row tiles) once there are at least two row blocks
-  const int pair_mode = g_pair_mode.load();
-  const bool pair = K > 0 && (pair_mode == 2 || (pair_mode == 0 && M > BM));
+  const bool pair = use_pair(M, K);
   const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM);
   if (g.num_tiles > (int64_t{1} << 31) - 1) return CODA_ERR_UNSUPPORTED;
   const size_t ws_need = workspace_bytes_for(M, g, c);
   if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
+  const bool split_room = split_eligible(g, pair) && workspace != nullptr &&
+                          workspace_bytes >= split_base(ws_need) + split_bytes(g);
   if (workspace && !aligned16(workspace)) return CODA_ERR_ALIGNMENT;
 
   DevInfo dev;
@@ -436,10 +515,33 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   int grid = dev.sms;
   if (cap > 0 && cap < grid) grid = cap;
   cudaError_t e;
-  // CTA pairs take the commuted-norm row scales from a pre-pass kernel (their A
-  // halves signal the pair leader's barrier, so no row-statistics warps)
-  const bool rowstat_warps = c.has_rms && !pair;
-  if (pair && c.has_rms) {
+  // Split over K when the tiles would leave SMs idle: the grid takes equal
+  // runs of (tile, k-block) units, each at least half a tile long so that a
+  // tile has at most kSplitSegs contributors.
+  bool split = false;
+  if (split_room) {
+    const int64_t units = g.num_tiles * g.num_kb;
+    int64_t G = units / ((g.num_kb + 1) / 2);
+    if (G > grid) G = grid;
+    const bool idle = g_split_mode.load() == 2 || g.num_tiles * 4 <= static_cast<int64_t>(grid) * 3;
+    if (idle && G > g.num_tiles) {
+      split = true;
+      grid = static_cast<int>(G);
+      p.split = 1;
+      p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + split_base(ws_need));
+      p.ws_cnt = reinterpret_cast<uint32_t*>(p.ws_part + static_cast<size_t>(g.num_tiles) * kSplitSegs * kPartFloats);
+      e = cudaMemsetAsync(p.ws_cnt, 0, static_cast<size_t>(g.num_tiles) * sizeof(uint32_t), st);
+      if (e != cudaSuccess) return CODA_ERR_CUDA;
+    }
+  }
+  // CTA pairs and split-K grids take the commuted-norm row scales from a
+  // pre-pass kernel (a pair's A halves signal the leader's barrier; a split
+  // CTA sees only part of each row), so they run no row-statistics warps.  So
+  // does a single-CTA grid with fewer tiles than SMs: such a problem is bound
+  // by the weight stream and the per-SM shared-memory traffic, and the
+  // side path's reads of every A stage add to the latter.
+  const bool rowstat_warps = c.has_rms && !pair && !split && g.num_tiles >= grid;
+  if (c.has_rms && !rowstat_warps) {
     float* mu_ws = c.is_ln ? rms_ws + M : nullptr;
     e = launch_rms_rowscale(A, M, K, p.inv_K, c.rms_eps, c.is_ln, rms_ws,
                             c.rms_slot >= 0 ? row_stats + static_cast<size_t>(c.rms_slot) * M : nullptr, mu_ws,
@@ -452,19 +554,25 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   }
   if (pair) {
     int pairs = 0;
-    e = c.glu ? max_pairs_glu(mn, rowstat_warps, smem, &pairs) : max_pairs_plain(mn, rowstat_warps, smem, &pairs);
+    e = max_pairs(c.glu, mn, smem, &pairs);
     if (e != cudaSuccess) return CODA_ERR_CUDA;
     if (pairs < 1) return CODA_ERR_UNSUPPORTED;
     if (pairs > grid / 2) pairs = grid / 2 > 0 ? grid / 2 : 1;
     if (g.num_tiles < pairs) pairs = static_cast<int>(g.num_tiles);
     grid = 2 * pairs;
-  } else if (g.num_tiles < grid) {
+  } else if (!split && g.num_tiles < grid) {
     grid = static_cast<int>(g.num_tiles);
   }
-  e = c.glu ? launch_gemm_glu(mn, rowstat_warps, pair, maps, p, grid, smem, st)
-            : launch_gemm_plain(mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  int seq = match_sequence(epi, c.glu);
+  e = launch_gemm_seq(seq, c.glu, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  if (e == cudaErrorNotSupported && seq != SEQ_INTERP) {
+    (void)cudaGetLastError();   // the sequence has no kernel for this variant: interpret
+    seq = SEQ_INTERP;
+    e = launch_gemm_seq(seq, c.glu, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
+  g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles, p.rms_vec != nullptr ? 1 : 0, seq};
   const bool need_keep = c.prog.has_dropout && row_keep_count != nullptr;
   if (c.prog.n_red > 0 || need_keep) {
     e = launch_finalize(p.ws_red, p.ws_keep, p.M, g.num_n_tiles, c.prog.n_red, c.prog.red,
@@ -609,5 +717,13 @@ void coda_set_pipeline_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns == 0 ? 10
 void coda_set_max_ctas(int32_t n) { g_max_ctas.store(n < 0 ? 0 : n); }
 
 void coda_set_cta_pair(int32_t mode) { g_pair_mode.store(mode < 0 || mode > 2 ? 0 : mode); }
+
+void coda_set_fixed_sequences(int32_t enable) { g_fixed_seqs.store(enable != 0 ? 1 : 0); }
+
+void coda_set_split_k(int32_t mode) { g_split_mode.store(mode < 0 || mode > 2 ? 0 : mode); }
+
+void coda_last_plan(coda_plan* out) {
+  if (out != nullptr) *out = g_last_plan;
+}
 
 }  // extern "C"

@@ -93,6 +93,54 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
   n_tile = local / gm;
 }
 
+// Work of one CTA.  Normally whole tiles, tile0, tile0 + step, ...  With the
+// split over K (stream-K, for problems with fewer tiles than SMs), the
+// num_tiles x num_kb (tile, k-block) units are cut into gridDim.x equal runs;
+// CTA c takes units [c U / G, (c+1) U / G), i.e. the tail of one tile, maybe
+// whole tiles, and the head of another.  Every role walks the same sequence.
+struct Item {
+  int tile, kb0, kb1;
+};
+
+struct WorkIter {
+  int64_t u, u_end;
+  int step;
+  bool split;
+  __device__ __forceinline__ WorkIter(const GemmParams& p, bool split_, int tile0, int tile_step) : split(split_) {
+    if (split) {
+      const int64_t U = static_cast<int64_t>(p.num_tiles) * p.num_kb;
+      u = U * blockIdx.x / gridDim.x;
+      u_end = U * (blockIdx.x + 1) / gridDim.x;
+      step = 0;
+    } else {
+      u = tile0;
+      u_end = p.num_tiles;
+      step = tile_step;
+    }
+  }
+  __device__ __forceinline__ bool next(const GemmParams& p, Item& w) {
+    if (u >= u_end) return false;
+    if (!split) {
+      w.tile = static_cast<int>(u);
+      w.kb0 = 0;
+      w.kb1 = p.num_kb;
+      u += step;
+      return true;
+    }
+    w.tile = static_cast<int>(u / p.num_kb);
+    w.kb0 = static_cast<int>(u - static_cast<int64_t>(w.tile) * p.num_kb);
+    const int64_t end = static_cast<int64_t>(w.kb0) + (u_end - u);
+    w.kb1 = end < p.num_kb ? static_cast<int>(end) : p.num_kb;
+    u += w.kb1 - w.kb0;
+    return true;
+  }
+};
+
+// The CTA whose run holds unit u: the largest c with floor(c U / G) <= u.
+__device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int64_t G) {
+  return static_cast<int>(((u + 1) * G + U - 1) / U) - 1;
+}
+
 // Warp-wide wait: lane 0 alone polls the barrier (32 lanes spinning on one
 // mbarrier serialise in shared memory and steal bandwidth from the MMA's
 // operand reads), then the outcome is broadcast and __syncwarp orders the other
@@ -121,7 +169,7 @@ struct SmemAux {
   }
 };
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi>
 __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
@@ -144,6 +192,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0u;
+  // split-K grids run the single-CTA kernel without row-statistics warps
+  const bool split = !kPair && !kRowStats && p.split != 0;
   const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
@@ -162,6 +212,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     for (int q = 0; q < kEpiWarps; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->auxfull[q][b], 1);
     mbar_init(&ctl->drain, 1);
+    mbar_init(&ctl->esync, kEpiWarps);
     ctl->abort_flag = 0u;
     fence_mbar_init();
     if (p.num_kb > 0) {
@@ -179,6 +230,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       tmem_relinquish();
     }
   }
+  __syncwarp();   // warp 0 diverged around the initialisation above
   tc_fence_before_sync();
   __syncthreads();
   if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before any remote use
@@ -193,7 +245,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_phase = 0;
       bool ok = true;
-      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step) {
+      WorkIter wi(p, split, tile0, tile_step);
+      Item w;
+      while (ok && wi.next(p, w)) {
+        const int tile = w.tile;
         int m_tile, n_tile;
         tile_coords(tile, p, m_tile, n_tile);
         const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
@@ -208,7 +263,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           nb0 = kGLU ? n_tile * (BN / 2) : n_tile * BN;
           nb1 = kGLU ? p.half + n_tile * (BN / 2) : nb0 + BN / 2;
         }
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!W(&ctl->empty[stage], phase ^ 1u, tile)) {
             ok = false;
             break;
@@ -269,7 +324,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = tile0; ok && tile < p.num_tiles; tile += tile_step, ++local) {
+      WorkIter wi(p, split, tile0, tile_step);
+      Item w;
+      for (; ok && wi.next(p, w); ++local) {
+        const int tile = w.tile;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!W(&ctl->tempty[acc], acc_phase ^ 1u, tile)) {
@@ -278,7 +336,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!W(&ctl->full[stage], phase, tile)) {
             ok = false;
             break;
@@ -292,9 +350,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
             const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
                                      : make_smem_desc(b_addr + k * 32, 16, 1024);
             if constexpr (kPair)
-              mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
             else
-              mma_bf16_ss(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              mma_bf16_ss(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
           }
           if constexpr (kPair)
             mma_commit_pair_mc(&ctl->empty[stage], 0x3);
@@ -350,7 +408,23 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       aux_armed |= 1u << b;
     };
 
-    for (int tile = tile0; tile < p.num_tiles; tile += tile_step, ++local) {
+    bool gd_waited = false;
+    uint32_t es_par = 0;      // parity of the next esync phase
+    // Meet the other epilogue warps: every warp arrives once per phase and
+    // waits (bounded) for the phase, so no warp runs more than a phase ahead
+    // and a warp that gave up (timeout, abort) cannot leave the others blocked.
+    // Warp 0 of the epilogue may publish a flag to eflag[phase parity] first.
+    auto esync = [&](int tile) -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->esync);
+      const bool r = warp_wait(W, &ctl->esync, es_par, tile, lane);
+      es_par ^= 1u;
+      return r;
+    };
+    WorkIter wi(p, split, tile0, tile_step);
+    Item w;
+    for (; wi.next(p, w); ++local) {
+      const int tile = w.tile;
       int m_tile, n_tile;
       tile_coords(tile, p, m_tile, n_tile);
       const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
@@ -361,7 +435,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       if (nch > kOutCols / kChunk) nch = kOutCols / kChunk;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
-      if (n_aux > 0) issue_aux(abuf, col_base, m0 + q * 32);
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+      const bool partial = split && !(w.kb0 == 0 && w.kb1 == p.num_kb);
+      if (n_aux > 0 && !partial) issue_aux(abuf, col_base, m0 + q * 32);
 
       bool okw = warp_wait(W, &ctl->tfull[acc], acc_phase, tile, lane);
       if (!okw) {
@@ -369,6 +445,72 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         break;
       }
       tc_fence_after_sync();
+
+      // Split tiles: the CTA that completes a tile's k-range last applies the
+      // epilogue to the sum of every segment's partial accumulator.  No CTA
+      // ever waits for another: each publishes its partial (fence, then a
+      // counter increment) and only the one that sees the count complete goes
+      // on (the fence-and-count reduction of the CUDA programming guide).
+      bool src_tmem = true;    // accumulator values come from tensor memory
+      int n_seg = 0;           // partial segments to add from the workspace
+      int skip_seg = -1;       // ... except this one (the CTA's own, still in tensor memory)
+      const float* seg_base = nullptr;
+      if (partial) {
+        const int64_t U = static_cast<int64_t>(p.num_tiles) * p.num_kb;
+        const int64_t tile_u = static_cast<int64_t>(tile) * p.num_kb;
+        const int first = unit_owner(tile_u, U, gridDim.x);
+        const int nseg = unit_owner(tile_u + p.num_kb - 1, U, gridDim.x) - first + 1;
+        const int seg = static_cast<int>(blockIdx.x) - first;
+        float* slots = p.ws_part + static_cast<size_t>(tile) * kSplitSegs * kPartFloats;
+        uint32_t* cnt = p.ws_cnt + tile;
+        const bool leader_thread = q == 0 && lane == 0;
+        // every other segment already published: finish from tensor memory
+        if (leader_thread) ctl->eflag[es_par] = ld_acquire_gpu(cnt) == static_cast<uint32_t>(nseg - 1) ? 1u : 0u;
+        if (!esync(tile)) {
+          ok = false;
+          break;
+        }
+        const bool last_now = ctl->eflag[es_par ^ 1u] != 0u;
+        if (last_now) {
+          __threadfence();
+          skip_seg = seg;
+        } else {
+          // partial layout: float4 (row r, columns 4q..4q+3) at index q * BM + r,
+          // so one store instruction of a warp covers 512 contiguous bytes
+          float4* mine = reinterpret_cast<float4*>(slots + static_cast<size_t>(seg) * kPartFloats) + r_in_tile;
+#pragma unroll 1
+          for (int c = 0; c < BN / kChunk; ++c) {
+            float v[32];
+            tmem_ld32(t_row + c * kChunk, v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              __stcg(mine + (c * 8 + j) * BM, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+          }
+          tc_fence_before_sync();
+          mbar_arrive(&ctl->tempty[acc]);
+          __threadfence();
+          if (!esync(tile)) {     // every partial store is fenced before the count
+            ok = false;
+            break;
+          }
+          if (leader_thread) {
+            __threadfence();
+            ctl->eflag[es_par] = atomicAdd(cnt, 1u) == static_cast<uint32_t>(nseg - 1) ? 1u : 0u;
+            __threadfence();
+          }
+          if (!esync(tile)) {
+            ok = false;
+            break;
+          }
+          if (ctl->eflag[es_par ^ 1u] == 0u) continue;
+          __threadfence();
+          src_tmem = false;
+        }
+        n_seg = nseg;
+        seg_base = slots + static_cast<size_t>(r_in_tile) * 4;
+        if (n_aux > 0) issue_aux(abuf, col_base, m0 + q * 32);
+      }
+
       float r_rms = 1.0f, mu = 0.0f;
       if (kRowStats) {
         okw = warp_wait(W, &ctl->rsfull[acc], acc_phase, tile, lane);
@@ -382,14 +524,16 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       } else if (p.rms_vec != nullptr) {
         // row statistics from the pre-pass kernel, which may still have been
         // running when this grid started: wait for it before the first read
-        if (local == 0) griddep_wait();
+        if (!gd_waited) {
+          griddep_wait();
+          gd_waited = true;
+        }
         r_rms = row_ok ? p.rms_vec[row] : 1.0f;
         if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
       }
 
       float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t keep = 0;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       for (int c = 0; c < nch; ++c) {
         const int col = col_base + c * kChunk;
         if (n_aux > 0) {
@@ -403,7 +547,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           aux_armed &= ~(1u << abuf);
         }
         float v[32], u[32];
-        if (p.num_kb > 0) {
+        if (p.num_kb > 0 && src_tmem) {
           tmem_ld32(t_row + c * kChunk, v);
           if (kGLU) tmem_ld32(t_row + BN / 2 + c * kChunk, u);
         } else {
@@ -413,7 +557,32 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
             u[j] = 0.0f;
           }
         }
-        if (c == nch - 1) {
+#pragma unroll 1
+        for (int sg = 0; sg < n_seg; ++sg) {
+          if (sg == skip_seg) continue;
+          const float4* sp = reinterpret_cast<const float4*>(seg_base + static_cast<size_t>(sg) * kPartFloats);
+          float4 a[8], b[8];   // all loads of this segment in flight before the adds
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a[j] = __ldcg(sp + (c * 8 + j) * BM);
+          if (kGLU) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) b[j] = __ldcg(sp + ((BN / 2) / 4 + c * 8 + j) * BM);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            v[4 * j] += a[j].x;
+            v[4 * j + 1] += a[j].y;
+            v[4 * j + 2] += a[j].z;
+            v[4 * j + 3] += a[j].w;
+            if (kGLU) {
+              u[4 * j] += b[j].x;
+              u[4 * j + 1] += b[j].y;
+              u[4 * j + 2] += b[j].z;
+              u[4 * j + 3] += b[j].w;
+            }
+          }
+        }
+        if (c == nch - 1 && src_tmem) {
           // accumulator drained: release it to the MMA warp (the leader's barrier)
           tc_fence_before_sync();
           if constexpr (kPair)
@@ -425,7 +594,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         if (nvalid > kChunk) nvalid = kChunk;
         const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
         const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
-        run_ops<32, kGLU>(p.prog, v, u, rc, ax, red, keep);
+        Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red, keep);
 
         // stage bf16 row chunk (64-byte swizzle) and TMA-store the 32x32 box
         uint8_t* ob = out_stage + sbuf * kBoxBytes;
@@ -474,7 +643,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     // Each A stage is read alongside the MMA as soon as it is in shared memory;
     // one arrival per warp frees the stage.  (CTA pairs get their row scales
     // from a pre-pass kernel instead: there the A halves signal the leader's
-    // barrier, not their own CTA's.)
+    // barrier, not their own CTA's.  So do split-K grids, where a CTA sees only
+    // part of a row's K range.)
     const int q = warp - 8;
     const int r = q * 32 + lane;
     const Waiter W{ctl, p.timeout_ns, p.err, ROLE_ROWSTATS};
@@ -536,6 +706,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     }
   }
 
+  // Lanes 1-31 of the producer and MMA warps got here while lane 0 was still in
+  // its loop: reconverge every warp first, so that the CTA barrier (an aligned
+  // barrier, which counts whole warps) waits for every role to finish
+  __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
   if constexpr (kPair) cluster_sync();   // neither CTA leaves while its peer may still signal it
@@ -548,14 +722,29 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   }
 }
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi>
 cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if constexpr (!kPair) {
-    kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
-    return cudaGetLastError();
+    if (p.rms_vec == nullptr) {
+      kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+      return cudaGetLastError();
+    }
+    // after the row-scale pre-pass (split-K grids): start the mainloop early,
+    // the epilogue waits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(kRowStats ? 384 : 256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -579,7 +768,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
 // Largest number of CTA pairs of this kernel that can be resident at once.
 template <bool kGLU, bool kBMN, bool kRowStats>
 cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true, EpiInterp>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -594,6 +783,33 @@ cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaOccupancyMaxActiveClusters(pairs, kern, &cfg);
+}
+
+}  // namespace coda
+
+namespace coda {
+
+// Launch the kernel variant for (B layout, row-statistics warps, CTA pair) with
+// epilogue policy Epi.  kRowStatsOK: the policy can be launched with
+// row-statistics warps (its op sequence has a commuted norm).
+template <class Epi, bool kGLU, bool kRowStatsOK>
+cudaError_t launch_variant(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps, const GemmParams& p,
+                           int grid, size_t smem, cudaStream_t st) {
+  if (pair) {
+    if (row_stats) return cudaErrorNotSupported;   // pairs take row scales from the pre-pass
+    return b_mn_major ? launch_gemm_t<kGLU, true, false, true, Epi>(maps, p, grid, smem, st)
+                      : launch_gemm_t<kGLU, false, false, true, Epi>(maps, p, grid, smem, st);
+  }
+  if (row_stats) {
+    if constexpr (kRowStatsOK) {
+      return b_mn_major ? launch_gemm_t<kGLU, true, true, false, Epi>(maps, p, grid, smem, st)
+                        : launch_gemm_t<kGLU, false, true, false, Epi>(maps, p, grid, smem, st);
+    } else {
+      return cudaErrorNotSupported;
+    }
+  }
+  return b_mn_major ? launch_gemm_t<kGLU, true, false, false, Epi>(maps, p, grid, smem, st)
+                    : launch_gemm_t<kGLU, false, false, false, Epi>(maps, p, grid, smem, st);
 }
 
 }  // namespace coda

@@ -29,6 +29,12 @@ constexpr int kPairStageBBytes = (BN / 2) * BK * 2;  // 16 KB
 constexpr int kPairStageBytes = kStageABytes + kPairStageBBytes;
 constexpr int kBoxBytes = 32 * kChunk * 2;         // 32 rows x 32 bf16 = 2 KB
 constexpr int kMaxStages = 8;
+// Split over K (stream-K): a tile's k-blocks may be shared by up to kSplitSegs
+// CTAs, each publishing a BM x BN fp32 partial accumulator as float4 vectors,
+// vector (row r, columns 4q..4q+3) at index q * BM + r (a warp's 32 rows of one
+// vector column are 512 contiguous bytes).
+constexpr int kSplitSegs = 3;
+constexpr int kPartFloats = BN * BM;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
 
 // aux tensor kinds (index into the aux tensor-map array)
@@ -89,7 +95,9 @@ struct GemmParams {
   const float* rms_vec;    // commuted-norm row scales r from the pre-pass kernel, or null
   const float* mu_vec;     // commuted LayerNorm row means from the pre-pass kernel, or null
   int32_t norm_ln;         // the row statistics are LayerNorm's (mean and centred variance)
-  int32_t pad2;
+  int32_t split;           // 1: CTAs take equal runs of (tile, k-block) units (stream-K)
+  float* ws_part;          // split: [num_tiles][kSplitSegs][kPartFloats] partial accumulators
+  uint32_t* ws_cnt;        // split: [num_tiles] arrival counters, zero at launch
   EpiProgram prog;
 };
 
@@ -104,6 +112,8 @@ struct Ctl {
   uint64_t rsempty[2];
   uint64_t auxfull[kEpiWarps][2];
   uint64_t drain;
+  uint64_t esync;          // the four epilogue warps meet here on split tiles (one arrival each)
+  uint32_t eflag[2];       // flag broadcast through esync, by phase parity
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];

@@ -10,13 +10,23 @@ namespace coda {
 
 // fused GEMM + epilogue; maps = {A, B, D, aux0, aux1, aux2}
 // pair: cta_group::2 on clusters of two CTAs (grid counts CTAs and is even)
-cudaError_t launch_gemm_glu(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps, const GemmParams& p,
-                            int grid, size_t smem, cudaStream_t st);
-cudaError_t launch_gemm_plain(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
-                              const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+// the op-list interpreter (any op list)
+cudaError_t launch_gemm_interp(bool glu, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                               const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+// fixed op sequences (coda_sequences.h); cudaErrorNotSupported for a sequence
+// or variant a translation unit does not hold
+cudaError_t launch_gemm_norm(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                             const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_norm_glu(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                                 const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_fwd(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                            const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_fwd_glu(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                                const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_bwd(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                            const GemmParams& p, int grid, size_t smem, cudaStream_t st);
 // how many CTA pairs of the pair kernel fit on the device at once
-cudaError_t max_pairs_glu(bool b_mn_major, bool row_stats, size_t smem, int* pairs);
-cudaError_t max_pairs_plain(bool b_mn_major, bool row_stats, size_t smem, int* pairs);
+cudaError_t max_pairs(bool glu, bool b_mn_major, size_t smem, int* pairs);
 
 cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
                             const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
@@ -34,5 +44,10 @@ cudaError_t launch_rmsnorm(const void* X, const void* gamma, int64_t M, int64_t 
 cudaError_t launch_epilogue_apply(const void* C, void* D, int64_t M, int N, int N_out, int half,
                                   const void* const* aux, float* row_stats, uint32_t* keep_count,
                                   const EpiProgram& prog, cudaStream_t st);
+
+// Workspace bytes for coda_gemm_epilogue: with_split = the size that allows the
+// split over K (what coda_workspace_size reports), else the minimum.
+coda_status workspace_need(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi, bool with_split,
+                           size_t* bytes);
 
 }  // namespace coda

@@ -25,6 +25,7 @@
 #include <mutex>
 
 #include "coda_internal.h"
+#include "coda_launch.h"
 
 namespace {
 
@@ -55,14 +56,15 @@ extern "C" CODA_API coda_status coda_gemm_epilogue_noalloc(const void* A, const 
                                                            int64_t K, int32_t b_layout, const coda_epilogue* epi,
                                                            const coda_aux* aux, void* D, float* row_stats,
                                                            uint32_t* row_keep_count, void* stream) {
+  // the minimum the problem needs; the whole buffer is offered, so the split
+  // over K runs when its partials fit as well
   size_t need = 0;
-  coda_status s = coda_workspace_size(M, N, K, epi, &need);
+  coda_status s = coda::workspace_need(M, N, K, epi, false, &need);
   if (s != CODA_OK) return s;
   if (need > static_cast<size_t>(CODA_NOALLOC_SCRATCH_BYTES)) return CODA_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (need > 0) {
-    s = scratch_address(&scratch);
-    if (s != CODA_OK) return s;
-  }
-  return coda_gemm_epilogue(A, B, M, N, K, b_layout, epi, aux, D, row_stats, row_keep_count, scratch, need, stream);
+  s = scratch_address(&scratch);
+  if (s != CODA_OK) return s;
+  return coda_gemm_epilogue(A, B, M, N, K, b_layout, epi, aux, D, row_stats, row_keep_count, scratch,
+                            CODA_NOALLOC_SCRATCH_BYTES, stream);
 }

@@ -19,20 +19,45 @@ constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kGeluC = 0.044715f;
 constexpr uint64_t kSplitmixGamma = 0x9E3779B97F4A7C15ull;
 
-__device__ __forceinline__ float gelu_tanh_f(float x) {
-  const float inner = kSqrt2OverPi * fmaf(kGeluC * x * x, x, x);
-  return 0.5f * x * (1.0f + tanhf(inner));
+// The logistic function and the activations built on it.  The epilogue has one
+// warp per scheduler and no other work to hide latency behind, so these use
+// the hardware exponential (__expf) and the fast division (__fdividef), whose
+// errors (a few ulp, ~1e-6 relative) are far below the bf16 rounding of the
+// output (2^-9 relative).  The argument is clamped to [-80, 80], where the
+// logistic function is 0 or 1 to fp32 precision, so that e^-x stays finite
+// and no inf/inf or 0*inf can arise.
+//   sigmoid(x) = 1 / (1 + e^-x),  1 - sigmoid(x) = e^-x sigmoid(x)
+__device__ __forceinline__ float sigmoid_f(float x, float& one_minus) {
+  const float e = __expf(-fminf(fmaxf(x, -80.0f), 80.0f));
+  const float s = __fdividef(1.0f, 1.0f + e);
+  one_minus = e * s;
+  return s;
 }
 
-// derivative of gelu_tanh_f: product rule on 0.5 x (1 + tanh(u(x)))
+__device__ __forceinline__ float silu_f(float x) {
+  float om;
+  return x * sigmoid_f(x, om);
+}
+
+// tanh-form GELU: 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3);
+// since (1 + tanh(u)) / 2 = sigmoid(2u), this is x sigmoid(2u)
+__device__ __forceinline__ float gelu_tanh_f(float x) {
+  const float u = kSqrt2OverPi * fmaf(kGeluC * x * x, x, x);
+  float om;
+  return x * sigmoid_f(2.0f * u, om);
+}
+
+// derivative of gelu_tanh_f: 0.5 (1 + t) + 0.5 z (1 - t^2) u'(z) with t = tanh(u);
+// with s = sigmoid(2u): (1 + t) / 2 = s and 1 - t^2 = 4 s (1 - s), so the
+// derivative is s + 2 z s (1 - s) u'(z), free of the cancellation in 1 - t^2
 __device__ __forceinline__ float gelu_tanh_grad_f(float z) {
   const float z2 = z * z;
-  const float t = tanhf(kSqrt2OverPi * fmaf(kGeluC * z2, z, z));
+  const float u = kSqrt2OverPi * fmaf(kGeluC * z2, z, z);
   const float du = kSqrt2OverPi * fmaf(3.0f * kGeluC, z2, 1.0f);
-  return 0.5f * (1.0f + t) + 0.5f * z * (1.0f - t * t) * du;
+  float om;
+  const float s = sigmoid_f(2.0f * u, om);
+  return fmaf(2.0f * z * du, s * om, s);
 }
-
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + expf(-x)); }
 
 // exact GELU: x * Phi(x), Phi the standard normal distribution function
 __device__ __forceinline__ float gelu_erf_f(float x) { return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f)); }
@@ -148,8 +173,187 @@ struct RowCtx {
   float mu;         // commuted-LayerNorm row mean of this row
 };
 
-// Run the op list on v (and, before SWIGLU, on u).  `aux.load(k, out)` fills
-// NE values of aux tensor k for this run.
+// One op of the list applied to v (and, before SWIGLU, to u: `pre`), with the
+// opcode fixed at compile time.  Both the op-list interpreter below and the
+// fixed op sequences call this, so every op has one implementation.
+// `aux.load(k, out)` fills NE values of aux tensor k for this run.
+template <uint32_t CODE, int NE, bool kGLU, class Aux>
+__device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, bool pre, float (&v)[NE], float (&u)[NE],
+                                         const RowCtx& c, const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS],
+                                         uint32_t& keep_cnt) {
+  switch (CODE) {
+    case CODA_OP_SCALE: {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] *= op.f0;
+      if (pre) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] *= op.f0;
+      }
+      break;
+    }
+    case CODA_OP_COL_SCALE:
+    case CODA_OP_BIAS: {
+      const uint16_t* vec = P.col_vec[op.slot];
+      float cv[NE];
+      load_colvec<NE>(vec, c.col, c.n_out, cv);
+      constexpr bool is_bias = CODE == CODA_OP_BIAS;
+      if constexpr (is_bias) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] += cv[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] *= cv[j];
+      }
+      if (pre) {
+        load_colvec<NE>(vec + c.half, c.col, c.n_out, cv);
+        if constexpr (is_bias) {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] += cv[j];
+        } else {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) u[j] *= cv[j];
+        }
+      }
+      break;
+    }
+    case CODA_OP_ROW_SCALE:
+    case CODA_OP_RMS_ROWSCALE: {
+      const float s = (CODE == CODA_OP_RMS_ROWSCALE) ? c.r_rms
+                      : (c.row_ok ? __ldg(P.row_vec[op.slot] + c.row) : 0.0f);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] *= s;
+      if (pre) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] *= s;
+      }
+      break;
+    }
+    case CODA_OP_LN_ROWSCALE: {
+      // r (x - mu c_j) + b_j
+      float cv[NE], bv[NE];
+      load_colvec_f32<NE>(P.ln_colsum, c.col, c.n_out, cv);
+      load_colvec_f32<NE>(P.ln_bias, c.col, c.n_out, bv);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], v[j]), bv[j]);
+      if (pre) {
+        load_colvec_f32<NE>(P.ln_colsum ? P.ln_colsum + c.half : nullptr, c.col, c.n_out, cv);
+        load_colvec_f32<NE>(P.ln_bias ? P.ln_bias + c.half : nullptr, c.col, c.n_out, bv);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], u[j]), bv[j]);
+      }
+      break;
+    }
+    case CODA_OP_GELU_TANH: {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] = gelu_tanh_f(v[j]);
+      if (pre) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] = gelu_tanh_f(u[j]);
+      }
+      break;
+    }
+    case CODA_OP_GELU_ERF: {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] = gelu_erf_f(v[j]);
+      if (pre) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] = gelu_erf_f(u[j]);
+      }
+      break;
+    }
+    case CODA_OP_GELU_ERF_GRAD: {
+      float z[NE];
+      aux.load(op.aux, z);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] *= gelu_erf_grad_f(z[j]);
+      break;
+    }
+    case CODA_OP_SILU: {
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]);
+      if (pre) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] = silu_f(u[j]);
+      }
+      break;
+    }
+    case CODA_OP_SWIGLU: {
+      if (kGLU) {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]) * u[j];
+      }
+      break;
+    }
+    case CODA_OP_GELU_TANH_GRAD: {
+      float z[NE];
+      aux.load(op.aux, z);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] *= gelu_tanh_grad_f(z[j]);
+      break;
+    }
+    case CODA_OP_DROPOUT: {
+      // element (row, col + j) is output n = row*N_out + col + j of the stream
+      const uint64_t n0 = static_cast<uint64_t>(c.row) * static_cast<uint64_t>(c.n_out) +
+                          static_cast<uint64_t>(c.col);
+      uint64_t state = P.seed + (n0 + 1ull) * kSplitmixGamma;
+      const bool keep_all = op.f0 == 0.0f;
+      uint32_t kc = 0;
+#pragma unroll
+      for (int j = 0; j < NE; ++j) {
+        const bool keep = keep_all || (splitmix_mix(state) < op.u);
+        state += kSplitmixGamma;
+        v[j] = keep ? v[j] * op.f1 : 0.0f;
+        kc += (keep && j < c.nvalid) ? 1u : 0u;
+      }
+      keep_cnt += kc;
+      break;
+    }
+    case CODA_OP_RESIDUAL: {
+      float r[NE];
+      aux.load(op.aux, r);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] = fmaf(op.f0, r[j], v[j]);
+      break;
+    }
+    case CODA_OP_STORE_PREACT: {
+      if (c.row_ok) {
+        uint16_t* base = P.preact + static_cast<size_t>(c.row) * static_cast<size_t>(P.preact_width);
+        store_row_bf16<NE>(base, c.col, c.n_out, v);
+        if (pre) store_row_bf16<NE>(base + c.half, c.col, c.n_out, u);
+      }
+      break;
+    }
+    case CODA_OP_ROW_SUM:
+    case CODA_OP_ROW_MEAN: {
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] : 0.0f;
+      add_red(red, op.red, s);
+      break;
+    }
+    case CODA_OP_ROW_SUMSQ: {
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * v[j] : 0.0f;
+      add_red(red, op.red, s);
+      break;
+    }
+    case CODA_OP_ROW_DOT_AUX: {
+      float x[NE];
+      aux.load(op.aux, x);
+      float s = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * x[j] : 0.0f;
+      add_red(red, op.red, s);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// Run the op list on v (and, before SWIGLU, on u): the interpreter, for any
+// list the library has no fixed sequence for.
 template <int NE, bool kGLU, class Aux>
 __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], float (&u)[NE], const RowCtx& c,
                                         const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS], uint32_t& keep_cnt) {
@@ -158,175 +362,101 @@ __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], flo
     const DevOp op = P.ops[o];
     const bool pre = kGLU && (o < P.glu_pos);
     switch (op.code) {
-      case CODA_OP_SCALE: {
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] *= op.f0;
-        if (pre) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] *= op.f0;
-        }
+      case CODA_OP_SCALE:
+        op_apply<CODA_OP_SCALE, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
       case CODA_OP_COL_SCALE:
-      case CODA_OP_BIAS: {
-        const uint16_t* vec = P.col_vec[op.slot];
-        float cv[NE];
-        load_colvec<NE>(vec, c.col, c.n_out, cv);
-        const bool is_bias = op.code == CODA_OP_BIAS;
-        if (is_bias) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) v[j] += cv[j];
-        } else {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) v[j] *= cv[j];
-        }
-        if (pre) {
-          load_colvec<NE>(vec + c.half, c.col, c.n_out, cv);
-          if (is_bias) {
-#pragma unroll
-            for (int j = 0; j < NE; ++j) u[j] += cv[j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < NE; ++j) u[j] *= cv[j];
-          }
-        }
+        op_apply<CODA_OP_COL_SCALE, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
+      case CODA_OP_BIAS:
+        op_apply<CODA_OP_BIAS, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
       case CODA_OP_ROW_SCALE:
-      case CODA_OP_RMS_ROWSCALE: {
-        const float s = (op.code == CODA_OP_RMS_ROWSCALE) ? c.r_rms
-                        : (c.row_ok ? __ldg(P.row_vec[op.slot] + c.row) : 0.0f);
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] *= s;
-        if (pre) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] *= s;
-        }
+        op_apply<CODA_OP_ROW_SCALE, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_LN_ROWSCALE: {
-        // r (x - mu c_j) + b_j
-        float cv[NE], bv[NE];
-        load_colvec_f32<NE>(P.ln_colsum, c.col, c.n_out, cv);
-        load_colvec_f32<NE>(P.ln_bias, c.col, c.n_out, bv);
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], v[j]), bv[j]);
-        if (pre) {
-          load_colvec_f32<NE>(P.ln_colsum ? P.ln_colsum + c.half : nullptr, c.col, c.n_out, cv);
-          load_colvec_f32<NE>(P.ln_bias ? P.ln_bias + c.half : nullptr, c.col, c.n_out, bv);
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], u[j]), bv[j]);
-        }
+      case CODA_OP_RMS_ROWSCALE:
+        op_apply<CODA_OP_RMS_ROWSCALE, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_GELU_TANH: {
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] = gelu_tanh_f(v[j]);
-        if (pre) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] = gelu_tanh_f(u[j]);
-        }
+      case CODA_OP_LN_ROWSCALE:
+        op_apply<CODA_OP_LN_ROWSCALE, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_GELU_ERF: {
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] = gelu_erf_f(v[j]);
-        if (pre) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] = gelu_erf_f(u[j]);
-        }
+      case CODA_OP_GELU_TANH:
+        op_apply<CODA_OP_GELU_TANH, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_GELU_ERF_GRAD: {
-        float z[NE];
-        aux.load(op.aux, z);
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] *= gelu_erf_grad_f(z[j]);
+      case CODA_OP_GELU_ERF:
+        op_apply<CODA_OP_GELU_ERF, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_SILU: {
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]);
-        if (pre) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) u[j] = silu_f(u[j]);
-        }
+      case CODA_OP_GELU_ERF_GRAD:
+        op_apply<CODA_OP_GELU_ERF_GRAD, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_SWIGLU: {
-        if (kGLU) {
-#pragma unroll
-          for (int j = 0; j < NE; ++j) v[j] = silu_f(v[j]) * u[j];
-        }
+      case CODA_OP_SILU:
+        op_apply<CODA_OP_SILU, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_GELU_TANH_GRAD: {
-        float z[NE];
-        aux.load(op.aux, z);
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] *= gelu_tanh_grad_f(z[j]);
+      case CODA_OP_SWIGLU:
+        op_apply<CODA_OP_SWIGLU, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_DROPOUT: {
-        // element (row, col + j) is output n = row*N_out + col + j of the stream
-        const uint64_t n0 = static_cast<uint64_t>(c.row) * static_cast<uint64_t>(c.n_out) +
-                            static_cast<uint64_t>(c.col);
-        uint64_t state = P.seed + (n0 + 1ull) * kSplitmixGamma;
-        const bool keep_all = op.f0 == 0.0f;
-        uint32_t kc = 0;
-#pragma unroll
-        for (int j = 0; j < NE; ++j) {
-          const bool keep = keep_all || (splitmix_mix(state) < op.u);
-          state += kSplitmixGamma;
-          v[j] = keep ? v[j] * op.f1 : 0.0f;
-          kc += (keep && j < c.nvalid) ? 1u : 0u;
-        }
-        keep_cnt += kc;
+      case CODA_OP_GELU_TANH_GRAD:
+        op_apply<CODA_OP_GELU_TANH_GRAD, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_RESIDUAL: {
-        float r[NE];
-        aux.load(op.aux, r);
-#pragma unroll
-        for (int j = 0; j < NE; ++j) v[j] = fmaf(op.f0, r[j], v[j]);
+      case CODA_OP_DROPOUT:
+        op_apply<CODA_OP_DROPOUT, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_STORE_PREACT: {
-        if (c.row_ok) {
-          uint16_t* base = P.preact + static_cast<size_t>(c.row) * static_cast<size_t>(P.preact_width);
-          store_row_bf16<NE>(base, c.col, c.n_out, v);
-          if (pre) store_row_bf16<NE>(base + c.half, c.col, c.n_out, u);
-        }
+      case CODA_OP_RESIDUAL:
+        op_apply<CODA_OP_RESIDUAL, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
+      case CODA_OP_STORE_PREACT:
+        op_apply<CODA_OP_STORE_PREACT, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
       case CODA_OP_ROW_SUM:
-      case CODA_OP_ROW_MEAN: {
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] : 0.0f;
-        add_red(red, op.red, s);
+        op_apply<CODA_OP_ROW_SUM, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_ROW_SUMSQ: {
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * v[j] : 0.0f;
-        add_red(red, op.red, s);
+      case CODA_OP_ROW_MEAN:
+        op_apply<CODA_OP_ROW_MEAN, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
-      case CODA_OP_ROW_DOT_AUX: {
-        float x[NE];
-        aux.load(op.aux, x);
-        float s = 0.0f;
-#pragma unroll
-        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * x[j] : 0.0f;
-        add_red(red, op.red, s);
+      case CODA_OP_ROW_SUMSQ:
+        op_apply<CODA_OP_ROW_SUMSQ, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
-      }
+      case CODA_OP_ROW_DOT_AUX:
+        op_apply<CODA_OP_ROW_DOT_AUX, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
       default:
         break;
     }
   }
 }
+
+// A fixed op sequence (the opcodes of a hot op list, known at compile time):
+// straight-line code without the interpreter's per-op dispatch.  The op
+// parameters (scalars, slots, aux indices) still come from the op list.
+template <uint32_t... Codes>
+struct OpSeq {
+  static constexpr int size = sizeof...(Codes);
+};
+
+template <int NE, bool kGLU, class Aux, uint32_t... Codes>
+__device__ __forceinline__ void run_seq(OpSeq<Codes...>, const EpiProgram& P, float (&v)[NE], float (&u)[NE],
+                                        const RowCtx& c, const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS],
+                                        uint32_t& keep_cnt) {
+  int o = 0;
+  ((op_apply<Codes, NE, kGLU>(P, P.ops[o], kGLU && (o < P.glu_pos), v, u, c, aux, red, keep_cnt), ++o), ...);
+}
+
+// Epilogue policies for the fused kernel: the interpreter, or one fixed sequence.
+struct EpiInterp {
+  template <int NE, bool kGLU, class Aux>
+  __device__ __forceinline__ static void run(const EpiProgram& P, float (&v)[NE], float (&u)[NE], const RowCtx& c,
+                                             const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS], uint32_t& keep_cnt) {
+    run_ops<NE, kGLU>(P, v, u, c, aux, red, keep_cnt);
+  }
+};
+
+template <uint32_t... Codes>
+struct EpiFixed {
+  template <int NE, bool kGLU, class Aux>
+  __device__ __forceinline__ static void run(const EpiProgram& P, float (&v)[NE], float (&u)[NE], const RowCtx& c,
+                                             const Aux& aux, float (&red)[CODA_MAX_REDUCTIONS], uint32_t& keep_cnt) {
+    run_seq<NE, kGLU>(OpSeq<Codes...>{}, P, v, u, c, aux, red, keep_cnt);
+  }
+};
 
 }  // namespace coda

@@ -306,3 +306,10 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace coda
+
+// GPU-scope acquire load of a counter that other CTAs increment
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}

@@ -216,8 +216,9 @@ CODA_API coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M,
  * CODA_NOALLOC_SCRATCH_BYTES that the library holds on every GPU it is loaded
  * on, for the life of the process.  Arguments, results and errors are those of
  * coda_gemm_epilogue, plus CODA_ERR_WORKSPACE when the problem needs more
- * scratch than the buffer holds (coda_workspace_size tells how much it needs;
- * problems without reductions or keep counts need none).  It calls no
+ * scratch than the buffer holds (coda_workspace_size tells how much it needs,
+ * less its split-K part: the split over K runs only when its partials fit as
+ * well; problems without reductions, keep counts or a commuted norm need none).  It calls no
  * allocating routine.  The first call on a device looks up the buffer's device
  * address (cudaGetSymbolAddress, with that device current); make that first
  * call before any stream capture.  All calls share the buffer: calls whose
@@ -230,8 +231,13 @@ CODA_API coda_status coda_gemm_epilogue_noalloc(const void* A, const void* B, in
                                                 void* D, float* row_stats, uint32_t* row_keep_count,
                                                 void* stream);
 
-/* Scratch bytes coda_gemm_epilogue needs for these sizes and this op list
- * (row-reduction and keep-count partials, one per 128/256-column tile). */
+/* Scratch bytes coda_gemm_epilogue wants for these sizes and this op list:
+ * row-reduction and keep-count partials (one per 128/256-column tile), the
+ * commuted-norm row statistics, and -- for a problem of at most 128 tiles of
+ * 128 rows with K >= 1024, which leaves SMs idle -- the split-K partial
+ * accumulators (3 x 128 KB per tile) and arrival counters.  A workspace that
+ * holds everything but the split-K part is accepted and runs without the split.
+ * The answer depends on coda_set_cta_pair / coda_set_split_k, not on the device. */
 CODA_API coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi,
                                 size_t* bytes);
 
@@ -315,6 +321,35 @@ CODA_API void coda_set_max_ctas(int32_t n);
 /* 0 (default): CTA pairs (tcgen05 cta_group::2 on 256-row tiles, two SMs per
  * tile) when M > 128; 1: single-CTA 128-row tiles only; 2: CTA pairs whenever K > 0. */
 CODA_API void coda_set_cta_pair(int32_t mode);
+/* Split over K (stream-K) for single-CTA problems with fewer tiles than SMs:
+ * the grid takes equal runs of (tile, 64-wide k-block) units, CTAs that share a
+ * tile publish fp32 partial accumulators to the workspace, and the last to
+ * finish applies the epilogue to their sum; no CTA waits for another.
+ * 0 (default): when at most 3/4 of the SMs would have a tile and the problem is
+ * eligible (see coda_workspace_size) and the workspace holds the partials;
+ * 1: never; 2: whenever a single-CTA problem has two k-blocks or more. */
+CODA_API void coda_set_split_k(int32_t mode);
+
+/* How the calling thread's last successful coda_gemm_epilogue call ran. */
+typedef struct {
+  int32_t pair;      /* 1: CTA-pair kernel (256-row tiles), 0: single CTA     */
+  int32_t split;     /* 1: K split over CTAs (stream-K)                       */
+  int32_t grid;      /* CTAs launched                                         */
+  int32_t stages;    /* shared-memory pipeline stages                         */
+  int64_t tiles;     /* output tiles                                          */
+  int32_t prepass;   /* 1: a row-statistics pre-pass kernel ran first         */
+  int32_t sequence;  /* 0: op-list interpreter; > 0: a fixed op sequence      */
+} coda_plan;
+CODA_API void coda_last_plan(coda_plan* out);
+
+/* Fixed op sequences (the CODA article, d9bl.com, §3.3, compiles each
+ * epilogue into a specialised kernel): for the op lists of the common blocks --
+ * plain GEMM; RMS_ROWSCALE; LN_ROWSCALE; RESIDUAL; BIAS, GELU_TANH, RESIDUAL;
+ * GELU_TANH_GRAD, ROW_DOT_AUX, ROW_SUM; SWIGLU; RMS_ROWSCALE, SWIGLU; SWIGLU,
+ * DROPOUT -- the library launches a kernel built with those opcodes fixed
+ * (straight-line epilogue code); every other list runs the op interpreter.
+ * Results are the same either way.  1 (default): use them; 0: interpret all. */
+CODA_API void coda_set_fixed_sequences(int32_t enable);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,7 @@ TIMEOUT = 5
 ROLES = {1: "producer", 2: "mma", 3: "epilogue", 4: "row statistics"}
 
 
-@pytest.mark.parametrize("mode", ["single", "pair"])
+@pytest.mark.parametrize("mode", ["single", "pair", "split"])
 def test_pipeline_wait_times_out_and_context_recovers(mode):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
@@ -35,7 +35,8 @@ def test_pipeline_wait_times_out_and_context_recovers(mode):
     ops = [("GELU_TANH",), ("ROW_SUM", 0)]
     st0, _ = coda.check_device_error()
     assert st0 == 0
-    coda.set_cta_pair(mode)
+    coda.set_cta_pair("pair" if mode == "pair" else "single")
+    coda.set_split_k("force" if mode == "split" else "off")
     try:
         coda.set_pipeline_timeout_ns(1)
         coda.gemm_epilogue(A, B, ops)          # enqueued fine; the kernel gives up
@@ -50,6 +51,7 @@ def test_pipeline_wait_times_out_and_context_recovers(mode):
     r = coda.gemm_epilogue(A, B, ops)
     st3, info3 = coda.check_device_error()
     coda.set_cta_pair("auto")
+    coda.set_split_k("auto")
     assert st3 == 0, info3
     ref = O.run_chain(O.to_f64(A), O.to_f64(B), ops)
     got = O.to_f64(r.D)

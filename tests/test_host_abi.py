@@ -160,3 +160,34 @@ def test_workspace_size_for_layernorm_op_list():
     M, N, K = 300, 264, 192
     assert coda.workspace_size(M, N, K, [("LN_ROWSCALE", 0, 1e-5)]) == 2 * M * 4
     assert coda.workspace_size(M, N, K, [("LN_ROWSCALE", -1, 1e-5), ("ROW_SUM", 2)]) >= 2 * M * 4
+
+
+def test_plan_struct_layout():
+    assert ctypes.sizeof(coda.CodaPlan) == 32
+
+
+def test_workspace_size_split_k_closed_form(L):
+    # split-K part: 3 partial accumulators of 256 x 128 fp32 per tile and a u32
+    # counter per tile, after the rest rounded up to 256 bytes
+    part = lambda tiles: tiles * (3 * 256 * 128 * 4 + 4)   # noqa: E731
+    up = lambda b: (b + 255) // 256 * 256                  # noqa: E731
+    # decode-sized SwiGLU up-projection: 86 tiles of 128 output columns, K = 4096
+    assert coda.workspace_size(128, 22016, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == up(128 * 4) + part(86)
+    # plain GEMM, 16 tiles, K = 1024 (16 k-blocks): eligible with no other scratch
+    assert coda.workspace_size(100, 4096, 1024, []) == part(16)
+    # K = 960 (15 k-blocks) or more than 128 tiles: not split automatically
+    assert coda.workspace_size(100, 4096, 960, []) == 0
+    assert coda.workspace_size(128, 129 * 256, 4096, []) == 0
+    # M > 128 runs on CTA pairs, which never split
+    assert coda.workspace_size(300, 4096, 4096, [("ROW_SUM", 0)]) == 16 * 300 * 4
+    try:
+        coda.set_split_k("off")
+        assert coda.workspace_size(100, 4096, 1024, []) == 0
+        coda.set_split_k("force")
+        coda.set_cta_pair("single")
+        # forced: any single-CTA problem with two k-blocks or more (3 x 2 tiles here)
+        assert coda.workspace_size(300, 264, 192, [("ROW_SUM", 0)]) == up(2 * 300 * 4) + part(6)
+        assert coda.workspace_size(300, 264, 64, [("ROW_SUM", 0)]) == 2 * 300 * 4
+    finally:
+        coda.set_split_k("auto")
+        coda.set_cta_pair("auto")
