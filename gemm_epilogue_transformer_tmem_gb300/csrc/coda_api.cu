@@ -296,16 +296,16 @@ bool use_pair(int64_t M, int64_t K) {
 }
 
 // Whether a single-CTA problem may split its K range over several CTAs
-// (stream-K).  Automatic: at most 128 tiles of 128 rows and at least 16
-// k-blocks (K >= 1024) -- problems that leave SMs idle and have a long K to
-// share; the decision to split also needs idle SMs on the device.  Forced:
-// any problem with two k-blocks or more.  Independent of the device, so that
-// coda_workspace_size is too.
+// (stream-K).  Automatic: at most 76 tiles of 128 rows (half of GB300's 152
+// SMs) and at least 16 k-blocks (K >= 1024) -- problems that leave most SMs
+// idle and have a long K to share; the decision to split also checks the
+// device's SM count.  Forced: any problem with two k-blocks or more.
+// Independent of the device, so that coda_workspace_size is too.
 bool split_eligible(const Geometry& g, bool pair) {
   const int mode = g_split_mode.load();
   if (pair || mode == 1 || g.num_kb < 2) return false;
   if (mode == 2) return g.num_tiles <= 4096;
-  return g.num_kb >= 16 && g.num_tiles <= 128;
+  return g.num_kb >= 16 && g.num_tiles <= 76;
 }
 
 // Split-K part of the workspace, after the rest rounded up to 256 bytes:
@@ -523,7 +523,11 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
     const int64_t units = g.num_tiles * g.num_kb;
     int64_t G = units / ((g.num_kb + 1) / 2);
     if (G > grid) G = grid;
-    const bool idle = g_split_mode.load() == 2 || g.num_tiles * 4 <= static_cast<int64_t>(grid) * 3;
+    // automatic: only when at most half the SMs would have a tile.  Above that
+    // the tiles' own weight streams already come close to HBM bandwidth
+    // (86 CTAs pull ~6 TB/s), and publishing and re-reading the fp32 partials
+    // costs more than the shorter mainloop saves.
+    const bool idle = g_split_mode.load() == 2 || g.num_tiles * 2 <= static_cast<int64_t>(grid);
     if (idle && G > g.num_tiles) {
       split = true;
       grid = static_cast<int>(G);

@@ -233,8 +233,8 @@ CODA_API coda_status coda_gemm_epilogue_noalloc(const void* A, const void* B, in
 
 /* Scratch bytes coda_gemm_epilogue wants for these sizes and this op list:
  * row-reduction and keep-count partials (one per 128/256-column tile), the
- * commuted-norm row statistics, and -- for a problem of at most 128 tiles of
- * 128 rows with K >= 1024, which leaves SMs idle -- the split-K partial
+ * commuted-norm row statistics, and -- for a problem of at most 76 tiles of
+ * 128 rows with K >= 1024, which leaves most SMs idle -- the split-K partial
  * accumulators (3 x 128 KB per tile) and arrival counters.  A workspace that
  * holds everything but the split-K part is accepted and runs without the split.
  * The answer depends on coda_set_cta_pair / coda_set_split_k, not on the device. */
@@ -325,8 +325,8 @@ CODA_API void coda_set_cta_pair(int32_t mode);
  * the grid takes equal runs of (tile, 64-wide k-block) units, CTAs that share a
  * tile publish fp32 partial accumulators to the workspace, and the last to
  * finish applies the epilogue to their sum; no CTA waits for another.
- * 0 (default): when at most 3/4 of the SMs would have a tile and the problem is
- * eligible (see coda_workspace_size) and the workspace holds the partials;
+ * 0 (default): when at most half of the SMs would have a tile and the problem
+ * is eligible (see coda_workspace_size) and the workspace holds the partials;
  * 1: never; 2: whenever a single-CTA problem has two k-blocks or more. */
 CODA_API void coda_set_split_k(int32_t mode);
 

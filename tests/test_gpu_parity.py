@@ -609,16 +609,24 @@ def test_split_k_plan_and_segments():
         coda.set_cta_pair("auto")
 
 
-def test_full_skinny_split_sampled():
-    # the decode-sized up-projection takes the split path by itself
+@pytest.mark.parametrize("split", ["auto", "force"])
+def test_full_skinny_sampled(split):
+    # the decode-sized up-projection: 86 tiles on one CTA each (automatic), and
+    # split over K across all SMs (forced)
     w = inputs.WORKLOADS["skinny"]
     t = inputs.make_skinny()
     Wf = coda.fold_gamma(cu(t["W"]), cu(t["gamma"]), "kn")
     ops = [("RMS_ROWSCALE", 0, inputs.EPS_RMS), ("SWIGLU",)]
-    r = coda.gemm_epilogue(cu(t["X"]), Wf, ops)
-    plan = coda.last_plan()
-    sync_ok()
-    assert plan["split"] == 1 and plan["prepass"] == 1 and plan["grid"] > plan["tiles"], plan
+    coda.set_split_k(split)
+    try:
+        r = coda.gemm_epilogue(cu(t["X"]), Wf, ops)
+        plan = coda.last_plan()
+        sync_ok()
+    finally:
+        coda.set_split_k("auto")
+    assert plan["prepass"] == 1 and plan["split"] == (1 if split == "force" else 0), plan
+    if split == "force":
+        assert plan["grid"] > plan["tiles"], plan
     assert r.D.shape == (w.M, w.N // 2)
     # As in the LLaMA block (the same weights at 128 tokens): the weight fold
     # bf16(gamma (.)_row W) is the documented preparation, rounded by the

@@ -171,13 +171,14 @@ def test_workspace_size_split_k_closed_form(L):
     # counter per tile, after the rest rounded up to 256 bytes
     part = lambda tiles: tiles * (3 * 256 * 128 * 4 + 4)   # noqa: E731
     up = lambda b: (b + 255) // 256 * 256                  # noqa: E731
-    # decode-sized SwiGLU up-projection: 86 tiles of 128 output columns, K = 4096
-    assert coda.workspace_size(128, 22016, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == up(128 * 4) + part(86)
+    # SwiGLU up-projection, 64 tiles of 128 output columns, K = 4096
+    assert coda.workspace_size(128, 16384, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == up(128 * 4) + part(64)
     # plain GEMM, 16 tiles, K = 1024 (16 k-blocks): eligible with no other scratch
     assert coda.workspace_size(100, 4096, 1024, []) == part(16)
-    # K = 960 (15 k-blocks) or more than 128 tiles: not split automatically
+    # K = 960 (15 k-blocks) or more than 76 tiles (the decode-sized 86): not split automatically
     assert coda.workspace_size(100, 4096, 960, []) == 0
-    assert coda.workspace_size(128, 129 * 256, 4096, []) == 0
+    assert coda.workspace_size(128, 77 * 256, 4096, []) == 0
+    assert coda.workspace_size(128, 22016, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == 128 * 4
     # M > 128 runs on CTA pairs, which never split
     assert coda.workspace_size(300, 4096, 4096, [("ROW_SUM", 0)]) == 16 * 300 * 4
     try:
