@@ -21,12 +21,14 @@ OPCODES = {
     "SCALE": 0, "COL_SCALE": 1, "BIAS": 2, "ROW_SCALE": 3, "RMS_ROWSCALE": 4, "GELU_TANH": 5,
     "SILU": 6, "SWIGLU": 7, "GELU_TANH_GRAD": 8, "DROPOUT": 9, "RESIDUAL": 10, "STORE_PREACT": 11,
     "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15, "GELU_ERF": 16, "GELU_ERF_GRAD": 17,
-    "LN_ROWSCALE": 18,
+    "LN_ROWSCALE": 18, "COL_SUM": 19, "COL_SUMSQ": 20, "COL_DOT_AUX": 21, "COL_DOT_NORM": 22,
 }
+COL_REDUCTIONS = ("COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM")
 REDUCTIONS = ("ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX")
 MAX_OPS = 16
 NO_SLOT = 0xFFFFFFFF
 B_LAYOUTS = {"kn": 0, "nk": 1}
+A_KM = 2   # flag: A is given as [K, M] (the weight gradient X^T @ dY from stored X)
 STATUS = {0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_UNSUPPORTED", 3: "CODA_ERR_ALIGNMENT",
           4: "CODA_ERR_CUDA", 5: "CODA_ERR_TIMEOUT", 6: "CODA_ERR_WORKSPACE"}
 
@@ -44,7 +46,7 @@ class CodaEpilogue(ctypes.Structure):
 class CodaAux(ctypes.Structure):
     _fields_ = [("col_vec", ctypes.c_void_p * 4), ("row_vec", ctypes.c_void_p * 2), ("residual", ctypes.c_void_p),
                 ("z", ctypes.c_void_p), ("xhat", ctypes.c_void_p), ("preact_out", ctypes.c_void_p),
-                ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p)]
+                ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p), ("col_stats", ctypes.c_void_p)]
 
 
 class CodaPlan(ctypes.Structure):
@@ -73,6 +75,7 @@ _SIGS = {
     "coda_rmsnorm": (ctypes.c_int, [_VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP, _VP]),
     "coda_fold_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
     "coda_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP]),
+    "coda_norm_backward": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _VP, _VP]),
     "coda_epilogue_apply": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "coda_check_device_error": (ctypes.c_int, [_VP, _VP]),
     "coda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -157,8 +160,9 @@ def make_epilogue(ops: Sequence, seed: int = 0) -> CodaEpilogue:
 
 
 def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None, ln_colsum=None,
-             ln_bias=None) -> CodaAux:
+             ln_bias=None, col_stats=None) -> CodaAux:
     a = CodaAux()
+    a.col_stats = _ptr(col_stats)
     a.ln_colsum = _ptr(ln_colsum)
     a.ln_bias = _ptr(ln_bias)
     for k, t in (col_vecs or {}).items():
@@ -186,6 +190,14 @@ def stat_slots(ops: Sequence) -> int:
     return n
 
 
+def col_slots(ops: Sequence) -> int:
+    n = 0
+    for name, slot, _ in _norm_ops(ops):
+        if name in COL_REDUCTIONS and slot != NO_SLOT:
+            n = max(n, slot + 1)
+    return n
+
+
 def workspace_size(M: int, N: int, K: int, ops: Sequence = ()) -> int:
     n = ctypes.c_size_t(0)
     e = make_epilogue(ops)
@@ -198,16 +210,21 @@ class Result:
     D: torch.Tensor
     row_stats: Optional[torch.Tensor]
     keep_count: Optional[torch.Tensor]
+    col_stats: Optional[torch.Tensor] = None
 
 
-def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_layout: str = "kn", seed: int = 0,
+def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_layout: str = "kn", a_layout: str = "mk",
+                  seed: int = 0,
                   col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None,
-                  ln_colsum=None, ln_bias=None,
+                  ln_colsum=None, ln_bias=None, col_stats: Optional[torch.Tensor] = None,
                   out: Optional[torch.Tensor] = None, row_stats: Optional[torch.Tensor] = None,
                   keep_count: Optional[torch.Tensor] = None, want_keep_count: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None) -> Result:
-    """D = f(A @ B) through coda_gemm_epilogue; allocates missing outputs with torch."""
-    M, K = A.shape
+    """D = f(A @ B) through coda_gemm_epilogue; allocates missing outputs with torch.
+    a_layout "km": A is [K, M] and the product is A^T @ B."""
+    if a_layout not in ("mk", "km"):
+        raise ValueError(a_layout)
+    M, K = A.shape if a_layout == "mk" else (A.shape[1], A.shape[0])
     N = B.shape[1] if b_layout == "kn" else B.shape[0]
     n_out = output_width(N, ops)
     dev = A.device
@@ -219,16 +236,20 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
     has_dropout = any(o[0] == "DROPOUT" for o in _norm_ops(ops))
     if keep_count is None and has_dropout and want_keep_count:
         keep_count = torch.empty((M,), dtype=torch.int32, device=dev)
+    nc = col_slots(ops)
+    if col_stats is None and nc > 0:
+        col_stats = torch.empty((nc, n_out), dtype=torch.float32, device=dev)
     wbytes = workspace_size(M, N, K, ops)
     if workspace is None and wbytes > 0:
         workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
     e = make_epilogue(ops, seed)
-    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias)
-    st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, B_LAYOUTS[b_layout], ctypes.byref(e), ctypes.byref(a),
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias, col_stats)
+    layout = B_LAYOUTS[b_layout] | (A_KM if a_layout == "km" else 0)
+    st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, layout, ctypes.byref(e), ctypes.byref(a),
                                   _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
                                   workspace.numel() if workspace is not None else 0, _stream(stream))
     _check(st, "coda_gemm_epilogue")
-    return Result(out, row_stats, keep_count)
+    return Result(out, row_stats, keep_count, col_stats)
 
 
 def gemm_epilogue_noalloc(A: torch.Tensor, B: torch.Tensor, ops: Sequence, *, out: torch.Tensor,
@@ -286,6 +307,18 @@ def layernorm(X: torch.Tensor, gamma: torch.Tensor, beta: Optional[torch.Tensor]
         out = torch.empty_like(X)
     _check(lib().coda_layernorm(_ptr(X), _ptr(gamma), _ptr(beta), M, K, eps, _ptr(out), _stream(stream)),
            "coda_layernorm")
+    return out
+
+
+def norm_backward(g: torch.Tensor, X: torch.Tensor, r: torch.Tensor, sum_gx: torch.Tensor,
+                  mu: Optional[torch.Tensor] = None, sum_g: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """dX of RMSNorm (mu = sum_g = None) or LayerNorm from g = gamma * dL/dy and its row sums."""
+    M, K = g.shape
+    if out is None:
+        out = torch.empty_like(g)
+    _check(lib().coda_norm_backward(_ptr(g), _ptr(X), _ptr(r), _ptr(mu), _ptr(sum_g), _ptr(sum_gx), M, K, _ptr(out),
+                                    _stream(stream)), "coda_norm_backward")
     return out
 
 

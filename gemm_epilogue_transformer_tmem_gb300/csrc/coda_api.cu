@@ -106,6 +106,7 @@ struct Compiled {
   float rms_eps = 0.0f;
   bool needs_row_stats = false;
   int max_stat_slot = -1;
+  float* col_stats = nullptr;   // column-reduction output (aux.col_stats)
 };
 
 coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int64_t N, int64_t K, bool fused,
@@ -253,6 +254,30 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         c.needs_row_stats = true;
         if (static_cast<int>(op.slot) > c.max_stat_slot) c.max_stat_slot = static_cast<int>(op.slot);
         break;
+      case CODA_OP_COL_SUM:
+      case CODA_OP_COL_SUMSQ:
+      case CODA_OP_COL_DOT_AUX:
+      case CODA_OP_COL_DOT_NORM:
+        if (!fused) return CODA_ERR_UNSUPPORTED;
+        if (op.opcode == CODA_OP_COL_DOT_NORM) {
+          if (ax.row_vec[0] == nullptr) return CODA_ERR_INVALID_ARG;
+          if (!aligned4(ax.row_vec[0]) || (ax.row_vec[1] && !aligned4(ax.row_vec[1]))) return CODA_ERR_ALIGNMENT;
+          c.prog.row_vec[0] = ax.row_vec[0];
+          c.prog.row_vec[1] = ax.row_vec[1];
+        }
+        if (!after_glu || op.slot >= CODA_MAX_STAT_SLOTS) return CODA_ERR_INVALID_ARG;
+        if (c.prog.n_colred >= CODA_MAX_COL_REDUCTIONS || ax.col_stats == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned4(ax.col_stats)) return CODA_ERR_ALIGNMENT;
+        if (op.opcode == CODA_OP_COL_DOT_AUX || op.opcode == CODA_OP_COL_DOT_NORM) {
+          if (ax.xhat == nullptr) return CODA_ERR_INVALID_ARG;
+          if (!aligned16(ax.xhat)) return CODA_ERR_ALIGNMENT;
+          d.aux = use_aux(AUX_XHAT, ax.xhat);
+        }
+        d.red = c.prog.n_colred;
+        c.prog.colred_slot[c.prog.n_colred] = static_cast<int32_t>(op.slot);
+        ++c.prog.n_colred;
+        c.col_stats = ax.col_stats;
+        break;
       default:
         return CODA_ERR_INVALID_ARG;
     }
@@ -281,11 +306,19 @@ Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu, int tile_m = BM) {
 
 // Workspace layout: row-reduction partials [n_red][column tiles][M] fp32, then
 // keep-count partials [column tiles][M] u32, then the commuted-norm row scales
-// [M] fp32 (written by the pre-pass kernel for CTA-pair tiles).
-size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
+// [M] fp32 (and means [M] for LayerNorm, written by the pre-pass kernel), then
+// column-reduction partials [n_colred][ceil(M/32)][N_out] fp32.
+size_t col_partials_offset(int64_t M, const Geometry& g, const Compiled& c) {
   size_t b = static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * static_cast<size_t>(M) * sizeof(float);
   if (c.prog.has_dropout) b += static_cast<size_t>(g.num_n_tiles) * static_cast<size_t>(M) * sizeof(uint32_t);
   if (c.has_rms) b += static_cast<size_t>(M) * sizeof(float) * (c.is_ln ? 2 : 1);   // r [M] (+ mu [M])
+  return b;
+}
+
+size_t workspace_bytes_for(int64_t M, const Geometry& g, const Compiled& c) {
+  size_t b = col_partials_offset(M, g, c);
+  b += static_cast<size_t>(c.prog.n_colred) * static_cast<size_t>((M + 31) / 32) * static_cast<size_t>(g.n_out) *
+       sizeof(float);
   return b;
 }
 
@@ -324,25 +357,25 @@ int match_sequence(const coda_epilogue* epi, bool glu) {
   return SEQ_INTERP;
 }
 
-cudaError_t launch_gemm_seq(int seq, bool glu, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
-                            const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
+cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
+                            const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
   switch (seq) {
     case SEQ_RMS:
     case SEQ_LN:
-      return launch_gemm_norm(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_norm(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_RMS_SWIGLU:
-      return launch_gemm_norm_glu(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_norm_glu(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_NONE:
     case SEQ_RESIDUAL:
     case SEQ_BIAS_GELU_RESIDUAL:
-      return launch_gemm_fwd(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_fwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_SWIGLU:
     case SEQ_SWIGLU_DROPOUT:
-      return launch_gemm_fwd_glu(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_fwd_glu(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_DGRAD:
-      return launch_gemm_bwd(seq, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_bwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     default:
-      return launch_gemm_interp(glu, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      return launch_gemm_interp(glu, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
   }
 }
 
@@ -380,6 +413,7 @@ coda_status workspace_need(int64_t M, int64_t N, int64_t K, const coda_epilogue*
   dummy.residual = dummy.z = dummy.xhat = kAligned;
   dummy.preact_out = const_cast<uint16_t*>(kAligned);
   dummy.ln_colsum = dummy.ln_bias = reinterpret_cast<const float*>(kAligned);
+  dummy.col_stats = const_cast<float*>(reinterpret_cast<const float*>(kAligned));
   s = compile_epilogue(epi, &dummy, N, K, true, c);
   if (s != CODA_OK) return s;
   const bool pair = use_pair(M, K);
@@ -404,10 +438,14 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
                                uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream) {
   coda_status s = check_dims(M, N, K);
   if (s != CODA_OK) return s;
-  if (b_layout != CODA_B_KN && b_layout != CODA_B_NK) return CODA_ERR_INVALID_ARG;
+  if ((b_layout & ~(CODA_B_NK | CODA_A_KM)) != 0) return CODA_ERR_INVALID_ARG;
+  const bool a_mn = (b_layout & CODA_A_KM) != 0;   // A given as [K, M]
+  b_layout &= CODA_B_NK;
+  if (a_mn && (M % 8) != 0) return CODA_ERR_INVALID_ARG;   // 16-byte rows of A [K, M]
   Compiled c;
   s = compile_epilogue(epi, aux, N, K, true, c);
   if (s != CODA_OK) return s;
+  if (a_mn && c.has_rms) return CODA_ERR_UNSUPPORTED;   // row statistics read A by rows
   if (M == 0 || N == 0) return CODA_OK;
   if (D == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return CODA_ERR_INVALID_ARG;
   if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return CODA_ERR_ALIGNMENT;
@@ -436,8 +474,12 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
                CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != CODA_OK) return s;
   if (K > 0) {
-    s = make_map(&maps[0], A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), BK, BM,
-                 CU_TENSOR_MAP_SWIZZLE_128B);
+    if (a_mn)   // [K, M]: two 64-wide boxes of M per 128-row tile, 64 rows of K
+      s = make_map(&maps[0], A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 64, BK,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      s = make_map(&maps[0], A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != CODA_OK) return s;
     if (b_layout == CODA_B_KN)
       s = make_map(&maps[1], B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, BK,
@@ -493,7 +535,10 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
                                                     static_cast<size_t>(c.prog.n_red) * g.num_n_tiles * M);
     if (c.prog.has_dropout && row_keep_count != nullptr) p.ws_keep = keep_ws;
     rms_ws = reinterpret_cast<float*>(keep_ws + (c.prog.has_dropout ? static_cast<size_t>(g.num_n_tiles) * M : 0));
+    if (c.prog.n_colred > 0)
+      c.prog.ws_col = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + col_partials_offset(M, g, c));
   }
+  c.prog.num_rb = static_cast<int32_t>((M + 31) / 32);
   p.epi_warp_bytes = static_cast<uint32_t>(2 * kBoxBytes + c.n_aux * 2 * kBoxBytes);
   const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * p.epi_warp_bytes;
   const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
@@ -568,15 +613,21 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
     grid = static_cast<int>(g.num_tiles);
   }
   int seq = match_sequence(epi, c.glu);
-  e = launch_gemm_seq(seq, c.glu, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  e = launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
   if (e == cudaErrorNotSupported && seq != SEQ_INTERP) {
     (void)cudaGetLastError();   // the sequence has no kernel for this variant: interpret
     seq = SEQ_INTERP;
-    e = launch_gemm_seq(seq, c.glu, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+    e = launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
   }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
   g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles, p.rms_vec != nullptr ? 1 : 0, seq};
+  if (c.prog.n_colred > 0) {
+    e = launch_finalize_cols(c.prog.ws_col, c.prog.n_colred, c.prog.num_rb, g.n_out, c.prog.colred_slot,
+                             c.col_stats, st);
+    if (e != cudaSuccess) return CODA_ERR_CUDA;
+    g_launches.fetch_add(1);
+  }
   const bool need_keep = c.prog.has_dropout && row_keep_count != nullptr;
   if (c.prog.n_red > 0 || need_keep) {
     e = launch_finalize(p.ws_red, p.ws_keep, p.M, g.num_n_tiles, c.prog.n_red, c.prog.red,
@@ -641,6 +692,25 @@ coda_status coda_layernorm(const void* X, const void* gamma, const void* beta, i
   s = device_info(dev);
   if (s != CODA_OK) return s;
   const cudaError_t e = launch_layernorm(X, gamma, beta, M, K, eps, Xn_out, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_norm_backward(const void* g, const void* X, const float* r, const float* mu, const float* sum_g,
+                               const float* sum_gx, int64_t M, int64_t K, void* dX, void* stream) {
+  coda_status s = check_dims(M, 8, K);
+  if (s != CODA_OK) return s;
+  if (K == 0 || M == 0) return CODA_OK;
+  if (!g || !X || !r || !sum_gx || !dX) return CODA_ERR_INVALID_ARG;
+  if ((mu == nullptr) != (sum_g == nullptr)) return CODA_ERR_INVALID_ARG;   // LayerNorm needs both
+  if (!aligned16(g) || !aligned16(X) || !aligned16(dX)) return CODA_ERR_ALIGNMENT;
+  if (!aligned4(r) || !aligned4(sum_gx) || (mu && !aligned4(mu)) || (sum_g && !aligned4(sum_g)))
+    return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e = launch_norm_backward(g, X, r, mu, sum_g, sum_gx, M, K, dX, dev.sms,
+                                             static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) g_launches.fetch_add(1);
   return from_cuda(e);
 }

@@ -5,11 +5,12 @@
 
 namespace coda {
 
-cudaError_t launch_gemm_bwd(int seq, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+cudaError_t launch_gemm_bwd(int seq, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
+                             const CUtensorMap* maps,
                             const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
   if (seq != SEQ_DGRAD) return cudaErrorNotSupported;
   return launch_variant<EpiFixed<CODA_OP_GELU_TANH_GRAD, CODA_OP_ROW_DOT_AUX, CODA_OP_ROW_SUM>, false, false>(
-      b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+      a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
 }
 
 }  // namespace coda

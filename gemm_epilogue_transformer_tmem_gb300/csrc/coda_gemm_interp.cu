@@ -5,10 +5,11 @@
 
 namespace coda {
 
-cudaError_t launch_gemm_interp(bool glu, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+cudaError_t launch_gemm_interp(bool glu, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
+                             const CUtensorMap* maps,
                                const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  return glu ? launch_variant<EpiInterp, true, true>(b_mn_major, row_stats, pair, maps, p, grid, smem, st)
-             : launch_variant<EpiInterp, false, true>(b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+  return glu ? launch_variant<EpiInterp, true, true, true>(a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st)
+             : launch_variant<EpiInterp, false, true, true>(a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
 }
 
 cudaError_t max_pairs(bool glu, bool b_mn_major, size_t smem, int* pairs) {

@@ -169,7 +169,9 @@ struct SmemAux {
   }
 };
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi>
+// kAMN: A is given as [K, M] (MN-major operand: the weight gradient X^T dY
+// reads the stored activations X [tokens, features] directly).
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN>
 __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
@@ -279,7 +281,12 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           uint8_t* b_dst = sB + stage * kStageB;
           if constexpr (kPair) {
             const uint32_t fbc = mapa_shared(smem_u32(fb), 0u);   // the leader's barrier
-            tma_load_2d_pair(a_dst, &tmA, fbc, k0, m0);
+            if (kAMN) {
+              tma_load_2d_pair(a_dst, &tmA, fbc, m0, k0);
+              tma_load_2d_pair(a_dst + 8192, &tmA, fbc, m0 + 64, k0);
+            } else {
+              tma_load_2d_pair(a_dst, &tmA, fbc, k0, m0);
+            }
             if (kBMN) {
               tma_load_2d_pair(b_dst, &tmB, fbc, nb0, k0);
               tma_load_2d_pair(b_dst + 8192, &tmB, fbc, nb0 + 64, k0);
@@ -287,7 +294,12 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
               tma_load_2d_pair(b_dst, &tmB, fbc, k0, nb0);
             }
           } else {
-            tma_load_2d(a_dst, &tmA, fb, k0, m0);
+            if (kAMN) {
+              tma_load_2d(a_dst, &tmA, fb, m0, k0);
+              tma_load_2d(a_dst + 8192, &tmA, fb, m0 + 64, k0);
+            } else {
+              tma_load_2d(a_dst, &tmA, fb, k0, m0);
+            }
             if (kBMN) {
               tma_load_2d(b_dst, &tmB, fb, nb0, k0);
               tma_load_2d(b_dst + 8192, &tmB, fb, nb0 + 64, k0);
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
-      constexpr uint32_t idesc = make_idesc_bf16(kTileM, BN, kBMN);
+      constexpr uint32_t idesc = make_idesc_bf16(kTileM, BN, kBMN, kAMN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -346,7 +358,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           const uint32_t b_addr = smem_u32(sB + stage * kStageB);
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
-            const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, 1024);
+            // MN-major operands: 64-element groups 8 KB apart, 16 k-rows of 128 B per UMMA_K
+            const uint64_t ad = kAMN ? make_smem_desc(a_addr + k * 2048, 8192, 1024)
+                                     : make_smem_desc(a_addr + k * 32, 16, 1024);
             const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
                                      : make_smem_desc(b_addr + k * 32, 16, 1024);
             if constexpr (kPair)
@@ -668,6 +682,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         const uint8_t* arow = sA + stage * kStageABytes + r * 128;
         if (kb == 0 && p.norm_ln)   // logical chunk 0 sits at physical chunk (r & 7)
           shift = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(arow + ((r & 7) << 4))) << 16);
+        // the last k-block may run past K: TMA fills those columns with zeros,
+        // which must not enter the shifted sums (x - shift would be -shift)
+        const int kvalid = p.K - kb * BK;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint4 w = *reinterpret_cast<const uint4*>(arow + ((j ^ (r & 7)) << 4));
@@ -675,7 +692,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           unpack8(w, x);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            const float d = x[e] - shift;
+            const float d = (8 * j + e < kvalid) ? x[e] - shift : 0.0f;
             s = fmaf(d, d, s);
             s1 += d;
           }
@@ -722,9 +739,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   }
 }
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN = false>
 cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if constexpr (!kPair) {
@@ -768,7 +785,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
 // Largest number of CTA pairs of this kernel that can be resident at once.
 template <bool kGLU, bool kBMN, bool kRowStats>
 cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true, EpiInterp>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true, EpiInterp, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -789,12 +806,25 @@ cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
 
 namespace coda {
 
-// Launch the kernel variant for (B layout, row-statistics warps, CTA pair) with
-// epilogue policy Epi.  kRowStatsOK: the policy can be launched with
-// row-statistics warps (its op sequence has a commuted norm).
-template <class Epi, bool kGLU, bool kRowStatsOK>
-cudaError_t launch_variant(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps, const GemmParams& p,
-                           int grid, size_t smem, cudaStream_t st) {
+// Launch the kernel variant for (A layout, B layout, row-statistics warps, CTA
+// pair) with epilogue policy Epi.  kRowStatsOK: the policy can be launched with
+// row-statistics warps (its op sequence has a commuted norm); kAMNOK: it is
+// built for A given as [K, M] too (never with row statistics).
+template <class Epi, bool kGLU, bool kRowStatsOK, bool kAMNOK = false>
+cudaError_t launch_variant(bool a_mn_major, bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                           const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
+  if (a_mn_major) {
+    if constexpr (kAMNOK) {
+      if (row_stats) return cudaErrorNotSupported;
+      if (pair)
+        return b_mn_major ? launch_gemm_t<kGLU, true, false, true, Epi, true>(maps, p, grid, smem, st)
+                          : launch_gemm_t<kGLU, false, false, true, Epi, true>(maps, p, grid, smem, st);
+      return b_mn_major ? launch_gemm_t<kGLU, true, false, false, Epi, true>(maps, p, grid, smem, st)
+                        : launch_gemm_t<kGLU, false, false, false, Epi, true>(maps, p, grid, smem, st);
+    } else {
+      return cudaErrorNotSupported;
+    }
+  }
   if (pair) {
     if (row_stats) return cudaErrorNotSupported;   // pairs take row scales from the pre-pass
     return b_mn_major ? launch_gemm_t<kGLU, true, false, true, Epi>(maps, p, grid, smem, st)

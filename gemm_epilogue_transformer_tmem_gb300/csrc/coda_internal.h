@@ -72,6 +72,10 @@ struct EpiProgram {
   int32_t pad;
   const float* ln_colsum;  // LN_ROWSCALE: c (fp32 [width])
   const float* ln_bias;    // LN_ROWSCALE: b (fp32 [width]) or null
+  int32_t n_colred;        // column reductions
+  int32_t num_rb;          // 32-row blocks, ceil(M / 32)
+  int32_t colred_slot[CODA_MAX_COL_REDUCTIONS];
+  float* ws_col;           // [n_colred][num_rb][N_out] per-32-row-block column partials
 };
 
 struct GemmParams {

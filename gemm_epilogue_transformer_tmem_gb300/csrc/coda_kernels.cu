@@ -45,6 +45,34 @@ cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M,
   return cudaGetLastError();
 }
 
+// Column reductions: col_stats[slot][j] = sum over the 32-row blocks of the
+// partials (block order, deterministic); a thread per column, coalesced in j.
+struct ColSlots {
+  int32_t s[CODA_MAX_COL_REDUCTIONS];
+};
+
+__global__ void finalize_cols_kernel(const float* __restrict__ ws_col, int n_colred, int num_rb, int64_t n_out,
+                                     ColSlots slots, float* __restrict__ col_stats) {
+  const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  if (j >= n_out) return;
+  for (int r = 0; r < n_colred; ++r) {
+    const float* src = ws_col + static_cast<size_t>(r) * num_rb * n_out + j;
+    float acc = 0.0f;
+    for (int b = 0; b < num_rb; ++b) acc += src[static_cast<size_t>(b) * n_out];
+    col_stats[static_cast<size_t>(slots.s[r]) * n_out + j] = acc;
+  }
+}
+
+cudaError_t launch_finalize_cols(const float* ws_col, int n_colred, int num_rb, int64_t n_out, const int32_t* slots,
+                                 float* col_stats, cudaStream_t st) {
+  ColSlots cs{};
+  for (int r = 0; r < n_colred && r < CODA_MAX_COL_REDUCTIONS; ++r) cs.s[r] = slots[r];
+  const int threads = 256;
+  finalize_cols_kernel<<<static_cast<unsigned>((n_out + threads - 1) / threads), threads, 0, st>>>(
+      ws_col, n_colred, num_rb, n_out, cs, col_stats);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------- commuted-norm row scales
 // Row statistics of A for the commuted norms: the side path for CTA-pair tiles,
 // run just before the GEMM as a full grid at memory bandwidth (a warp per row,
@@ -170,6 +198,48 @@ cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K
   const int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
   rms_rowscale_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
       static_cast<const uint16_t*>(A), M, K, inv_K, eps, layernorm ? 1 : 0, r, r_copy, mu, mu_copy);
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------- norm backward
+// dX = r (g - sum_g / K - x_hat S / K), x_hat = (x - mu) r, S = r (sum_gx - mu sum_g);
+// RMSNorm: mu = sum_g = null.  Eight elements per thread, grid-stride over the
+// [M, K] tensors (K % 8 == 0), 16-byte loads and stores.
+__global__ void norm_backward_kernel(const uint4* __restrict__ g, const uint4* __restrict__ X,
+                                     const float* __restrict__ r, const float* __restrict__ mu,
+                                     const float* __restrict__ sum_g, const float* __restrict__ sum_gx, int64_t M,
+                                     int64_t K, float inv_K, uint4* __restrict__ dX) {
+  const int64_t k8 = K >> 3;
+  const int64_t total = M * k8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = i / k8;
+    const float rr = __ldg(r + row);
+    const float m = mu ? __ldg(mu + row) : 0.0f;
+    const float s1 = sum_g ? __ldg(sum_g + row) : 0.0f;
+    const float S = rr * (__ldg(sum_gx + row) - m * s1);
+    float gv[8], xv[8], out[8];
+    unpack8(__ldg(g + i), gv);
+    unpack8(__ldg(X + i), xv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float xh = (xv[j] - m) * rr;
+      out[j] = rr * (gv[j] - s1 * inv_K - xh * S * inv_K);
+    }
+    dX[i] = pack8(out);
+  }
+}
+
+cudaError_t launch_norm_backward(const void* g, const void* X, const float* r, const float* mu, const float* sum_g,
+                                 const float* sum_gx, int64_t M, int64_t K, void* dX, int num_sms, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t work = M * (K >> 3);
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  norm_backward_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint4*>(g), static_cast<const uint4*>(X), r, mu, sum_g, sum_gx, M, K,
+      static_cast<float>(1.0 / static_cast<double>(K)), static_cast<uint4*>(dX));
   return cudaGetLastError();
 }
 

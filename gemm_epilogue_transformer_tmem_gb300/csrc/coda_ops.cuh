@@ -160,6 +160,23 @@ __device__ __forceinline__ void add_red(float (&red)[CODA_MAX_REDUCTIONS], int i
   else red[3] += s;
 }
 
+// Sums of 32 columns over the 32 rows (lanes) of a warp: after five rounds of
+// exchanging half of the remaining columns with the lane `s` apart and adding,
+// a[0] of lane l holds the sum over all lanes of column l (31 shuffles).
+__device__ __forceinline__ void warp_column_sums(float (&a)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? a[i] : a[i + s];
+      const float keep = upper ? a[i + s] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, s);
+    }
+  }
+}
+
 // Where the row values of one output row live for this run of NE columns.
 struct RowCtx {
   int row;          // absolute output row
@@ -347,6 +364,36 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
       add_red(red, op.red, s);
       break;
     }
+    case CODA_OP_COL_SUM:
+    case CODA_OP_COL_SUMSQ:
+    case CODA_OP_COL_DOT_AUX:
+    case CODA_OP_COL_DOT_NORM: {
+      // the warp's 32 rows of NE = 32 columns: per-column partial over this
+      // 32-row block, finished over the row blocks by a second kernel
+      if constexpr (NE == 32) {
+        float x[NE];
+        if constexpr (CODE == CODA_OP_COL_DOT_AUX || CODE == CODA_OP_COL_DOT_NORM) aux.load(op.aux, x);
+        if constexpr (CODE == CODA_OP_COL_DOT_NORM) {
+          // x_hat = r (aux - mu) with r = rowvec[0], mu = rowvec[1] (or 0)
+          const float rr = c.row_ok ? __ldg(P.row_vec[0] + c.row) : 0.0f;
+          const float mm = (c.row_ok && P.row_vec[1] != nullptr) ? __ldg(P.row_vec[1] + c.row) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < NE; ++j) x[j] = rr * (x[j] - mm);
+        }
+        float a[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float t = (CODE == CODA_OP_COL_SUM) ? v[j] : (CODE == CODA_OP_COL_SUMSQ) ? v[j] * v[j] : v[j] * x[j];
+          a[j] = c.row_ok ? t : 0.0f;
+        }
+        warp_column_sums(a);
+        const int lane = threadIdx.x & 31;
+        const int rb = c.row >> 5;
+        if (rb < P.num_rb && lane < c.nvalid)
+          P.ws_col[(static_cast<size_t>(op.red) * P.num_rb + rb) * c.n_out + c.col + lane] = a[0];
+      }
+      break;
+    }
     default:
       break;
   }
@@ -418,6 +465,18 @@ __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], flo
         break;
       case CODA_OP_ROW_DOT_AUX:
         op_apply<CODA_OP_ROW_DOT_AUX, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
+      case CODA_OP_COL_SUM:
+        op_apply<CODA_OP_COL_SUM, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
+      case CODA_OP_COL_SUMSQ:
+        op_apply<CODA_OP_COL_SUMSQ, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
+      case CODA_OP_COL_DOT_AUX:
+        op_apply<CODA_OP_COL_DOT_AUX, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
+      case CODA_OP_COL_DOT_NORM:
+        op_apply<CODA_OP_COL_DOT_NORM, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
       default:
         break;

@@ -209,9 +209,10 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
 // D format (bits 4-5) = 1 (f32), A format (7-9) = 1 (bf16), B format (10-12) = 1,
-// transpose-B (bit 16) set when B is MN-major, N>>3 in bits 17-22, M>>4 in 24-28.
-__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+// transpose-A (bit 15) set when A is MN-major, transpose-B (bit 16) when B is,
+// N>>3 in bits 17-22, M>>4 in 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_bf16(int m, int n, bool b_mn_major, bool a_mn_major = false) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

@@ -68,8 +68,12 @@ typedef enum {
 /* Storage of the B operand. */
 typedef enum {
   CODA_B_KN = 0,   /* B is [K, N] row-major: C = A @ B   (weights as x @ W)    */
-  CODA_B_NK = 1    /* B is [N, K] row-major: C = A @ B^T (dgrad dY @ W^T, or an
+  CODA_B_NK = 1,   /* B is [N, K] row-major: C = A @ B^T (dgrad dY @ W^T, or an
                       nn.Linear weight stored [out, in])                        */
+  CODA_A_KM = 2    /* flag, OR-ed with either of the above: A is given as [K, M]
+                      row-major, C = A^T @ B (the weight gradient X^T @ dY from
+                      the stored activations X [tokens, features]); M must be a
+                      multiple of 8; not with RMS_ROWSCALE / LN_ROWSCALE        */
 } coda_b_layout;
 
 /*
@@ -117,6 +121,16 @@ typedef enum {
  *   ROW_MEAN       row_stats[slot*M + i] = sum_j x / width
  *   ROW_SUMSQ      row_stats[slot*M + i] = sum_j x^2
  *   ROW_DOT_AUX    row_stats[slot*M + i] = sum_j x * xhat[i,j]  (aux.xhat [M,N_out])
+ * Reductions over the M rows of each output column (agentlenshq.com
+ * "Reductions", along the other dimension; the bias and norm-parameter
+ * gradients of a backward pass), fused kernel only:
+ *   COL_SUM        col_stats[slot*N_out + j] = sum_i x
+ *   COL_SUMSQ      col_stats[slot*N_out + j] = sum_i x^2
+ *   COL_DOT_AUX    col_stats[slot*N_out + j] = sum_i x * xhat[i,j]
+ *   COL_DOT_NORM   col_stats[slot*N_out + j] = sum_i x * r_i (xhat[i,j] - mu_i), with
+ *                  r = rowvec[0] and mu = rowvec[1] (NULL: 0): with xhat = the norm's
+ *                  input X and x = dL/d(norm output), this is dL/dgamma
+ *                  (col_stats = aux.col_stats, fp32; at most CODA_MAX_COL_REDUCTIONS)
  *
  * Ops that read an [M, N_out] aux tensor, reductions and DROPOUT must come
  * after SWIGLU when the list has one.  At most CODA_MAX_REDUCTIONS reductions.
@@ -141,7 +155,11 @@ typedef enum {
   CODA_OP_GELU_ERF = 16,
   CODA_OP_GELU_ERF_GRAD = 17,
   CODA_OP_LN_ROWSCALE = 18,
-  CODA_OP_COUNT_ = 19
+  CODA_OP_COL_SUM = 19,
+  CODA_OP_COL_SUMSQ = 20,
+  CODA_OP_COL_DOT_AUX = 21,
+  CODA_OP_COL_DOT_NORM = 22,
+  CODA_OP_COUNT_ = 23
 } coda_opcode;
 
 #define CODA_MAX_OPS 16
@@ -149,6 +167,7 @@ typedef enum {
 #define CODA_MAX_ROW_VECS 2
 #define CODA_MAX_STAT_SLOTS 8
 #define CODA_MAX_REDUCTIONS 4
+#define CODA_MAX_COL_REDUCTIONS 2
 #define CODA_NO_SLOT 0xFFFFFFFFu
 
 typedef struct {
@@ -174,6 +193,7 @@ typedef struct {
   void* preact_out;                        /* bf16 [M, width at the op]     */
   const float* ln_colsum;                  /* fp32 [width], LN_ROWSCALE     */
   const float* ln_bias;                    /* fp32 [width], LN_ROWSCALE     */
+  float* col_stats;                        /* fp32 [slots][N_out], COL_* ops (output) */
 } coda_aux;
 
 /*
@@ -182,7 +202,7 @@ typedef struct {
  * op list applied to the drained tile, bf16 (round-to-nearest-even) TMA store.
  * Row reductions and keep counts are finished by a second small kernel.
  *
- *   A        bf16 [M, K]
+ *   A        bf16 [M, K], or [K, M] with the CODA_A_KM flag in b_layout
  *   B        bf16 [K, N] (CODA_B_KN) or [N, K] (CODA_B_NK)
  *   M, N, K  M >= 0, N >= 0, K >= 0, each < 2^31.  N and K must be multiples of
  *            8 (16-byte rows); with SWIGLU, N must be a multiple of 16.  M == 0
@@ -282,6 +302,27 @@ CODA_API coda_status coda_rmsnorm(const void* X, const void* gamma, int64_t M, i
  */
 CODA_API coda_status coda_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K,
                                     float eps, void* Xn_out, void* stream);
+
+/*
+ * coda_norm_backward -- the input gradient of RMSNorm / LayerNorm from the
+ * gradient at the normalised value, g = gamma (.) dL/dy (y the norm's output),
+ * and two row sums of it, all of which a dgrad GEMM's epilogue produces:
+ *     x_hat = (x - mu) r,   S = r (sum_gx - mu sum_g)   (= sum_k g x_hat)
+ *     dX    = r (g - sum_g / K - x_hat S / K)
+ * RMSNorm: mu = NULL and sum_g = NULL (their terms are 0).  The CODA article
+ * (d9bl.com, Fig. 4) decomposes the norms' gradients into a GEMM stage and an
+ * epilogue stage; this correction needs the full-row sums of the GEMM output,
+ * so it runs after it.  Typical chain (commuted LayerNorm forward, W unfolded):
+ *   dgrad GEMM  A = dY, B = W (CODA_B_NK), ops
+ *     COL_SUM(dbeta), COL_DOT_NORM(dgamma; rowvec r, mu; xhat = X),
+ *     COL_SCALE(gamma), ROW_SUM(sum_g), ROW_DOT_AUX(sum_gx; xhat = X)
+ *   -> D = g, then coda_norm_backward(g, X, r, mu, sum_g, sum_gx) -> dX.
+ *   g, X, dX   bf16 [M, K] (16-byte aligned, K % 8 == 0); r, mu, sum_g,
+ *   sum_gx fp32 [M].  dX must not overlap g or X.
+ */
+CODA_API coda_status coda_norm_backward(const void* g, const void* X, const float* r, const float* mu,
+                                        const float* sum_g, const float* sum_gx, int64_t M, int64_t K, void* dX,
+                                        void* stream);
 
 /*
  * coda_epilogue_apply -- the same op list applied by a separate memory-bound

@@ -54,6 +54,7 @@ OP_NAMES = (
     "SCALE", "COL_SCALE", "BIAS", "ROW_SCALE", "RMS_ROWSCALE", "GELU_TANH", "SILU",
     "SWIGLU", "GELU_TANH_GRAD", "DROPOUT", "RESIDUAL", "STORE_PREACT",
     "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX", "GELU_ERF", "GELU_ERF_GRAD", "LN_ROWSCALE",
+    "COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM",
 )
 
 _U64 = np.uint64
@@ -122,6 +123,37 @@ def layernorm(X, gamma, beta, eps):
 def layernorm_project(X, gamma, beta, W, eps, b_layout="kn"):
     """Normalise-then-project: layernorm(X) @ W (the unfused reading)."""
     return gemm(layernorm(X, gamma, beta, eps), W, b_layout)
+
+
+def rmsnorm_backward(X, gamma, dY, eps):
+    """Gradients of sum(rmsnorm(X; gamma) * dY): y = gamma x_hat, x_hat = x r,
+    r = 1/sqrt(mean_k x^2 + eps).  With g = gamma dY (the gradient at x_hat):
+      dX = r (g - x_hat mean_k(g x_hat)),  dgamma = sum_i dY x_hat.
+    Returns (dX, dgamma)."""
+    X = np.asarray(X, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    r = rms_rstd(X, eps)
+    xh = X * r[:, None]
+    g = dY * gamma[None, :]
+    dX = r[:, None] * (g - xh * np.mean(g * xh, axis=1)[:, None])
+    return dX, np.sum(dY * xh, axis=0)
+
+
+def layernorm_backward(X, gamma, dY, eps):
+    """Gradients of sum(layernorm(X; gamma, beta) * dY): y = gamma x_hat + beta,
+    x_hat = (x - mu) r.  With g = gamma dY:
+      dX = r (g - mean_k g - x_hat mean_k(g x_hat)),
+      dgamma = sum_i dY x_hat,  dbeta = sum_i dY.
+    Returns (dX, dgamma, dbeta)."""
+    X = np.asarray(X, dtype=np.float64)
+    dY = np.asarray(dY, dtype=np.float64)
+    gamma = np.asarray(gamma, dtype=np.float64)
+    mu, r = ln_stats(X, eps)
+    xh = (X - mu[:, None]) * r[:, None]
+    g = dY * gamma[None, :]
+    dX = r[:, None] * (g - np.mean(g, axis=1)[:, None] - xh * np.mean(g * xh, axis=1)[:, None])
+    return dX, np.sum(dY * xh, axis=0), np.sum(dY, axis=0)
 
 
 # ---------------------------------------------------------------------------
@@ -267,6 +299,11 @@ def residual(x, R, beta=1.0):
 # ---------------------------------------------------------------------------
 # row reductions (agentlenshq.com, "Reductions": sum or mean along a dimension)
 # ---------------------------------------------------------------------------
+def col_sum(X) -> np.ndarray:
+    """sum_i X[i, j]: the reduction over the rows (the M dimension)."""
+    return np.sum(np.asarray(X, dtype=np.float64), axis=0)
+
+
 def row_sum(x):
     return np.sum(x, axis=1)
 
@@ -306,8 +343,10 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
 
     Returns dict with D (fp64), stats {slot: fp64[M]}, stat_scale {slot: fp64[M]}
     (the L2 norm of each row reduction's summands: the scale of its rounding
-    error when the summands carry independent relative errors), keep_count
-    (int64[M] or None), keep (bool mask or None), preact (fp64 or None).
+    error when the summands carry independent relative errors), col_stats
+    {slot: fp64[N_out]} and col_stat_scale (the same for the column reductions,
+    which need all M rows: not with `rows`), keep_count (int64[M] or None),
+    keep (bool mask or None), preact (fp64 or None).
     """
     A = np.asarray(A, dtype=np.float64)
     col_vecs = col_vecs or {}
@@ -342,6 +381,8 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
     keep = None
     preact = None
     stat_scale = {}
+    col_stats = {}
+    col_stat_scale = {}
     for name, slot, f0 in ops[start:]:
         if name == "SCALE":
             x = scale(x, f0)
@@ -397,9 +438,24 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
         elif name == "ROW_DOT_AUX":
             stats[slot] = row_dot(x, xhat)
             stat_scale[slot] = np.sqrt(row_sumsq(x * np.asarray(xhat, dtype=np.float64)))
+        elif name in ("COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM"):
+            if name == "COL_SUM":
+                t = x
+            elif name == "COL_SUMSQ":
+                t = x * x
+            elif name == "COL_DOT_AUX":
+                t = x * np.asarray(xhat, dtype=np.float64)
+            else:
+                # x_hat = r (aux - mu), r = row vector 0, mu = row vector 1 (or 0)
+                rr = np.asarray(row_vecs[0], dtype=np.float64)
+                mm = np.asarray(row_vecs[1], dtype=np.float64) if 1 in row_vecs else np.zeros_like(rr)
+                t = x * (rr[:, None] * (np.asarray(xhat, dtype=np.float64) - mm[:, None]))
+            col_stats[slot] = col_sum(t)
+            col_stat_scale[slot] = np.sqrt(col_sum(t * t))
         else:
             raise ValueError(f"unknown op {name}")
-    return dict(D=x, stats=stats, stat_scale=stat_scale, keep_count=keep_count, keep=keep, preact=preact)
+    return dict(D=x, stats=stats, stat_scale=stat_scale, col_stats=col_stats, col_stat_scale=col_stat_scale,
+                keep_count=keep_count, keep=keep, preact=preact)
 
 
 def round_bf16(x) -> np.ndarray:

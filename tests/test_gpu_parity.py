@@ -288,6 +288,125 @@ def test_unmatched_op_list_runs_interpreter():
     sync_ok()
 
 
+# -------------------------------------------------------- column reductions
+def assert_col_close(got, ref, scale, what=""):
+    """Column reductions: the same bound as the row reductions, over the M summands."""
+    got = np.asarray(got, dtype=np.float64)
+    bound = ATOL + RTOL * np.maximum(np.abs(ref), scale)
+    err = np.abs(got - ref)
+    if (err > bound).any():
+        j = int(np.argmax(err - bound))
+        raise AssertionError(f"{what}: {(err > bound).sum()} columns out of tolerance, worst column {j}: "
+                             f"gpu {got[j]!r} ref {ref[j]!r} bound {bound[j]!r}")
+
+
+COL_CASES = {
+    "gelu_colsum_dot_rowsum": [("GELU_TANH",), ("COL_SUM", 0), ("COL_DOT_AUX", 1), ("ROW_SUM", 0)],
+    "swiglu_colsumsq": [("SWIGLU",), ("COL_SUMSQ", 1), ("SCALE", 0, 2.0), ("COL_SUM", 0)],
+    "dgrad_dbias": [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1), ("COL_SUM", 0)],
+}
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+@pytest.mark.parametrize("case", sorted(COL_CASES))
+def test_column_reductions(case, layout, mode):
+    ops = COL_CASES[case]
+    A, B, N, n_out, col, row, aux = _op_case_tensors(ops, layout, 500 + len(case))
+    r = coda.gemm_epilogue(cu(A), cu(B), ops, b_layout=layout, z=cu(aux["z"]), xhat=cu(aux["xhat"]))
+    sync_ok()
+    ref = O.run_chain(f64(A), f64(B), ops, b_layout=layout, z=f64(aux["z"]), xhat=f64(aux["xhat"]))
+    assert_close(f64(r.D), ref["D"], case)
+    check_stats(r, ref, case)
+    for slot, v in ref["col_stats"].items():
+        assert_col_close(f64(r.col_stats[slot]), v, ref["col_stat_scale"][slot], f"{case} col {slot}")
+
+
+def test_column_sums_exact_small_integers(mode):
+    # integer-valued D (small-integer GEMM, exact in fp32): column sums are exact
+    M, K, N = 300, 128, 264
+    A = inputs.small_int_bf16((M, K), 3, 521)
+    B = inputs.small_int_bf16((K, N), 3, 522)
+    r = coda.gemm_epilogue(cu(A), cu(B), [("COL_SUM", 0), ("COL_SUMSQ", 1)])
+    sync_ok()
+    D = f64(A) @ f64(B)
+    np.testing.assert_array_equal(f64(r.col_stats[0]), D.sum(axis=0))
+    np.testing.assert_array_equal(f64(r.col_stats[1]), (D * D).sum(axis=0))
+
+
+# ------------------------------------------------------ A given as [K, M]
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_a_km_small_integer_bit_exact(layout, mode):
+    if mode == "persist4":
+        pytest.skip("same kernel as single")
+    M, K, N = 264, 192, 264
+    At = inputs.small_int_bf16((K, M), 4, 531)           # A^T stored [K, M]
+    B = inputs.small_int_bf16((K, N) if layout == "kn" else (N, K), 4, 532)
+    r = coda.gemm_epilogue(cu(At), cu(B), [], b_layout=layout, a_layout="km")
+    sync_ok()
+    # the integer sums are exact in fp32; D is their bf16 rounding (RNE)
+    ref = O.round_bf16(O.gemm(f64(At).T, f64(B), layout))
+    np.testing.assert_array_equal(f64(r.D), ref)
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_wgrad_scale_accumulate_in_place(layout, mode):
+    # dW = s * X^T dH + dW_old, written over dW_old (output and residual alias),
+    # with the per-row sums of squares (gradient-norm partials) and column sums
+    T, K_in, N = 384, 264, 520          # tokens (the reduction), features, outputs
+    X = rand((T, K_in), 541)
+    dH = rand((T, N) if layout == "kn" else (N, T), 542, 1.0 / math.sqrt(T))
+    dW_old = rand((K_in, N), 543)
+    ops = [("SCALE", 0, 0.5), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0), ("COL_SUM", 0)]
+    dW = cu(dW_old.clone())
+    r = coda.gemm_epilogue(cu(X), cu(dH), ops, b_layout=layout, a_layout="km", residual=dW, out=dW)
+    sync_ok()
+    ref = O.run_chain(f64(X).T, f64(dH), ops, b_layout=layout, residual_t=f64(dW_old))
+    assert_close(f64(dW), ref["D"], "wgrad")
+    check_stats(r, ref, "wgrad")
+    assert_col_close(f64(r.col_stats[0]), ref["col_stats"][0], ref["col_stat_scale"][0], "wgrad colsum")
+
+
+# ------------------------------------------------------------ norm backward
+@pytest.mark.parametrize("kind", ["layernorm", "rmsnorm"])
+def test_norm_backward_chain(kind, mode):
+    # forward: commuted norm projection (row statistics from the GPU forward);
+    # backward: dgrad GEMM with dbeta, dgamma, g = gamma * dXn and its row sums
+    # in the epilogue, then the correction kernel -> dX
+    M, K_in, N = 300, 264, 520
+    eps = 1e-5 if kind == "layernorm" else 1e-6
+    X = rand((M, K_in), 601)
+    if kind == "layernorm":
+        X = (X.float() + 0.7).to(torch.bfloat16)
+    g = inputs.uniform_bf16((K_in,), 0.5, 1.5, 602)
+    W = rand((K_in, N), 603, 1.0 / math.sqrt(K_in))
+    dY = rand((M, N), 604)
+    if kind == "layernorm":
+        Wf, c, b = coda.fold_layernorm(cu(W), cu(g), None, "kn")
+        fwd = coda.gemm_epilogue(cu(X), Wf, [("LN_ROWSCALE", 0, eps)], ln_colsum=c)
+        r, mu = fwd.row_stats[0].contiguous(), fwd.row_stats[1].contiguous()
+        ops = [("COL_SUM", 1), ("COL_DOT_NORM", 0), ("COL_SCALE", 0), ("ROW_SUM", 0), ("ROW_DOT_AUX", 1)]
+        row_vecs = {0: r, 1: mu}
+    else:
+        Wf = coda.fold_gamma(cu(W), cu(g), "kn")
+        fwd = coda.gemm_epilogue(cu(X), Wf, [("RMS_ROWSCALE", 0, eps)])
+        r, mu = fwd.row_stats[0].contiguous(), None
+        ops = [("COL_DOT_NORM", 0), ("COL_SCALE", 0), ("ROW_DOT_AUX", 1)]
+        row_vecs = {0: r}
+    bwd = coda.gemm_epilogue(cu(dY), cu(W), ops, b_layout="nk", col_vecs={0: cu(g)}, row_vecs=row_vecs,
+                             xhat=cu(X))
+    sum_g = bwd.row_stats[0].contiguous() if kind == "layernorm" else None
+    dX = coda.norm_backward(bwd.D, cu(X), r, bwd.row_stats[1].contiguous(), mu=mu, sum_g=sum_g)
+    sync_ok()
+    dXn = f64(dY) @ f64(W).T
+    if kind == "layernorm":
+        dX_ref, dg_ref, db_ref = O.layernorm_backward(f64(X), f64(g), dXn, eps)
+        assert_col_close(f64(bwd.col_stats[1]), db_ref, np.sqrt((dXn ** 2).sum(axis=0)), "dbeta")
+    else:
+        dX_ref, dg_ref = O.rmsnorm_backward(f64(X), f64(g), dXn, eps)
+    assert_col_close(f64(bwd.col_stats[0]), dg_ref, np.sqrt((dXn ** 2).sum(axis=0)) * 3.0, "dgamma")
+    assert_close(f64(dX), dX_ref, f"{kind} dX")
+
+
 # ------------------------------------------------------------------ dropout
 @pytest.mark.parametrize("seed", [0, 12345])
 @pytest.mark.parametrize("glu", [False, True])
@@ -422,7 +541,7 @@ def _ln_problem(M, K, N, layout, seed, mean=0.5):
 
 
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-@pytest.mark.parametrize("M,K,N", [(300, 192, 264), (128, 2048, 512), (520, 512, 136)])
+@pytest.mark.parametrize("M,K,N", [(300, 192, 264), (128, 2048, 512), (520, 512, 136), (300, 264, 264)])
 def test_commuted_layernorm(layout, M, K, N, mode):
     X, g, beta, W = _ln_problem(M, K, N, layout, 91)
     Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta), layout)

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_struct_layouts():
     assert ctypes.sizeof(coda.CodaOp) == 16
     assert ctypes.sizeof(coda.CodaEpilogue) == 16 + 16 * 16
-    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4 + 2)
+    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4 + 2 + 1)
 
 
 def test_opcode_values_match_header():
@@ -117,7 +117,7 @@ def _gemm(L, A, B, M, N, K, ops=(), aux=None, D=0x1000, stats=None, ws=None, ws_
 
 def test_gemm_validation_before_device(L):
     # every one of these fails in host validation, before any CUDA call
-    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=2) == INVALID
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=4) == INVALID
     assert _gemm(L, 0x1008, 0x2000, 64, 64, 64) == ALIGN
     assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, D=0x1004) == ALIGN
     assert _gemm(L, None, 0x2000, 64, 64, 64) == INVALID
@@ -192,3 +192,33 @@ def test_workspace_size_split_k_closed_form(L):
     finally:
         coda.set_split_k("auto")
         coda.set_cta_pair("auto")
+
+
+def test_workspace_size_column_reductions(L):
+    # one fp32 partial per (column reduction, 32-row block, output column)
+    M, N, K = 300, 264, 64
+    assert coda.workspace_size(M, N, K, [("COL_SUM", 0)]) == 10 * N * 4
+    assert coda.workspace_size(M, N, K, [("COL_SUM", 0), ("COL_DOT_AUX", 1)]) == 2 * 10 * N * 4
+    # after the row-reduction partials (SwiGLU: 128-column tiles, 3 of them for 264
+    # output columns); the column partials span the output width N/2
+    assert coda.workspace_size(M, 2 * N, K, [("SWIGLU",), ("ROW_SUM", 0), ("COL_SUMSQ", 0)]) == \
+        3 * M * 4 + 10 * N * 4
+
+
+@pytest.mark.parametrize("ops,why", [
+    ([("COL_SUM", 0)] * 3, "three column reductions"),
+    ([("COL_SUM", 0), ("SWIGLU",)], "column reduction before SWIGLU"),
+    ([("COL_SUM", 9)], "slot out of range"),
+])
+def test_column_reduction_lists_rejected(L, ops, why):
+    st, _ = _ws(L, 300, 528, 64, ops)
+    assert st == INVALID, why
+
+
+def test_a_km_layout_validation(L):
+    # A as [K, M] needs M a multiple of 8, and no commuted norm (row statistics read A by rows)
+    assert _gemm(L, 0x1000, 0x2000, 100, 64, 64, layout=2) == INVALID
+    e = coda.make_epilogue([("RMS_ROWSCALE", -1, 1e-6)])
+    st = L.coda_gemm_epilogue(0x1000, 0x2000, 128, 64, 64, 2, ctypes.byref(e), None, 0x3000, None, None, None, 0,
+                              None)
+    assert st == UNSUPPORTED

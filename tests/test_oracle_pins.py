@@ -393,3 +393,94 @@ def test_commuted_layernorm_identity():
     np.testing.assert_allclose(out["D"], lhs, rtol=1e-11, atol=1e-11)
     np.testing.assert_allclose(out["stats"][0], r, rtol=1e-14)
     np.testing.assert_allclose(out["stats"][1], mu, rtol=1e-14)
+
+
+def test_column_reductions_transpose_identity():
+    # column sums of A @ B are the row sums of (A @ B)^T = B^T @ A^T, which the
+    # oracle computes through its row-reduction path
+    A = rng.standard_normal((37, 20))
+    B = rng.standard_normal((20, 11))
+    Xh = rng.standard_normal((37, 11))
+    cols = O.run_chain(A, B, [("COL_SUM", 0), ("COL_SUMSQ", 1), ("COL_DOT_AUX", 2)], xhat=Xh)
+    rows = O.run_chain(B.T, A.T, [("ROW_SUM", 0), ("ROW_SUMSQ", 1), ("ROW_DOT_AUX", 2)], xhat=Xh.T)
+    for s in range(3):
+        np.testing.assert_allclose(cols["col_stats"][s], rows["stats"][s], rtol=1e-12, atol=1e-12)
+    # both orders total the same
+    rs = O.run_chain(A, B, [("ROW_SUM", 0)])["stats"][0]
+    assert abs(rs.sum() - cols["col_stats"][0].sum()) < 1e-9
+
+
+def test_column_reductions_closed_forms():
+    M, N = 13, 6
+    # D = 1 everywhere (A one-hot column of ones, B a row of ones): sum = M, sumsq = M
+    A = np.ones((M, 1))
+    B = np.ones((1, N))
+    out = O.run_chain(A, B, [("COL_SUM", 0), ("COL_SUMSQ", 1), ("COL_DOT_AUX", 2)], xhat=np.full((M, N), 2.0))
+    np.testing.assert_array_equal(out["col_stats"][0], np.full(N, M))
+    np.testing.assert_array_equal(out["col_stats"][1], np.full(N, M))
+    np.testing.assert_array_equal(out["col_stats"][2], np.full(N, 2 * M))
+    # reductions see the chain value at their position: after SCALE 3 the sum triples
+    out = O.run_chain(A, B, [("COL_SUM", 0), ("SCALE", 0, 3.0), ("COL_SUM", 1)])
+    np.testing.assert_array_equal(out["col_stats"][1], 3 * out["col_stats"][0])
+
+
+def _fd_grad(f, X, h=1e-6):
+    """Central differences of a scalar function of X, element by element."""
+    G = np.zeros_like(X)
+    for idx in np.ndindex(X.shape):
+        Xp = X.copy()
+        Xm = X.copy()
+        Xp[idx] += h
+        Xm[idx] -= h
+        G[idx] = (f(Xp) - f(Xm)) / (2 * h)
+    return G
+
+
+def test_rmsnorm_backward_matches_finite_differences():
+    X = rng.standard_normal((4, 9))
+    g = rng.uniform(0.5, 1.5, 9)
+    dY = rng.standard_normal((4, 9))
+    dX, dg = O.rmsnorm_backward(X, g, dY, 1e-6)
+    np.testing.assert_allclose(dX, _fd_grad(lambda Z: np.sum(O.rmsnorm(Z, g, 1e-6) * dY), X), atol=1e-7)
+    np.testing.assert_allclose(dg, _fd_grad(lambda gg: np.sum(O.rmsnorm(X, gg, 1e-6) * dY), g), atol=1e-7)
+
+
+def test_layernorm_backward_matches_finite_differences():
+    X = rng.standard_normal((4, 9)) + 1.5
+    g = rng.uniform(0.5, 1.5, 9)
+    b = rng.standard_normal(9)
+    dY = rng.standard_normal((4, 9))
+    dX, dg, db = O.layernorm_backward(X, g, dY, 1e-5)
+    np.testing.assert_allclose(dX, _fd_grad(lambda Z: np.sum(O.layernorm(Z, g, b, 1e-5) * dY), X), atol=1e-7)
+    np.testing.assert_allclose(dg, _fd_grad(lambda gg: np.sum(O.layernorm(X, gg, b, 1e-5) * dY), g), atol=1e-7)
+    np.testing.assert_allclose(db, _fd_grad(lambda bb: np.sum(O.layernorm(X, g, bb, 1e-5) * dY), b), atol=1e-7)
+    # a row's dX sums to zero (the mean is removed); with eps = 0 it is also
+    # orthogonal to x_hat (layernorm is then invariant to scaling a row)
+    np.testing.assert_allclose(dX.sum(axis=1), 0, atol=1e-12)
+    dX0, _, _ = O.layernorm_backward(X, g, dY, 0.0)
+    mu, r = O.ln_stats(X, 0.0)
+    xh = (X - mu[:, None]) * r[:, None]
+    np.testing.assert_allclose((dX0 * xh).sum(axis=1), 0, atol=1e-10)
+
+
+def test_norm_backward_chain_through_the_op_list():
+    # the dgrad epilogue's reductions, evaluated by run_chain on G = dY @ W^T,
+    # give layernorm_backward's dbeta and dgamma, and the correction formula
+    # applied to its row sums gives dX
+    M, K, N = 6, 10, 7
+    X = rng.standard_normal((M, K)) + 0.5
+    g = rng.uniform(0.5, 1.5, K)
+    W = rng.standard_normal((K, N))
+    dY = rng.standard_normal((M, N))
+    mu, r = O.ln_stats(X, 1e-5)
+    ops = [("COL_SUM", 1), ("COL_DOT_NORM", 0), ("COL_SCALE", 0), ("ROW_SUM", 0), ("ROW_DOT_AUX", 1)]
+    out = O.run_chain(dY, W, ops, b_layout="nk", col_vecs={0: g}, row_vecs={0: r, 1: mu}, xhat=X)
+    dX_ref, dg_ref, db_ref = O.layernorm_backward(X, g, dY @ W.T, 1e-5)
+    np.testing.assert_allclose(out["col_stats"][1], db_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["col_stats"][0], dg_ref, rtol=1e-12, atol=1e-12)
+    G = out["D"]
+    s1, sgx = out["stats"][0], out["stats"][1]
+    xh = (X - mu[:, None]) * r[:, None]
+    S = r * (sgx - mu * s1)
+    dX = r[:, None] * (G - s1[:, None] / K - xh * S[:, None] / K)
+    np.testing.assert_allclose(dX, dX_ref, rtol=1e-10, atol=1e-12)
