@@ -1,6 +1,6 @@
 """Benchmark of the fused GEMM + on-chip epilogue path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|dgrad|llama|skinny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|dgrad|wgrad|llama|skinny]
                     [--impl coda|reference]
 
 Default workload: the commuted-RMSNorm projection D = rsqrt(mean(X^2)+1e-6) *
@@ -52,9 +52,11 @@ DESCRIPTIONS = {
     "swiglu": "SwiGLU up-projection [G|U] = X[8192,4096] @ W[4096,22016], SiLU(G)*U, dropout p=0.1",
     "dgrad": "dgrad dX = (dY[8192,4096] @ W[16384,4096]^T) * GELU'(Z), rows sum(dX*Xhat), sum(dX)",
     "skinny": "decode-sized MLP up-projection: rmsnorm(X[128,4096]) @ W[4096,22016] (commuted), SiLU(G)*U",
+    "wgrad": "weight gradient dW[11008,4096] = up[16384,11008]^T @ dY[16384,4096] / 8 + dW (in place), "
+             "row sums of squares",
     "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs)",
 }
-DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000}
+DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300}
 
 
 def kernel_hash() -> str:
@@ -181,9 +183,12 @@ class OracleSample:
         from oracle import coda_oracle as O
         self.w, self.I, self.O = workload, inputs, O
         gen = dict(rmsproj=inputs.make_rmsproj, lnproj=inputs.make_lnproj, swiglu=inputs.make_swiglu,
-                   dgrad=inputs.make_dgrad, llama=inputs.make_llama_block, skinny=inputs.make_skinny)[workload]
+                   dgrad=inputs.make_dgrad, llama=inputs.make_llama_block, skinny=inputs.make_skinny,
+                   wgrad=inputs.make_wgrad)[workload]
         self.t = {k: O.to_f64(v) for k, v in gen(0).items()}
-        self.Mmax = next(iter(self.t.values())).shape[0] if workload != "llama" else self.t["X"].shape[0]
+        self.Mmax = dict(llama=self.t["X"].shape[0] if "X" in self.t else 0,
+                         wgrad=self.t["dW_old"].shape[0] if "dW_old" in self.t else 0).get(
+            workload, next(iter(self.t.values())).shape[0])
         self.rows = 32
 
     def run(self, rows: int):
@@ -198,6 +203,11 @@ class OracleSample:
             O.run_chain(t["X"][r], t["W"], [("LN_ROWSCALE", 0, I.EPS_LN)], norm_gamma=t["gamma"],
                         norm_beta=t["beta"])
             fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "wgrad":
+            # rows of dW = features of up: the sample takes the first `rows` of them
+            O.run_chain(t["up"][:, r].T, t["dY"], [("SCALE", 0, I.WGRAD_SCALE), ("RESIDUAL", 0, 1.0),
+                                                   ("ROW_SUMSQ", 0)], residual_t=t["dW_old"][r])
+            fl = 2 * rows * t["dY"].shape[0] * t["dY"].shape[1]
         elif self.w == "skinny":
             O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", None, I.EPS_RMS), ("SWIGLU",)],
                         norm_gamma=t["gamma"])

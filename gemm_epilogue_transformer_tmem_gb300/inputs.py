@@ -26,6 +26,11 @@ workload descriptions:
            batch): commuted RMSNorm -> SwiGLU, X[128,4096] ~ N(0,1),
            gamma ~ U(0.5,1.5), W[4096,2*11008] ~ N(0, std 0.02).  180 MB of
            weights against 23 GFLOP: bound by HBM, not by the tensor cores
+  wgrad    the LLaMA MLP down-projection's weight gradient at 16384 tokens:
+           dW = s * up^T @ dY + dW_old (scaled, accumulated in place) with the
+           per-row sums of squares (gradient-norm partials); up[16384,11008]
+           ~ N(0, 0.5^2) (a SwiGLU output), dY[16384,4096] ~ N(0, 0.01^2),
+           dW_old ~ N(0, 0.01^2), s = 1/8 (eight accumulation steps)
   llama    LLaMA-7B-like non-attention block at 16384 tokens, d=4096,
            ffn=11008, weights N(0, std 0.02), gammas U(0.5,1.5)
 
@@ -83,6 +88,7 @@ LLAMA_BLOCK = dict(tokens=16384, d=4096, ffn=11008)
 
 EPS_RMS = 1e-6
 EPS_LN = 1e-5
+WGRAD_SCALE = 0.125
 DROPOUT_P = 0.1
 DROPOUT_SEED = 0
 
@@ -152,6 +158,14 @@ def make_skinny(seed: int = 0, M: int = 128, K: int = 4096, N_out: int = 11008) 
         X=randn_bf16((M, K), 1.0, seed + 61),
         gamma=uniform_bf16((K,), 0.5, 1.5, seed + 62),
         W=randn_bf16((K, 2 * N_out), 0.02, seed + 63),
+    )
+
+
+def make_wgrad(seed: int = 0, T: int = 16384, d: int = 4096, ffn: int = 11008) -> dict:
+    return dict(
+        up=randn_bf16((T, ffn), 0.5, seed + 71),
+        dY=randn_bf16((T, d), 0.01, seed + 72),
+        dW_old=randn_bf16((ffn, d), 0.01, seed + 73),
     )
 
 

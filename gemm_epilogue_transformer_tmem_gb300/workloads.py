@@ -165,6 +165,34 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
                 outputs=dict(D=D, D_unfused=Du))
 
 
+def build_wgrad(dev="cuda", seed=0, T=16384, d=4096, ffn=11008, t=None) -> Step:
+    """dW = s * up^T @ dY + dW (in place), per-row sums of squares of the new dW:
+    the down-projection's weight gradient, A read as [K, M] (the stored
+    activations, tokens x features)."""
+    t = t or inputs.make_wgrad(seed, T, d, ffn)
+    up, dY, dW0 = (t[k].to(dev) for k in ("up", "dY", "dW_old"))
+    ops = [("SCALE", 0, inputs.WGRAD_SCALE), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)]
+    dW = dW0.clone()
+    rs = torch.empty((1, ffn), dtype=torch.float32, device=dev)
+    ws, _ = _ws(ffn, d, T, ops, dev)
+    C = torch.empty((ffn, d), dtype=torch.bfloat16, device=dev)
+    dWu = dW0.clone()
+    rsu = torch.empty_like(rs)
+
+    def fused():
+        coda.gemm_epilogue(up, dY, ops, a_layout="km", residual=dW, out=dW, row_stats=rs, workspace=ws)
+
+    def unfused():
+        coda.gemm_epilogue(up, dY, [], a_layout="km", out=C)
+        coda.epilogue_apply(C, ops, residual=dWu, out=dWu, row_stats=rsu)
+
+    fb = (T * ffn + T * d + 2 * ffn * d) * BF16 + ffn * F32
+    ub = (T * ffn + T * d + ffn * d) * BF16 + (3 * ffn * d * BF16 + ffn * F32)
+    return Step("wgrad", 2 * ffn * d * T, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
+                host_outputs=dict(norms=rs), kernels_per_fused=2, kernels_per_unfused=3,
+                outputs=dict(dW=dW, norms=rs))
+
+
 def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
     """dX = (dY @ W^T) * GELU'(Z), sum_j dX*Xhat and sum_j dX per row."""
     t = t or inputs.make_dgrad(seed, M, K, N)
@@ -265,4 +293,4 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,
-                llama=build_llama, skinny=build_skinny)
+                llama=build_llama, skinny=build_skinny, wgrad=build_wgrad)

@@ -762,6 +762,19 @@ def test_full_skinny_sampled(split):
     assert np.linalg.norm(got - ref0["D"]) / np.linalg.norm(ref0["D"]) <= FRO
 
 
+def test_full_wgrad_sampled():
+    # dW = s * up^T dY + dW_old written in place, on the full-size shapes
+    t = inputs.make_wgrad()
+    ops = [("SCALE", 0, inputs.WGRAD_SCALE), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)]
+    dW = cu(t["dW_old"].clone())
+    r = coda.gemm_epilogue(cu(t["up"]), cu(t["dY"]), ops, a_layout="km", residual=dW, out=dW)
+    sync_ok()
+    rows = _sampled(t["dW_old"].shape[0], 5)
+    ref = O.run_chain(f64(t["up"][:, rows]).T, f64(t["dY"]), ops, residual_t=f64(t["dW_old"][rows]))
+    assert_close(f64(dW[rows]), ref["D"], "wgrad")
+    assert_stat_close(f64(r.row_stats[0][rows]), ref["stats"][0], ref["stat_scale"][0], "wgrad row sumsq")
+
+
 def test_full_swiglu_dropout_sampled():
     w = inputs.WORKLOADS["swiglu"]
     t = inputs.make_swiglu()
