@@ -1,6 +1,6 @@
 """Benchmark of the fused GEMM + on-chip epilogue path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|dgrad|wgrad|llama|skinny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|fp8swiglu|dgrad|wgrad|llama|skinny]
                     [--impl coda|reference]
 
 Default workload: the commuted-RMSNorm projection D = rsqrt(mean(X^2)+1e-6) *
@@ -54,9 +54,11 @@ DESCRIPTIONS = {
     "skinny": "decode-sized MLP up-projection: rmsnorm(X[128,4096]) @ W[4096,22016] (commuted), SiLU(G)*U",
     "wgrad": "weight gradient dW[11008,4096] = up[16384,11008]^T @ dY[16384,4096] / 8 + dW (in place), "
              "row sums of squares",
+    "fp8swiglu": "SwiGLU up-projection in FP8 E4M3: X[8192,4096] quantised per row each step, W[22016,4096] "
+                 "per channel once, dequantised in the epilogue, SiLU(G)*U",
     "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs)",
 }
-DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300}
+DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300, "fp8swiglu": 300}
 
 
 def kernel_hash() -> str:
@@ -184,12 +186,15 @@ class OracleSample:
         self.w, self.I, self.O = workload, inputs, O
         gen = dict(rmsproj=inputs.make_rmsproj, lnproj=inputs.make_lnproj, swiglu=inputs.make_swiglu,
                    dgrad=inputs.make_dgrad, llama=inputs.make_llama_block, skinny=inputs.make_skinny,
-                   wgrad=inputs.make_wgrad)[workload]
+                   wgrad=inputs.make_wgrad, fp8swiglu=inputs.make_swiglu)[workload]
         self.t = {k: O.to_f64(v) for k, v in gen(0).items()}
         self.Mmax = dict(llama=self.t["X"].shape[0] if "X" in self.t else 0,
                          wgrad=self.t["dW_old"].shape[0] if "dW_old" in self.t else 0).get(
             workload, next(iter(self.t.values())).shape[0])
         self.rows = 32
+        if workload == "fp8swiglu":   # weight preparation, outside the timed sample
+            w8, self.sw = O.quantize_rows_e4m3(self.t["W"].T)
+            self.w8 = O.e4m3_decode(w8)
 
     def run(self, rows: int):
         """Returns (seconds, flops) of the oracle on the first `rows` rows."""
@@ -208,6 +213,13 @@ class OracleSample:
             O.run_chain(t["up"][:, r].T, t["dY"], [("SCALE", 0, I.WGRAD_SCALE), ("RESIDUAL", 0, 1.0),
                                                    ("ROW_SUMSQ", 0)], residual_t=t["dW_old"][r])
             fl = 2 * rows * t["dY"].shape[0] * t["dY"].shape[1]
+        elif self.w == "fp8swiglu":
+            # per-row E4M3 quantisation of the sample rows (W's output channels were
+            # quantised once, as weight preparation), then the dequantised GEMM and SwiGLU
+            x8, sx = O.quantize_rows_e4m3(t["X"][r])
+            O.run_chain(O.e4m3_decode(x8), self.w8, [("ROW_SCALE", 0), ("COL_SCALE_F32",), ("SWIGLU",)],
+                        b_layout="nk", row_vecs={0: sx}, col_scale_f32=self.sw)
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
         elif self.w == "skinny":
             O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", None, I.EPS_RMS), ("SWIGLU",)],
                         norm_gamma=t["gamma"])
@@ -387,10 +399,12 @@ def main():
                     "frac": round(achieved / peak, 4), "peak_source": f"HBM copy, of {peak_src}"}
     else:
         # the fused kernels are timed in short bursts between L2 flushes: burst peak
-        peak = float(peaks["bf16_tflops"])
+        # (FP8 operands: the measured bf16 peak times the nominal FP8 / bf16 ratio 2)
+        peak = float(peaks["bf16_tflops"]) * step.peak_scale
         achieved = step.flops / call_s / 1e12
+        src = "bf16 burst" if step.peak_scale == 1.0 else f"bf16 burst x {step.peak_scale:g} (nominal fp8/bf16)"
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                    "frac": round(achieved / peak, 4), "peak_source": f"bf16 burst, of {peak_src}"}
+                    "frac": round(achieved / peak, 4), "peak_source": f"{src}, of {peak_src}"}
     roofline.update(traffic=traffic["bytes_per_launch"] if traffic else None, algorithmic_bytes=step.fused_bytes)
 
     cpu = None

@@ -22,6 +22,7 @@ OPCODES = {
     "SILU": 6, "SWIGLU": 7, "GELU_TANH_GRAD": 8, "DROPOUT": 9, "RESIDUAL": 10, "STORE_PREACT": 11,
     "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15, "GELU_ERF": 16, "GELU_ERF_GRAD": 17,
     "LN_ROWSCALE": 18, "COL_SUM": 19, "COL_SUMSQ": 20, "COL_DOT_AUX": 21, "COL_DOT_NORM": 22,
+    "COL_SCALE_F32": 23,
 }
 COL_REDUCTIONS = ("COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM")
 REDUCTIONS = ("ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX")
@@ -29,6 +30,7 @@ MAX_OPS = 16
 NO_SLOT = 0xFFFFFFFF
 B_LAYOUTS = {"kn": 0, "nk": 1}
 A_KM = 2   # flag: A is given as [K, M] (the weight gradient X^T @ dY from stored X)
+AB_E4M3 = 4   # flag: A [M, K] and B [N, K] are FP8 E4M3 bytes
 STATUS = {0: "CODA_OK", 1: "CODA_ERR_INVALID_ARG", 2: "CODA_ERR_UNSUPPORTED", 3: "CODA_ERR_ALIGNMENT",
           4: "CODA_ERR_CUDA", 5: "CODA_ERR_TIMEOUT", 6: "CODA_ERR_WORKSPACE"}
 
@@ -46,7 +48,8 @@ class CodaEpilogue(ctypes.Structure):
 class CodaAux(ctypes.Structure):
     _fields_ = [("col_vec", ctypes.c_void_p * 4), ("row_vec", ctypes.c_void_p * 2), ("residual", ctypes.c_void_p),
                 ("z", ctypes.c_void_p), ("xhat", ctypes.c_void_p), ("preact_out", ctypes.c_void_p),
-                ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p), ("col_stats", ctypes.c_void_p)]
+                ("ln_colsum", ctypes.c_void_p), ("ln_bias", ctypes.c_void_p), ("col_stats", ctypes.c_void_p),
+                ("col_scale_f32", ctypes.c_void_p)]
 
 
 class CodaPlan(ctypes.Structure):
@@ -76,6 +79,7 @@ _SIGS = {
     "coda_fold_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, ctypes.c_int32, _VP]),
     "coda_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP]),
     "coda_norm_backward": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _VP, _VP]),
+    "coda_quantize_e4m3_rows": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "coda_epilogue_apply": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "coda_check_device_error": (ctypes.c_int, [_VP, _VP]),
     "coda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -160,9 +164,10 @@ def make_epilogue(ops: Sequence, seed: int = 0) -> CodaEpilogue:
 
 
 def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None, ln_colsum=None,
-             ln_bias=None, col_stats=None) -> CodaAux:
+             ln_bias=None, col_stats=None, col_scale_f32=None) -> CodaAux:
     a = CodaAux()
     a.col_stats = _ptr(col_stats)
+    a.col_scale_f32 = _ptr(col_scale_f32)
     a.ln_colsum = _ptr(ln_colsum)
     a.ln_bias = _ptr(ln_bias)
     for k, t in (col_vecs or {}).items():
@@ -216,12 +221,14 @@ class Result:
 def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_layout: str = "kn", a_layout: str = "mk",
                   seed: int = 0,
                   col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, preact_out=None,
-                  ln_colsum=None, ln_bias=None, col_stats: Optional[torch.Tensor] = None,
+                  ln_colsum=None, ln_bias=None, col_stats: Optional[torch.Tensor] = None, col_scale_f32=None,
+                  e4m3: bool = False,
                   out: Optional[torch.Tensor] = None, row_stats: Optional[torch.Tensor] = None,
                   keep_count: Optional[torch.Tensor] = None, want_keep_count: bool = True,
                   workspace: Optional[torch.Tensor] = None, stream=None) -> Result:
     """D = f(A @ B) through coda_gemm_epilogue; allocates missing outputs with torch.
-    a_layout "km": A is [K, M] and the product is A^T @ B."""
+    a_layout "km": A is [K, M] and the product is A^T @ B.  e4m3: A [M, K] and
+    B [N, K] (b_layout "nk") are uint8 tensors of FP8 E4M3 codes."""
     if a_layout not in ("mk", "km"):
         raise ValueError(a_layout)
     M, K = A.shape if a_layout == "mk" else (A.shape[1], A.shape[0])
@@ -243,8 +250,8 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
     if workspace is None and wbytes > 0:
         workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
     e = make_epilogue(ops, seed)
-    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias, col_stats)
-    layout = B_LAYOUTS[b_layout] | (A_KM if a_layout == "km" else 0)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias, col_stats, col_scale_f32)
+    layout = B_LAYOUTS[b_layout] | (A_KM if a_layout == "km" else 0) | (AB_E4M3 if e4m3 else 0)
     st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, layout, ctypes.byref(e), ctypes.byref(a),
                                   _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
                                   workspace.numel() if workspace is not None else 0, _stream(stream))
@@ -322,6 +329,19 @@ def norm_backward(g: torch.Tensor, X: torch.Tensor, r: torch.Tensor, sum_gx: tor
     return out
 
 
+def quantize_e4m3_rows(X: torch.Tensor, out: Optional[torch.Tensor] = None,
+                       scale: Optional[torch.Tensor] = None, stream=None):
+    """Per-row FP8 E4M3 quantisation: (codes uint8 [M, K], scale fp32 [M])."""
+    M, K = X.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.uint8, device=X.device)
+    if scale is None:
+        scale = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(lib().coda_quantize_e4m3_rows(_ptr(X), M, K, _ptr(out), _ptr(scale), _stream(stream)),
+           "coda_quantize_e4m3_rows")
+    return out, scale
+
+
 def rmsnorm(X: torch.Tensor, gamma: torch.Tensor, eps: float, out: Optional[torch.Tensor] = None,
             rstd: Optional[torch.Tensor] = None, stream=None):
     M, K = X.shape
@@ -335,7 +355,7 @@ def rmsnorm(X: torch.Tensor, gamma: torch.Tensor, eps: float, out: Optional[torc
 
 
 def epilogue_apply(C: torch.Tensor, ops: Sequence, *, seed: int = 0, col_vecs=None, row_vecs=None, residual=None,
-                   z=None, xhat=None, preact_out=None, out: Optional[torch.Tensor] = None,
+                   z=None, xhat=None, preact_out=None, col_scale_f32=None, out: Optional[torch.Tensor] = None,
                    row_stats: Optional[torch.Tensor] = None, keep_count: Optional[torch.Tensor] = None,
                    stream=None) -> Result:
     """The unfused form: the op list applied to a bf16 tensor C already in memory."""
@@ -349,7 +369,7 @@ def epilogue_apply(C: torch.Tensor, ops: Sequence, *, seed: int = 0, col_vecs=No
     if keep_count is None and any(o[0] == "DROPOUT" for o in _norm_ops(ops)):
         keep_count = torch.empty((M,), dtype=torch.int32, device=C.device)
     e = make_epilogue(ops, seed)
-    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, col_scale_f32=col_scale_f32)
     _check(lib().coda_epilogue_apply(_ptr(C), M, N, ctypes.byref(e), ctypes.byref(a), _ptr(out), _ptr(row_stats),
                                      _ptr(keep_count), _stream(stream)), "coda_epilogue_apply")
     return Result(out, row_stats, keep_count)

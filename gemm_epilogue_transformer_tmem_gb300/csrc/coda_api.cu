@@ -78,14 +78,15 @@ coda_status encoder() {
   return g_encode ? CODA_OK : CODA_ERR_CUDA;
 }
 
-// bf16 2-D row-major tensor [outer, inner] with box [box_outer, box_inner]
+// 2-D row-major tensor [outer, inner] of bf16 (or, u8 = true, of bytes) with box [box_outer, box_inner]
 coda_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                     uint32_t box_outer, CUtensorMapSwizzle sw) {
+                     uint32_t box_outer, CUtensorMapSwizzle sw, bool u8 = false) {
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {inner * (u8 ? 1 : 2)};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  const CUresult r = g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                              const_cast<void*>(base), dims, strides, box,
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_CUDA;
@@ -165,6 +166,11 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         if (op.slot >= CODA_MAX_COL_VECS || ax.col_vec[op.slot] == nullptr) return CODA_ERR_INVALID_ARG;
         if (!aligned16(ax.col_vec[op.slot])) return CODA_ERR_ALIGNMENT;
         c.prog.col_vec[op.slot] = static_cast<const uint16_t*>(ax.col_vec[op.slot]);
+        break;
+      case CODA_OP_COL_SCALE_F32:
+        if (ax.col_scale_f32 == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned16(ax.col_scale_f32)) return CODA_ERR_ALIGNMENT;
+        c.prog.col_scale_f32 = ax.col_scale_f32;
         break;
       case CODA_OP_ROW_SCALE:
         if (op.slot >= CODA_MAX_ROW_VECS || ax.row_vec[op.slot] == nullptr) return CODA_ERR_INVALID_ARG;
@@ -292,14 +298,15 @@ struct Geometry {
   int64_t num_tiles;
 };
 
-// tile_m: rows per tile (128 for one CTA, 256 for a CTA pair)
-Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu, int tile_m = BM) {
+// tile_m: rows per tile (128 for one CTA, 256 for a CTA pair); fp8: 128 elements of K per k-block
+Geometry geometry(int64_t M, int64_t N, int64_t K, bool glu, int tile_m = BM, bool fp8 = false) {
   Geometry g{};
   g.n_out = glu ? N / 2 : N;
   g.out_cols = glu ? BN / 2 : BN;
   g.num_m_tiles = static_cast<int>((M + tile_m - 1) / tile_m);
   g.num_n_tiles = static_cast<int>((g.n_out + g.out_cols - 1) / g.out_cols);
-  g.num_kb = static_cast<int>((K + BK - 1) / BK);
+  const int bk = fp8 ? 2 * BK : BK;
+  g.num_kb = static_cast<int>((K + bk - 1) / bk);
   g.num_tiles = static_cast<int64_t>(g.num_m_tiles) * g.num_n_tiles;
   return g;
 }
@@ -374,6 +381,9 @@ cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major,
       return launch_gemm_fwd_glu(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_DGRAD:
       return launch_gemm_bwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_DEQUANT:
+    case SEQ_DEQUANT_SWIGLU:
+      return cudaErrorNotSupported;   // built for FP8 operands only
     default:
       return launch_gemm_interp(glu, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
   }
@@ -414,6 +424,7 @@ coda_status workspace_need(int64_t M, int64_t N, int64_t K, const coda_epilogue*
   dummy.preact_out = const_cast<uint16_t*>(kAligned);
   dummy.ln_colsum = dummy.ln_bias = reinterpret_cast<const float*>(kAligned);
   dummy.col_stats = const_cast<float*>(reinterpret_cast<const float*>(kAligned));
+  dummy.col_scale_f32 = reinterpret_cast<const float*>(kAligned);
   s = compile_epilogue(epi, &dummy, N, K, true, c);
   if (s != CODA_OK) return s;
   const bool pair = use_pair(M, K);
@@ -438,14 +449,16 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
                                uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream) {
   coda_status s = check_dims(M, N, K);
   if (s != CODA_OK) return s;
-  if ((b_layout & ~(CODA_B_NK | CODA_A_KM)) != 0) return CODA_ERR_INVALID_ARG;
+  if ((b_layout & ~(CODA_B_NK | CODA_A_KM | CODA_AB_E4M3)) != 0) return CODA_ERR_INVALID_ARG;
   const bool a_mn = (b_layout & CODA_A_KM) != 0;   // A given as [K, M]
+  const bool fp8 = (b_layout & CODA_AB_E4M3) != 0;  // A and B are E4M3 bytes
   b_layout &= CODA_B_NK;
   if (a_mn && (M % 8) != 0) return CODA_ERR_INVALID_ARG;   // 16-byte rows of A [K, M]
+  if (fp8 && (a_mn || b_layout != CODA_B_NK || (K % 16) != 0)) return CODA_ERR_INVALID_ARG;
   Compiled c;
   s = compile_epilogue(epi, aux, N, K, true, c);
   if (s != CODA_OK) return s;
-  if (a_mn && c.has_rms) return CODA_ERR_UNSUPPORTED;   // row statistics read A by rows
+  if ((a_mn || fp8) && c.has_rms) return CODA_ERR_UNSUPPORTED;   // row statistics read bf16 A by rows
   if (M == 0 || N == 0) return CODA_OK;
   if (D == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return CODA_ERR_INVALID_ARG;
   if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return CODA_ERR_ALIGNMENT;
@@ -454,7 +467,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   if (row_keep_count && !aligned4(row_keep_count)) return CODA_ERR_ALIGNMENT;
   // CTA pairs (cta_group::2, 256-row tiles) once there are at least two row blocks
   const bool pair = use_pair(M, K);
-  const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM);
+  const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM, fp8);
   if (g.num_tiles > (int64_t{1} << 31) - 1) return CODA_ERR_UNSUPPORTED;
   const size_t ws_need = workspace_bytes_for(M, g, c);
   if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
@@ -474,14 +487,20 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
                CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != CODA_OK) return s;
   if (K > 0) {
-    if (a_mn)   // [K, M]: two 64-wide boxes of M per 128-row tile, 64 rows of K
+    if (fp8)   // E4M3 bytes: 128-byte rows of 128 elements of K
+      s = make_map(&maps[0], A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), 2 * BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B, true);
+    else if (a_mn)   // [K, M]: two 64-wide boxes of M per 128-row tile, 64 rows of K
       s = make_map(&maps[0], A, static_cast<uint64_t>(M), static_cast<uint64_t>(K), 64, BK,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     else
       s = make_map(&maps[0], A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), BK, BM,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != CODA_OK) return s;
-    if (b_layout == CODA_B_KN)
+    if (fp8)
+      s = make_map(&maps[1], B, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 2 * BK, BN / 2,
+                   CU_TENSOR_MAP_SWIZZLE_128B, true);
+    else if (b_layout == CODA_B_KN)
       s = make_map(&maps[1], B, static_cast<uint64_t>(N), static_cast<uint64_t>(K), 64, BK,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     else
@@ -613,11 +632,13 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
     grid = static_cast<int>(g.num_tiles);
   }
   int seq = match_sequence(epi, c.glu);
-  e = launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  e = fp8 ? launch_gemm_fp8(seq, c.glu, pair, maps, p, grid, smem, st)
+          : launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
   if (e == cudaErrorNotSupported && seq != SEQ_INTERP) {
     (void)cudaGetLastError();   // the sequence has no kernel for this variant: interpret
     seq = SEQ_INTERP;
-    e = launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+    e = fp8 ? launch_gemm_fp8(seq, c.glu, pair, maps, p, grid, smem, st)
+            : launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
   }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
@@ -711,6 +732,21 @@ coda_status coda_norm_backward(const void* g, const void* X, const float* r, con
   if (s != CODA_OK) return s;
   const cudaError_t e = launch_norm_backward(g, X, r, mu, sum_g, sum_gx, M, K, dX, dev.sms,
                                              static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+coda_status coda_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void* Q, float* scale, void* stream) {
+  coda_status s = check_dims(M, 16, K);
+  if (s != CODA_OK) return s;
+  if ((K % 16) != 0) return CODA_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return CODA_OK;
+  if (!X || !Q || !scale) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q) || !aligned4(scale)) return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e = launch_quantize_e4m3_rows(X, M, K, Q, scale, static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) g_launches.fetch_add(1);
   return from_cuda(e);
 }

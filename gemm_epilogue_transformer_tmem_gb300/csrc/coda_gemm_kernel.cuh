@@ -171,7 +171,9 @@ struct SmemAux {
 
 // kAMN: A is given as [K, M] (MN-major operand: the weight gradient X^T dY
 // reads the stored activations X [tokens, features] directly).
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN>
+// kFP8: A and B are FP8 E4M3, both K-major; a stage then holds 128 elements of
+// K (the same 128-byte rows), four MMAs of K = 32 (kind::f8f6f4).
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN, bool kFP8>
 __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
@@ -276,7 +278,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           }
-          const int k0 = kb * BK;
+          const int k0 = kb * (kFP8 ? 2 * BK : BK);   // elements of K
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * kStageB;
           if constexpr (kPair) {
@@ -331,7 +333,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
-      constexpr uint32_t idesc = make_idesc_bf16(kTileM, BN, kBMN, kAMN);
+      constexpr uint32_t idesc = kFP8 ? make_idesc_e4m3(kTileM, BN) : make_idesc_bf16(kTileM, BN, kBMN, kAMN);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -363,10 +365,18 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
                                      : make_smem_desc(a_addr + k * 32, 16, 1024);
             const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
                                      : make_smem_desc(b_addr + k * 32, 16, 1024);
-            if constexpr (kPair)
-              mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
-            else
-              mma_bf16_ss(d_tmem, ad, bd, idesc, (kb != w.kb0 || k != 0) ? 1u : 0u);
+            const uint32_t acc_in = (kb != w.kb0 || k != 0) ? 1u : 0u;
+            if constexpr (kFP8) {
+              if constexpr (kPair)
+                mma_f8_ss_pair(d_tmem, ad, bd, idesc, acc_in);
+              else
+                mma_f8_ss(d_tmem, ad, bd, idesc, acc_in);
+            } else {
+              if constexpr (kPair)
+                mma_bf16_ss_pair(d_tmem, ad, bd, idesc, acc_in);
+              else
+                mma_bf16_ss(d_tmem, ad, bd, idesc, acc_in);
+            }
           }
           if constexpr (kPair)
             mma_commit_pair_mc(&ctl->empty[stage], 0x3);
@@ -739,9 +749,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   }
 }
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN = false>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN = false, bool kFP8 = false>
 cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN, kFP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   if constexpr (!kPair) {
@@ -785,7 +795,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
 // Largest number of CTA pairs of this kernel that can be resident at once.
 template <bool kGLU, bool kBMN, bool kRowStats>
 cudaError_t max_active_pairs_t(size_t smem, int* pairs) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true, EpiInterp, false>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, true, EpiInterp, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -840,6 +850,14 @@ cudaError_t launch_variant(bool a_mn_major, bool b_mn_major, bool row_stats, boo
   }
   return b_mn_major ? launch_gemm_t<kGLU, true, false, false, Epi>(maps, p, grid, smem, st)
                     : launch_gemm_t<kGLU, false, false, false, Epi>(maps, p, grid, smem, st);
+}
+
+// FP8 E4M3 operands (A [M, K], B [N, K], both K-major; no row statistics)
+template <class Epi, bool kGLU>
+cudaError_t launch_variant_fp8(bool pair, const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem,
+                               cudaStream_t st) {
+  return pair ? launch_gemm_t<kGLU, false, false, true, Epi, false, true>(maps, p, grid, smem, st)
+              : launch_gemm_t<kGLU, false, false, false, Epi, false, true>(maps, p, grid, smem, st);
 }
 
 }  // namespace coda

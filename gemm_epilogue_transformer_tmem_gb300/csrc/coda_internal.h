@@ -76,6 +76,7 @@ struct EpiProgram {
   int32_t num_rb;          // 32-row blocks, ceil(M / 32)
   int32_t colred_slot[CODA_MAX_COL_REDUCTIONS];
   float* ws_col;           // [n_colred][num_rb][N_out] per-32-row-block column partials
+  const float* col_scale_f32;  // COL_SCALE_F32: fp32 [width]
 };
 
 struct GemmParams {

@@ -201,6 +201,53 @@ cudaError_t launch_rms_rowscale(const void* A, int64_t M, int64_t K, float inv_K
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------- FP8 quantisation
+// One warp per row: amax over the row, inv = 448 / amax and scale = amax / 448
+// (IEEE fp32 divisions), then each element x * inv (fp32 product) converted
+// to E4M3 with round-to-nearest-even and saturation (cvt.rn.satfinite).
+// Sixteen elements (two 16-byte loads, one 16-byte store) per lane step.
+__global__ void quantize_e4m3_rows_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
+                                          uint8_t* __restrict__ Q, float* __restrict__ scale) {
+  const int64_t row = blockIdx.x * static_cast<int64_t>(blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + row * K);
+  const int64_t n8 = K >> 3;
+  float amax = 0.0f;
+  for (int64_t i = lane; i < n8; i += 32) {
+    float x[8];
+    unpack8(__ldg(xr + i), x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const float inv = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 0.0f;
+  if (lane == 0) scale[row] = __fdiv_rn(amax, 448.0f);
+  uint4* qr = reinterpret_cast<uint4*>(Q + row * K);
+  for (int64_t i = lane; 2 * i < n8; i += 32) {
+    float x[16];
+    unpack8(__ldg(xr + 2 * i), x);
+    unpack8(__ldg(xr + 2 * i + 1), x + 8);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * q], inv), __fmul_rn(x[4 * q + 1], inv));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * q + 2], inv), __fmul_rn(x[4 * q + 3], inv));
+      w[q] = lo | (hi << 16);
+    }
+    qr[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+cudaError_t launch_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void* Q, float* scale, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t blocks = (M + threads / 32 - 1) / (threads / 32);
+  quantize_e4m3_rows_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint16_t*>(X), M, K, static_cast<uint8_t*>(Q), scale);
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------- norm backward
 // dX = r (g - sum_g / K - x_hat S / K), x_hat = (x - mu) r, S = r (sum_gx - mu sum_g);
 // RMSNorm: mu = sum_g = null.  Eight elements per thread, grid-stride over the

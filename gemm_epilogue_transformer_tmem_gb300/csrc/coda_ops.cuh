@@ -233,6 +233,18 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
       }
       break;
     }
+    case CODA_OP_COL_SCALE_F32: {
+      float cv[NE];
+      load_colvec_f32<NE>(P.col_scale_f32, c.col, c.n_out, cv);
+#pragma unroll
+      for (int j = 0; j < NE; ++j) v[j] *= cv[j];
+      if (pre) {
+        load_colvec_f32<NE>(P.col_scale_f32 + c.half, c.col, c.n_out, cv);
+#pragma unroll
+        for (int j = 0; j < NE; ++j) u[j] *= cv[j];
+      }
+      break;
+    }
     case CODA_OP_ROW_SCALE:
     case CODA_OP_RMS_ROWSCALE: {
       const float s = (CODE == CODA_OP_RMS_ROWSCALE) ? c.r_rms
@@ -477,6 +489,9 @@ __device__ __forceinline__ void run_ops(const EpiProgram& P, float (&v)[NE], flo
         break;
       case CODA_OP_COL_DOT_NORM:
         op_apply<CODA_OP_COL_DOT_NORM, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
+        break;
+      case CODA_OP_COL_SCALE_F32:
+        op_apply<CODA_OP_COL_SCALE_F32, NE, kGLU>(P, op, pre, v, u, c, aux, red, keep_cnt);
         break;
       default:
         break;

@@ -25,6 +25,8 @@ enum SeqId : int {
   SEQ_SWIGLU,             // SwiGLU up-projection
   SEQ_RMS_SWIGLU,         // commuted RMSNorm -> SwiGLU
   SEQ_SWIGLU_DROPOUT,     // SwiGLU -> dropout
+  SEQ_DEQUANT,            // FP8 dequantisation: row scale x column scale
+  SEQ_DEQUANT_SWIGLU,     // FP8 dequantisation -> SwiGLU
   SEQ_COUNT_
 };
 
@@ -45,6 +47,8 @@ constexpr SeqDef kSeqDefs[] = {
     {SEQ_SWIGLU, true, 1, {CODA_OP_SWIGLU, 0, 0, 0}},
     {SEQ_RMS_SWIGLU, true, 2, {CODA_OP_RMS_ROWSCALE, CODA_OP_SWIGLU, 0, 0}},
     {SEQ_SWIGLU_DROPOUT, true, 2, {CODA_OP_SWIGLU, CODA_OP_DROPOUT, 0, 0}},
+    {SEQ_DEQUANT, false, 2, {CODA_OP_ROW_SCALE, CODA_OP_COL_SCALE_F32, 0, 0}},
+    {SEQ_DEQUANT_SWIGLU, true, 3, {CODA_OP_ROW_SCALE, CODA_OP_COL_SCALE_F32, CODA_OP_SWIGLU, 0}},
 };
 
 }  // namespace coda

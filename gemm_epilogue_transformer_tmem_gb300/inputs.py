@@ -26,6 +26,9 @@ workload descriptions:
            batch): commuted RMSNorm -> SwiGLU, X[128,4096] ~ N(0,1),
            gamma ~ U(0.5,1.5), W[4096,2*11008] ~ N(0, std 0.02).  180 MB of
            weights against 23 GFLOP: bound by HBM, not by the tensor cores
+  fp8swiglu the swiglu up-projection with FP8 E4M3 operands: X quantised per
+           row each step, W[2*11008,4096] ([N, K]) quantised per output
+           channel once; D = SiLU(G)*U of the dequantised product
   wgrad    the LLaMA MLP down-projection's weight gradient at 16384 tokens:
            dW = s * up^T @ dY + dW_old (scaled, accumulated in place) with the
            per-row sums of squares (gradient-norm partials); up[16384,11008]
@@ -122,6 +125,17 @@ def small_int_bf16(shape, lim: int, seed: int) -> torch.Tensor:
     """Integers in [-lim, lim], exactly representable in bf16 for lim <= 256."""
     t = torch.randint(-lim, lim + 1, shape, generator=_gen(seed), dtype=torch.int32)
     return t.to(torch.bfloat16)
+
+
+def random_e4m3_codes(shape, seed: int, exp_lo: int = 7, exp_hi: int = 10) -> torch.Tensor:
+    """Random FP8 E4M3 bytes: uniform sign and 3-bit mantissa, exponent field
+    uniform in [exp_lo, exp_hi] (the default gives magnitudes 1 to 15.5, all
+    multiples of 1/8).  Raw bit patterns: no arithmetic of the method."""
+    g = _gen(seed)
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int32) << 7
+    expo = torch.randint(exp_lo, exp_hi + 1, shape, generator=g, dtype=torch.int32) << 3
+    mant = torch.randint(0, 8, shape, generator=g, dtype=torch.int32)
+    return (sign | expo | mant).to(torch.uint8)
 
 
 def make_pr1(seed: int = 0, M: int = 256, K: int = 256, N: int = 256) -> dict:

@@ -31,6 +31,7 @@ class Step:
     host_inputs: dict = field(default_factory=dict)    # name -> device tensor fed per step in e2e mode
     host_outputs: dict = field(default_factory=dict)   # name -> device tensor read back per step
     bound: str = "tensor"     # what bounds the fused kernel: "tensor" or "hbm"
+    peak_scale: float = 1.0   # tensor peak relative to bf16 (2 for FP8 operands)
     kernels_per_fused: int = 1
     kernels_per_unfused: int = 1
     prep: Optional[Callable[[], None]] = None           # weight preparation (gamma fold)
@@ -165,6 +166,43 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
                 outputs=dict(D=D, D_unfused=Du))
 
 
+def build_fp8swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
+    """The swiglu up-projection with FP8 E4M3 operands: X quantised per row in
+    the step, W ([N, K], output channels as rows) quantised per row once;
+    out = SiLU(G) * U of s_x (.)_row (X8 W8^T) (.)_col s_w."""
+    t = t or inputs.make_swiglu(seed, M, K, N_out)
+    X = t["X"].to(dev)
+    W = t["W"].to(dev).t().contiguous()          # [2*N_out, K]
+    N = 2 * N_out
+    w8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N,), dtype=torch.float32, device=dev)
+    prep = lambda: coda.quantize_e4m3_rows(W, out=w8, scale=sw)   # noqa: E731
+    prep()
+    x8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    ops = [("ROW_SCALE", 0), ("COL_SCALE_F32",), ("SWIGLU",)]
+    D = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
+    ws, _ = _ws(M, N, K, ops, dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Du = torch.empty_like(D)
+
+    def fused():
+        coda.quantize_e4m3_rows(X, out=x8, scale=sx)
+        coda.gemm_epilogue(x8, w8, ops, b_layout="nk", e4m3=True, row_vecs={0: sx}, col_scale_f32=sw, out=D,
+                           workspace=ws)
+
+    def unfused():
+        coda.quantize_e4m3_rows(X, out=x8, scale=sx)
+        coda.gemm_epilogue(x8, w8, [], b_layout="nk", e4m3=True, out=C)
+        coda.epilogue_apply(C, ops, row_vecs={0: sx}, col_scale_f32=sw, out=Du)
+
+    q = M * K * BF16 + M * K + M * F32
+    fb = q + (M * K + N * K) + (M + N) * F32 + M * N_out * BF16
+    ub = q + (M * K + N * K) + M * N * BF16 + (M * N * BF16 + (M + N) * F32 + M * N_out * BF16)
+    return Step("fp8swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
+                peak_scale=2.0, kernels_per_fused=2, kernels_per_unfused=3, prep=prep, outputs=dict(D=D, D_unfused=Du))
+
+
 def build_wgrad(dev="cuda", seed=0, T=16384, d=4096, ffn=11008, t=None) -> Step:
     """dW = s * up^T @ dY + dW (in place), per-row sums of squares of the new dW:
     the down-projection's weight gradient, A read as [K, M] (the stored
@@ -293,4 +331,4 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,
-                llama=build_llama, skinny=build_skinny, wgrad=build_wgrad)
+                llama=build_llama, skinny=build_skinny, wgrad=build_wgrad, fp8swiglu=build_fp8swiglu)

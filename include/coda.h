@@ -70,10 +70,15 @@ typedef enum {
   CODA_B_KN = 0,   /* B is [K, N] row-major: C = A @ B   (weights as x @ W)    */
   CODA_B_NK = 1,   /* B is [N, K] row-major: C = A @ B^T (dgrad dY @ W^T, or an
                       nn.Linear weight stored [out, in])                        */
-  CODA_A_KM = 2    /* flag, OR-ed with either of the above: A is given as [K, M]
+  CODA_A_KM = 2,   /* flag, OR-ed with either of the above: A is given as [K, M]
                       row-major, C = A^T @ B (the weight gradient X^T @ dY from
                       the stored activations X [tokens, features]); M must be a
                       multiple of 8; not with RMS_ROWSCALE / LN_ROWSCALE        */
+  CODA_AB_E4M3 = 4 /* flag: A [M, K] and B [N, K] (CODA_B_NK) are FP8 E4M3 bytes
+                      (tcgen05 kind::f8f6f4, fp32 accumulation); K must be a
+                      multiple of 16; the dequantisation scales are epilogue ops
+                      (ROW_SCALE for A's rows, COL_SCALE_F32 for B's); not with
+                      CODA_A_KM, RMS_ROWSCALE or LN_ROWSCALE                    */
 } coda_b_layout;
 
 /*
@@ -86,6 +91,8 @@ typedef enum {
  *   COL_SCALE      x *= colvec[slot][j]         (bf16 vector of `width` entries)
  *   BIAS           x += colvec[slot][j]         (bf16 vector of `width` entries)
  *   ROW_SCALE      x *= rowvec[slot][i]         (fp32 vector of M entries)
+ *   COL_SCALE_F32  x *= aux.col_scale_f32[j]    (fp32 vector of `width` entries: e.g.
+ *                  the per-channel dequantisation scale of an FP8 weight)
  *   RMS_ROWSCALE   x *= r_i, r_i = 1/sqrt(sum_k A[i,k]^2 / K + f0) gathered from
  *                  the A tiles the mainloop streams (commuted RMSNorm, zeli.app);
  *                  f0 = eps.  If slot != CODA_NO_SLOT, r_i is also written to
@@ -159,7 +166,8 @@ typedef enum {
   CODA_OP_COL_SUMSQ = 20,
   CODA_OP_COL_DOT_AUX = 21,
   CODA_OP_COL_DOT_NORM = 22,
-  CODA_OP_COUNT_ = 23
+  CODA_OP_COL_SCALE_F32 = 23,
+  CODA_OP_COUNT_ = 24
 } coda_opcode;
 
 #define CODA_MAX_OPS 16
@@ -194,6 +202,7 @@ typedef struct {
   const float* ln_colsum;                  /* fp32 [width], LN_ROWSCALE     */
   const float* ln_bias;                    /* fp32 [width], LN_ROWSCALE     */
   float* col_stats;                        /* fp32 [slots][N_out], COL_* ops (output) */
+  const float* col_scale_f32;              /* fp32 [width], COL_SCALE_F32   */
 } coda_aux;
 
 /*
@@ -323,6 +332,17 @@ CODA_API coda_status coda_layernorm(const void* X, const void* gamma, const void
 CODA_API coda_status coda_norm_backward(const void* g, const void* X, const float* r, const float* mu,
                                         const float* sum_g, const float* sum_gx, int64_t M, int64_t K, void* dX,
                                         void* stream);
+
+/*
+ * coda_quantize_e4m3_rows -- per-row FP8 quantisation for the E4M3 GEMM:
+ *     amax_i = max_k |X[i,k]|,  scale_i = amax_i / 448,
+ *     Q[i,k] = e4m3(X[i,k] * (448 / amax_i))   (round to nearest even, saturated
+ *     to +-448; each product and quotient rounded to fp32; a zero row gives Q = 0,
+ *     scale = 0), so X ~= e4m3 value * scale.
+ *   X bf16 [M, K] (16-byte aligned, K % 16 == 0), Q uint8 [M, K], scale fp32 [M].
+ */
+CODA_API coda_status coda_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void* Q, float* scale,
+                                             void* stream);
 
 /*
  * coda_epilogue_apply -- the same op list applied by a separate memory-bound

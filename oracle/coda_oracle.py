@@ -54,7 +54,7 @@ OP_NAMES = (
     "SCALE", "COL_SCALE", "BIAS", "ROW_SCALE", "RMS_ROWSCALE", "GELU_TANH", "SILU",
     "SWIGLU", "GELU_TANH_GRAD", "DROPOUT", "RESIDUAL", "STORE_PREACT",
     "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX", "GELU_ERF", "GELU_ERF_GRAD", "LN_ROWSCALE",
-    "COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM",
+    "COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM", "COL_SCALE_F32",
 )
 
 _U64 = np.uint64
@@ -325,7 +325,7 @@ def row_dot(x, aux):
 # ---------------------------------------------------------------------------
 def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
               residual_t=None, z=None, xhat=None, norm_gamma=None, norm_beta=None, ln_colsum=None,
-              ln_bias=None, rows=None):
+              ln_bias=None, col_scale_f32=None, rows=None):
     """Evaluate D = f(A @ B) for an op list, one unfused pass per op.
 
     ops: sequence of (name, slot, f0) tuples, names from OP_NAMES; f0 is taken
@@ -390,6 +390,8 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
             x = col_scale(x, col_vecs[slot])
         elif name == "BIAS":
             x = bias(x, col_vecs[slot])
+        elif name == "COL_SCALE_F32":
+            x = col_scale(x, col_scale_f32)
         elif name == "ROW_SCALE":
             x = row_scale(x, row_vecs[slot])
         elif name == "RMS_ROWSCALE":
@@ -466,6 +468,59 @@ def round_bf16(x) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
     m, e = np.frexp(x)                    # x = m * 2^e, 0.5 <= |m| < 1
     return np.ldexp(np.round(m * 256.0) / 256.0, e)   # np.round: half to even
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 (the OCP 8-bit floating-point format with 4 exponent bits, bias 7,
+# 3 mantissa bits, no infinities; S.1111.111 is NaN, so the largest finite
+# magnitude is 1.75 * 2^8 = 448; exponent field 0 holds the subnormals m/8 * 2^-6)
+# ---------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code) -> np.ndarray:
+    """Value of each E4M3 byte (fp64); NaN for the two NaN codes."""
+    c = np.asarray(code, dtype=np.int64) & 0xFF
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_decode(np.arange(0, 0x7F))     # the 127 non-negative finite values, codes 0x00..0x7E
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Nearest E4M3 code to each value, ties to the even code (mantissa LSB 0),
+    magnitudes beyond 448 saturated to 448 (the 'satfinite' convention), NaN to
+    0x7F, and the sign kept (a negative value that rounds to zero gives 0x80).
+    For each magnitude the two neighbouring entries of the table of finite
+    values are compared (searchsorted over the sorted table)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, len(_E4M3_POS) - 1)
+    lo = np.clip(hi - 1, 0, len(_E4M3_POS) - 1)
+    d_lo = np.abs(a - _E4M3_POS[lo])
+    d_hi = np.abs(_E4M3_POS[hi] - a)
+    code = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = code.astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def quantize_rows_e4m3(X):
+    """Per-row FP8 quantisation, in float32 arithmetic (as the GPU kernel):
+    amax_i = max_k |x_ik|, scale_i = amax_i / 448, q_ik = e4m3(x_ik * (448 / amax_i))
+    (each product and quotient rounded to float32), q = 0 and scale = 0 for a zero row.
+    Returns (codes uint8 [M, K], scale float32 [M]); x ~= decode(q) * scale."""
+    X = np.asarray(X, dtype=np.float32)
+    amax = np.max(np.abs(X), axis=1)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax > 0, np.float32(E4M3_MAX) / amax, np.float32(0)).astype(np.float32)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    y = (X * inv[:, None]).astype(np.float32)
+    return e4m3_encode(y.astype(np.float64)), scale
 
 
 def to_f64(t) -> np.ndarray:

@@ -407,6 +407,76 @@ def test_norm_backward_chain(kind, mode):
     assert_close(f64(dX), dX_ref, f"{kind} dX")
 
 
+# ------------------------------------------------------------------- FP8
+def test_quantize_e4m3_rows_bit_exact():
+    # rows of very different magnitudes, a zero row and a constant row: codes and
+    # scales equal the oracle's float32 arithmetic bit for bit
+    M, K = 300, 528
+    X = rand((M, K), 701).float()
+    X[1] = 0.0
+    X[2] = 3.0
+    X[3] *= 1e-30
+    X[4] *= 1e30
+    X = X.to(torch.bfloat16)
+    q, sc = coda.quantize_e4m3_rows(cu(X))
+    sync_ok()
+    q_ref, sc_ref = O.quantize_rows_e4m3(X.float().numpy())
+    np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+
+
+@pytest.mark.parametrize("M,K,N", [(300, 256, 264), (128, 512, 512), (520, 128, 136)])
+def test_e4m3_gemm_exact(M, K, N, mode):
+    # values are multiples of 1/8 below 16, so every fp32 partial sum is exact
+    # and D is the bf16 rounding of the exact product
+    A8 = inputs.random_e4m3_codes((M, K), 711)
+    B8 = inputs.random_e4m3_codes((N, K), 712)
+    r = coda.gemm_epilogue(cu(A8), cu(B8), [], b_layout="nk", e4m3=True)
+    sync_ok()
+    ref = O.round_bf16(O.gemm(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), "nk"))
+    np.testing.assert_array_equal(f64(r.D), ref)
+
+
+@pytest.mark.parametrize("glu", [False, True])
+def test_e4m3_gemm_dequant_epilogue(glu, mode):
+    # D = f(s_a (.)_row (A8 B8^T) (.)_col s_b): the dequantisation as epilogue ops
+    M, K, n_out = 300, 384, 264
+    N = 2 * n_out if glu else n_out
+    A8 = inputs.random_e4m3_codes((M, K), 721, 0, 15)
+    A8 = torch.where((A8 & 0x7F) == 0x7F, A8 & 0xF0, A8)     # no NaN codes
+    B8 = inputs.random_e4m3_codes((N, K), 722, 0, 15)
+    B8 = torch.where((B8 & 0x7F) == 0x7F, B8 & 0xF0, B8)
+    sa = torch.rand((M,), generator=torch.Generator().manual_seed(723)) * 1e-3 + 1e-4
+    sb = torch.rand((N,), generator=torch.Generator().manual_seed(724)) * 1e-2 + 1e-3
+    ops = [("ROW_SCALE", 0), ("COL_SCALE_F32",)] + ([("SWIGLU",)] if glu else [("ROW_SUM", 0)])
+    r = coda.gemm_epilogue(cu(A8), cu(B8), ops, b_layout="nk", e4m3=True, row_vecs={0: cu(sa)},
+                           col_scale_f32=cu(sb))
+    plan = coda.last_plan()
+    sync_ok()
+    assert plan["sequence"] > 0 if glu else True
+    ref = O.run_chain(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), ops, b_layout="nk",
+                      row_vecs={0: sa.double().numpy()}, col_scale_f32=sb.double().numpy())
+    assert_close(f64(r.D), ref["D"], "e4m3 dequant")
+    check_stats(r, ref, "e4m3 dequant")
+
+
+def test_e4m3_pipeline_approximates_bf16_gemm():
+    # quantise X per row and W per output channel on the GPU, multiply in FP8 and
+    # dequantise in the epilogue: the result stays within FP8's rounding
+    # (2^-4 relative per operand) of the exact product of the bf16 operands
+    M, K, N = 512, 1024, 768
+    X = rand((M, K), 731)
+    W = rand((N, K), 732, 1.0 / math.sqrt(K))
+    xq, xs = coda.quantize_e4m3_rows(cu(X))
+    wq, ws_ = coda.quantize_e4m3_rows(cu(W))
+    r = coda.gemm_epilogue(xq, wq, [("ROW_SCALE", 0), ("COL_SCALE_F32",)], b_layout="nk", e4m3=True,
+                           row_vecs={0: xs}, col_scale_f32=ws_)
+    sync_ok()
+    ref = f64(X) @ f64(W).T
+    err = np.linalg.norm(f64(r.D) - ref) / np.linalg.norm(ref)
+    assert err < 0.05, err
+
+
 # ------------------------------------------------------------------ dropout
 @pytest.mark.parametrize("seed", [0, 12345])
 @pytest.mark.parametrize("glu", [False, True])

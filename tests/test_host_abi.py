@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(L):
 def test_struct_layouts():
     assert ctypes.sizeof(coda.CodaOp) == 16
     assert ctypes.sizeof(coda.CodaEpilogue) == 16 + 16 * 16
-    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4 + 2 + 1)
+    assert ctypes.sizeof(coda.CodaAux) == 8 * (4 + 2 + 4 + 2 + 1 + 1)
 
 
 def test_opcode_values_match_header():
@@ -117,7 +117,7 @@ def _gemm(L, A, B, M, N, K, ops=(), aux=None, D=0x1000, stats=None, ws=None, ws_
 
 def test_gemm_validation_before_device(L):
     # every one of these fails in host validation, before any CUDA call
-    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=4) == INVALID
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=8) == INVALID
     assert _gemm(L, 0x1008, 0x2000, 64, 64, 64) == ALIGN
     assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, D=0x1004) == ALIGN
     assert _gemm(L, None, 0x2000, 64, 64, 64) == INVALID
@@ -222,3 +222,24 @@ def test_a_km_layout_validation(L):
     st = L.coda_gemm_epilogue(0x1000, 0x2000, 128, 64, 64, 2, ctypes.byref(e), None, 0x3000, None, None, None, 0,
                               None)
     assert st == UNSUPPORTED
+
+
+def test_e4m3_layout_validation(L):
+    # FP8 operands: B as [N, K] only, A as [M, K] only, K a multiple of 16, no commuted norm
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=4) == INVALID          # B as [K, N]
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 64, layout=4 | 1 | 2) == INVALID  # A as [K, M]
+    assert _gemm(L, 0x1000, 0x2000, 64, 64, 40, layout=4 | 1) == INVALID      # K % 16
+    e = coda.make_epilogue([("RMS_ROWSCALE", -1, 1e-6)])
+    st = L.coda_gemm_epilogue(0x1000, 0x2000, 128, 64, 64, 4 | 1, ctypes.byref(e), None, 0x3000, None, None, None,
+                              0, None)
+    assert st == UNSUPPORTED
+
+
+def test_workspace_size_accepts_every_opcode(L):
+    # sizing validates an op list without its aux tensors: every opcode is accepted
+    for name in coda.OPCODES:
+        ops = [(name, 0, 0.1 if name == "DROPOUT" else 1e-5)]
+        if name == "SWIGLU":
+            ops = [("SWIGLU",)]
+        st, _ = _ws(L, 300, 528, 64, ops)
+        assert st == OK, name

@@ -484,3 +484,54 @@ def test_norm_backward_chain_through_the_op_list():
     S = r * (sgx - mu * s1)
     dX = r[:, None] * (G - s1[:, None] / K - xh * S[:, None] / K)
     np.testing.assert_allclose(dX, dX_ref, rtol=1e-10, atol=1e-12)
+
+
+def test_e4m3_decode_known_values():
+    # format facts: 1.0 = 0.0111.000, 448 = 0.1111.110 (largest finite), 2^-6 =
+    # 0.0001.000 (smallest normal), 2^-9 = 0.0000.001 (smallest subnormal)
+    assert O.e4m3_decode(0x38) == 1.0
+    assert O.e4m3_decode(0x7E) == 448.0
+    assert O.e4m3_decode(0x08) == 2.0 ** -6
+    assert O.e4m3_decode(0x01) == 2.0 ** -9
+    assert O.e4m3_decode(0x07) == 7 * 2.0 ** -9
+    assert O.e4m3_decode(0xB8) == -1.0
+    assert O.e4m3_decode(0x40) == 2.0 and O.e4m3_decode(0x3C) == 1.5
+    assert np.isnan(O.e4m3_decode(0x7F)) and np.isnan(O.e4m3_decode(0xFF))
+    assert O.e4m3_decode(0x80) == 0.0 and np.signbit(O.e4m3_decode(0x80))
+    # consecutive positive codes increase
+    v = O.e4m3_decode(np.arange(0x7F))
+    assert (np.diff(v) > 0).all()
+
+
+def test_e4m3_encode_roundtrip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)
+    # midpoints between neighbours go to the even code
+    for c in range(0x00, 0x7E):
+        mid = (O.e4m3_decode(c) + O.e4m3_decode(c + 1)) / 2
+        want = c if c % 2 == 0 else c + 1
+        assert O.e4m3_encode(mid) == want, hex(c)
+        assert O.e4m3_encode(-mid) == want | 0x80
+    # just off a midpoint goes to the nearer value
+    assert O.e4m3_encode(1.0625 + 1e-9) == 0x39 and O.e4m3_encode(1.0625 - 1e-9) == 0x38
+    # saturation and the special values
+    assert O.e4m3_encode(448.0) == 0x7E and O.e4m3_encode(464.0) == 0x7E and O.e4m3_encode(1e30) == 0x7E
+    assert O.e4m3_encode(-1e30) == 0xFE
+    assert O.e4m3_encode(float("nan")) == 0x7F
+    assert O.e4m3_encode(2.0 ** -11) == 0x00 and O.e4m3_encode(-(2.0 ** -11)) == 0x80
+
+
+def test_quantize_rows_e4m3():
+    X = np.array([[0.0, 1.0, -2.0, 4.0], [0.0, 0.0, 0.0, 0.0], [3.0, -3.0, 1.5, 0.75]], dtype=np.float32)
+    q, s = O.quantize_rows_e4m3(X)
+    # row 0: amax 4 -> scale 4/448, x*112 = 0, 112, -224, 448
+    assert s[0] == np.float32(4.0) / np.float32(448.0)
+    np.testing.assert_array_equal(q[0], O.e4m3_encode([0.0, 112.0, -224.0, 448.0]))
+    np.testing.assert_array_equal(q[1], [0, 0, 0, 0]) and s[1] == 0
+    # the row's largest magnitude maps to 448 exactly, and decode * scale recovers x within 2^-4 relative
+    rng_ = np.random.default_rng(3)
+    Y = rng_.standard_normal((8, 64)).astype(np.float32)
+    q, s = O.quantize_rows_e4m3(Y)
+    assert (np.abs(O.e4m3_decode(q)).max(axis=1) == 448.0).all()
+    back = O.e4m3_decode(q) * s[:, None]
+    assert (np.abs(back - Y) <= 2.0 ** -4 * np.abs(Y) + 2.0 ** -9 * s[:, None] * 8).all()
