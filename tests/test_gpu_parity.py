@@ -460,6 +460,34 @@ def test_e4m3_gemm_dequant_epilogue(glu, mode):
     check_stats(r, ref, "e4m3 dequant")
 
 
+@pytest.mark.parametrize("M,K,N", [(1, 16, 8), (129, 16, 264), (7, 4096, 40)])
+def test_e4m3_gemm_edge_shapes(M, K, N):
+    # one row; K below one 128-element k-block (zero-filled tail); a long K with a
+    # narrow output
+    A8 = inputs.random_e4m3_codes((M, K), 741)
+    B8 = inputs.random_e4m3_codes((N, K), 742)
+    r = coda.gemm_epilogue(cu(A8), cu(B8), [("ROW_SUM", 0)], b_layout="nk", e4m3=True)
+    sync_ok()
+    ref = O.run_chain(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), [("ROW_SUM", 0)], b_layout="nk")
+    assert_close(f64(r.D), ref["D"], "e4m3 edge")
+    check_stats(r, ref, "e4m3 edge")
+
+
+@pytest.mark.parametrize("M,N", [(1, 8), (33, 40), (31, 264)])
+def test_column_reductions_edge_shapes(M, N):
+    # a single row, a partial last 32-row block, a partial last 32-column chunk
+    K = 64
+    A = rand((M, K), 751)
+    B = rand((K, N), 752, 0.2)
+    Xh = rand((M, N), 753)
+    ops = [("COL_SUM", 0), ("COL_DOT_AUX", 1)]
+    r = coda.gemm_epilogue(cu(A), cu(B), ops, xhat=cu(Xh))
+    sync_ok()
+    ref = O.run_chain(f64(A), f64(B), ops, xhat=f64(Xh))
+    for slot in (0, 1):
+        assert_col_close(f64(r.col_stats[slot]), ref["col_stats"][slot], ref["col_stat_scale"][slot], f"col {slot}")
+
+
 def test_e4m3_pipeline_approximates_bf16_gemm():
     # quantise X per row and W per output channel on the GPU, multiply in FP8 and
     # dequantise in the epilogue: the result stays within FP8's rounding

@@ -4,8 +4,9 @@ its memory footprint at start-up, since cudaMalloc can synchronise the device
 and has no latency bound).  It keeps its row-reduction and keep-count partials
 in the library's own fixed scratch buffer instead of a caller workspace.
 
-Checked here through the C ABI: two calls in a row, on different problems that
-both use the scratch buffer, each against the regular entry point (which gets a
+Checked here through the C ABI: three calls in a row, on different problems that
+all use the scratch buffer (row reductions and keep counts, then column-reduction
+partials with FP8 operands), each against the regular entry point (which gets a
 workspace from the caller), within the parity tolerance of the other GPU tests;
 and the refusal of a problem that needs more scratch than the buffer holds.
 This file is collected last so a stop-at-first-failure run has already run
@@ -74,6 +75,25 @@ def test_noalloc_matches_regular_entry_point_two_calls():
     _close(out2, ref2.D, "call 2 D")
     _close(st2, ref2.row_stats, "call 2 row sum")
     assert torch.equal(kc2, ref2.keep_count)
+
+    # call 3: FP8 operands with a column reduction (partials in the scratch buffer)
+    A8 = inputs.random_e4m3_codes((M, 256), 907)
+    B8 = inputs.random_e4m3_codes((264, 256), 908)
+    ops3 = [("COL_SUM", 0)]
+    out3 = torch.empty((M, 264), dtype=torch.bfloat16, device=dev)
+    cs3 = torch.empty((1, 264), dtype=torch.float32, device=dev)
+    A8d, B8d = A8.to(dev), B8.to(dev)     # kept alive until the kernels have run
+    e3 = coda.make_epilogue(ops3)
+    a3 = coda.make_aux(col_stats=cs3)
+    st = coda.lib().coda_gemm_epilogue_noalloc(A8d.data_ptr(), B8d.data_ptr(), M, 264, 256,
+                                               coda.B_LAYOUTS["nk"] | coda.AB_E4M3, ctypes.byref(e3),
+                                               ctypes.byref(a3), out3.data_ptr(), None, None,
+                                               torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    ref3 = coda.gemm_epilogue(A8d, B8d, ops3, b_layout="nk", e4m3=True)
+    torch.cuda.synchronize()
+    _close(out3, ref3.D, "call 3 D")
+    _close(cs3, ref3.col_stats, "call 3 column sums")
 
     # a problem needing more scratch than the buffer holds is refused up front
     big_M = 70000
