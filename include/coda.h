@@ -121,7 +121,8 @@ typedef enum {
  *                  OOPSLA 2014).  At most once.  Per-row keep counts go to
  *                  row_keep_count when it is non-NULL.
  * Accumulation (agentlenshq.com "Accumulation"; beta*C_prev of CODA §3.1):
- *   RESIDUAL       x += f0 * residual[i,j]      (bf16 [M, N_out], aux.residual)
+ *   RESIDUAL       x += f0 * residual[i,j]      (bf16 [M, N_out], aux.residual; it may
+ *                  be D itself, for accumulation in place)
  *   STORE_PREACT   writes bf16(x) to aux.preact_out[i, j] ([M, width]); at most once
  * Reductions over the row's `width` columns (agentlenshq.com "Reductions"):
  *   ROW_SUM        row_stats[slot*M + i] = sum_j x
