@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["coda_api.cu", "coda_kernels.cu", "coda_noalloc.cu", "coda_gemm_interp.cu", "coda_gemm_norm.cu",
            "coda_gemm_norm_glu.cu", "coda_gemm_fwd.cu", "coda_gemm_fwd_glu.cu", "coda_gemm_bwd.cu",
-           "coda_gemm_fp8.cu"]
+           "coda_gemm_fp8.cu", "coda_gemm_gpt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]

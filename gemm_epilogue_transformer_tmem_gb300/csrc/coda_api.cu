@@ -381,6 +381,12 @@ cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major,
       return launch_gemm_fwd_glu(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_DGRAD:
       return launch_gemm_bwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_BIAS:
+    case SEQ_BIAS_GELU:
+    case SEQ_BIAS_GELU_ERF:
+    case SEQ_BIAS_RESIDUAL:
+    case SEQ_GELU:
+      return launch_gemm_gpt(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_DEQUANT:
     case SEQ_DEQUANT_SWIGLU:
       return cudaErrorNotSupported;   // built for FP8 operands only

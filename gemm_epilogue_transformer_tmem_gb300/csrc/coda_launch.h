@@ -31,6 +31,8 @@ cudaError_t launch_gemm_fwd_glu(int seq, bool a_mn_major, bool b_mn_major, bool 
 cudaError_t launch_gemm_bwd(int seq, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
                              const CUtensorMap* maps,
                             const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_gpt(int seq, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
+                            const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st);
 // FP8 E4M3 operands: the interpreter and the FP8 fixed sequences
 cudaError_t launch_gemm_fp8(int seq, bool glu, bool pair, const CUtensorMap* maps, const GemmParams& p, int grid,
                             size_t smem, cudaStream_t st);

@@ -27,6 +27,11 @@ enum SeqId : int {
   SEQ_SWIGLU_DROPOUT,     // SwiGLU -> dropout
   SEQ_DEQUANT,            // FP8 dequantisation: row scale x column scale
   SEQ_DEQUANT_SWIGLU,     // FP8 dequantisation -> SwiGLU
+  SEQ_BIAS,               // projection + bias
+  SEQ_BIAS_GELU,          // bias -> GELU(tanh): GPT-2 MLP up-projection
+  SEQ_BIAS_GELU_ERF,      // bias -> GELU(erf): BERT MLP up-projection
+  SEQ_BIAS_RESIDUAL,      // bias -> + residual: attention out / MLP down-projection
+  SEQ_GELU,               // GELU(tanh) without bias
   SEQ_COUNT_
 };
 
@@ -49,6 +54,11 @@ constexpr SeqDef kSeqDefs[] = {
     {SEQ_SWIGLU_DROPOUT, true, 2, {CODA_OP_SWIGLU, CODA_OP_DROPOUT, 0, 0}},
     {SEQ_DEQUANT, false, 2, {CODA_OP_ROW_SCALE, CODA_OP_COL_SCALE_F32, 0, 0}},
     {SEQ_DEQUANT_SWIGLU, true, 3, {CODA_OP_ROW_SCALE, CODA_OP_COL_SCALE_F32, CODA_OP_SWIGLU, 0}},
+    {SEQ_BIAS, false, 1, {CODA_OP_BIAS, 0, 0, 0}},
+    {SEQ_BIAS_GELU, false, 2, {CODA_OP_BIAS, CODA_OP_GELU_TANH, 0, 0}},
+    {SEQ_BIAS_GELU_ERF, false, 2, {CODA_OP_BIAS, CODA_OP_GELU_ERF, 0, 0}},
+    {SEQ_BIAS_RESIDUAL, false, 2, {CODA_OP_BIAS, CODA_OP_RESIDUAL, 0, 0}},
+    {SEQ_GELU, false, 1, {CODA_OP_GELU_TANH, 0, 0, 0}},
 };
 
 }  // namespace coda

@@ -406,9 +406,11 @@ CODA_API void coda_last_plan(coda_plan* out);
 
 /* Fixed op sequences (the CODA article, d9bl.com, §3.3, compiles each
  * epilogue into a specialised kernel): for the op lists of the common blocks --
- * plain GEMM; RMS_ROWSCALE; LN_ROWSCALE; RESIDUAL; BIAS, GELU_TANH, RESIDUAL;
+ * plain GEMM; RMS_ROWSCALE; LN_ROWSCALE; RESIDUAL; BIAS; BIAS, GELU_TANH;
+ * BIAS, GELU_ERF; BIAS, RESIDUAL; GELU_TANH; BIAS, GELU_TANH, RESIDUAL;
  * GELU_TANH_GRAD, ROW_DOT_AUX, ROW_SUM; SWIGLU; RMS_ROWSCALE, SWIGLU; SWIGLU,
- * DROPOUT -- the library launches a kernel built with those opcodes fixed
+ * DROPOUT; and, with FP8 operands, ROW_SCALE, COL_SCALE_F32 (, SWIGLU) --
+ * the library launches a kernel built with those opcodes fixed
  * (straight-line epilogue code); every other list runs the op interpreter.
  * Results are the same either way.  1 (default): use them; 0: interpret all. */
 CODA_API void coda_set_fixed_sequences(int32_t enable);

@@ -182,11 +182,15 @@ OP_CASES = {
     "none": [],
     "bias_gelu_residual": [("BIAS", 0), ("GELU_TANH",), ("RESIDUAL", 0, 1.0)],
     "dgrad": [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)],
+    "bias_gelu": [("BIAS", 0), ("GELU_TANH",)],
+    "bias_gelu_erf": [("BIAS", 0), ("GELU_ERF",)],
+    "bias_residual": [("BIAS", 0), ("RESIDUAL", 0, 1.0)],
 }
 
 # op lists the library runs as fixed op sequences (straight-line epilogues);
 # every other list runs the interpreter
-FIXED_SEQUENCE_CASES = ["none", "residual", "bias_gelu_residual", "dgrad", "swiglu"]
+FIXED_SEQUENCE_CASES = ["none", "residual", "bias_gelu_residual", "dgrad", "swiglu", "bias", "bias_gelu",
+                        "bias_gelu_erf", "bias_residual", "gelu"]
 
 
 def _op_case_tensors(ops, layout, seed):
@@ -281,7 +285,7 @@ def test_unmatched_op_list_runs_interpreter():
     A, B = cu(rand((200, 128), 401)), cu(rand((128, 264), 402, 0.1))
     coda.gemm_epilogue(A, B, [("GELU_TANH",), ("SCALE", 0, 2.0)])
     assert coda.last_plan()["sequence"] == 0
-    coda.gemm_epilogue(A, B, [("GELU_TANH",)])
+    coda.gemm_epilogue(A, B, [("SILU",)])
     assert coda.last_plan()["sequence"] == 0
     coda.gemm_epilogue(A, B, [("RESIDUAL", 0, 1.0)], residual=cu(rand((200, 264), 403)))
     assert coda.last_plan()["sequence"] > 0
