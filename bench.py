@@ -291,6 +291,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-library", action="store_true")
+    ap.add_argument("--tile-order", default="static", choices=["static", "dynamic"],
+                    help="tile order of grids with more tiles than clusters (library knob; default static)")
     ap.add_argument("--split-k", default="auto", choices=["auto", "off", "force"],
                     help="split over K for single-CTA problems (library knob; default auto)")
     args = ap.parse_args()
@@ -315,6 +318,7 @@ def main():
     entry.build()
     from gemm_epilogue_transformer_tmem_gb300 import coda, workloads
     coda.set_split_k(args.split_k)
+    coda.set_tile_scheduler(args.tile_order)
 
     dev = torch.device("cuda", local)
     step = workloads.BUILDERS[args.workload](dev=dev)
@@ -360,6 +364,19 @@ def main():
         unfused = {"ms_per_step": round(u_ms, 5), "value": round(step.flops / (u_ms * 1e-3) / 1e12, 2),
                    "unit": UNIT, "kernels_per_step": u_launched / u_steps,
                    "speedup_fused": round(u_ms / ms, 3)}
+
+    # ---- the step's GEMMs alone through torch.matmul (cuBLAS): a reference point
+    library = None
+    if not args.no_library and step.library is not None and rank == 0:
+        try:
+            l_steps = max(steps // 2, 3)
+            _, l_total, _ = timed_loop([step.library], l_steps, warmup, flush, stream)
+            l_ms = l_total / l_steps
+            library = {"what": "torch.matmul (cuBLAS) of the step's GEMMs on the same operands, no epilogue",
+                       "ms_per_step": round(l_ms, 5), "value": round(step.flops / (l_ms * 1e-3) / 1e12, 2),
+                       "unit": UNIT, "fused_step_vs_library_gemm": round(l_ms / ms, 3)}
+        except RuntimeError as exc:
+            library = {"unavailable": str(exc).splitlines()[0][:200]}
 
     # ---- end to end through host buffers (pinned), copies inside the timed region
     e2e = None
@@ -429,6 +446,7 @@ def main():
         "dram_bytes": {"fused_algorithmic": step.fused_bytes, "unfused_algorithmic": step.unfused_bytes,
                        "ncu_fused_per_launch": traffic["bytes_per_launch"] if traffic else None},
         "unfused": unfused,
+        "library_gemm": library,
         "e2e": e2e,
         "gpu_launches": int(launches),
         "clocks": clocks,

@@ -55,7 +55,7 @@ class CodaAux(ctypes.Structure):
 class CodaPlan(ctypes.Structure):
     _fields_ = [("pair", ctypes.c_int32), ("split", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64), ("prepass", ctypes.c_int32),
-                ("sequence", ctypes.c_int32)]
+                ("sequence", ctypes.c_int32), ("dynamic", ctypes.c_int32)]
 
 
 class CodaError(RuntimeError):
@@ -88,6 +88,7 @@ _SIGS = {
     "coda_set_max_ctas": (None, [ctypes.c_int32]),
     "coda_set_cta_pair": (None, [ctypes.c_int32]),
     "coda_set_split_k": (None, [ctypes.c_int32]),
+    "coda_set_tile_scheduler": (None, [ctypes.c_int32]),
     "coda_last_plan": (None, [_VP]),
     "coda_set_fixed_sequences": (None, [ctypes.c_int32]),
 }
@@ -419,3 +420,11 @@ def set_fixed_sequences(enable: bool) -> None:
 def set_split_k(mode: str) -> None:
     """'auto' (split K over idle SMs for eligible problems), 'off' or 'force'."""
     lib().coda_set_split_k(SPLIT_MODES[mode])
+
+
+def set_tile_scheduler(mode: str) -> None:
+    """'static' (default: persistent round robin) or 'dynamic' (one cluster per
+    tile, running clusters take over the tiles of clusters not yet started)."""
+    if mode not in ("dynamic", "static"):
+        raise ValueError(f"tile scheduler {mode!r}: 'dynamic' or 'static'")
+    lib().coda_set_tile_scheduler(1 if mode == "dynamic" else 0)

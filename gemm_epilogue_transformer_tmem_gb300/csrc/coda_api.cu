@@ -26,6 +26,7 @@ std::atomic<uint64_t> g_timeout_ns{1000000000ull};
 std::atomic<int> g_max_ctas{0};
 std::atomic<int> g_pair_mode{0};   // 0 auto, 1 single CTAs only, 2 CTA pairs whenever K > 0
 std::atomic<int> g_split_mode{0};  // 0 auto, 1 never split over K, 2 split whenever eligible
+std::atomic<int> g_dynamic_tiles{0};  // 1: cluster-launch-control tile order where it applies
 std::atomic<int> g_fixed_seqs{1};  // 1: use the fixed op sequences, 0: always the interpreter
 thread_local coda_plan g_last_plan{};
 
@@ -637,6 +638,15 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   } else if (!split && g.num_tiles < grid) {
     grid = static_cast<int>(g.num_tiles);
   }
+  // Dynamic tile order: one cluster per tile, where the tiles outnumber the
+  // clusters that are resident at once (otherwise every cluster has one tile)
+  const int csize = pair ? 2 : 1;
+  p.clc = 0;
+  if (g_dynamic_tiles.load() != 0 && !split && !rowstat_warps && cap == 0 && g.num_kb > 0 &&
+      g.num_tiles > static_cast<int64_t>(grid / csize) && g.num_tiles * csize <= 0x7FFFFFFF) {
+    p.clc = 1;
+    grid = static_cast<int>(g.num_tiles * csize);
+  }
   int seq = match_sequence(epi, c.glu);
   e = fp8 ? launch_gemm_fp8(seq, c.glu, pair, maps, p, grid, smem, st)
           : launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
@@ -648,7 +658,8 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
-  g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles, p.rms_vec != nullptr ? 1 : 0, seq};
+  g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles, p.rms_vec != nullptr ? 1 : 0, seq,
+                          p.clc};
   if (c.prog.n_colred > 0) {
     e = launch_finalize_cols(c.prog.ws_col, c.prog.n_colred, c.prog.num_rb, g.n_out, c.prog.colred_slot,
                              c.col_stats, st);
@@ -837,6 +848,8 @@ void coda_set_cta_pair(int32_t mode) { g_pair_mode.store(mode < 0 || mode > 2 ? 
 void coda_set_fixed_sequences(int32_t enable) { g_fixed_seqs.store(enable != 0 ? 1 : 0); }
 
 void coda_set_split_k(int32_t mode) { g_split_mode.store(mode < 0 || mode > 2 ? 0 : mode); }
+
+void coda_set_tile_scheduler(int32_t dynamic) { g_dynamic_tiles.store(dynamic != 0 ? 1 : 0); }
 
 void coda_last_plan(coda_plan* out) {
   if (out != nullptr) *out = g_last_plan;

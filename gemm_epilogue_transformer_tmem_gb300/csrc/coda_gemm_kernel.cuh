@@ -45,13 +45,18 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t role, uint3
   }
 }
 
+// Longest sleep of one barrier poll: bounds how late a waiter sees the abort
+// flag or its time limit.
+constexpr uint32_t kWaitSleepNs = 20000;
+
 static __device__ __noinline__ bool wait_slow(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                        uint64_t timeout_ns, uint32_t* err, uint32_t role, uint32_t tile) {
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  for (;;) {
+    // sleep on the barrier between checks of the abort flag and the clock
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
-    if ((it & 15u) == 0u && globaltimer_ns() - t0 > timeout_ns) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       record_error(err, role, tile);
       *abort_flag = 1u;
       return false;
@@ -106,7 +111,16 @@ struct WorkIter {
   int64_t u, u_end;
   int step;
   bool split;
-  __device__ __forceinline__ WorkIter(const GemmParams& p, bool split_, int tile0, int tile_step) : split(split_) {
+  // Dynamic order (cluster launch control, p.clc): the grid has one cluster per
+  // tile; a cluster starts with its own tile and takes each later one from the
+  // scheduler thread's responses, which every tile-walking role reads in turn
+  // from a ring of kSchedSlots and releases on the leader CTA's barrier.
+  bool dyn;
+  bool started;
+  int slot;
+  uint32_t ph;
+  __device__ __forceinline__ WorkIter(const GemmParams& p, bool split_, int tile0, int tile_step)
+      : split(split_), dyn(!split_ && p.clc != 0), started(false), slot(0), ph(0) {
     if (split) {
       const int64_t U = static_cast<int64_t>(p.num_tiles) * p.num_kb;
       u = U * blockIdx.x / gridDim.x;
@@ -118,7 +132,40 @@ struct WorkIter {
       step = tile_step;
     }
   }
-  __device__ __forceinline__ bool next(const GemmParams& p, Item& w) {
+  // One thread (or, with warp_call, a whole warp whose lane 0 waits) takes the
+  // next item.  `sched_ok` turns false when the wait for a response gave up.
+  __device__ __forceinline__ bool next(const GemmParams& p, Item& w, Ctl* ctl, const Waiter& W, uint32_t rank,
+                                       int csize, bool warp_call, int lane, bool& sched_ok) {
+    if (dyn) {
+      int tile = static_cast<int>(u);
+      if (started) {
+        if (!warp_call || lane == 0) {
+          if (W(&ctl->sched_full[slot], ph, static_cast<uint32_t>(u))) {
+            tile = clc_response_ctaid_x(smem_u32(&ctl->sched_resp[slot][0]));
+            if (tile >= 0) tile /= csize;
+            if (rank == 0)
+              mbar_arrive(&ctl->sched_empty[slot]);
+            else
+              mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sched_empty[slot]), 0u));
+          } else {
+            tile = -2;
+          }
+        }
+        if (warp_call) tile = __shfl_sync(0xFFFFFFFFu, tile, 0);
+        if (++slot == kSchedSlots) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+      started = true;
+      if (tile == -2) sched_ok = false;
+      if (tile < 0) return false;
+      u = tile;
+      w.tile = tile;
+      w.kb0 = 0;
+      w.kb1 = p.num_kb;
+      return true;
+    }
     if (u >= u_end) return false;
     if (!split) {
       w.tile = static_cast<int>(u);
@@ -182,6 +229,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   // Per-CTA tile geometry.  A CTA pair shares one 256-row tile: rank r of the
   // pair owns rows r*128 .. r*128+127 of it and stages half of B.
   constexpr int kTileM = kPair ? 2 * BM : BM;
+  constexpr int kCsize = kPair ? 2 : 1;   // CTAs per cluster
   constexpr int kStageB = kPair ? kPairStageBBytes : kStageBBytes;
   // bytes the leader's full barrier expects per stage (both CTAs' loads for a pair)
   constexpr uint32_t kExpectTx = kPair ? 2u * kPairStageBytes : static_cast<uint32_t>(kStageBytes);
@@ -217,6 +265,12 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->auxfull[q][b], 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->esync, kEpiWarps);
+    for (int s = 0; s < kSchedSlots; ++s) {
+      mbar_init(&ctl->sched_full[s], 1);
+      // tile-walking roles: the producers, the MMA issuer and the epilogue warps
+      // of the cluster (the row-statistics variant runs in static order)
+      mbar_init(&ctl->sched_empty[s], kPair ? 2 + 1 + 2 * kEpiWarps : 1 + 1 + kEpiWarps);
+    }
     ctl->abort_flag = 0u;
     fence_mbar_init();
     if (p.num_kb > 0) {
@@ -251,7 +305,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       bool ok = true;
       WorkIter wi(p, split, tile0, tile_step);
       Item w;
-      while (ok && wi.next(p, w)) {
+      while (ok && wi.next(p, w, ctl, W, rank, kCsize, false, lane, ok)) {
         const int tile = w.tile;
         int m_tile, n_tile;
         tile_coords(tile, p, m_tile, n_tile);
@@ -340,7 +394,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       bool ok = true;
       WorkIter wi(p, split, tile0, tile_step);
       Item w;
-      for (; ok && wi.next(p, w); ++local) {
+      for (; ok && wi.next(p, w, ctl, W, rank, kCsize, false, lane, ok); ++local) {
         const int tile = w.tile;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
@@ -400,6 +454,41 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         mma_commit(&ctl->drain);
       wait_drain(&ctl->drain, 0u, 2000000ull);
     }
+  } else if (warp == 3) {
+    // ------------------------------------------------- tile scheduler (dynamic order)
+    // The leader asks for the tile of a cluster that has not started, at most
+    // kSchedSlots responses ahead of the slowest role; each CTA arms its own
+    // barrier for the response, which lands in every CTA of the cluster.  After
+    // the first response that took nothing, no further request is made.
+    if (lane == 0 && p.clc != 0 && !split) {
+      const Waiter W{ctl, p.timeout_ns, p.err, ROLE_SCHEDULER};
+      int slot = 0;
+      uint32_t ph = 0;
+      for (int i = 0;; ++i) {
+        if (leader && i >= kSchedSlots && !W(&ctl->sched_empty[slot], ph ^ 1u, 0u)) break;
+        mbar_arrive_expect_tx(&ctl->sched_full[slot], 16u);
+        if (leader) {
+          fence_proxy_async_smem();   // the roles' reads of the previous response come first
+          clc_try_cancel<kPair>(smem_u32(&ctl->sched_resp[slot][0]), smem_u32(&ctl->sched_full[slot]));
+        }
+        if (!W(&ctl->sched_full[slot], ph, 0u)) {
+          // a request may still be in flight: give it a bounded time to land
+          // (in a pair the other CTA's copy too, as after the producer's abort)
+          wait_drain(&ctl->sched_full[slot], ph, 2000000ull);
+          if (kPair) {
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 200000ull) {
+            }
+          }
+          break;
+        }
+        if (clc_response_ctaid_x(smem_u32(&ctl->sched_resp[slot][0])) < 0) break;
+        if (++slot == kSchedSlots) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+    }
   } else if (warp >= 4 && warp < 4 + kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const int q = warp - 4;
@@ -447,7 +536,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     };
     WorkIter wi(p, split, tile0, tile_step);
     Item w;
-    for (; wi.next(p, w); ++local) {
+    for (; ok && wi.next(p, w, ctl, W, rank, kCsize, true, lane, ok); ++local) {
       const int tile = w.tile;
       int m_tile, n_tile;
       tile_coords(tile, p, m_tile, n_tile);

@@ -36,6 +36,8 @@ constexpr int kMaxStages = 8;
 constexpr int kSplitSegs = 3;
 constexpr int kPartFloats = BN * BM;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
+// Dynamic tile order (cluster launch control): responses in flight at once
+constexpr int kSchedSlots = 2;
 
 // aux tensor kinds (index into the aux tensor-map array)
 enum AuxKind : int { AUX_RESIDUAL = 0, AUX_Z = 1, AUX_XHAT = 2 };
@@ -103,6 +105,8 @@ struct GemmParams {
   int32_t split;           // 1: CTAs take equal runs of (tile, k-block) units (stream-K)
   float* ws_part;          // split: [num_tiles][kSplitSegs][kPartFloats] partial accumulators
   uint32_t* ws_cnt;        // split: [num_tiles] arrival counters, zero at launch
+  int32_t clc;             // 1: one cluster launched per tile; running clusters take
+                           // the tiles of clusters not yet started (cluster launch control)
   EpiProgram prog;
 };
 
@@ -119,6 +123,9 @@ struct Ctl {
   uint64_t drain;
   uint64_t esync;          // the four epilogue warps meet here on split tiles (one arrival each)
   uint32_t eflag[2];       // flag broadcast through esync, by phase parity
+  uint64_t sched_full[kSchedSlots];    // a cluster-launch-control response landed (16 bytes)
+  uint64_t sched_empty[kSchedSlots];   // every tile-walking role read it (leader CTA's barrier)
+  alignas(16) uint32_t sched_resp[kSchedSlots][4];
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];
@@ -126,6 +133,6 @@ struct Ctl {
 };
 
 // device error word layout: [0] code, [1] block, [2] role, [3] tile
-enum ErrRole : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_ROWSTATS = 4 };
+enum ErrRole : uint32_t { ROLE_PRODUCER = 1, ROLE_MMA = 2, ROLE_EPILOGUE = 3, ROLE_ROWSTATS = 4, ROLE_SCHEDULER = 5 };
 
 }  // namespace coda

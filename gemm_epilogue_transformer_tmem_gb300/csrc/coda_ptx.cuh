@@ -56,6 +56,57 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbarrier_try_wait, but the thread may sleep up to `hint_ns` for the phase
+// instead of a short system-dependent limit: a poller that sleeps issues no
+// instructions while it waits (the phase completing wakes it).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// ------------------------------------------------- cluster launch control
+// Ask to take over the work of a cluster of this grid that has not started
+// yet (PTX ISA "clusterlaunchcontrol"): the 16-byte response lands in shared
+// memory at `resp` and completes 16 transaction bytes on `bar`; with kMulticast
+// it lands at the same offsets in every CTA of the cluster.
+template <bool kMulticast>
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  if constexpr (kMulticast)
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes"
+        ".multicast::cluster::all.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+  else
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+
+// The x index of the first CTA of the cluster a response took over, or -1 when
+// it took none (no cluster was left to start).
+__device__ __forceinline__ int clc_response_ctaid_x(uint32_t resp) {
+  uint32_t x = 0, taken = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 r;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(x), "=r"(taken)
+      : "r"(resp)
+      : "memory");
+  return taken ? static_cast<int>(x) : -1;
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

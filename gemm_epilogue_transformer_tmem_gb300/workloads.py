@@ -36,6 +36,10 @@ class Step:
     kernels_per_unfused: int = 1
     prep: Optional[Callable[[], None]] = None           # weight preparation (gamma fold)
     outputs: dict = field(default_factory=dict)
+    # the step's GEMMs alone (no epilogue) through torch.matmul, i.e. the vendor
+    # library (cuBLAS), on the same operands: a measured reference point for the
+    # GEMM core, not part of the step
+    library: Optional[Callable[[], None]] = None
 
 
 def _ws(M, N, K, ops, dev):
@@ -65,11 +69,14 @@ def build_rmsproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
         coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn, rstd=rstd)
         coda.gemm_epilogue(Xn, W, [], out=Du)
 
+    Cl = torch.empty_like(D)
+    library = lambda: torch.matmul(X, Wf, out=Cl)   # noqa: E731
+
     fb = M * K * BF16 + K * N * BF16 + M * N * BF16 + M * F32
     ub = (M * K * BF16 + K * BF16 + M * K * BF16 + M * F32) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
     return Step("rmsproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
                 host_outputs=dict(D=D, r=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
-                outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn))
+                outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn), library=library)
 
 
 def build_lnproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
@@ -99,11 +106,14 @@ def build_lnproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
         coda.layernorm(X, g, beta, inputs.EPS_LN, out=Xn)
         coda.gemm_epilogue(Xn, W, [], out=Du)
 
+    Cl = torch.empty_like(D)
+    library = lambda: torch.matmul(X, prepared["Wf"], out=Cl)   # noqa: E731
+
     fb = M * K * BF16 + K * N * BF16 + 2 * N * F32 + M * N * BF16 + 2 * M * F32
     ub = (M * K * BF16 + 2 * K * BF16 + M * K * BF16) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
     return Step("lnproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
                 host_outputs=dict(D=D, stats=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
-                outputs=dict(D=D, stats=rs, D_unfused=Du, Xn=Xn))
+                outputs=dict(D=D, stats=rs, D_unfused=Du, Xn=Xn), library=library)
 
 
 def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
@@ -128,10 +138,13 @@ def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Ste
         coda.epilogue_apply(C, [("SWIGLU",)], out=H)
         coda.epilogue_apply(H, [("DROPOUT", 0, inputs.DROPOUT_P)], seed=inputs.DROPOUT_SEED, out=Du, keep_count=kcu)
 
+    library = lambda: torch.matmul(X, W, out=C)   # noqa: E731
+
     fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16 + M * 4
     ub = (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16 + (2 * M * N_out * BF16 + M * 4)
     return Step("swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
-                kernels_per_fused=2, kernels_per_unfused=3, outputs=dict(D=D, keep=kc, D_unfused=Du))
+                kernels_per_fused=2, kernels_per_unfused=3, outputs=dict(D=D, keep=kc, D_unfused=Du),
+                library=library)
 
 
 def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step:
@@ -159,11 +172,13 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
         coda.gemm_epilogue(Xn, W, [], out=C)
         coda.epilogue_apply(C, [("SWIGLU",)], out=Du)
 
+    library = lambda: torch.matmul(X, Wf, out=C)   # noqa: E731
+
     fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16
     ub = (2 * M * K * BF16 + K * BF16) + (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16
     return Step("skinny", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
                 bound="hbm", kernels_per_fused=1, kernels_per_unfused=3, prep=prep,
-                outputs=dict(D=D, D_unfused=Du))
+                outputs=dict(D=D, D_unfused=Du), library=library)
 
 
 def build_fp8swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
@@ -224,11 +239,13 @@ def build_wgrad(dev="cuda", seed=0, T=16384, d=4096, ffn=11008, t=None) -> Step:
         coda.gemm_epilogue(up, dY, [], a_layout="km", out=C)
         coda.epilogue_apply(C, ops, residual=dWu, out=dWu, row_stats=rsu)
 
+    library = lambda: torch.matmul(up.t(), dY, out=C)   # noqa: E731
+
     fb = (T * ffn + T * d + 2 * ffn * d) * BF16 + ffn * F32
     ub = (T * ffn + T * d + ffn * d) * BF16 + (3 * ffn * d * BF16 + ffn * F32)
     return Step("wgrad", 2 * ffn * d * T, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
                 host_outputs=dict(norms=rs), kernels_per_fused=2, kernels_per_unfused=3,
-                outputs=dict(dW=dW, norms=rs))
+                outputs=dict(dW=dW, norms=rs), library=library)
 
 
 def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
@@ -252,11 +269,13 @@ def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
         coda.epilogue_apply(C, [("GELU_TANH_GRAD",)], z=Z, out=Du)
         coda.epilogue_apply(Du, [("ROW_DOT_AUX", 0), ("ROW_SUM", 1)], xhat=Xh, out=Dz, row_stats=rsu)
 
+    library = lambda: torch.matmul(dY, W.t(), out=C)   # noqa: E731
+
     fb = (M * K + N * K + 3 * M * N) * BF16 + 2 * M * F32
     ub = (M * K + N * K + M * N) * BF16 + 3 * M * N * BF16 + (2 * M * N * BF16 + 2 * M * F32)
     return Step("dgrad", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
                 host_outputs=dict(D=D, stats=rs), kernels_per_fused=2, kernels_per_unfused=3,
-                outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu))
+                outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu), library=library)
 
 
 def llama_block_forward(t: dict, prepared: Optional[dict] = None, out: Optional[dict] = None) -> dict:
@@ -320,6 +339,12 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
 
     flops = 2 * T * d * (3 * d) + 2 * T * d * d + 2 * T * d * (2 * ffn) + 2 * T * ffn * d
     act = T * d * BF16
+    def library():
+        torch.matmul(t["X"], prepared["W_qkv"], out=un["qkv"])
+        torch.matmul(t["attn_out"], t["W_o"], out=un["c_o"])
+        torch.matmul(un["h"], prepared["W_up"], out=un["c_up"])
+        torch.matmul(un["up"], t["W_down"], out=un["c_down"])
+
     fb = (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (2 * act + d * d * BF16 + act) + \
          (act + d * 2 * ffn * BF16 + T * ffn * BF16) + (T * ffn * BF16 + ffn * d * BF16 + 2 * act)
     ub = (2 * act) + (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (act + d * d * BF16 + act) + 3 * act + \
@@ -327,7 +352,7 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
          (T * ffn * BF16 + ffn * d * BF16 + act) + 3 * act
     return Step("llama", flops, fb, ub, fused, unfused, host_inputs=dict(X=t["X"], attn_out=t["attn_out"]),
                 host_outputs=dict(y=out["y"], qkv=out["qkv"]), kernels_per_fused=4, kernels_per_unfused=9,
-                prep=prep, outputs=out)
+                prep=prep, outputs=out, library=library)
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,

@@ -391,6 +391,15 @@ CODA_API void coda_set_cta_pair(int32_t mode);
  * is eligible (see coda_workspace_size) and the workspace holds the partials;
  * 1: never; 2: whenever a single-CTA problem has two k-blocks or more. */
 CODA_API void coda_set_split_k(int32_t mode);
+/* Tile order of grids with more tiles than resident CTAs (clusters).
+ * 0 (default): static -- a persistent grid walks tile0, tile0 + grid, ...;
+ * 1: dynamic -- one cluster is launched per tile, and a running cluster takes
+ * over the tile of a cluster that has not started yet (PTX cluster launch
+ * control) whenever it is ready for more work, so clusters on faster SMs do
+ * more tiles.  Split-K grids, a capped grid (coda_set_max_ctas) and the variant
+ * with in-kernel row statistics always run the static order.  Results are
+ * bit-identical either way. */
+CODA_API void coda_set_tile_scheduler(int32_t dynamic);
 
 /* How the calling thread's last successful coda_gemm_epilogue call ran. */
 typedef struct {
@@ -401,6 +410,7 @@ typedef struct {
   int64_t tiles;     /* output tiles                                          */
   int32_t prepass;   /* 1: a row-statistics pre-pass kernel ran first         */
   int32_t sequence;  /* 0: op-list interpreter; > 0: a fixed op sequence      */
+  int32_t dynamic;   /* 1: dynamic tile order (cluster launch control)        */
 } coda_plan;
 CODA_API void coda_last_plan(coda_plan* out);
 

@@ -21,25 +21,29 @@ from oracle import coda_oracle as O
 pytestmark = pytest.mark.gpu
 
 TIMEOUT = 5
-ROLES = {1: "producer", 2: "mma", 3: "epilogue", 4: "row statistics"}
+ROLES = {1: "producer", 2: "mma", 3: "epilogue", 4: "row statistics", 5: "tile scheduler"}
 
 
-@pytest.mark.parametrize("mode", ["single", "pair", "split"])
+@pytest.mark.parametrize("mode", ["single", "pair", "split", "dynamic_single", "dynamic_pair"])
 def test_pipeline_wait_times_out_and_context_recovers(mode):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     entry.build()
-    M, K, N = 512, 1024, 512
+    # the dynamic modes have more tiles than resident clusters (one cluster per
+    # tile, later tiles taken over through cluster launch control)
+    M, K, N = (2048, 256, 4096) if mode.startswith("dynamic") else (512, 1024, 512)
     A = inputs.randn_bf16((M, K), 1.0, 71).cuda()
     B = inputs.randn_bf16((K, N), 1.0 / math.sqrt(K), 72).cuda()
     ops = [("GELU_TANH",), ("ROW_SUM", 0)]
     st0, _ = coda.check_device_error()
     assert st0 == 0
-    coda.set_cta_pair("pair" if mode == "pair" else "single")
+    coda.set_cta_pair("pair" if mode.endswith("pair") else "single")
+    coda.set_tile_scheduler("dynamic" if mode.startswith("dynamic") else "static")
     coda.set_split_k("force" if mode == "split" else "off")
     try:
         coda.set_pipeline_timeout_ns(1)
         coda.gemm_epilogue(A, B, ops)          # enqueued fine; the kernel gives up
+        assert coda.last_plan()["dynamic"] == (1 if mode.startswith("dynamic") else 0)
         st, info = coda.check_device_error()
         assert coda.STATUS[st] == "CODA_ERR_TIMEOUT", (st, info)
         assert info[0] == TIMEOUT and info[2] in ROLES, info
@@ -52,6 +56,7 @@ def test_pipeline_wait_times_out_and_context_recovers(mode):
     st3, info3 = coda.check_device_error()
     coda.set_cta_pair("auto")
     coda.set_split_k("auto")
+    coda.set_tile_scheduler("static")
     assert st3 == 0, info3
     ref = O.run_chain(O.to_f64(A), O.to_f64(B), ops)
     got = O.to_f64(r.D)

@@ -261,6 +261,69 @@ def test_fixed_sequence_matches_interpreter(case, layout, mode):
         coda.set_fixed_sequences(True)
 
 
+# ------------------------------------------------------- dynamic tile order
+# More tiles than resident clusters, so that running clusters take over the
+# tiles of clusters that have not started (cluster launch control): single-CTA
+# 128x256 tiles, 16 x 11 = 176 on 152 SMs; CTA pairs, 256x256 tiles, 8 x 11 =
+# 88 on 76 clusters.  Ragged in M, N and K; K small so that the oracle is quick.
+M_T, K_T, N_T = 2000, 104, 2600
+TILE_ORDER_CASES = ["none", "bias_gelu_residual", "swiglu", "dgrad", "reductions", "chain", "rms",
+                    "bias_swiglu_bias_sum"]
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+@pytest.mark.parametrize("case", TILE_ORDER_CASES)
+def test_dynamic_tile_order(case, kernel):
+    # the same call in the dynamic and the static tile order: bit-identical
+    # (each tile's arithmetic does not depend on which cluster ran it), and
+    # within the oracle's bound
+    ops = [("RMS_ROWSCALE", 0, 1e-6)] if case == "rms" else OP_CASES[case]
+    glu = any(o[0] == "SWIGLU" for o in ops)
+    N = 2 * N_T if glu else N_T
+    n_out = N_T
+    A = rand((M_T, K_T), 900 + len(case))
+    B = rand((K_T, N), 901 + len(case), 1.0 / math.sqrt(K_T))
+    pos = [i for i, o in enumerate(ops) if o[0] == "SWIGLU"]
+    gpos = pos[0] if pos else len(ops)
+    col = {o[1]: rand((N if i < gpos else n_out,), 910 + o[1])
+           for i, o in enumerate(ops) if o[0] in ("COL_SCALE", "BIAS")}
+    row = {0: torch.rand((M_T,), generator=torch.Generator().manual_seed(920)) + 0.5}
+    aux = dict(residual=rand((M_T, n_out), 930), z=rand((M_T, n_out), 931), xhat=rand((M_T, n_out), 932))
+    args = dict(col_vecs={k: cu(v) for k, v in col.items()}, row_vecs={0: cu(row[0])},
+                residual=cu(aux["residual"]), z=cu(aux["z"]), xhat=cu(aux["xhat"]), seed=5)
+    coda.set_cta_pair(kernel)
+    coda.set_split_k("off")
+    out = {}
+    try:
+        for order in ("dynamic", "static"):
+            coda.set_tile_scheduler(order)
+            r = coda.gemm_epilogue(cu(A), cu(B), ops, **args)
+            plan = coda.last_plan()
+            sync_ok()
+            # the single-CTA commuted norm with tiles filling the grid computes its
+            # row statistics in the kernel, a variant that keeps the static order
+            dyn = order == "dynamic" and not (case == "rms" and kernel == "single")
+            assert plan["dynamic"] == (1 if dyn else 0), plan
+            assert plan["pair"] == (1 if kernel == "pair" else 0), plan
+            if dyn:
+                assert plan["grid"] == plan["tiles"] * (2 if kernel == "pair" else 1), plan
+            out[order] = r
+    finally:
+        coda.set_tile_scheduler("static")
+        coda.set_cta_pair("auto")
+        coda.set_split_k("auto")
+    d, s_ = out["dynamic"], out["static"]
+    ref = O.run_chain(f64(A), f64(B), ops, col_vecs={k: f64(v) for k, v in col.items()}, row_vecs={0: f64(row[0])},
+                      residual_t=f64(aux["residual"]), z=f64(aux["z"]), xhat=f64(aux["xhat"]), seed=5)
+    assert torch.equal(d.D, s_.D), f"{case}: dynamic and static tile orders differ"
+    for slot in ref["stats"]:      # the slots the op list writes
+        assert torch.equal(d.row_stats[slot], s_.row_stats[slot]), f"{case}: row statistic {slot} differs"
+    if d.keep_count is not None:
+        assert torch.equal(d.keep_count, s_.keep_count)
+    assert_close(f64(d.D), ref["D"], f"{case} {kernel} dynamic order")
+    check_stats(d, ref, f"{case} {kernel} dynamic order")
+
+
 @pytest.mark.parametrize("fixed", [True, False])
 def test_swiglu_dropout_sequence_mask_bit_exact(fixed, mode):
     M, K, n_out = 333, 192, 264

@@ -163,7 +163,7 @@ def test_workspace_size_for_layernorm_op_list():
 
 
 def test_plan_struct_layout():
-    assert ctypes.sizeof(coda.CodaPlan) == 32
+    assert ctypes.sizeof(coda.CodaPlan) == 40
 
 
 def test_workspace_size_split_k_closed_form(L):
