@@ -42,7 +42,8 @@ import torch  # noqa: E402
 METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 bf16 roofline; DRAM bytes vs unfused"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["coda_gemm_kernel.cuh", "coda_ops.cuh", "coda_ptx.cuh", "coda_internal.h", "coda_sequences.h"]
+KERNEL_SOURCES = ["coda_gemm_kernel.cuh", "coda_ops.cuh", "coda_ptx.cuh", "coda_internal.h", "coda_sequences.h",
+                  "coda_api.cu"]
 L2_FLUSH_BYTES = 256 << 20
 
 DESCRIPTIONS = {
