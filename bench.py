@@ -295,6 +295,8 @@ def main():
     ap.add_argument("--no-library", action="store_true")
     ap.add_argument("--tile-order", default="static", choices=["static", "dynamic"],
                     help="tile order of grids with more tiles than clusters (library knob; default static)")
+    ap.add_argument("--tail-helpers", default="on", choices=["on", "off"],
+                    help="non-epilogue warps share each CTA's last-tile epilogue (library knob; default on)")
     ap.add_argument("--split-k", default="auto", choices=["auto", "off", "force"],
                     help="split over K for single-CTA problems (library knob; default auto)")
     args = ap.parse_args()
@@ -320,6 +322,7 @@ def main():
     from gemm_epilogue_transformer_tmem_gb300 import coda, workloads
     coda.set_split_k(args.split_k)
     coda.set_tile_scheduler(args.tile_order)
+    coda.set_tail_helpers(args.tail_helpers == "on")
 
     dev = torch.device("cuda", local)
     step = workloads.BUILDERS[args.workload](dev=dev)

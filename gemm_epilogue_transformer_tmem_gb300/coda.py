@@ -89,6 +89,7 @@ _SIGS = {
     "coda_set_cta_pair": (None, [ctypes.c_int32]),
     "coda_set_split_k": (None, [ctypes.c_int32]),
     "coda_set_tile_scheduler": (None, [ctypes.c_int32]),
+    "coda_set_tail_helpers": (None, [ctypes.c_int32]),
     "coda_last_plan": (None, [_VP]),
     "coda_set_fixed_sequences": (None, [ctypes.c_int32]),
 }
@@ -420,6 +421,11 @@ def set_fixed_sequences(enable: bool) -> None:
 def set_split_k(mode: str) -> None:
     """'auto' (split K over idle SMs for eligible problems), 'off' or 'force'."""
     lib().coda_set_split_k(SPLIT_MODES[mode])
+
+
+def set_tail_helpers(enable: bool) -> None:
+    """Let the non-epilogue warps share the epilogue of each CTA's last tile (default on)."""
+    lib().coda_set_tail_helpers(1 if enable else 0)
 
 
 def set_tile_scheduler(mode: str) -> None:

@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->auxfull[q][b], 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->esync, kEpiWarps);
+    for (int q = 0; q < kEpiWarps; ++q) mbar_init(&ctl->helpdone[q], 1);
     for (int s = 0; s < kSchedSlots; ++s) {
       mbar_init(&ctl->sched_full[s], 1);
       // tile-walking roles: the producers, the MMA issuer and the epilogue warps
@@ -447,9 +448,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         else
           mma_commit(&ctl->tfull[acc]);
       }
-      // no MMA may still write tensor memory when it is freed
+      // no MMA may still write tensor memory when it is freed (in a pair both
+      // CTAs learn it: their helper warps wait for it too)
       if constexpr (kPair)
-        mma_commit_pair(&ctl->drain);
+        mma_commit_pair_mc(&ctl->drain, 0x3);
       else
         mma_commit(&ctl->drain);
       wait_drain(&ctl->drain, 0u, 2000000ull);
@@ -645,9 +647,15 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
       }
 
-      float red[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+      // The CTA's last tile (static order): the helper warp of this lane quarter
+      // takes its odd chunks.  Row reductions keep even and odd chunks apart in
+      // every tile, so that the sum does not depend on who took which chunk.
+      const bool helped = !kRowStats && p.helpers != 0 && !split && tile + tile_step >= p.num_tiles;
+      float red0[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+      float red1[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t keep = 0;
       for (int c = 0; c < nch; ++c) {
+        if (helped && (c & 1)) continue;
         const int col = col_base + c * kChunk;
         if (n_aux > 0) {
           if (c + 1 < nch) issue_aux(abuf ^ 1, col + kChunk, m0 + q * 32);
@@ -707,7 +715,19 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         if (nvalid > kChunk) nvalid = kChunk;
         const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
         const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
-        Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red, keep);
+        if constexpr (kRowStats) {   // never helped: one running sum
+          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red0, keep);
+        } else {
+          float cred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, cred, keep);
+          if (c & 1) {
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red1[r] += cred[r];
+          } else {
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red0[r] += cred[r];
+          }
+        }
 
         // stage bf16 row chunk (64-byte swizzle) and TMA-store the 32x32 box
         uint8_t* ob = out_stage + sbuf * kBoxBytes;
@@ -730,12 +750,22 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         if (n_aux > 0) abuf ^= 1;
       }
       if (!ok) break;
+      if (helped && (p.prog.n_red > 0 || p.ws_keep != nullptr)) {
+        if (!warp_wait(W, &ctl->helpdone[q], 0u, tile, lane)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
+          if (r < p.prog.n_red) red1[r] = ctl->hred[q][r][lane];
+        keep += ctl->hkeep[q][lane];
+      }
       if (row_ok) {
         const size_t Ms = static_cast<size_t>(p.M);
 #pragma unroll
         for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
           if (r < p.prog.n_red)
-            p.ws_red[(static_cast<size_t>(r) * p.num_n_tiles + n_tile) * Ms + row] = red[r];
+            p.ws_red[(static_cast<size_t>(r) * p.num_n_tiles + n_tile) * Ms + row] = red0[r] + red1[r];
         if (p.ws_keep != nullptr) p.ws_keep[static_cast<size_t>(n_tile) * Ms + row] = keep;
         if (kRowStats && p.rms_slot >= 0 && n_tile == 0) {
           p.row_stats[static_cast<size_t>(p.rms_slot) * Ms + row] = r_rms;
@@ -819,6 +849,90 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         ctl->rs[acc][r] = rsqrtf(fmaf(s, p.inv_K, p.rms_eps));
       }
       mbar_arrive(&ctl->rsfull[acc]);
+    }
+  }
+
+  if constexpr (!kRowStats) {
+    // ------------------------------------------ helpers on the CTA's last tile
+    // Once the last accumulator is complete nothing is left to load or issue:
+    // the producer, MMA, allocator and scheduler warps (lane quarters 0-3) take
+    // the odd chunks of the CTA's last tile, halving the epilogue that nothing
+    // overlaps.  Only in the static order, without aux tensors or a split.
+    if (p.helpers != 0 && !split && warp < kEpiWarps) {
+      __syncwarp();
+      const int q = warp;
+      const Waiter W{ctl, p.timeout_ns, p.err, ROLE_EPILOGUE};
+      const int n_local = tile0 < p.num_tiles ? (p.num_tiles - 1 - tile0) / tile_step + 1 : 0;
+      if (n_local > 0 && p.num_kb > 0) {
+        constexpr int kOutCols = kGLU ? BN / 2 : BN;
+        const int local = n_local - 1;
+        const int tile = tile0 + local * tile_step;
+        int m_tile, n_tile;
+        tile_coords(tile, p, m_tile, n_tile);
+        const int m0 = m_tile * kTileM + static_cast<int>(rank) * BM;
+        const int row = m0 + q * 32 + lane;
+        const bool row_ok = row < p.M;
+        const int col_base = n_tile * kOutCols;
+        int nch = (p.N_out - col_base + kChunk - 1) / kChunk;
+        if (nch > kOutCols / kChunk) nch = kOutCols / kChunk;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (local & 1) * kAccCols;
+        // every MMA of the CTA has completed (used once: no phase ambiguity)
+        if (warp_wait(W, &ctl->drain, 0u, static_cast<uint32_t>(tile), lane)) {
+          tc_fence_after_sync();
+          float r_rms = 1.0f, mu = 0.0f;
+          if (p.rms_vec != nullptr) {
+            griddep_wait();
+            r_rms = row_ok ? p.rms_vec[row] : 1.0f;
+            if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
+          }
+          const uint64_t stream_policy = policy_evict_first();
+          // staging in the ring, whose copies have all landed and been consumed
+          uint8_t* hstage = smem + q * (2 * kBoxBytes);
+          const SmemAux ax{hstage, lane};   // unused: no aux tensors here
+          float hred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+          uint32_t keep = 0;
+          int sbuf = 0;
+          for (int c = 1; c < nch; c += 2) {
+            const int col = col_base + c * kChunk;
+            float v[32], u[32];
+            tmem_ld32(t_row + c * kChunk, v);
+            if (kGLU) tmem_ld32(t_row + BN / 2 + c * kChunk, u);
+            int nvalid = p.N_out - col;
+            if (nvalid > kChunk) nvalid = kChunk;
+            const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
+            float cred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+            Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, cred, keep);
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) hred[r] += cred[r];
+            uint8_t* ob = hstage + sbuf * kBoxBytes;
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            {
+              uint8_t* rowp = ob + lane * 64;
+              const int sw = (lane >> 1) & 3;
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = pack8(v + 8 * cc);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d_hint(&tmD, ob, col, m0 + q * 32, stream_policy);
+              bulk_commit_group();
+            }
+            sbuf ^= 1;
+          }
+          if (p.prog.n_red > 0 || p.ws_keep != nullptr) {
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->hred[q][r][lane] = hred[r];
+            ctl->hkeep[q][lane] = keep;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->helpdone[q]);
+          }
+          if (lane == 0) bulk_wait_group<0>();
+          __syncwarp();
+        }
+      }
     }
   }
 

@@ -107,6 +107,7 @@ struct GemmParams {
   uint32_t* ws_cnt;        // split: [num_tiles] arrival counters, zero at launch
   int32_t clc;             // 1: one cluster launched per tile; running clusters take
                            // the tiles of clusters not yet started (cluster launch control)
+  int32_t helpers;         // 1: warps 0-3 take the odd chunks of each CTA's last tile
   EpiProgram prog;
 };
 
@@ -126,6 +127,9 @@ struct Ctl {
   uint64_t sched_full[kSchedSlots];    // a cluster-launch-control response landed (16 bytes)
   uint64_t sched_empty[kSchedSlots];   // every tile-walking role read it (leader CTA's barrier)
   alignas(16) uint32_t sched_resp[kSchedSlots][4];
+  uint64_t helpdone[kEpiWarps];                           // a helper warp's row partials are in place
+  float hred[kEpiWarps][CODA_MAX_REDUCTIONS][32];         // helper row-reduction partials (last tile)
+  uint32_t hkeep[kEpiWarps][32];                          // helper dropout keep counts (last tile)
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];

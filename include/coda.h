@@ -400,6 +400,11 @@ CODA_API void coda_set_split_k(int32_t mode);
  * with in-kernel row statistics always run the static order.  Results are
  * bit-identical either way. */
 CODA_API void coda_set_tile_scheduler(int32_t dynamic);
+/* 1 (default): once a CTA's last accumulator is complete, its producer, MMA and
+ * other non-epilogue warps take half of that tile's epilogue chunks (static tile
+ * order, op lists without aux tensors, no split over K, at most 16 tiles per
+ * cluster); 0: the epilogue warps alone.  Results are bit-identical either way. */
+CODA_API void coda_set_tail_helpers(int32_t enable);
 
 /* How the calling thread's last successful coda_gemm_epilogue call ran. */
 typedef struct {

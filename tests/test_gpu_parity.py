@@ -388,6 +388,52 @@ def test_column_reductions(case, layout, mode):
         assert_col_close(f64(r.col_stats[slot]), v, ref["col_stat_scale"][slot], f"{case} col {slot}")
 
 
+HELPER_CASES = {
+    "none": [],
+    "reductions": [("ROW_SUM", 0), ("ROW_MEAN", 1), ("ROW_SUMSQ", 2), ("ROW_DOT_AUX", 3)],
+    "swiglu_dropout": [("SWIGLU",), ("DROPOUT", 0, 0.1)],
+    "scale_preact_swiglu": [("SCALE", 0, 2.0), ("STORE_PREACT",), ("SWIGLU",), ("ROW_SUMSQ", 1)],
+    "gelu_colsum_rowsum": [("GELU_TANH",), ("COL_SUM", 0), ("ROW_SUM", 0)],
+    "rms_swiglu": [("RMS_ROWSCALE", 0, 1e-6), ("SWIGLU",)],
+}
+
+
+@pytest.mark.parametrize("case", sorted(HELPER_CASES))
+def test_tail_helpers_bit_identical(case, mode):
+    # the non-epilogue warps taking half of each CTA's last tile change nothing:
+    # outputs, row and column statistics and keep counts are bit-identical
+    ops = HELPER_CASES[case]
+    if case == "reductions":
+        ops = [o for o in ops if o[0] != "ROW_DOT_AUX"]    # an aux tensor disables the helpers
+    A, B, N, n_out, col, row, aux = _op_case_tensors(ops, "kn", 700 + len(case))
+    preact = None
+    if any(o[0] == "STORE_PREACT" for o in ops):
+        preact = torch.zeros((M_R, N), dtype=torch.bfloat16, device="cuda")
+    out = []
+    try:
+        for helpers in (True, False):
+            coda.set_tail_helpers(helpers)
+            if preact is not None:
+                preact.zero_()
+            r = coda.gemm_epilogue(cu(A), cu(B), ops, seed=9, preact_out=preact)
+            sync_ok()
+            out.append((r, None if preact is None else preact.clone()))
+    finally:
+        coda.set_tail_helpers(True)
+    (a, pa), (b, pb) = out
+    assert torch.equal(a.D, b.D), case
+    ref = O.run_chain(f64(A), f64(B), ops, seed=9)
+    for slot in ref["stats"]:
+        assert torch.equal(a.row_stats[slot], b.row_stats[slot]), (case, slot)
+    for slot in ref.get("col_stats", {}):
+        assert torch.equal(a.col_stats[slot], b.col_stats[slot]), (case, slot)
+    if a.keep_count is not None:
+        assert torch.equal(a.keep_count, b.keep_count)
+    if pa is not None:
+        assert torch.equal(pa, pb)
+    assert_close(f64(a.D), ref["D"], f"{case} with helpers")
+
+
 def test_column_sums_exact_small_integers(mode):
     # integer-valued D (small-integer GEMM, exact in fp32): column sums are exact
     M, K, N = 300, 128, 264
