@@ -58,7 +58,7 @@ extern "C" {
 typedef enum {
   CODA_OK = 0,
   CODA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, bad op list         */
-  CODA_ERR_UNSUPPORTED = 2,   /* valid request this build cannot run         */
+  CODA_ERR_UNSUPPORTED = 2,   /* valid request the library does not support  */
   CODA_ERR_ALIGNMENT = 3,     /* pointer or row stride not 16-byte aligned   */
   CODA_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed           */
   CODA_ERR_TIMEOUT = 5,       /* a device-side wait exceeded its time limit  */

@@ -1,5 +1,5 @@
 """The benchmark's reference arm (the fp64 oracle timed on the host cores) and
-its JSON line, run as the driver runs it, on CPU."""
+its JSON line: the command line a benchmark harness runs, on CPU."""
 import json
 import os
 import subprocess
