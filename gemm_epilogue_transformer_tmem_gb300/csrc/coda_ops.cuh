@@ -20,18 +20,26 @@ constexpr float kGeluC = 0.044715f;
 constexpr uint64_t kSplitmixGamma = 0x9E3779B97F4A7C15ull;
 
 // The logistic function and the activations built on it.  The epilogue has one
-// warp per scheduler and no other work to hide latency behind, so these use
-// the hardware exponential (__expf) and the fast division (__fdividef), whose
-// errors (a few ulp, ~1e-6 relative) are far below the bf16 rounding of the
-// output (2^-9 relative).  The argument is clamped to [-80, 80], where the
-// logistic function is 0 or 1 to fp32 precision, so that e^-x stays finite
-// and no inf/inf or 0*inf can arise.
-//   sigmoid(x) = 1 / (1 + e^-x),  1 - sigmoid(x) = e^-x sigmoid(x)
+// warp per scheduler and little to hide latency behind, and the special-function
+// unit is its busiest pipe (SiLU and GELU took two of its operations per element
+// with an exponential and a reciprocal).  So the logistic function is taken from
+// the hardware tanh (PTX tanh.approx.f32, one operation, relative error about
+// 2^-11):  sigmoid(x) = (1 + tanh(x/2)) / 2,  1 - sigmoid(x) = (1 - tanh(x/2)) / 2.
+// Its absolute error is at most 2^-12 (about 2.4e-4): SiLU and GELU carry at
+// most 2.4e-4 |x|, below the bf16 rounding of the output (2^-9 to 2^-8) where
+// the output is not near zero; in the negative tail, where sigmoid(x) itself is
+// below 1e-3, the error is absolute, not relative.  tanh saturates to +-1, so
+// no argument overflows.
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float sigmoid_f(float x, float& one_minus) {
-  const float e = __expf(-fminf(fmaxf(x, -80.0f), 80.0f));
-  const float s = __fdividef(1.0f, 1.0f + e);
-  one_minus = e * s;
-  return s;
+  const float t = tanh_hw(0.5f * x);
+  one_minus = fmaf(-0.5f, t, 0.5f);
+  return fmaf(0.5f, t, 0.5f);
 }
 
 __device__ __forceinline__ float silu_f(float x) {

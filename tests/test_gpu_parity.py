@@ -324,6 +324,36 @@ def test_dynamic_tile_order(case, kernel):
     check_stats(d, ref, f"{case} {kernel} dynamic order")
 
 
+@pytest.mark.parametrize("op", ["SILU", "GELU_TANH", "GELU_TANH_GRAD"])
+def test_activation_error_bound(op):
+    # D = I @ B leaves the accumulator equal to B (exact), so the op sees bf16
+    # inputs spread over [-20, 20]; with the logistic function taken from the
+    # hardware tanh (absolute error <= 2^-12), SiLU and GELU may differ from the
+    # exact function by 2.5e-4 |x| on top of the bf16 rounding of the output
+    # (half an ulp: at most 2^-8 relative); GELU'(z) (z from the aux tensor,
+    # B = 1) by 2.5e-4 (1 + 2|z u'(z)|)
+    n = 256
+    A = torch.eye(n, dtype=torch.float32).bfloat16()
+    x = torch.linspace(-20.0, 20.0, n * n, dtype=torch.float64).reshape(n, n)
+    xb = x.to(torch.bfloat16)
+    if op == "GELU_TANH_GRAD":
+        B = torch.ones((n, n), dtype=torch.bfloat16)
+        r = coda.gemm_epilogue(cu(A), cu(B), [(op,)], z=cu(xb))
+        ref = O.run_chain(f64(A), f64(B), [(op,)], z=f64(xb))["D"]
+        zz = f64(xb)
+        du = math.sqrt(2.0 / math.pi) * (1.0 + 3.0 * 0.044715 * zz * zz)
+        allow = 2.5e-4 * (1.0 + 2.0 * np.abs(zz * du))
+    else:
+        r = coda.gemm_epilogue(cu(A), cu(xb), [(op,)])
+        ref = O.run_chain(f64(A), f64(xb), [(op,)])["D"]
+        allow = 2.5e-4 * np.abs(f64(xb))
+    sync_ok()
+    got = f64(r.D)
+    err = np.abs(got - ref)
+    bound = 1.01 * allow + 2.0 ** -8 * np.abs(ref) + 1e-30
+    assert (err <= bound).all(), f"{op}: worst excess {np.max(err - bound)!r}"
+
+
 @pytest.mark.parametrize("fixed", [True, False])
 def test_swiglu_dropout_sequence_mask_bit_exact(fixed, mode):
     M, K, n_out = 333, 192, 264
