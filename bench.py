@@ -23,6 +23,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -63,10 +64,16 @@ DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "
 
 
 def kernel_hash() -> str:
+    """Hash of the kernel and planner sources with comments and whitespace
+    removed: a committed ncu traffic figure stays valid while only the prose
+    around the code changes."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "gemm_epilogue_transformer_tmem_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "gemm_epilogue_transformer_tmem_gb300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -15,6 +15,8 @@
 //   warp 1      MMA issuer: tcgen05.mma (M=128, N=256, K=16) into one of two
 //               fp32 accumulators in tensor memory (2 x 256 columns)
 //   warp 2      allocates / frees the 512 tensor-memory columns
+//   warp 3      (dynamic tile order only) asks cluster launch control for the
+//               tile of a cluster that has not started yet
 //   warps 4-7   epilogue: tcgen05.ld drains the accumulator one 32-column chunk
 //               at a time (thread = row), runs the op list, packs bf16 (RNE)
 //               into swizzled staging and TMA-stores it; aux tiles (residual,
@@ -24,6 +26,8 @@
 //               memory and accumulate sum_k x^2 for their row, then
 //               r = rsqrt(s/K+eps).  A CTA pair takes r from a pre-pass kernel
 //               that overlaps the pair's mainloop (programmatic dependent launch).
+// On each CTA's last tile warps 0-3 (one per tensor-memory lane quarter) join
+// the epilogue once the last accumulator is complete and take its odd chunks.
 // Every mbarrier wait is bounded: on expiry the kernel records a timeout in the
 // device error word, lets in-flight copies land, frees tensor memory and exits.
 #pragma once
