@@ -243,3 +243,17 @@ def test_workspace_size_accepts_every_opcode(L):
             ops = [("SWIGLU",)]
         st, _ = _ws(L, 300, 528, 64, ops)
         assert st == OK, name
+
+
+def test_tuning_knobs_round_trip(L):
+    # the knobs are host-side settings; setting and restoring them launches nothing
+    before = L.coda_launch_count()
+    coda.set_tile_scheduler("dynamic")
+    coda.set_tile_scheduler("static")
+    coda.set_tail_helpers(False)
+    coda.set_tail_helpers(True)
+    coda.set_split_k("off")
+    coda.set_split_k("auto")
+    assert L.coda_launch_count() == before
+    with pytest.raises(ValueError):
+        coda.set_tile_scheduler("round-robin")
