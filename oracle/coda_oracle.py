@@ -54,7 +54,7 @@ OP_NAMES = (
     "SCALE", "COL_SCALE", "BIAS", "ROW_SCALE", "RMS_ROWSCALE", "GELU_TANH", "SILU",
     "SWIGLU", "GELU_TANH_GRAD", "DROPOUT", "RESIDUAL", "STORE_PREACT",
     "ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX", "GELU_ERF", "GELU_ERF_GRAD", "LN_ROWSCALE",
-    "COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM", "COL_SCALE_F32",
+    "COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM", "COL_SCALE_F32", "RMS_SUMSQ_ROWSCALE",
 )
 
 _U64 = np.uint64
@@ -100,6 +100,15 @@ def rmsnorm(X: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
 def rmsnorm_project(X, gamma, W, eps, b_layout="kn"):
     """Normalise-then-project: rmsnorm(X) @ W (the unfused reading)."""
     return gemm(rmsnorm(X, gamma, eps), W, b_layout)
+
+
+def rms_rstd_from_sumsq(sumsq, K: int, eps: float) -> np.ndarray:
+    """r_i = 1 / sqrt(s_i / K + eps) from given row sums of squares s_i = sum_k x_ik^2
+    (the same r as rms_rstd when s is X's own): the commuted norm whose row
+    statistics were gathered by an earlier pass over X (for X produced by a
+    residual epilogue, that epilogue's row sum of squares)."""
+    s = np.asarray(sumsq, dtype=np.float64)
+    return 1.0 / np.sqrt(s / float(K) + eps)
 
 
 def ln_stats(X: np.ndarray, eps: float):
@@ -332,18 +341,23 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
         as the float32 the op list carries (widened exactly to fp64).
     col_vecs / row_vecs: dict slot -> vector (bf16 values widened).
     residual_t, z, xhat: [M, N_out] aux tensors (or only the sampled rows).
-    norm_gamma: if given, the op list must begin with RMS_ROWSCALE or
-        LN_ROWSCALE; the GEMM is then evaluated as rmsnorm(A; gamma) @ B or
-        layernorm(A; gamma, norm_beta) @ B (normalise, then project), with B the
-        *unscaled* weight.
+    norm_gamma: if given, the op list must begin with RMS_ROWSCALE,
+        RMS_SUMSQ_ROWSCALE or LN_ROWSCALE; the GEMM is then evaluated as
+        rmsnorm(A; gamma) @ B or layernorm(A; gamma, norm_beta) @ B (normalise,
+        then project), with B the *unscaled* weight (RMS_SUMSQ_ROWSCALE takes
+        its row sums of squares from row_vecs[slot] instead of from A).
+        Without norm_gamma these ops scale the product by the row factor r_i
+        (B then already holds gamma (.)_row W).
     ln_colsum / ln_bias: the c and b vectors of an LN_ROWSCALE evaluated as
         written (x = r (x - mu c) + b) when the norm is not given unfused.
     rows: absolute row indices of the rows of A given (used by dropout's
         counter and nothing else); default 0..M-1.
 
     Returns dict with D (fp64), stats {slot: fp64[M]}, stat_scale {slot: fp64[M]}
-    (the L2 norm of each row reduction's summands: the scale of its rounding
-    error when the summands carry independent relative errors), col_stats
+    (the error scale of each row reduction: the L2 norm over its summands of
+    d(summand)/d(log x), i.e. how far the sum moves when every chain value x
+    carries an independent relative error of 1 -- the summand itself for the
+    linear reductions, twice it for the sums of squares), col_stats
     {slot: fp64[N_out]} and col_stat_scale (the same for the column reductions,
     which need all M rows: not with `rows`), keep_count (int64[M] or None),
     keep (bool mask or None), preact (fp64 or None).
@@ -371,8 +385,13 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
                 mu, r = ln_stats(A, eps)
                 stats[slot] = r
                 stats[slot + 1] = mu
+        elif name == "RMS_SUMSQ_ROWSCALE":
+            # normalise with r from the given row sums of squares, then project
+            r = rms_rstd_from_sumsq(row_vecs[slot], A.shape[1], eps)
+            xn = (r[:, None] * A) * np.asarray(norm_gamma, dtype=np.float64)[None, :]
+            x = gemm(xn, B, b_layout)
         else:
-            raise ValueError("norm_gamma needs RMS_ROWSCALE or LN_ROWSCALE as the first op")
+            raise ValueError("norm_gamma needs RMS_ROWSCALE, RMS_SUMSQ_ROWSCALE or LN_ROWSCALE as the first op")
         start = 1
     else:
         x = gemm(A, B, b_layout)
@@ -399,6 +418,8 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
             x = row_scale(x, r)
             if slot is not None and slot >= 0:
                 stats[slot] = r
+        elif name == "RMS_SUMSQ_ROWSCALE":
+            x = row_scale(x, rms_rstd_from_sumsq(row_vecs[slot], A.shape[1], f0))
         elif name == "LN_ROWSCALE":
             mu, r = ln_stats(A, f0)
             c = np.asarray(ln_colsum, dtype=np.float64)
@@ -436,7 +457,7 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
             stat_scale[slot] = np.sqrt(row_sumsq(x)) / x.shape[1]
         elif name == "ROW_SUMSQ":
             stats[slot] = row_sumsq(x)
-            stat_scale[slot] = np.sqrt(row_sumsq(x * x))
+            stat_scale[slot] = 2.0 * np.sqrt(row_sumsq(x * x))
         elif name == "ROW_DOT_AUX":
             stats[slot] = row_dot(x, xhat)
             stat_scale[slot] = np.sqrt(row_sumsq(x * np.asarray(xhat, dtype=np.float64)))
@@ -453,7 +474,7 @@ def run_chain(A, B, ops, *, b_layout="kn", seed=0, col_vecs=None, row_vecs=None,
                 mm = np.asarray(row_vecs[1], dtype=np.float64) if 1 in row_vecs else np.zeros_like(rr)
                 t = x * (rr[:, None] * (np.asarray(xhat, dtype=np.float64) - mm[:, None]))
             col_stats[slot] = col_sum(t)
-            col_stat_scale[slot] = np.sqrt(col_sum(t * t))
+            col_stat_scale[slot] = (2.0 if name == "COL_SUMSQ" else 1.0) * np.sqrt(col_sum(t * t))
         else:
             raise ValueError(f"unknown op {name}")
     return dict(D=x, stats=stats, stat_scale=stat_scale, col_stats=col_stats, col_stat_scale=col_stat_scale,

@@ -284,6 +284,67 @@ def test_chain_commuted_norm_reads_unscaled_weight():
     np.testing.assert_allclose(out["D"], r[:, None] * (X @ (gamma[:, None] * W)), rtol=1e-12)
 
 
+def _brute_rmsnorm_project(X, gamma, W, eps, sumsq=None):
+    """Normalise, then project, written out element by element: the textbook
+    definition rmsnorm(X; gamma) @ W, with the mean of squares taken over the
+    K entries of each row (or from the given row sums of squares)."""
+    M, K = len(X), len(X[0])
+    N = len(W[0])
+    out = [[0.0] * N for _ in range(M)]
+    for i in range(M):
+        ss = sum(X[i][k] * X[i][k] for k in range(K)) if sumsq is None else sumsq[i]
+        r = 1.0 / math.sqrt(ss / K + eps)
+        xn = [X[i][k] * r * gamma[k] for k in range(K)]
+        for j in range(N):
+            out[i][j] = sum(xn[k] * W[k][j] for k in range(K))
+    return np.array(out)
+
+
+def test_chain_rms_rowscale_on_folded_weight_hand_values():
+    # RMS_ROWSCALE without norm_gamma: the product is scaled by r_i taken from
+    # A's own rows.  Row [3, 4] has mean square 12.5 and row [0, -2] mean square
+    # 2, so with eps = 0 and B = I the outputs are x / sqrt(12.5) = x sqrt(2)/5
+    # and x / sqrt(2).
+    X = np.array([[3.0, 4.0], [0.0, -2.0]])
+    out = O.run_chain(X, np.eye(2), [("RMS_ROWSCALE", 0, 0.0)])
+    s2 = math.sqrt(2.0)
+    np.testing.assert_allclose(out["D"], [[3 * s2 / 5, 4 * s2 / 5], [0.0, -s2]], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(out["stats"][0], [s2 / 5, 1 / s2], rtol=1e-15)
+
+
+def test_chain_rms_rowscale_on_folded_weight_brute_force():
+    # the folded weight gamma (.)_row W with RMS_ROWSCALE gives the textbook
+    # normalise-then-project result, element by element
+    X = rng.standard_normal((5, 12))
+    gamma = rng.uniform(0.5, 1.5, 12)
+    W = rng.standard_normal((12, 7))
+    out = O.run_chain(X, gamma[:, None] * W, [("RMS_ROWSCALE", None, 1e-6)])
+    ref = _brute_rmsnorm_project(X.tolist(), gamma.tolist(), W.tolist(), 1e-6)
+    np.testing.assert_allclose(out["D"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_chain_rms_from_sumsq_hand_values_and_brute_force():
+    # RMS_SUMSQ_ROWSCALE: the same row factor from given sums of squares.  With
+    # the rows' own sums (25 and 4 for the hand rows above) it reproduces the
+    # hand values; with norm_gamma it is normalise-then-project; with other sums
+    # it follows them (s = 2 K: r = 1/sqrt(2 + eps))
+    X = np.array([[3.0, 4.0], [0.0, -2.0]])
+    out = O.run_chain(X, np.eye(2), [("RMS_SUMSQ_ROWSCALE", 0, 0.0)], row_vecs={0: np.array([25.0, 4.0])})
+    s2 = math.sqrt(2.0)
+    np.testing.assert_allclose(out["D"], [[3 * s2 / 5, 4 * s2 / 5], [0.0, -s2]], rtol=1e-15, atol=0)
+    out = O.run_chain(X, np.eye(2), [("RMS_SUMSQ_ROWSCALE", 0, 0.0)], row_vecs={0: np.array([4.0, 4.0])})
+    np.testing.assert_allclose(out["D"], X / s2, rtol=1e-15, atol=0)
+    Xr = rng.standard_normal((4, 10))
+    gamma = rng.uniform(0.5, 1.5, 10)
+    W = rng.standard_normal((10, 6))
+    ss = [sum(v * v for v in row) for row in Xr.tolist()]
+    ref = _brute_rmsnorm_project(Xr.tolist(), gamma.tolist(), W.tolist(), 1e-6, sumsq=ss)
+    folded = O.run_chain(Xr, gamma[:, None] * W, [("RMS_SUMSQ_ROWSCALE", 1, 1e-6)], row_vecs={1: np.array(ss)})
+    np.testing.assert_allclose(folded["D"], ref, rtol=1e-12, atol=1e-12)
+    unfused = O.run_chain(Xr, W, [("RMS_SUMSQ_ROWSCALE", 1, 1e-6)], row_vecs={1: np.array(ss)}, norm_gamma=gamma)
+    np.testing.assert_allclose(unfused["D"], ref, rtol=1e-12, atol=1e-12)
+
+
 def test_chain_dgrad_form():
     dY = rng.standard_normal((5, 7))
     W = rng.standard_normal((9, 7))     # [N, K]
