@@ -544,6 +544,89 @@ def quantize_rows_e4m3(X):
     return e4m3_encode(y.astype(np.float64)), scale
 
 
+# ---------------------------------------------------------------------------
+# MX (microscaling) E4M3 -- block-scaled FP8: the agentlenshq.com summary's
+# scaling primitive (section "仕組み": scaling by a vector) applied per block
+# of 32 elements along K.  The format is the OCP Microscaling Formats (MX)
+# specification v1.0 (2023): a block of 32 E4M3 elements P_i shares one E8M0
+# scale X (a bare exponent byte e, X = 2^(e-127), e = 255 is NaN); the block's
+# values are X * P_i.  Conversion (the specification's algorithm): the shared
+# exponent is floor(log2(max_i |V_i|)) - emax_elem, with emax_elem = 8 for E4M3
+# (448 = 1.75 * 2^8), clamped to the scale's range [-127, 127]; then
+# P_i = e4m3(V_i / X), rounded to nearest even and saturated at +-448.
+# ---------------------------------------------------------------------------
+MX_BLOCK = 32
+E4M3_EMAX = 8
+
+
+def e8m0_decode(e) -> np.ndarray:
+    """X = 2^(e - 127) for each scale byte, NaN for 255."""
+    e = np.asarray(e, dtype=np.int64) & 0xFF
+    return np.where(e == 255, np.nan, np.exp2(e.astype(np.float64) - 127.0))
+
+
+def quantize_mx_e4m3(X):
+    """MX E4M3 quantisation of each row of X [R, K] in blocks of 32 along K (the
+    last block of a row may be shorter).  Returns (codes uint8 [R, K], scale
+    bytes uint8 [R, ceil(K/32)]).  A block of zeros gets scale byte 0 and zero
+    codes.  Written element by element from the definition: the shared exponent
+    from the exact binary exponent of the block maximum (math.frexp), the
+    division by a power of two exact in fp64, then round-to-nearest-even onto
+    the E4M3 grid with saturation (e4m3_encode)."""
+    X = np.asarray(X, dtype=np.float64)
+    R, K = X.shape
+    nb = (K + MX_BLOCK - 1) // MX_BLOCK
+    codes = np.zeros((R, K), dtype=np.uint8)
+    sexp = np.zeros((R, nb), dtype=np.uint8)
+    for i in range(R):
+        for b in range(nb):
+            blk = X[i, b * MX_BLOCK:(b + 1) * MX_BLOCK]
+            amax = float(np.max(np.abs(blk)))
+            if amax == 0.0:
+                shared = -127
+            else:
+                _, e = math.frexp(amax)            # amax = m 2^e, 0.5 <= m < 1: floor(log2 amax) = e - 1
+                shared = min(max((e - 1) - E4M3_EMAX, -127), 127)
+            sexp[i, b] = shared + 127
+            codes[i, b * MX_BLOCK:(b + 1) * MX_BLOCK] = e4m3_encode(blk / math.ldexp(1.0, shared))
+    return codes, sexp
+
+
+def dequantize_mx(codes, sexp) -> np.ndarray:
+    """fp64 values X_block * P_i of MX E4M3 data (codes [R, K], scale bytes [R, ceil(K/32)])."""
+    codes = np.asarray(codes)
+    R, K = codes.shape
+    scale = np.repeat(e8m0_decode(sexp), MX_BLOCK, axis=1)[:, :K]
+    return e4m3_decode(codes) * scale
+
+
+def mx_scale_offset(r: int, j: int, K: int) -> int:
+    """Byte offset of the scale of row r, 32-element block j in the library's
+    tiled scale storage (the layout coda.h defines for MX operands): rows in
+    groups of 128 and blocks in groups of 4 form 512-byte tiles, tiles ordered
+    by row group then block group, and inside a tile the scale of (row r,
+    block j) at (r % 32) * 16 + ((r % 128) // 32) * 4 + (j % 4)."""
+    kb = (K + 127) // 128
+    return ((r // 128) * kb + j // 4) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + (j % 4)
+
+
+def mx_scale_bytes(R: int, K: int) -> int:
+    """Size of the tiled scale storage of an [R, K] MX operand (rows padded to
+    128, blocks to 4 per row)."""
+    return ((R + 127) // 128) * ((K + 127) // 128) * 512
+
+
+def mx_scales_from_tiled(buf, R: int, K: int) -> np.ndarray:
+    """Scale bytes [R, ceil(K/32)] read out of the tiled storage, element by element."""
+    buf = np.asarray(buf, dtype=np.uint8).reshape(-1)
+    nb = (K + MX_BLOCK - 1) // MX_BLOCK
+    out = np.zeros((R, nb), dtype=np.uint8)
+    for r in range(R):
+        for j in range(nb):
+            out[r, j] = buf[mx_scale_offset(r, j, K)]
+    return out
+
+
 def to_f64(t) -> np.ndarray:
     """Widen a tensor (torch bf16/fp32 or numpy) to an fp64 numpy array exactly."""
     try:

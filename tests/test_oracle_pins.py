@@ -596,3 +596,78 @@ def test_quantize_rows_e4m3():
     assert (np.abs(O.e4m3_decode(q)).max(axis=1) == 448.0).all()
     back = O.e4m3_decode(q) * s[:, None]
     assert (np.abs(back - Y) <= 2.0 ** -4 * np.abs(Y) + 2.0 ** -9 * s[:, None] * 8).all()
+
+
+# ------------------------------------------------------------ MX E4M3 -------
+# OCP Microscaling Formats (MX) v1.0: E8M0 scale X = 2^(e-127) shared by 32
+# E4M3 elements; conversion takes the shared exponent floor(log2 amax) - 8.
+def test_e8m0_decode_known_values():
+    assert O.e8m0_decode(127) == 1.0
+    assert O.e8m0_decode(130) == 8.0
+    assert O.e8m0_decode(0) == 2.0 ** -127
+    assert O.e8m0_decode(254) == 2.0 ** 127
+    assert np.isnan(O.e8m0_decode(255))
+
+
+def test_mx_quantize_hand_values():
+    V = np.zeros((6, 32))
+    V[0, :4] = [1.0, 0.5, -0.25, 0.125]          # amax 1: X = 2^-8, P = 256 V
+    V[1, :3] = [448.0, 1.0, -2.0]                 # amax 448: X = 1
+    V[2, :2] = [500.0, 3.0]                       # amax 500: X = 1, 500 saturates to 448
+    V[3, :] = 0.0                                 # zero block: byte 0, zero codes
+    V[4, 0] = 1.5 * 2.0 ** 127                    # X = 2^119, P = 384
+    V[5, 0] = 3.0 * 2.0 ** -140                   # scale clamped to 2^-127; P = 3 2^-13 rounds to 0
+    codes, sexp = O.quantize_mx_e4m3(V)
+    assert list(sexp[:, 0]) == [119, 127, 127, 0, 246, 0]
+    assert list(codes[0, :5]) == [0x78, 0x70, 0xE8, 0x60, 0x00]   # 256, 128, -64, 32, 0
+    assert list(codes[1, :3]) == [0x7E, 0x38, 0xC0]              # 448, 1, -2
+    assert list(codes[2, :2]) == [0x7E, 0x44]                    # 448 (saturated), 3 = 1.5 * 2^1
+    assert not codes[3].any()
+    assert codes[4, 0] == 0x7C                                   # 384 = 1.5 * 2^8
+    assert codes[5, 0] == 0x00
+
+
+def test_mx_roundtrip_error_bound_and_ragged_block():
+    # elements whose scaled value lies in E4M3's normal range and below 448 are
+    # within half an E4M3 ulp (2^-4 relative); the last block of a row may be short
+    rng2 = np.random.default_rng(7)
+    V = rng2.standard_normal((8, 70)) * np.exp2(rng2.integers(-20, 20, (8, 1)))
+    codes, sexp = O.quantize_mx_e4m3(V)
+    assert sexp.shape == (8, 3)
+    back = O.dequantize_mx(codes, sexp)
+    X = np.repeat(O.e8m0_decode(sexp), 32, axis=1)[:, :70]
+    P = np.abs(V) / X
+    ok = (P >= 2.0 ** -6) & (P <= 448.0)
+    assert ok.mean() > 0.9
+    assert (np.abs(back - V)[ok] <= 2.0 ** -4 * np.abs(V)[ok] * (1 + 1e-12)).all()
+    # the block maximum's exponent sets X: amax / X in [256, 512)
+    amax = np.maximum.reduceat(np.abs(V), [0, 32, 64], axis=1)
+    assert ((amax / O.e8m0_decode(sexp) >= 256) & (amax / O.e8m0_decode(sexp) < 512)).all()
+
+
+def test_mx_dequantized_gemm_closed_form():
+    # A's row: 32 ones at scale 1, then 32 ones at scale 2 (byte 128); B all ones at
+    # scale 1: every output is 32 * 1 + 32 * 2 = 96; an off-by-one block index
+    # would give 64 or 128
+    codes_a = np.full((2, 64), 0x38, dtype=np.uint8)
+    sexp_a = np.array([[127, 128], [128, 127]], dtype=np.uint8)
+    codes_b = np.full((3, 64), 0x38, dtype=np.uint8)
+    sexp_b = np.full((3, 2), 127, dtype=np.uint8)
+    A = O.dequantize_mx(codes_a, sexp_a)
+    B = O.dequantize_mx(codes_b, sexp_b)
+    np.testing.assert_array_equal(O.gemm(A, B, "nk"), np.full((2, 3), 96.0))
+
+
+def test_mx_scale_tiled_offsets():
+    # K = 160: 5 blocks of 32 per row, 2 groups of 4 blocks
+    assert O.mx_scale_offset(0, 0, 160) == 0
+    assert O.mx_scale_offset(0, 1, 160) == 1
+    assert O.mx_scale_offset(1, 0, 160) == 16
+    assert O.mx_scale_offset(32, 0, 160) == 4
+    assert O.mx_scale_offset(127, 3, 160) == 31 * 16 + 3 * 4 + 3
+    assert O.mx_scale_offset(0, 4, 160) == 512
+    assert O.mx_scale_offset(128, 0, 160) == 2 * 512
+    assert O.mx_scale_bytes(130, 160) == 2 * 2 * 512
+    # every (row, block) of a 200 x 5 matrix has its own byte
+    offs = {O.mx_scale_offset(r, j, 160) for r in range(200) for j in range(5)}
+    assert len(offs) == 1000 and max(offs) < O.mx_scale_bytes(200, 160)
