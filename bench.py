@@ -1,15 +1,26 @@
 """Benchmark of the fused GEMM + on-chip epilogue path on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload rmsproj|lnproj|swiglu|fp8swiglu|dgrad|wgrad|llama|skinny]
-                    [--impl coda|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama|rmsproj|lnproj|swiglu|fp8swiglu|dgrad|wgrad|skinny]
+                    [--impl coda|reference] [--profile-steps]
 
-Default workload: the commuted-RMSNorm projection D = rsqrt(mean(X^2)+1e-6) *
-(X @ (gamma (.) W)), X[4096,2048], W[2048,8192], bf16 in, fp32 accumulate.
+Default workload: the LLaMA-7B-like non-attention block at 16384 tokens (d 4096,
+ffn 11008): commuted RMSNorm -> QKV projection, out-projection + residual,
+commuted RMSNorm -> SwiGLU up-projection, down-projection + residual; four fused
+GEMM+epilogue calls, bf16 in, fp32 accumulate, 6.63 TFLOP per step.  The other
+workloads are the single calls of the same family (the commuted-RMSNorm
+projection, the SwiGLU up-projection with dropout, the dgrad, ...).
 One step = one pass of the fused path over the synthetic batch.  Prints one
 JSON line (rank 0): fused TFLOP/s, the roofline of the fused GEMM kernel, the
 same chain run unfused through the library's own kernels, DRAM bytes fused vs
 unfused, an end-to-end figure through host buffers, clocks, and the fp64
 oracle timed on the host cores as the CPU baseline.
+
+--profile-steps runs, after the warm-up, one fused step and then one unfused
+step, each between full L2 flushes and each followed by a read-only pass over
+a 256 MiB buffer, and exits: under ncu (one metric group, --cache-control none)
+every kernel of a step is captured in order, and the read-only pass after it
+writes back exactly the step's outputs still dirty in L2, so the step's DRAM
+bytes are its kernels' reads and writes plus that pass's writes.
 
 Timing: W warm-up steps, then K steps, each bracketed by CUDA events on the
 launching stream, with a 256 MiB device write and a 256 MiB read between steps
@@ -43,8 +54,6 @@ import torch  # noqa: E402
 METRIC = "fused GEMM+epilogue TFLOP/s and % of GB300 bf16 roofline; DRAM bytes vs unfused"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["coda_gemm_kernel.cuh", "coda_ops.cuh", "coda_ptx.cuh", "coda_internal.h", "coda_sequences.h",
-                  "coda_api.cu"]
 L2_FLUSH_BYTES = 256 << 20
 
 DESCRIPTIONS = {
@@ -58,23 +67,12 @@ DESCRIPTIONS = {
              "row sums of squares",
     "fp8swiglu": "SwiGLU up-projection in FP8 E4M3: X[8192,4096] quantised per row each step, W[22016,4096] "
                  "per channel once, dequantised in the epilogue, SiLU(G)*U",
-    "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs)",
+    "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs): commuted "
+             "RMSNorm->QKV, out-proj+residual, commuted RMSNorm->SwiGLU up-proj, down-proj+residual; one layer of "
+             "a stack: the norms' row sums of squares come from the preceding residual epilogues (the input's "
+             "with the input, the next layer's emitted by the down-projection)",
 }
 DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300, "fp8swiglu": 300}
-
-
-def kernel_hash() -> str:
-    """Hash of the kernel and planner sources with comments and whitespace
-    removed: a committed ncu traffic figure stays valid while only the prose
-    around the code changes."""
-    h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "gemm_epilogue_transformer_tmem_gb300", "csrc", f), encoding="utf-8") as fh:
-            src = fh.read()
-        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        src = re.sub(r"//[^\n]*", "", src)
-        h.update("".join(src.split()).encode())
-    return h.hexdigest()[:16]
 
 
 def load_peaks():
@@ -87,8 +85,10 @@ def load_peaks():
 
 
 def load_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    or None when the kernel sources changed since that capture."""
+    """DRAM bytes of the fused and unfused steps and of the dominant kernel from
+    the committed ncu summary, or None when the kernel sources changed since
+    that capture."""
+    from gemm_epilogue_transformer_tmem_gb300.traffic import kernel_hash
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -243,10 +243,10 @@ class OracleSample:
             eps = I.EPS_RMS
             X = t["X"][r]
             O.run_chain(X, t["W_qkv"], [("RMS_ROWSCALE", None, eps)], norm_gamma=t["gamma_attn"])
-            h = O.run_chain(t["attn_out"][r], t["W_o"], [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
+            h = O.run_chain(t["attn_out"][r], t["W_o"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual_t=X)["D"]
             up = O.run_chain(h, t["W_up"], [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
                              norm_gamma=t["gamma_mlp"])["D"]
-            O.run_chain(up, t["W_down"], [("RESIDUAL", 0, 1.0)], residual_t=h)
+            O.run_chain(up, t["W_down"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual_t=h)
             d, f = t["W_o"].shape[0], t["W_down"].shape[0]
             fl = 2 * rows * d * (3 * d + d + 2 * f) + 2 * rows * f * d
         return time.perf_counter() - t0, fl
@@ -294,7 +294,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="rmsproj", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--workload", default="llama", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--impl", default="coda", choices=["coda", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true")
@@ -306,6 +306,11 @@ def main():
                     help="non-epilogue warps share each CTA's last-tile epilogue (library knob; default on)")
     ap.add_argument("--split-k", default="auto", choices=["auto", "off", "force"],
                     help="split over K for single-CTA problems (library knob; default auto)")
+    ap.add_argument("--raster", default="auto", choices=["auto", "rows", "cols"],
+                    help="tile order of the persistent grid (library knob; default auto)")
+    ap.add_argument("--raster-group", type=int, default=0, help="blocks per raster group (0: the library's)")
+    ap.add_argument("--profile-steps", action="store_true",
+                    help="one fused and one unfused step between L2 flushes, for an ncu capture; no JSON line")
     args = ap.parse_args()
     steps = args.steps if args.steps is not None else DEFAULT_STEPS[args.workload]
     warmup = max(args.warmup, 3)
@@ -330,6 +335,7 @@ def main():
     coda.set_split_k(args.split_k)
     coda.set_tile_scheduler(args.tile_order)
     coda.set_tail_helpers(args.tail_helpers == "on")
+    coda.set_raster(args.raster, args.raster_group)
 
     dev = torch.device("cuda", local)
     step = workloads.BUILDERS[args.workload](dev=dev)
@@ -346,6 +352,22 @@ def main():
         flush_buf.zero_()
         torch.sum(flush_rd, dim=0, out=flush_out)
 
+    if args.profile_steps:
+        for _ in range(warmup):
+            flush()
+            step.fused()
+        for call in (step.fused, step.unfused):
+            flush()
+            call()
+            # read-only pass: evicts the step's dirty lines (its writes) and writes nothing itself
+            torch.sum(flush_rd, dim=0, out=flush_out)
+        torch.cuda.synchronize()
+        st, info = coda.check_device_error()
+        if st != 0:
+            raise RuntimeError(f"device error {st}: {info}")
+        print(f"profile steps done: {args.workload}", flush=True)
+        return
+
     # ---- fused step, device-resident inputs
     sampler = ClockSampler(local) if rank == 0 else None
     if pg:
@@ -354,7 +376,10 @@ def main():
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    per_call, total_ms, launches = timed_loop([step.fused], steps, warmup, flush, stream, coda.launch_count)
+    # a step of several calls is timed call by call (events between them), so
+    # that the roofline of its dominant call is measured on that call alone
+    calls = [c for _, c, _ in step.parts] if step.parts else [step.fused]
+    per_call, total_ms, launches = timed_loop(calls, steps, warmup, flush, stream, coda.launch_count)
     clocks = sampler.stop() if sampler else None
     plan = coda.last_plan()      # how the step's last GEMM call ran
     st, info = coda.check_device_error()
@@ -418,6 +443,10 @@ def main():
 
     peaks, peak_src = load_peaks()
     call_s = sum(per_call) / steps * 1e-3
+    dom_name, dom_flops, dom_s = args.workload, step.flops, call_s
+    if step.parts:
+        i = max(range(len(step.parts)), key=lambda j: step.parts[j][2])
+        dom_name, dom_flops, dom_s = step.parts[i][0], step.parts[i][2], per_call[i] / steps * 1e-3
     traffic = load_traffic(args.workload)
     if step.bound == "hbm":
         # the weight stream bounds the step: algorithmic bytes against the measured copy bandwidth
@@ -429,11 +458,19 @@ def main():
         # the fused kernels are timed in short bursts between L2 flushes: burst peak
         # (FP8 operands: the measured bf16 peak times the nominal FP8 / bf16 ratio 2)
         peak = float(peaks["bf16_tflops"]) * step.peak_scale
-        achieved = step.flops / call_s / 1e12
+        achieved = dom_flops / dom_s / 1e12
         src = "bf16 burst" if step.peak_scale == 1.0 else f"bf16 burst x {step.peak_scale:g} (nominal fp8/bf16)"
         roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                     "frac": round(achieved / peak, 4), "peak_source": f"{src}, of {peak_src}"}
-    roofline.update(traffic=traffic["bytes_per_launch"] if traffic else None, algorithmic_bytes=step.fused_bytes)
+    roofline.update(kernel=f"{dom_name}: the fused GEMM call" + (", timed alone within the step" if step.parts else
+                                                                 " (with its finishing kernels)"),
+                    traffic=traffic.get("dominant_kernel_bytes", traffic.get("bytes_per_launch")) if traffic else None,
+                    algorithmic_bytes=step.parts_bytes.get(dom_name, step.fused_bytes) if step.parts else
+                    step.fused_bytes)
+    if step.parts:
+        roofline["calls"] = {n: {"ms": round(per_call[j] / steps, 5),
+                                 "tflops": round(fl / (per_call[j] / steps * 1e-3) / 1e12, 2)}
+                             for j, (n, _, fl) in enumerate(step.parts)}
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -455,7 +492,9 @@ def main():
                    "plan_of_last_gemm": plan},
         "roofline": roofline,
         "dram_bytes": {"fused_algorithmic": step.fused_bytes, "unfused_algorithmic": step.unfused_bytes,
-                       "ncu_fused_per_launch": traffic["bytes_per_launch"] if traffic else None},
+                       "fused_measured": traffic.get("fused_step_bytes") if traffic else None,
+                       "unfused_measured": traffic.get("unfused_step_bytes") if traffic else None,
+                       "measured_by": traffic.get("source") if traffic else None},
         "unfused": unfused,
         "library_gemm": library,
         "e2e": e2e,

@@ -22,7 +22,7 @@ OPCODES = {
     "SILU": 6, "SWIGLU": 7, "GELU_TANH_GRAD": 8, "DROPOUT": 9, "RESIDUAL": 10, "STORE_PREACT": 11,
     "ROW_SUM": 12, "ROW_MEAN": 13, "ROW_SUMSQ": 14, "ROW_DOT_AUX": 15, "GELU_ERF": 16, "GELU_ERF_GRAD": 17,
     "LN_ROWSCALE": 18, "COL_SUM": 19, "COL_SUMSQ": 20, "COL_DOT_AUX": 21, "COL_DOT_NORM": 22,
-    "COL_SCALE_F32": 23,
+    "COL_SCALE_F32": 23, "RMS_SUMSQ_ROWSCALE": 24,
 }
 COL_REDUCTIONS = ("COL_SUM", "COL_SUMSQ", "COL_DOT_AUX", "COL_DOT_NORM")
 REDUCTIONS = ("ROW_SUM", "ROW_MEAN", "ROW_SUMSQ", "ROW_DOT_AUX")
@@ -92,6 +92,7 @@ _SIGS = {
     "coda_set_tail_helpers": (None, [ctypes.c_int32]),
     "coda_last_plan": (None, [_VP]),
     "coda_set_fixed_sequences": (None, [ctypes.c_int32]),
+    "coda_set_raster": (None, [ctypes.c_int32, ctypes.c_int32]),
 }
 
 
@@ -426,6 +427,16 @@ def set_split_k(mode: str) -> None:
 def set_tail_helpers(enable: bool) -> None:
     """Let the non-epilogue warps share the epilogue of each CTA's last tile (default on)."""
     lib().coda_set_tail_helpers(1 if enable else 0)
+
+
+RASTER_MODES = {"auto": 0, "rows": 1, "cols": 2}
+
+
+def set_raster(mode: str = "auto", group: int = 0) -> None:
+    """Tile order: 'rows' (groups of `group` row blocks, row fastest), 'cols'
+    (groups of `group` column blocks, column fastest) or 'auto' (the library's
+    choice); group <= 0 takes the library's 48 MB group."""
+    lib().coda_set_raster(RASTER_MODES[mode], int(group))
 
 
 def set_tile_scheduler(mode: str) -> None:

@@ -29,6 +29,8 @@ std::atomic<int> g_split_mode{0};  // 0 auto, 1 never split over K, 2 split when
 std::atomic<int> g_dynamic_tiles{0};  // 1: cluster-launch-control tile order where it applies
 std::atomic<int> g_tail_helpers{1};   // 1: warps 0-3 help with each CTA's last tile where it applies
 std::atomic<int> g_fixed_seqs{1};  // 1: use the fixed op sequences, 0: always the interpreter
+std::atomic<int> g_raster_mode{0};   // 0 auto, 1 row groups, 2 column groups
+std::atomic<int> g_raster_group{0};  // blocks per group (<= 0: the 48 MB group)
 thread_local coda_plan g_last_plan{};
 
 constexpr int kMaxDevices = 64;
@@ -107,6 +109,7 @@ struct Compiled {
   int n_aux = 0;
   const void* aux_ptr[kMaxAux] = {nullptr, nullptr, nullptr};
   bool has_rms = false;   // RMS_ROWSCALE or LN_ROWSCALE (row statistics of A)
+  const float* rms_sumsq = nullptr;   // RMS_SUMSQ_ROWSCALE: the caller's row sums of squares of A
   bool is_ln = false;     // ... and it is LN_ROWSCALE
   int rms_slot = -1;
   float rms_eps = 0.0f;
@@ -184,7 +187,7 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         break;
       case CODA_OP_RMS_ROWSCALE:
         if (!fused) return CODA_ERR_UNSUPPORTED;
-        if (c.has_rms || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
+        if (c.has_rms || c.rms_sumsq || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
         if (op.slot != CODA_NO_SLOT) {
           if (op.slot >= CODA_MAX_STAT_SLOTS) return CODA_ERR_INVALID_ARG;
           c.rms_slot = static_cast<int>(op.slot);
@@ -194,9 +197,20 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
         c.has_rms = true;
         c.rms_eps = op.f0;
         break;
+      case CODA_OP_RMS_SUMSQ_ROWSCALE:
+        // r_i from the caller's sums of squares: the kernels then apply the row
+        // factor exactly as for RMS_ROWSCALE, without a pass over A
+        if (!fused) return CODA_ERR_UNSUPPORTED;
+        if (c.has_rms || c.rms_sumsq || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
+        if (op.slot >= CODA_MAX_ROW_VECS || ax.row_vec[op.slot] == nullptr) return CODA_ERR_INVALID_ARG;
+        if (!aligned4(ax.row_vec[op.slot])) return CODA_ERR_ALIGNMENT;
+        c.rms_sumsq = ax.row_vec[op.slot];
+        c.rms_eps = op.f0;
+        d.code = CODA_OP_RMS_ROWSCALE;
+        break;
       case CODA_OP_LN_ROWSCALE:
         if (!fused) return CODA_ERR_UNSUPPORTED;
-        if (c.has_rms || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
+        if (c.has_rms || c.rms_sumsq || K <= 0 || op.f0 < 0.0f) return CODA_ERR_INVALID_ARG;
         if (ax.ln_colsum == nullptr) return CODA_ERR_INVALID_ARG;
         if (!aligned16(ax.ln_colsum) || (ax.ln_bias != nullptr && !aligned16(ax.ln_bias))) return CODA_ERR_ALIGNMENT;
         if (op.slot != CODA_NO_SLOT) {
@@ -357,13 +371,18 @@ bool split_eligible(const Geometry& g, bool pair) {
 // partial accumulators [tiles][kSplitSegs][BN x BM] fp32, then a u32 arrival
 // counter per tile.
 // The fixed op sequence whose opcodes are exactly this list's, or SEQ_INTERP.
+// RMS_SUMSQ_ROWSCALE runs as RMS_ROWSCALE (only the source of r differs).
 int match_sequence(const coda_epilogue* epi, bool glu) {
   if (!g_fixed_seqs.load()) return SEQ_INTERP;
   const uint32_t n = epi ? epi->n_ops : 0u;
   for (const SeqDef& d : kSeqDefs) {
     if (d.glu != glu || static_cast<uint32_t>(d.n) != n) continue;
     bool same = true;
-    for (uint32_t o = 0; o < n && same; ++o) same = epi->ops[o].opcode == d.codes[o];
+    for (uint32_t o = 0; o < n && same; ++o) {
+      uint32_t code = epi->ops[o].opcode;
+      if (code == CODA_OP_RMS_SUMSQ_ROWSCALE) code = CODA_OP_RMS_ROWSCALE;
+      same = code == d.codes[o];
+    }
     if (same) return d.id;
   }
   return SEQ_INTERP;
@@ -380,6 +399,7 @@ cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major,
     case SEQ_NONE:
     case SEQ_RESIDUAL:
     case SEQ_BIAS_GELU_RESIDUAL:
+    case SEQ_RESIDUAL_SUMSQ:
       return launch_gemm_fwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_SWIGLU:
     case SEQ_SWIGLU_DROPOUT:
@@ -398,6 +418,32 @@ cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major,
     default:
       return launch_gemm_interp(glu, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
   }
+}
+
+// Tile order: groups of row blocks (A's group resident in L2, B streamed once
+// per group) or of column blocks (B's group resident, A streamed once per
+// group), each group holding about 48 MB of its resident operand.  Automatic:
+// the order with fewer modelled DRAM reads (A + B x row groups, or B + A x
+// column groups); row groups on a tie.
+void raster_plan(const Geometry& g, int tile_m, int64_t K, int elem_bytes, int32_t& group, int32_t& cols) {
+  const int64_t kk = K > 0 ? K : 1;
+  const int64_t budget = int64_t{48} << 20;
+  const int64_t a_blk = static_cast<int64_t>(tile_m) * kk * elem_bytes;
+  const int64_t b_blk = static_cast<int64_t>(BN) * kk * elem_bytes;
+  auto clamp = [](int64_t v, int64_t hi) { return v < 1 ? int64_t{1} : (v > hi ? hi : v); };
+  const int64_t gr = clamp(budget / a_blk, g.num_m_tiles);
+  const int64_t gc = clamp(budget / b_blk, g.num_n_tiles);
+  const double a_tot = static_cast<double>(g.num_m_tiles) * static_cast<double>(a_blk);
+  const double b_tot = static_cast<double>(g.num_n_tiles) * static_cast<double>(b_blk);
+  const double tr = a_tot + b_tot * static_cast<double>((g.num_m_tiles + gr - 1) / gr);
+  const double tc = b_tot + a_tot * static_cast<double>((g.num_n_tiles + gc - 1) / gc);
+  const int mode = g_raster_mode.load();
+  const int want = g_raster_group.load();
+  bool use_cols = mode == 2 || (mode == 0 && tc < tr);
+  int64_t n = use_cols ? gc : gr;
+  if (mode != 0 && want > 0) n = clamp(want, use_cols ? g.num_n_tiles : g.num_m_tiles);
+  group = static_cast<int32_t>(n);
+  cols = use_cols ? 1 : 0;
 }
 
 size_t split_base(size_t b) { return (b + 255) & ~size_t(255); }
@@ -540,14 +586,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   p.N_out = static_cast<int32_t>(g.n_out);
   p.half = c.glu ? static_cast<int32_t>(N / 2) : 0;
   p.num_m_tiles = g.num_m_tiles;
-  {
-    // rasterization group: about 48 MB of A rows kept hot in the 129 MB L2
-    const int64_t block_bytes = static_cast<int64_t>(pair ? 2 * BM : BM) * (K > 0 ? K : 1) * 2;
-    int64_t gm = (int64_t{48} << 20) / block_bytes;
-    if (gm < 1) gm = 1;
-    if (gm > g.num_m_tiles) gm = g.num_m_tiles;
-    p.group_m = static_cast<int32_t>(gm);
-  }
+  raster_plan(g, pair ? 2 * BM : BM, K, fp8 ? 1 : 2, p.group_m, p.raster_cols);
   p.num_n_tiles = g.num_n_tiles;
   p.num_tiles = static_cast<int32_t>(g.num_tiles);
   p.num_kb = g.num_kb;
@@ -620,6 +659,10 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   // by the weight stream and the per-SM shared-memory traffic, and the
   // side path's reads of every A stage add to the latter.
   const bool rowstat_warps = c.has_rms && !pair && !split && g.num_tiles >= grid;
+  if (c.rms_sumsq != nullptr) {   // the caller's row sums of squares: no pre-pass
+    p.rms_vec = c.rms_sumsq;
+    p.rms_from_sumsq = 1;
+  }
   if (c.has_rms && !rowstat_warps) {
     float* mu_ws = c.is_ln ? rms_ws + M : nullptr;
     e = launch_rms_rowscale(A, M, K, p.inv_K, c.rms_eps, c.is_ln, rms_ws,
@@ -668,8 +711,8 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
-  g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles, p.rms_vec != nullptr ? 1 : 0, seq,
-                          p.clc};
+  g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles,
+                          (p.rms_vec != nullptr && !p.rms_from_sumsq) ? 1 : 0, seq, p.clc};
   if (c.prog.n_colred > 0) {
     e = launch_finalize_cols(c.prog.ws_col, c.prog.n_colred, c.prog.num_rb, g.n_out, c.prog.colred_slot,
                              c.col_stats, st);
@@ -862,6 +905,11 @@ void coda_set_split_k(int32_t mode) { g_split_mode.store(mode < 0 || mode > 2 ? 
 void coda_set_tile_scheduler(int32_t dynamic) { g_dynamic_tiles.store(dynamic != 0 ? 1 : 0); }
 
 void coda_set_tail_helpers(int32_t enable) { g_tail_helpers.store(enable != 0 ? 1 : 0); }
+
+void coda_set_raster(int32_t mode, int32_t group) {
+  g_raster_mode.store(mode < 0 || mode > 2 ? 0 : mode);
+  g_raster_group.store(group);
+}
 
 void coda_last_plan(coda_plan* out) {
   if (out != nullptr) *out = g_last_plan;

@@ -17,6 +17,9 @@ cudaError_t launch_gemm_fwd(int seq, bool a_mn_major, bool b_mn_major, bool row_
     case SEQ_BIAS_GELU_RESIDUAL:
       return launch_variant<EpiFixed<CODA_OP_BIAS, CODA_OP_GELU_TANH, CODA_OP_RESIDUAL>, false, false>(
           a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
+    case SEQ_RESIDUAL_SUMSQ:
+      return launch_variant<EpiFixed<CODA_OP_RESIDUAL, CODA_OP_ROW_SUMSQ>, false, false>(
+          a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     default:
       return cudaErrorNotSupported;
   }

@@ -91,15 +91,28 @@ struct Waiter {
 // Tile order: groups of `group_m` row blocks; within a group the row block
 // varies fastest, then the column block.  The CTAs working at any moment share
 // a few row blocks of A and a few column blocks of B, so A is read from DRAM
-// once and B once per group, instead of A once per column block.
+// once and B once per group, instead of A once per column block.  With
+// raster_cols the roles swap: groups of column blocks, the column block
+// fastest, so B is read once and A once per group (for a B smaller than A).
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& m_tile, int& n_tile) {
-  const int group_tiles = p.group_m * p.num_n_tiles;
+  const int outer = p.raster_cols ? p.num_n_tiles : p.num_m_tiles;
+  const int inner = p.raster_cols ? p.num_m_tiles : p.num_n_tiles;
+  const int group_tiles = p.group_m * inner;
   const int g = tile / group_tiles;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.group_m, p.num_m_tiles - first_m);
+  const int first = g * p.group_m;
+  const int gsz = min(p.group_m, outer - first);
   const int local = tile - g * group_tiles;
-  m_tile = first_m + local % gm;
-  n_tile = local / gm;
+  const int a = first + local % gsz;
+  const int b = local / gsz;
+  m_tile = p.raster_cols ? b : a;
+  n_tile = p.raster_cols ? a : b;
+}
+
+// Row scale of the commuted norm for one row, from the pre-pass kernel's r or
+// from the caller's row sums of squares of A
+__device__ __forceinline__ float row_rms_scale(const GemmParams& p, int row) {
+  const float v = p.rms_vec[row];
+  return p.rms_from_sumsq ? rsqrtf(fmaf(v, p.inv_K, p.rms_eps)) : v;
 }
 
 // Work of one CTA.  Normally whole tiles, tile0, tile0 + step, ...  With the
@@ -647,7 +660,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           griddep_wait();
           gd_waited = true;
         }
-        r_rms = row_ok ? p.rms_vec[row] : 1.0f;
+        r_rms = row_ok ? row_rms_scale(p, row) : 1.0f;
         if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
       }
 
@@ -886,7 +899,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           float r_rms = 1.0f, mu = 0.0f;
           if (p.rms_vec != nullptr) {
             griddep_wait();
-            r_rms = row_ok ? p.rms_vec[row] : 1.0f;
+            r_rms = row_ok ? row_rms_scale(p, row) : 1.0f;
             if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
           }
           const uint64_t stream_policy = policy_evict_first();
@@ -961,8 +974,13 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
   auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN, kFP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // Programmatic launch only behind the row-scale pre-pass, whose one output
+  // (r) the epilogue reads after griddepcontrol.wait.  Row sums of squares
+  // supplied by the caller come with an A that the previous kernel on the stream
+  // may have written itself, and the mainloop reads A without such a wait.
+  const bool after_prepass = p.rms_vec != nullptr && !p.rms_from_sumsq;
   if constexpr (!kPair) {
-    if (p.rms_vec == nullptr) {
+    if (!after_prepass) {
       kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
       return cudaGetLastError();
     }
@@ -994,7 +1012,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = p.rms_vec != nullptr ? 2 : 1;
+    cfg.numAttrs = after_prepass ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
   }
 }

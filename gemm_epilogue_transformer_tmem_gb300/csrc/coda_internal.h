@@ -86,7 +86,8 @@ struct GemmParams {
   int32_t N_out;           // output width (N/2 with SWIGLU)
   int32_t half;            // N/2 with SWIGLU, else 0
   int32_t num_m_tiles, num_n_tiles, num_tiles, num_kb, stages;
-  int32_t group_m;         // row blocks per rasterization group (see tile_coords)
+  int32_t group_m;         // row (or, with raster_cols, column) blocks per rasterization group
+  int32_t raster_cols;     // 1: groups of column blocks, column block fastest (see tile_coords)
   int32_t n_aux;           // aux tensors staged by TMA
   int32_t rms_slot;        // row-stat slot for r_i, -1 if none
   float rms_eps;
@@ -99,7 +100,9 @@ struct GemmParams {
   uint32_t smem_ctl_off;   // offset of the control block
   uint32_t epi_warp_bytes; // staging bytes per epilogue warp
   uint32_t* err;           // device error word (4 x u32)
-  const float* rms_vec;    // commuted-norm row scales r from the pre-pass kernel, or null
+  const float* rms_vec;    // commuted-norm row scales r from the pre-pass kernel (or, with
+                           // rms_from_sumsq, the caller's row sums of squares of A), or null
+  int32_t rms_from_sumsq;  // 1: rms_vec holds sum_k A[i,k]^2; r = rsqrt(s / K + eps)
   const float* mu_vec;     // commuted LayerNorm row means from the pre-pass kernel, or null
   int32_t norm_ln;         // the row statistics are LayerNorm's (mean and centred variance)
   int32_t split;           // 1: CTAs take equal runs of (tile, k-block) units (stream-K)

@@ -32,6 +32,7 @@ enum SeqId : int {
   SEQ_BIAS_GELU_ERF,      // bias -> GELU(erf): BERT MLP up-projection
   SEQ_BIAS_RESIDUAL,      // bias -> + residual: attention out / MLP down-projection
   SEQ_GELU,               // GELU(tanh) without bias
+  SEQ_RESIDUAL_SUMSQ,     // + residual, row sums of squares (the next norm's statistics)
   SEQ_COUNT_
 };
 
@@ -59,6 +60,7 @@ constexpr SeqDef kSeqDefs[] = {
     {SEQ_BIAS_GELU_ERF, false, 2, {CODA_OP_BIAS, CODA_OP_GELU_ERF, 0, 0}},
     {SEQ_BIAS_RESIDUAL, false, 2, {CODA_OP_BIAS, CODA_OP_RESIDUAL, 0, 0}},
     {SEQ_GELU, false, 1, {CODA_OP_GELU_TANH, 0, 0, 0}},
+    {SEQ_RESIDUAL_SUMSQ, false, 2, {CODA_OP_RESIDUAL, CODA_OP_ROW_SUMSQ, 0, 0}},
 };
 
 }  // namespace coda

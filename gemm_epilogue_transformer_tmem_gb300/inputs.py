@@ -214,12 +214,14 @@ def make_llama_block(seed: int = 0, tokens: int = 16384, d: int = 4096, ffn: int
 
 
 def sample_rows(M: int, n: int, seed: int, tile: int = 128) -> list[int]:
-    """Rows for sampled full-size comparison: first, last, tile edges, random."""
+    """Rows for sampled full-size comparison: the first and last row, both rows
+    on each side of every `tile`-row boundary (128-row tiles, and so every
+    256-row CTA-pair tile too), and `n` distinct random rows."""
     rows = {0, M - 1}
-    for t in range(tile, M, tile * max(1, (M // tile) // 8)):
+    for t in range(tile, M, tile):
         rows.add(t - 1)
         rows.add(t)
     g = _gen(seed)
-    extra = torch.randint(0, M, (n,), generator=g).tolist()
-    rows.update(extra)
+    perm = torch.randperm(M, generator=g)[: min(n, M)].tolist()
+    rows.update(perm)
     return sorted(r for r in rows if 0 <= r < M)

@@ -40,6 +40,11 @@ class Step:
     # library (cuBLAS), on the same operands: a measured reference point for the
     # GEMM core, not part of the step
     library: Optional[Callable[[], None]] = None
+    # the fused step as its separate calls, (name, call, GEMM flops), when it has
+    # more than one: the bench times each call with its own events, so that the
+    # roofline of the dominant call is measured on that call alone
+    parts: Optional[list] = None
+    parts_bytes: dict = field(default_factory=dict)    # name -> algorithmic DRAM bytes of that call
 
 
 def _ws(M, N, K, ops, dev):
@@ -278,28 +283,73 @@ def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
                 outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu), library=library)
 
 
-def llama_block_forward(t: dict, prepared: Optional[dict] = None, out: Optional[dict] = None) -> dict:
-    """LLaMA-like non-attention block on device tensors, four fused calls:
-      qkv = rmsnorm(X; g_attn) @ W_qkv                 (commuted RMSNorm)
-      h   = attn_out @ W_o + X                          (residual)
-      up  = silu(G) * U, [G|U] = rmsnorm(h; g_mlp) @ W_up   (commuted RMSNorm + SwiGLU)
-      y   = up @ W_down + h                             (residual)
-    attn_out stands in for the attention output (attention is not part of this path)."""
+def llama_block_calls(t: dict, prepared: dict, out: dict) -> list:
+    """The LLaMA-like non-attention block's four fused calls, in order, as
+    closures over `out` (preallocated outputs, filled in when missing), as one
+    layer of a stack whose hidden states carry their row sums of squares:
+      qkv = rmsnorm(X; g_attn) @ W_qkv          commuted RMSNorm, r from sum_k X^2
+      h   = attn_out @ W_o + X,  sum_j h^2      residual; the MLP norm's statistics
+      up  = silu(G) * U, [G|U] = rmsnorm(h; g_mlp) @ W_up   commuted, r from sum_j h^2
+      y   = up @ W_down + h,     sum_j y^2      residual; the next layer's statistics
+    t["X_sumsq"] (fp32 [tokens]) holds sum_k X^2 as the previous layer's
+    down-projection emits it; without it the qkv call gathers r itself (a
+    pre-pass over X).  attn_out stands in for the attention output (attention
+    is not part of this path).  prepared: W_qkv and W_up with gamma folded in."""
     eps = inputs.EPS_RMS
+    ws = out.get("ws", {})
+
+    def qkv():
+        x_ss = t.get("X_sumsq")
+        if x_ss is None:
+            r = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_ROWSCALE", None, eps)], out=out.get("qkv"))
+        else:
+            r = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_SUMSQ_ROWSCALE", 0, eps)],
+                                   row_vecs={0: x_ss}, out=out.get("qkv"))
+        out["qkv"] = r.D
+
+    def oproj():
+        r = coda.gemm_epilogue(t["attn_out"], t["W_o"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual=t["X"],
+                               out=out.get("h"), row_stats=out.get("h_sumsq"), workspace=ws.get("h"))
+        out["h"], out["h_sumsq"] = r.D, r.row_stats
+
+    def up():
+        r = coda.gemm_epilogue(out["h"], prepared["W_up"], [("RMS_SUMSQ_ROWSCALE", 0, eps), ("SWIGLU",)],
+                               row_vecs={0: out["h_sumsq"][0]}, out=out.get("up"))
+        out["up"] = r.D
+
+    def down():
+        r = coda.gemm_epilogue(out["up"], t["W_down"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual=out["h"],
+                               out=out.get("y"), row_stats=out.get("y_sumsq"), workspace=ws.get("y"))
+        out["y"], out["y_sumsq"] = r.D, r.row_stats
+
+    return [("qkv", qkv), ("out", oproj), ("up", up), ("down", down)]
+
+
+def llama_block_forward(t: dict, prepared: Optional[dict] = None, out: Optional[dict] = None) -> dict:
+    """The block's four calls (see llama_block_calls) run in order; returns the
+    outputs qkv, h, up, y and the row sums of squares h_sumsq, y_sumsq."""
     if prepared is None:
         prepared = dict(W_qkv=coda.fold_gamma(t["W_qkv"], t["gamma_attn"], "kn"),
                         W_up=coda.fold_gamma(t["W_up"], t["gamma_mlp"], "kn"))
-    out = out or {}
-    qkv = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_ROWSCALE", None, eps)], out=out.get("qkv")).D
-    h = coda.gemm_epilogue(t["attn_out"], t["W_o"], [("RESIDUAL", 0, 1.0)], residual=t["X"], out=out.get("h")).D
-    up = coda.gemm_epilogue(h, prepared["W_up"], [("RMS_ROWSCALE", None, eps), ("SWIGLU",)], out=out.get("up")).D
-    y = coda.gemm_epilogue(up, t["W_down"], [("RESIDUAL", 0, 1.0)], residual=h, out=out.get("y")).D
-    return dict(qkv=qkv, h=h, up=up, y=y)
+    out = {} if out is None else out
+    for _, call in llama_block_calls(t, prepared, out):
+        call()
+    return dict(qkv=out["qkv"], h=out["h"], up=out["up"], y=out["y"], h_sumsq=out["h_sumsq"][0],
+                y_sumsq=out["y_sumsq"][0])
+
+
+def row_sumsq(X: torch.Tensor) -> torch.Tensor:
+    """sum_k X[i,k]^2 (fp32 [M]) of a bf16 matrix, through the library's unfused
+    epilogue kernel: the statistics a residual epilogue's ROW_SUMSQ would have
+    produced with X (used to seed a block's input)."""
+    return coda.epilogue_apply(X, [("ROW_SUMSQ", 0)]).row_stats[0].contiguous()
 
 
 def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> Step:
     t = t or inputs.make_llama_block(seed, tokens, d, ffn)
     t = {k: v.to(dev) for k, v in t.items()}
+    # the block's input arrives with its row sums of squares (one layer of a stack)
+    t["X_sumsq"] = row_sumsq(t["X"])
     prepared = {}
 
     def prep():
@@ -308,10 +358,14 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
 
     prep()
     T = tokens
+    res_ops = [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)]
     out = dict(qkv=torch.empty((T, 3 * d), dtype=torch.bfloat16, device=dev),
                h=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
                up=torch.empty((T, ffn), dtype=torch.bfloat16, device=dev),
-               y=torch.empty((T, d), dtype=torch.bfloat16, device=dev))
+               y=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
+               h_sumsq=torch.empty((1, T), dtype=torch.float32, device=dev),
+               y_sumsq=torch.empty((1, T), dtype=torch.float32, device=dev),
+               ws=dict(h=_ws(T, d, d, res_ops, dev)[0], y=_ws(T, d, ffn, res_ops, dev)[0]))
     un = dict(xn=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
               qkv=torch.empty((T, 3 * d), dtype=torch.bfloat16, device=dev),
               c_o=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
@@ -322,8 +376,11 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
               c_down=torch.empty((T, d), dtype=torch.bfloat16, device=dev),
               y=torch.empty((T, d), dtype=torch.bfloat16, device=dev))
 
+    calls = llama_block_calls(t, prepared, out)
+
     def fused():
-        llama_block_forward(t, prepared, out)
+        for _, call in calls:
+            call()
 
     def unfused():
         eps = inputs.EPS_RMS
@@ -337,22 +394,30 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
         coda.gemm_epilogue(un["up"], t["W_down"], [], out=un["c_down"])
         coda.epilogue_apply(un["c_down"], [("RESIDUAL", 0, 1.0)], residual=un["h"], out=un["y"])
 
-    flops = 2 * T * d * (3 * d) + 2 * T * d * d + 2 * T * d * (2 * ffn) + 2 * T * ffn * d
+    part_flops = dict(qkv=2 * T * d * (3 * d), out=2 * T * d * d, up=2 * T * d * (2 * ffn), down=2 * T * ffn * d)
+    flops = sum(part_flops.values())
     act = T * d * BF16
+    rowvec = T * F32
+
     def library():
         torch.matmul(t["X"], prepared["W_qkv"], out=un["qkv"])
         torch.matmul(t["attn_out"], t["W_o"], out=un["c_o"])
         torch.matmul(un["h"], prepared["W_up"], out=un["c_up"])
         torch.matmul(un["up"], t["W_down"], out=un["c_down"])
 
-    fb = (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (2 * act + d * d * BF16 + act) + \
-         (act + d * 2 * ffn * BF16 + T * ffn * BF16) + (T * ffn * BF16 + ffn * d * BF16 + 2 * act)
+    part_bytes = dict(qkv=act + rowvec + d * 3 * d * BF16 + T * 3 * d * BF16,
+                      out=2 * act + d * d * BF16 + act + rowvec,
+                      up=act + rowvec + d * 2 * ffn * BF16 + T * ffn * BF16,
+                      down=T * ffn * BF16 + ffn * d * BF16 + 2 * act + rowvec)
+    fb = sum(part_bytes.values())
     ub = (2 * act) + (act + d * 3 * d * BF16 + T * 3 * d * BF16) + (act + d * d * BF16 + act) + 3 * act + \
          (2 * act) + (act + d * 2 * ffn * BF16 + T * 2 * ffn * BF16) + (T * 2 * ffn * BF16 + T * ffn * BF16) + \
          (T * ffn * BF16 + ffn * d * BF16 + act) + 3 * act
-    return Step("llama", flops, fb, ub, fused, unfused, host_inputs=dict(X=t["X"], attn_out=t["attn_out"]),
-                host_outputs=dict(y=out["y"], qkv=out["qkv"]), kernels_per_fused=4, kernels_per_unfused=9,
-                prep=prep, outputs=out, library=library)
+    return Step("llama", flops, fb, ub, fused, unfused,
+                host_inputs=dict(X=t["X"], X_sumsq=t["X_sumsq"], attn_out=t["attn_out"]),
+                host_outputs=dict(y=out["y"], y_sumsq=out["y_sumsq"], qkv=out["qkv"]), kernels_per_fused=6,
+                kernels_per_unfused=9, prep=prep, outputs=out, library=library,
+                parts=[(name, call, part_flops[name]) for name, call in calls], parts_bytes=part_bytes)
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,

@@ -103,8 +103,17 @@ typedef enum {
  *                  gathered from A like RMS_ROWSCALE (f0 = eps), c = aux.ln_colsum
  *                  and b = aux.ln_bias (fp32 vectors of `width` entries, b may be
  *                  NULL).  With B, c and b from coda_fold_layernorm the result is
- *                  layernorm(A; gamma, beta) @ W.  At most one RMS_ROWSCALE or
- *                  LN_ROWSCALE per list.
+ *                  layernorm(A; gamma, beta) @ W.  At most one RMS_ROWSCALE,
+ *                  RMS_SUMSQ_ROWSCALE or LN_ROWSCALE per list.
+ *   RMS_SUMSQ_ROWSCALE  x *= r_i, r_i = 1/sqrt(rowvec[slot][i] / K + f0): the
+ *                  commuted RMSNorm with the row sums of squares of A supplied
+ *                  (fp32 [M], sum_k A[i,k]^2), f0 = eps.  When A is the output
+ *                  of an earlier call whose epilogue ended in RESIDUAL (a
+ *                  Transformer block's hidden state), that call's ROW_SUMSQ gives
+ *                  these sums while the tile is on chip, so the norm costs no
+ *                  pass over A at all: the row statistics of the zeli.app
+ *                  comment's commuted norm, gathered one call earlier.  With
+ *                  B = bf16(gamma (.)_row W) the result is rmsnorm(A; gamma) @ W.
  * Elementwise transforms (agentlenshq.com "Pairwise Transformations"):
  *   GELU_TANH      x = 0.5 x (1 + tanh(sqrt(2/pi)(x + 0.044715 x^3)))
  *   SILU           x = x / (1 + exp(-x))
@@ -168,7 +177,8 @@ typedef enum {
   CODA_OP_COL_DOT_AUX = 21,
   CODA_OP_COL_DOT_NORM = 22,
   CODA_OP_COL_SCALE_F32 = 23,
-  CODA_OP_COUNT_ = 24
+  CODA_OP_RMS_SUMSQ_ROWSCALE = 24,
+  CODA_OP_COUNT_ = 25
 } coda_opcode;
 
 #define CODA_MAX_OPS 16
@@ -400,6 +410,17 @@ CODA_API void coda_set_split_k(int32_t mode);
  * with in-kernel row statistics always run the static order.  Results are
  * bit-identical either way. */
 CODA_API void coda_set_tile_scheduler(int32_t dynamic);
+/* Tile order (rasterisation) of the persistent grid, for measurement.  Tiles
+ * run in groups: 1 = groups of `group` row blocks, the row block varying
+ * fastest (A's rows of the group stay in L2 while B streams through once per
+ * group); 2 = groups of `group` column blocks, the column block varying fastest
+ * (B's columns of the group stay in L2 while A streams once per group);
+ * 0 (default) = the library's choice: of the two, the one whose modelled DRAM
+ * reads (A once + B once per row group, or B once + A once per column group,
+ * with a group holding about 48 MB of the resident operand) are fewer.
+ * group <= 0 with mode 1 or 2 takes the 48 MB group.  Results are bit-identical
+ * in every order. */
+CODA_API void coda_set_raster(int32_t mode, int32_t group);
 /* 1 (default): once a CTA's last accumulator is complete, its producer, MMA and
  * other non-epilogue warps take half of that tile's epilogue chunks (static tile
  * order, op lists without aux tensors, no split over K, at most 16 tiles per
@@ -421,10 +442,11 @@ CODA_API void coda_last_plan(coda_plan* out);
 
 /* Fixed op sequences (the CODA article, d9bl.com, §3.3, compiles each
  * epilogue into a specialised kernel): for the op lists of the common blocks --
- * plain GEMM; RMS_ROWSCALE; LN_ROWSCALE; RESIDUAL; BIAS; BIAS, GELU_TANH;
- * BIAS, GELU_ERF; BIAS, RESIDUAL; GELU_TANH; BIAS, GELU_TANH, RESIDUAL;
- * GELU_TANH_GRAD, ROW_DOT_AUX, ROW_SUM; SWIGLU; RMS_ROWSCALE, SWIGLU; SWIGLU,
- * DROPOUT; and, with FP8 operands, ROW_SCALE, COL_SCALE_F32 (, SWIGLU) --
+ * plain GEMM; RMS_ROWSCALE; LN_ROWSCALE; RESIDUAL; RESIDUAL, ROW_SUMSQ; BIAS;
+ * BIAS, GELU_TANH; BIAS, GELU_ERF; BIAS, RESIDUAL; GELU_TANH; BIAS, GELU_TANH,
+ * RESIDUAL; GELU_TANH_GRAD, ROW_DOT_AUX, ROW_SUM; SWIGLU; RMS_ROWSCALE, SWIGLU;
+ * SWIGLU, DROPOUT (RMS_SUMSQ_ROWSCALE counts as RMS_ROWSCALE here); and, with
+ * FP8 operands, ROW_SCALE, COL_SCALE_F32 (, SWIGLU) --
  * the library launches a kernel built with those opcodes fixed
  * (straight-line epilogue code); every other list runs the op interpreter.
  * Results are the same either way.  1 (default): use them; 0: interpret all. */

@@ -79,13 +79,50 @@ def assert_close(got, ref, what=""):
         assert fro <= FRO, f"{what}: relative Frobenius error {fro:.3e}"
 
 
-def assert_stat_close(got, ref, scale, what=""):
-    """Row reductions: each summand carries the elementwise error of the output
-    (relative 1e-2 at most), and independent errors add in quadrature, so the
-    bound is 1e-2 + 1e-2 * max(|ref|, ||summands||_2) (scale = the L2 norm)."""
+# Row and column statistics are fp32 sums of fp32 chain values (never of the
+# bf16 outputs), so their error is not the output tolerance above.  Each
+# summand carries the relative error tau of the chain value it is taken from:
+#   TAU_LIN   GEMM and linear ops in fp32: accumulation over K (about
+#             sqrt(K) 2^-24 relative) and a few ulps per op; 2^-16 covers K up to 2^14
+#   TAU_ACT   an activation on the way: SiLU and the tanh-form GELU use the
+#             hardware tanh (logistic absolute error <= 2^-12, i.e. <= 2^-12 |x|
+#             on f(x), which stays below 2^-10 |f(x)| wherever f(x) is not near 0)
+#   TAU_FOLD  the bf16 gamma fold on the way: 2^-9 relative per weight
+# Independent errors add in quadrature, so the sum moves by tau * scale, scale
+# being the oracle's error scale (the L2 norm of d(summand)/d(log x)); the
+# fp32 rounding of the sum adds 2^-24 sqrt(n) * scale the same way.  The bound
+# allows 6 standard deviations of both.  On top of that the tensor cores'
+# fp32 accumulation is biased towards zero (measured: sums of squares of a
+# K = 16384 GEMM output 3.2e-5 low on every row), about one ulp per MMA step
+# of 16 elements of K: a relative bias b = (K/16) 2^-24 in every chain value,
+# which moves a reduction by up to 2 b |ref| (sums of squares) and does not
+# average out.  A summand left out of the sum moves it by |s_j|, which is far
+# above all this on every full-size workload; the exact integer reductions
+# (test_reductions_exact) catch a missing summand of any size.
+TAU_LIN = 2.0 ** -16
+TAU_ACT = 2.0 ** -10
+TAU_FOLD = 2.0 ** -9
+ACTIVATIONS = {"GELU_TANH", "SILU", "SWIGLU", "GELU_TANH_GRAD", "GELU_ERF", "GELU_ERF_GRAD"}
+
+
+def chain_tau(ops, fold=False):
+    """Relative error budget of the chain values an op list reduces."""
+    tau = TAU_ACT if any(o[0] in ACTIVATIONS for o in ops) else TAU_LIN
+    return max(tau, TAU_FOLD) if fold else tau
+
+
+def stat_bound(ref, scale, n, tau, K):
+    """Bound on |gpu - ref| of a reduction over n summands of a GEMM with reduction depth K."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    bias = 2.0 * (max(K, 16) / 16.0) * 2.0 ** -24
+    return 1e-6 + (2.0 ** -20 + bias) * ref + 6.0 * (tau + 2.0 ** -24 * math.sqrt(max(n, 1))) * np.asarray(scale)
+
+
+def assert_stat_close(got, ref, scale, n, tau, K, what=""):
+    """Row reductions over n columns of a GEMM with reduction depth K (see stat_bound)."""
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
-    bound = ATOL + RTOL * np.maximum(np.abs(ref), scale)
+    bound = stat_bound(ref, scale, n, tau, K)
     err = np.abs(got - ref)
     if (err > bound).any():
         i = int(np.argmax(err - bound))
@@ -93,10 +130,11 @@ def assert_stat_close(got, ref, scale, what=""):
                              f"gpu {got[i]!r} ref {ref[i]!r} bound {bound[i]!r}")
 
 
-def check_stats(r, ref, what):
+def check_stats(r, ref, what, tau, K):
+    n = ref["D"].shape[1] if "D" in ref else 1
     for slot, v in ref["stats"].items():
         if slot in ref["stat_scale"]:
-            assert_stat_close(f64(r.row_stats[slot]), v, ref["stat_scale"][slot], f"{what} stat {slot}")
+            assert_stat_close(f64(r.row_stats[slot]), v, ref["stat_scale"][slot], n, tau, K, f"{what} stat {slot}")
         else:
             assert_close(f64(r.row_stats[slot]), v, f"{what} stat {slot}")
 
@@ -231,7 +269,7 @@ def test_op(case, layout, mode):
                       row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
                       xhat=f64(aux["xhat"]))
     assert_close(f64(r.D), ref["D"], case)
-    check_stats(r, ref, case)
+    check_stats(r, ref, case, chain_tau(ops), K_R)
     if preact is not None:
         assert_close(f64(preact), ref["preact"], f"{case} preact")
 
@@ -256,7 +294,7 @@ def test_fixed_sequence_matches_interpreter(case, layout, mode):
             sync_ok()
             assert (plan["sequence"] > 0) == fixed, plan
             assert_close(f64(r.D), ref["D"], f"{case} fixed={fixed}")
-            check_stats(r, ref, f"{case} fixed={fixed}")
+            check_stats(r, ref, f"{case} fixed={fixed}", chain_tau(ops), K_R)
     finally:
         coda.set_fixed_sequences(True)
 
@@ -321,7 +359,7 @@ def test_dynamic_tile_order(case, kernel):
     if d.keep_count is not None:
         assert torch.equal(d.keep_count, s_.keep_count)
     assert_close(f64(d.D), ref["D"], f"{case} {kernel} dynamic order")
-    check_stats(d, ref, f"{case} {kernel} dynamic order")
+    check_stats(d, ref, f"{case} {kernel} dynamic order", chain_tau(ops), K_T)
 
 
 @pytest.mark.parametrize("op", ["SILU", "GELU_TANH", "GELU_TANH_GRAD"])
@@ -386,10 +424,10 @@ def test_unmatched_op_list_runs_interpreter():
 
 
 # -------------------------------------------------------- column reductions
-def assert_col_close(got, ref, scale, what=""):
-    """Column reductions: the same bound as the row reductions, over the M summands."""
+def assert_col_close(got, ref, scale, n, tau, K, what=""):
+    """Column reductions over n rows: the bound of the row reductions."""
     got = np.asarray(got, dtype=np.float64)
-    bound = ATOL + RTOL * np.maximum(np.abs(ref), scale)
+    bound = stat_bound(ref, scale, n, tau, K)
     err = np.abs(got - ref)
     if (err > bound).any():
         j = int(np.argmax(err - bound))
@@ -413,9 +451,37 @@ def test_column_reductions(case, layout, mode):
     sync_ok()
     ref = O.run_chain(f64(A), f64(B), ops, b_layout=layout, z=f64(aux["z"]), xhat=f64(aux["xhat"]))
     assert_close(f64(r.D), ref["D"], case)
-    check_stats(r, ref, case)
+    check_stats(r, ref, case, chain_tau(ops), K_R)
     for slot, v in ref["col_stats"].items():
-        assert_col_close(f64(r.col_stats[slot]), v, ref["col_stat_scale"][slot], f"{case} col {slot}")
+        assert_col_close(f64(r.col_stats[slot]), v, ref["col_stat_scale"][slot], ref["D"].shape[0], chain_tau(ops),
+                         K_R, f"{case} col {slot}")
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_reductions_exact(layout, mode):
+    # Integer operands |a|, |b| <= 1 and K = 128: every product, partial sum and
+    # accumulator value is an integer of magnitude <= 128, and every row and
+    # column reduction below stays under 2^24 (sum of squares <= 520 * 128^2), so
+    # the fp32 results are exact whatever the order of summation.  Any summand
+    # left out, counted twice or taken from the wrong row or column changes an
+    # integer result: the comparison is bit for bit.
+    M, K, N = 300, 128, 520
+    A = inputs.small_int_bf16((M, K), 1, 161)
+    B = inputs.small_int_bf16((K, N) if layout == "kn" else (N, K), 1, 162)
+    Xh = inputs.small_int_bf16((M, N), 2, 163)
+    ops = [("ROW_SUM", 0), ("ROW_SUMSQ", 1), ("ROW_DOT_AUX", 2), ("ROW_MEAN", 3), ("COL_SUM", 0),
+           ("COL_DOT_AUX", 1)]
+    r = coda.gemm_epilogue(cu(A), cu(B), ops, b_layout=layout, xhat=cu(Xh))
+    sync_ok()
+    ref = O.run_chain(f64(A), f64(B), ops, b_layout=layout, xhat=f64(Xh))
+    np.testing.assert_array_equal(f64(r.D), ref["D"])
+    for slot in (0, 1, 2):
+        np.testing.assert_array_equal(f64(r.row_stats[slot]), ref["stats"][slot], err_msg=f"row stat {slot}")
+    # the mean is the exact sum times float32(1/N), one fp32 rounding
+    mean32 = ref["stats"][0].astype(np.float32) * np.float32(1.0 / N)
+    np.testing.assert_array_equal(r.row_stats[3].cpu().numpy(), mean32)
+    for slot in (0, 1):
+        np.testing.assert_array_equal(f64(r.col_stats[slot]), ref["col_stats"][slot], err_msg=f"col stat {slot}")
 
 
 HELPER_CASES = {
@@ -505,8 +571,9 @@ def test_wgrad_scale_accumulate_in_place(layout, mode):
     sync_ok()
     ref = O.run_chain(f64(X).T, f64(dH), ops, b_layout=layout, residual_t=f64(dW_old))
     assert_close(f64(dW), ref["D"], "wgrad")
-    check_stats(r, ref, "wgrad")
-    assert_col_close(f64(r.col_stats[0]), ref["col_stats"][0], ref["col_stat_scale"][0], "wgrad colsum")
+    check_stats(r, ref, "wgrad", TAU_LIN, T)
+    assert_col_close(f64(r.col_stats[0]), ref["col_stats"][0], ref["col_stat_scale"][0], K_in, TAU_LIN, T,
+                     "wgrad colsum")
 
 
 # ------------------------------------------------------------ norm backward
@@ -543,10 +610,11 @@ def test_norm_backward_chain(kind, mode):
     dXn = f64(dY) @ f64(W).T
     if kind == "layernorm":
         dX_ref, dg_ref, db_ref = O.layernorm_backward(f64(X), f64(g), dXn, eps)
-        assert_col_close(f64(bwd.col_stats[1]), db_ref, np.sqrt((dXn ** 2).sum(axis=0)), "dbeta")
+        assert_col_close(f64(bwd.col_stats[1]), db_ref, np.sqrt((dXn ** 2).sum(axis=0)), M, TAU_LIN, N, "dbeta")
     else:
         dX_ref, dg_ref = O.rmsnorm_backward(f64(X), f64(g), dXn, eps)
-    assert_col_close(f64(bwd.col_stats[0]), dg_ref, np.sqrt((dXn ** 2).sum(axis=0)) * 3.0, "dgamma")
+    # dgamma's summands are dXn * x_hat with x_hat of unit RMS: 3 ||dXn|| bounds their L2 norm generously
+    assert_col_close(f64(bwd.col_stats[0]), dg_ref, np.sqrt((dXn ** 2).sum(axis=0)) * 3.0, M, TAU_LIN, N, "dgamma")
     assert_close(f64(dX), dX_ref, f"{kind} dX")
 
 
@@ -600,7 +668,7 @@ def test_e4m3_gemm_dequant_epilogue(glu, mode):
     ref = O.run_chain(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), ops, b_layout="nk",
                       row_vecs={0: sa.double().numpy()}, col_scale_f32=sb.double().numpy())
     assert_close(f64(r.D), ref["D"], "e4m3 dequant")
-    check_stats(r, ref, "e4m3 dequant")
+    check_stats(r, ref, "e4m3 dequant", TAU_LIN, K)
 
 
 @pytest.mark.parametrize("M,K,N", [(1, 16, 8), (129, 16, 264), (7, 4096, 40)])
@@ -613,7 +681,7 @@ def test_e4m3_gemm_edge_shapes(M, K, N):
     sync_ok()
     ref = O.run_chain(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), [("ROW_SUM", 0)], b_layout="nk")
     assert_close(f64(r.D), ref["D"], "e4m3 edge")
-    check_stats(r, ref, "e4m3 edge")
+    check_stats(r, ref, "e4m3 edge", TAU_LIN, K)
 
 
 @pytest.mark.parametrize("M,N", [(1, 8), (33, 40), (31, 264)])
@@ -628,7 +696,8 @@ def test_column_reductions_edge_shapes(M, N):
     sync_ok()
     ref = O.run_chain(f64(A), f64(B), ops, xhat=f64(Xh))
     for slot in (0, 1):
-        assert_col_close(f64(r.col_stats[slot]), ref["col_stats"][slot], ref["col_stat_scale"][slot], f"col {slot}")
+        assert_col_close(f64(r.col_stats[slot]), ref["col_stats"][slot], ref["col_stat_scale"][slot], M, TAU_LIN, K,
+                         f"col {slot}")
 
 
 def test_e4m3_pipeline_approximates_bf16_gemm():
@@ -743,7 +812,91 @@ def test_commuted_rmsnorm_then_swiglu(exact_gamma, mode):
     if exact_gamma:
         assert_close(f64(r.row_stats[1]), ref["stats"][1], "row sum (exact fold)")
     else:
-        check_stats(r, ref, "rms -> swiglu")
+        check_stats(r, ref, "rms -> swiglu", chain_tau(ops, fold=True), K)
+
+
+@pytest.mark.parametrize("glu", [False, True])
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_commuted_rmsnorm_from_row_sumsq(layout, glu, mode):
+    # RMS_SUMSQ_ROWSCALE: r_i from the row sums of squares of A supplied by the
+    # caller (here by the library's own unfused ROW_SUMSQ pass over A), no
+    # pre-pass; the result is rmsnorm(A; gamma) @ W, the oracle's
+    # normalise-then-project, within the bound of the fold (the weights are the
+    # bf16 fold gamma (.)_row W)
+    M, K, n_out = 300, 192, 264
+    N = 2 * n_out if glu else n_out
+    X = rand((M, K), 171)
+    g = inputs.uniform_bf16((K,), 0.5, 1.5, 172)
+    W = rand((K, N) if layout == "kn" else (N, K), 173, 1.0 / math.sqrt(K))
+    Wf = coda.fold_gamma(cu(W), cu(g), layout)
+    ss = coda.epilogue_apply(cu(X), [("ROW_SUMSQ", 0)]).row_stats[0].contiguous()
+    ops = [("RMS_SUMSQ_ROWSCALE", 1, 1e-6)] + ([("SWIGLU",)] if glu else []) + [("ROW_SUM", 0)]
+    before = coda.launch_count()
+    r = coda.gemm_epilogue(cu(X), Wf, ops, b_layout=layout, row_vecs={1: ss})
+    plan = coda.last_plan()
+    launched = coda.launch_count() - before
+    sync_ok()
+    assert plan["prepass"] == 0, plan
+    # the GEMM and the row sum's finishing kernel, nothing else (no pass over A)
+    assert launched == 2, launched
+    # elementwise against the oracle given the prepared weights (the fold
+    # bf16(gamma (.)_row W), rounded by the oracle itself: its 2^-9 rounding
+    # reaches the bound in silu(G) * U where U is near zero), and within the
+    # Frobenius bound of the pages' normalise-then-project with exact gamma
+    ss64 = O.row_sumsq(f64(X))
+    Wp = O.round_bf16(f64(g)[:, None] * f64(W) if layout == "kn" else f64(W) * f64(g)[None, :])
+    ref = O.run_chain(f64(X), Wp, ops, b_layout=layout, row_vecs={1: ss64})
+    assert_close(f64(r.D), ref["D"], "rms from sums of squares")
+    check_stats(r, ref, "rms from sums of squares", chain_tau(ops), K)
+    ref0 = O.run_chain(f64(X), f64(W), ops, b_layout=layout, norm_gamma=f64(g), row_vecs={1: ss64})
+    assert np.linalg.norm(f64(r.D) - ref0["D"]) / np.linalg.norm(ref0["D"]) <= FRO
+    # the supplied sums themselves: fp32 sums of exact bf16 squares
+    assert_stat_close(f64(ss), ss64, 2.0 * np.sqrt(O.row_sumsq(f64(X) ** 2)), K, TAU_LIN, 0, "sumsq")
+
+
+def test_rms_from_row_sumsq_rejections():
+    X = cu(rand((64, 64), 181))
+    ss = torch.ones((64,), dtype=torch.float32, device="cuda")
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):
+        coda.epilogue_apply(X, [("RMS_SUMSQ_ROWSCALE", 0, 1e-6)], row_vecs={0: ss})
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):     # no row vector in the slot
+        coda.gemm_epilogue(X, X, [("RMS_SUMSQ_ROWSCALE", 1, 1e-6)], row_vecs={0: ss})
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):     # two norms
+        coda.gemm_epilogue(X, X, [("RMS_SUMSQ_ROWSCALE", 0, 1e-6), ("RMS_ROWSCALE", None, 1e-6)],
+                           row_vecs={0: ss})
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_raster_orders_bit_identical(kernel):
+    # the same call in row-group and column-group tile orders of several group
+    # sizes: every tile's arithmetic is the same wherever it runs, so D and the
+    # row and column statistics are bit-identical; more tiles than resident
+    # CTAs (pairs) in both dimensions, ragged M, N and K
+    M, K, N = 2000, 104, 2600
+    A = rand((M, K), 191)
+    B = rand((K, N), 192, 1.0 / math.sqrt(K))
+    b = rand((N,), 193)
+    ops = [("BIAS", 0), ("GELU_TANH",), ("ROW_SUM", 0), ("ROW_SUMSQ", 1), ("COL_SUM", 0)]
+    coda.set_cta_pair(kernel)
+    coda.set_split_k("off")
+    outs = []
+    try:
+        for mode, grp in (("rows", 1), ("rows", 3), ("cols", 1), ("cols", 4), ("cols", 0), ("auto", 0)):
+            coda.set_raster(mode, grp)
+            outs.append(coda.gemm_epilogue(cu(A), cu(B), ops, col_vecs={0: cu(b)}))
+            sync_ok()
+    finally:
+        coda.set_raster("auto", 0)
+        coda.set_cta_pair("auto")
+        coda.set_split_k("auto")
+    r0 = outs[0]
+    for r in outs[1:]:
+        assert torch.equal(r.D, r0.D)
+        assert torch.equal(r.row_stats, r0.row_stats)
+        assert torch.equal(r.col_stats, r0.col_stats)
+    ref = O.run_chain(f64(A), f64(B), ops, col_vecs={0: f64(b)})
+    assert_close(f64(r0.D), ref["D"], "raster orders")
+    check_stats(r0, ref, "raster orders", chain_tau(ops), K)
 
 
 # ------------------------------------------------------ commuted LayerNorm
@@ -836,7 +989,8 @@ def test_commuted_layernorm_then_swiglu(mode):
     ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g), norm_beta=f64(beta))
     assert_close(f64(r.D), ref["D"], "ln -> swiglu")
     assert_close(f64(r.row_stats[0]), ref["stats"][0], "ln r")
-    check_stats(r, {"stats": {2: ref["stats"][2]}, "stat_scale": ref["stat_scale"]}, "ln -> swiglu")
+    check_stats(r, {"D": ref["D"], "stats": {2: ref["stats"][2]}, "stat_scale": ref["stat_scale"]}, "ln -> swiglu",
+                chain_tau(ops, fold=True), K)
 
 
 def test_layernorm_rowscale_rejected_unfused_and_without_colsum():
@@ -859,7 +1013,7 @@ def test_dgrad_small(mode):
     sync_ok()
     ref = O.run_chain(f64(dY), f64(W), ops, b_layout="nk", z=f64(Z), xhat=f64(Xh))
     assert_close(f64(r.D), ref["D"], "dgrad dX")
-    check_stats(r, ref, "dgrad")
+    check_stats(r, ref, "dgrad", chain_tau(ops), K)
 
 
 # --------------------------------------------------------- unfused kernels
@@ -895,7 +1049,7 @@ def test_unfused_epilogue_apply(case):
                       row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
                       xhat=f64(aux["xhat"]))
     assert_close(f64(r.D), ref["D"], f"apply {case}")
-    check_stats(r, ref, f"apply {case}")
+    check_stats(r, ref, f"apply {case}", chain_tau(ops), 0)
 
 
 def test_unfused_dropout_matches_fused_mask():
@@ -910,7 +1064,9 @@ def test_unfused_dropout_matches_fused_mask():
 
 # ------------------------------------------------- full-size, sampled rows
 def _sampled(M, seed):
-    return inputs.sample_rows(M, 40, seed)
+    """512 random rows, the first and last row, and both rows at every 128-row
+    boundary (so at every 256-row CTA-pair tile boundary too)."""
+    return inputs.sample_rows(M, 512, seed)
 
 
 def test_full_rmsproj_sampled():
@@ -955,7 +1111,7 @@ def test_split_k_plan_and_segments():
         assert plan["split"] == 1 and plan["pair"] == 0 and plan["tiles"] == 6 and plan["grid"] == 9, plan
         ref = O.run_chain(f64(X), f64(W), ops)
         assert_close(f64(r.D), ref["D"], "split GEMM")
-        check_stats(r, ref, "split GEMM")
+        check_stats(r, ref, "split GEMM", chain_tau(ops), K)
         # too small a workspace for the partials: same result without the split
         need = coda.workspace_size(M, N, K, ops)
         small = torch.empty((2 * M * 4,), dtype=torch.uint8, device="cuda")
@@ -1000,7 +1156,12 @@ def test_full_skinny_sampled(split):
     assert_close(f64(r.row_stats[0]), ref["stats"][0], "skinny r")
     ref0 = O.run_chain(f64(t["X"]), W, ops, norm_gamma=g)
     got = f64(r.D)
-    assert np.linalg.norm(got - ref0["D"]) / np.linalg.norm(ref0["D"]) <= FRO
+    fro0 = np.linalg.norm(got - ref0["D"]) / np.linalg.norm(ref0["D"])
+    over = np.abs(got - ref0["D"]) > ATOL + RTOL * np.abs(ref0["D"])
+    print(f"skinny ({split}) against the unprepared oracle: {int(over.sum())} of {over.size} elements over the "
+          f"elementwise bound, worst excess {float(np.max(np.abs(got - ref0['D']) - ATOL - RTOL * np.abs(ref0['D']))):.3e}, "
+          f"relative Frobenius {fro0:.3e}")
+    assert fro0 <= FRO
 
 
 def test_full_wgrad_sampled():
@@ -1013,7 +1174,8 @@ def test_full_wgrad_sampled():
     rows = _sampled(t["dW_old"].shape[0], 5)
     ref = O.run_chain(f64(t["up"][:, rows]).T, f64(t["dY"]), ops, residual_t=f64(t["dW_old"][rows]))
     assert_close(f64(dW[rows]), ref["D"], "wgrad")
-    assert_stat_close(f64(r.row_stats[0][rows]), ref["stats"][0], ref["stat_scale"][0], "wgrad row sumsq")
+    assert_stat_close(f64(r.row_stats[0][rows]), ref["stats"][0], ref["stat_scale"][0], dW.shape[1], TAU_LIN,
+                      t["up"].shape[0], "wgrad row sumsq")
 
 
 def test_full_swiglu_dropout_sampled():
@@ -1045,19 +1207,44 @@ def test_full_dgrad_sampled():
                       xhat=f64(t["Xhat"][rows]))
     assert_close(f64(r.D[rows]), ref["D"], "dgrad")
     for slot in (0, 1):
-        assert_stat_close(f64(r.row_stats[slot][rows]), ref["stats"][slot], ref["stat_scale"][slot],
-                          f"dgrad stat {slot}")
+        assert_stat_close(f64(r.row_stats[slot][rows]), ref["stats"][slot], ref["stat_scale"][slot], w.N,
+                          chain_tau(ops), w.K, f"dgrad stat {slot}")
 
 
 def test_full_llama_block_chain_sampled():
+    # one layer of the stack: the input arrives with its row sums of squares
+    # (here from the library's unfused ROW_SUMSQ pass), the out-projection's
+    # residual epilogue emits those of h for the MLP norm, the down-projection
+    # those of y; no call runs a pre-pass over its A operand
     from gemm_epilogue_transformer_tmem_gb300 import workloads
     t = inputs.make_llama_block()
-    out = workloads.llama_block_forward({k: cu(v) for k, v in t.items()})
+    td = {k: cu(v) for k, v in t.items()}
+    td["X_sumsq"] = workloads.row_sumsq(td["X"])
+    prepared = dict(W_qkv=coda.fold_gamma(td["W_qkv"], td["gamma_attn"], "kn"),
+                    W_up=coda.fold_gamma(td["W_up"], td["gamma_mlp"], "kn"))
+    before = coda.launch_count()
+    out = workloads.llama_block_forward(td, prepared)
+    launched = coda.launch_count() - before
     sync_ok()
+    assert launched == 6, f"{launched} launches: four GEMMs and two row-sum finishing kernels expected"
     rows = _sampled(inputs.LLAMA_BLOCK["tokens"], 4)
     ref = workloads_oracle_llama(t, rows, prepared=True)
     for name in ("qkv", "h", "up"):
         assert_close(f64(out[name][rows]), ref[name], f"llama {name}")
+    d = inputs.LLAMA_BLOCK["d"]
+    X = f64(t["X"][rows])
+    assert_stat_close(f64(td["X_sumsq"][rows]), O.row_sumsq(X), 2.0 * np.sqrt(O.row_sumsq(X * X)), d, TAU_LIN, 0,
+                      "llama X sum of squares")
+    # the row sums of squares of each residual call, against the oracle of that
+    # call on the bf16 tensors it read (h's inputs are the block's own inputs;
+    # y's are the GPU's up and h)
+    assert_stat_close(f64(out["h_sumsq"][rows]), ref["h_sumsq"], ref["h_sumsq_scale"], d, TAU_LIN, d,
+                      "llama h sum of squares")
+    ffn = inputs.LLAMA_BLOCK["ffn"]
+    yo = O.run_chain(f64(out["up"][rows]), f64(t["W_down"]), [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
+                     residual_t=f64(out["h"][rows]))
+    assert_stat_close(f64(out["y_sumsq"][rows]), yo["stats"][0], yo["stat_scale"][0], d, TAU_LIN, ffn,
+                      "llama y sum of squares")
     # h is a bf16 output that later calls read.  It is computed from exact
     # inputs, and the GPU (fp32) and oracle (fp64) values agree to ~1e-6
     # relative, so their bf16 roundings are equal except where the two straddle
@@ -1081,8 +1268,13 @@ def test_full_llama_block_chain_sampled():
     # against the unprepared block (gamma applied in fp64, no bf16 weight
     # preparation): the whole-block deviation stays within the Frobenius bound
     ref0 = workloads_oracle_llama(t, rows, prepared=False)
-    y = f64(out["y"][rows])
-    assert np.linalg.norm(y - ref0["y"]) / np.linalg.norm(ref0["y"]) <= FRO
+    for name in ("qkv", "up", "y"):
+        got = f64(out[name][rows])
+        fro0 = np.linalg.norm(got - ref0[name]) / np.linalg.norm(ref0[name])
+        over = np.abs(got - ref0[name]) > ATOL + RTOL * np.abs(ref0[name])
+        print(f"llama {name} against the unprepared oracle: {int(over.sum())} of {over.size} sampled elements over "
+              f"the elementwise bound, relative Frobenius {fro0:.3e}")
+        assert fro0 <= FRO, name
 
 
 def bf16_ulp(v):
@@ -1109,7 +1301,9 @@ def workloads_oracle_llama(t, rows, prepared):
         return O.run_chain(A, W, [("RMS_ROWSCALE", None, eps)] + extra, norm_gamma=g)["D"]
 
     qkv = norm_proj(X, t["W_qkv"], t["gamma_attn"], [])
-    h = O.run_chain(f64(t["attn_out"][rows]), f64(t["W_o"]), [("RESIDUAL", 0, 1.0)], residual_t=X)["D"]
+    ho = O.run_chain(f64(t["attn_out"][rows]), f64(t["W_o"]), [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual_t=X)
+    h = ho["D"]
     up = norm_proj(R(h), t["W_up"], t["gamma_mlp"], [("SWIGLU",)])
-    y = O.run_chain(R(up), f64(t["W_down"]), [("RESIDUAL", 0, 1.0)], residual_t=R(h))["D"]
-    return dict(qkv=qkv, h=h, up=up, y=y)
+    yo = O.run_chain(R(up), f64(t["W_down"]), [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual_t=R(h))
+    return dict(qkv=qkv, h=h, up=up, y=yo["D"], h_sumsq=ho["stats"][0], h_sumsq_scale=ho["stat_scale"][0],
+                y_sumsq=yo["stats"][0], y_sumsq_scale=yo["stat_scale"][0])

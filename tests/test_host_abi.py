@@ -84,6 +84,9 @@ def test_workspace_size_closed_form(L):
     ([("ROW_SUM", 0)] * 5, "five reductions"),
     ([("RESIDUAL", 0, 1.0), ("SWIGLU",)], "residual before SWIGLU"),
     ([("SCALE", 0, float("nan"))], "nan parameter"),
+    ([("RMS_ROWSCALE", 0, 1e-6), ("RMS_SUMSQ_ROWSCALE", 0, 1e-6)], "two norms"),
+    ([("RMS_SUMSQ_ROWSCALE", 2, 1e-6)], "row-vector slot out of range"),
+    ([("RMS_SUMSQ_ROWSCALE", 0, -1.0)], "negative eps"),
 ])
 def test_invalid_op_lists(L, ops, why):
     st, _ = _ws(L, 64, 64, 64, ops)
@@ -254,6 +257,11 @@ def test_tuning_knobs_round_trip(L):
     coda.set_tail_helpers(True)
     coda.set_split_k("off")
     coda.set_split_k("auto")
+    coda.set_raster("cols", 4)
+    coda.set_raster("rows", 0)
+    coda.set_raster("auto", 0)
     assert L.coda_launch_count() == before
+    with pytest.raises(KeyError):
+        coda.set_raster("diagonal", 1)
     with pytest.raises(ValueError):
         coda.set_tile_scheduler("round-robin")
