@@ -67,12 +67,15 @@ DESCRIPTIONS = {
              "row sums of squares",
     "fp8swiglu": "SwiGLU up-projection in FP8 E4M3: X[8192,4096] quantised per row each step, W[22016,4096] "
                  "per channel once, dequantised in the epilogue, SiLU(G)*U",
+    "mxfp8swiglu": "SwiGLU up-projection in MXFP8 (E4M3 codes, an E8M0 scale per 32 elements of K applied by the "
+                   "tensor cores): X[8192,4096] quantised each step, W[22016,4096] once, SiLU(G)*U",
     "llama": "LLaMA-7B-like non-attention block, 16384 tokens, d=4096, ffn=11008 (4 fused GEMMs): commuted "
              "RMSNorm->QKV, out-proj+residual, commuted RMSNorm->SwiGLU up-proj, down-proj+residual; one layer of "
              "a stack: the norms' row sums of squares come from the preceding residual epilogues (the input's "
              "with the input, the next layer's emitted by the down-projection)",
 }
-DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300, "fp8swiglu": 300}
+DEFAULT_STEPS = {"rmsproj": 3000, "lnproj": 3000, "swiglu": 300, "dgrad": 300, "llama": 60, "skinny": 3000, "wgrad": 300, "fp8swiglu": 300,
+                 "mxfp8swiglu": 300}
 
 
 def load_peaks():
@@ -194,7 +197,7 @@ class OracleSample:
         self.w, self.I, self.O = workload, inputs, O
         gen = dict(rmsproj=inputs.make_rmsproj, lnproj=inputs.make_lnproj, swiglu=inputs.make_swiglu,
                    dgrad=inputs.make_dgrad, llama=inputs.make_llama_block, skinny=inputs.make_skinny,
-                   wgrad=inputs.make_wgrad, fp8swiglu=inputs.make_swiglu)[workload]
+                   wgrad=inputs.make_wgrad, fp8swiglu=inputs.make_swiglu, mxfp8swiglu=inputs.make_swiglu)[workload]
         self.t = {k: O.to_f64(v) for k, v in gen(0).items()}
         self.Mmax = dict(llama=self.t["X"].shape[0] if "X" in self.t else 0,
                          wgrad=self.t["dW_old"].shape[0] if "dW_old" in self.t else 0).get(
@@ -203,6 +206,8 @@ class OracleSample:
         if workload == "fp8swiglu":   # weight preparation, outside the timed sample
             w8, self.sw = O.quantize_rows_e4m3(self.t["W"].T)
             self.w8 = O.e4m3_decode(w8)
+        if workload == "mxfp8swiglu":   # weight preparation, outside the timed sample
+            self.wmx = O.dequantize_mx(*O.quantize_mx_e4m3(self.t["W"].T))
 
     def run(self, rows: int):
         """Returns (seconds, flops) of the oracle on the first `rows` rows."""
@@ -227,6 +232,12 @@ class OracleSample:
             x8, sx = O.quantize_rows_e4m3(t["X"][r])
             O.run_chain(O.e4m3_decode(x8), self.w8, [("ROW_SCALE", 0), ("COL_SCALE_F32",), ("SWIGLU",)],
                         b_layout="nk", row_vecs={0: sx}, col_scale_f32=self.sw)
+            fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
+        elif self.w == "mxfp8swiglu":
+            # MXFP8 quantisation of the sample rows (W quantised once, as weight
+            # preparation), the product of the dequantised operands, SwiGLU
+            xa = O.dequantize_mx(*O.quantize_mx_e4m3(t["X"][r]))
+            O.run_chain(xa, self.wmx, [("SWIGLU",)], b_layout="nk")
             fl = 2 * rows * t["W"].shape[0] * t["W"].shape[1]
         elif self.w == "skinny":
             O.run_chain(t["X"][r], t["W"], [("RMS_ROWSCALE", None, I.EPS_RMS), ("SWIGLU",)],

@@ -80,6 +80,10 @@ _SIGS = {
     "coda_layernorm": (ctypes.c_int, [_VP, _VP, _VP, _I64, _I64, ctypes.c_float, _VP, _VP]),
     "coda_norm_backward": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _VP, _VP]),
     "coda_quantize_e4m3_rows": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP]),
+    "coda_quantize_mx_e4m3": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP]),
+    "coda_mx_scale_bytes": (ctypes.c_size_t, [_I64, _I64]),
+    "coda_gemm_epilogue_mx": (ctypes.c_int, [_VP, _VP, _VP, _VP, _I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP,
+                                             ctypes.c_size_t, _VP]),
     "coda_epilogue_apply": (ctypes.c_int, [_VP, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP]),
     "coda_check_device_error": (ctypes.c_int, [_VP, _VP]),
     "coda_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -259,6 +263,59 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
                                   _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
                                   workspace.numel() if workspace is not None else 0, _stream(stream))
     _check(st, "coda_gemm_epilogue")
+    return Result(out, row_stats, keep_count, col_stats)
+
+
+def mx_scale_bytes(R: int, K: int) -> int:
+    """Bytes of the tiled E8M0 scale storage of an [R, K] MX operand."""
+    return int(lib().coda_mx_scale_bytes(R, K))
+
+
+def quantize_mx_e4m3(X: torch.Tensor, out: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None,
+                     stream=None):
+    """MXFP8 quantisation of X bf16 [R, K] (K % 32 == 0): (codes uint8 [R, K],
+    scales uint8 [mx_scale_bytes(R, K)] in the library's tiled storage)."""
+    R, K = X.shape
+    if out is None:
+        out = torch.empty((R, K), dtype=torch.uint8, device=X.device)
+    if scales is None:
+        scales = torch.empty((max(mx_scale_bytes(R, K), 16),), dtype=torch.uint8, device=X.device)
+    _check(lib().coda_quantize_mx_e4m3(_ptr(X), R, K, _ptr(out), _ptr(scales), _stream(stream)),
+           "coda_quantize_mx_e4m3")
+    return out, scales
+
+
+def gemm_epilogue_mx(A: torch.Tensor, scale_A: torch.Tensor, B: torch.Tensor, scale_B: torch.Tensor,
+                     ops: Sequence = (), *, seed: int = 0, col_vecs=None, row_vecs=None, residual=None, z=None,
+                     xhat=None, preact_out=None, col_stats: Optional[torch.Tensor] = None, col_scale_f32=None,
+                     out: Optional[torch.Tensor] = None, row_stats: Optional[torch.Tensor] = None,
+                     keep_count: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> Result:
+    """D = f(A @ B^T) with MXFP8 operands: A uint8 E4M3 [M, K], B uint8 E4M3 [N, K],
+    scale_A / scale_B their tiled E8M0 scales (coda_gemm_epilogue_mx)."""
+    M, K = A.shape
+    N = B.shape[0]
+    n_out = output_width(N, ops)
+    dev = A.device
+    if out is None:
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device=dev)
+    ns = stat_slots(ops)
+    if row_stats is None and ns > 0:
+        row_stats = torch.empty((ns, M), dtype=torch.float32, device=dev)
+    if keep_count is None and any(o[0] == "DROPOUT" for o in _norm_ops(ops)):
+        keep_count = torch.empty((M,), dtype=torch.int32, device=dev)
+    nc = col_slots(ops)
+    if col_stats is None and nc > 0:
+        col_stats = torch.empty((nc, n_out), dtype=torch.float32, device=dev)
+    wbytes = workspace_size(M, N, K, ops)
+    if workspace is None and wbytes > 0:
+        workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
+    e = make_epilogue(ops, seed)
+    a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, None, None, col_stats, col_scale_f32)
+    st = lib().coda_gemm_epilogue_mx(_ptr(A), _ptr(scale_A), _ptr(B), _ptr(scale_B), M, N, K, ctypes.byref(e),
+                                     ctypes.byref(a), _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
+                                     workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(st, "coda_gemm_epilogue_mx")
     return Result(out, row_stats, keep_count, col_stats)
 
 

@@ -99,6 +99,19 @@ coda_status make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_CUDA;
 }
 
+// The tiled MX scales of an operand as `chunks` 512-byte tiles (128 words each),
+// one tile per box
+coda_status make_map_sf(CUtensorMap* m, const void* base, uint64_t chunks) {
+  cuuint64_t dims[2] = {128, chunks};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CODA_OK : CODA_ERR_CUDA;
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -501,24 +514,39 @@ coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epil
   return workspace_need(M, N, K, epi, true, bytes);
 }
 
-coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int32_t b_layout,
-                               const coda_epilogue* epi, const coda_aux* aux, void* D, float* row_stats,
-                               uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace coda {
+namespace {
+
+// The fused call.  sfa / sfb: the tiled MX scales of A and B (MX operands, with
+// CODA_AB_E4M3 | CODA_B_NK), or null.
+coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int32_t b_layout,
+                      const coda_epilogue* epi, const coda_aux* aux, void* D, float* row_stats,
+                      uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream,
+                      const void* sfa, const void* sfb) {
   coda_status s = check_dims(M, N, K);
   if (s != CODA_OK) return s;
   if ((b_layout & ~(CODA_B_NK | CODA_A_KM | CODA_AB_E4M3)) != 0) return CODA_ERR_INVALID_ARG;
   const bool a_mn = (b_layout & CODA_A_KM) != 0;   // A given as [K, M]
   const bool fp8 = (b_layout & CODA_AB_E4M3) != 0;  // A and B are E4M3 bytes
+  const bool mx = sfa != nullptr;                   // ... with MX block scales
   b_layout &= CODA_B_NK;
   if (a_mn && (M % 8) != 0) return CODA_ERR_INVALID_ARG;   // 16-byte rows of A [K, M]
   if (fp8 && (a_mn || b_layout != CODA_B_NK || (K % 16) != 0)) return CODA_ERR_INVALID_ARG;
+  if (mx && (!fp8 || (K % 32) != 0)) return CODA_ERR_INVALID_ARG;
   Compiled c;
   s = compile_epilogue(epi, aux, N, K, true, c);
   if (s != CODA_OK) return s;
   if ((a_mn || fp8) && c.has_rms) return CODA_ERR_UNSUPPORTED;   // row statistics read bf16 A by rows
+  if (mx && c.rms_sumsq) return CODA_ERR_UNSUPPORTED;
+  // the U half of an MX SwiGLU weight must start on a 128-row scale tile
+  if (mx && c.glu && ((N / 2) % BM) != 0) return CODA_ERR_UNSUPPORTED;
   if (M == 0 || N == 0) return CODA_OK;
   if (D == nullptr || (K > 0 && (A == nullptr || B == nullptr))) return CODA_ERR_INVALID_ARG;
   if (!aligned16(D) || (K > 0 && (!aligned16(A) || !aligned16(B)))) return CODA_ERR_ALIGNMENT;
+  if (mx && K > 0 && (sfb == nullptr || !aligned16(sfa) || !aligned16(sfb))) return sfb ? CODA_ERR_ALIGNMENT
+                                                                                      : CODA_ERR_INVALID_ARG;
   if (c.needs_row_stats && row_stats == nullptr) return CODA_ERR_INVALID_ARG;
   if (row_stats && !aligned4(row_stats)) return CODA_ERR_ALIGNMENT;
   if (row_keep_count && !aligned4(row_keep_count)) return CODA_ERR_ALIGNMENT;
@@ -528,7 +556,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   if (g.num_tiles > (int64_t{1} << 31) - 1) return CODA_ERR_UNSUPPORTED;
   const size_t ws_need = workspace_bytes_for(M, g, c);
   if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
-  const bool split_room = split_eligible(g, pair) && workspace != nullptr &&
+  const bool split_room = !mx && split_eligible(g, pair) && workspace != nullptr &&
                           workspace_bytes >= split_base(ws_need) + split_bytes(g);
   if (workspace && !aligned16(workspace)) return CODA_ERR_ALIGNMENT;
 
@@ -538,7 +566,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   s = encoder();
   if (s != CODA_OK) return s;
 
-  CUtensorMap maps[6];
+  CUtensorMap maps[8];   // A, B, D, aux 0-2, MX scales of A and B
   std::memset(maps, 0, sizeof(maps));
   s = make_map(&maps[2], D, static_cast<uint64_t>(g.n_out), static_cast<uint64_t>(M), kChunk, 32,
                CU_TENSOR_MAP_SWIZZLE_64B);
@@ -577,6 +605,16 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
       maps[3 + k] = maps[2];
     }
   }
+  if (mx && K > 0) {
+    const uint64_t kbt = static_cast<uint64_t>((K + 127) / 128);
+    s = make_map_sf(&maps[6], sfa, static_cast<uint64_t>((M + BM - 1) / BM) * kbt);
+    if (s != CODA_OK) return s;
+    s = make_map_sf(&maps[7], sfb, static_cast<uint64_t>((N + BM - 1) / BM) * kbt);
+    if (s != CODA_OK) return s;
+  } else {
+    maps[6] = maps[2];
+    maps[7] = maps[2];
+  }
 
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -612,7 +650,7 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * p.epi_warp_bytes;
   const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
   const size_t fixed = 1024 + epi_bytes + ctl_bytes;
-  const size_t stage_bytes = pair ? kPairStageBytes : kStageBytes;
+  const size_t stage_bytes = (pair ? kPairStageBytes : kStageBytes) + (mx ? kMxStageSFBytes : 0);
   if (static_cast<size_t>(dev.max_smem) < fixed + 2 * stage_bytes) return CODA_ERR_UNSUPPORTED;
   int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -701,13 +739,16 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
   p.helpers = (g_tail_helpers.load() != 0 && !split && p.clc == 0 && c.n_aux == 0 && !rowstat_warps &&
                g.num_kb > 0 && tiles_per_cluster <= 16) ? 1 : 0;
   int seq = match_sequence(epi, c.glu);
-  e = fp8 ? launch_gemm_fp8(seq, c.glu, pair, maps, p, grid, smem, st)
-          : launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+  auto launch = [&](int sq) {
+    return mx ? launch_gemm_mx(sq, c.glu, pair, maps, p, grid, smem, st)
+              : (fp8 ? launch_gemm_fp8(sq, c.glu, pair, maps, p, grid, smem, st)
+                     : launch_gemm_seq(sq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st));
+  };
+  e = launch(seq);
   if (e == cudaErrorNotSupported && seq != SEQ_INTERP) {
     (void)cudaGetLastError();   // the sequence has no kernel for this variant: interpret
     seq = SEQ_INTERP;
-    e = fp8 ? launch_gemm_fp8(seq, c.glu, pair, maps, p, grid, smem, st)
-            : launch_gemm_seq(seq, c.glu, a_mn, mn, rowstat_warps, pair, maps, p, grid, smem, st);
+    e = launch(seq);
   }
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
@@ -728,6 +769,29 @@ coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t 
     g_launches.fetch_add(1);
   }
   return CODA_OK;
+}
+
+}  // namespace
+}  // namespace coda
+
+extern "C" {
+
+coda_status coda_gemm_epilogue(const void* A, const void* B, int64_t M, int64_t N, int64_t K, int32_t b_layout,
+                               const coda_epilogue* epi, const coda_aux* aux, void* D, float* row_stats,
+                               uint32_t* row_keep_count, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_impl(A, B, M, N, K, b_layout, epi, aux, D, row_stats, row_keep_count, workspace, workspace_bytes,
+                   stream, nullptr, nullptr);
+}
+
+coda_status coda_gemm_epilogue_mx(const void* A, const void* scale_A, const void* B, const void* scale_B, int64_t M,
+                                  int64_t N, int64_t K, const coda_epilogue* epi, const coda_aux* aux, void* D,
+                                  float* row_stats, uint32_t* row_keep_count, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  if (K > 0 && M > 0 && N > 0 && (scale_A == nullptr || scale_B == nullptr)) return CODA_ERR_INVALID_ARG;
+  // K == 0 has no scales to read; the kernel path still needs a non-null marker
+  static const uint8_t kNone[16] __attribute__((aligned(16))) = {};
+  return gemm_impl(A, B, M, N, K, CODA_B_NK | CODA_AB_E4M3, epi, aux, D, row_stats, row_keep_count, workspace,
+                   workspace_bytes, stream, scale_A ? scale_A : kNone, scale_B ? scale_B : kNone);
 }
 
 coda_status coda_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, int32_t b_layout,
@@ -817,6 +881,27 @@ coda_status coda_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void* Q
   s = device_info(dev);
   if (s != CODA_OK) return s;
   const cudaError_t e = launch_quantize_e4m3_rows(X, M, K, Q, scale, static_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess) g_launches.fetch_add(1);
+  return from_cuda(e);
+}
+
+size_t coda_mx_scale_bytes(int64_t R, int64_t K) {
+  if (R <= 0 || K <= 0) return 0;
+  return static_cast<size_t>((R + 127) / 128) * static_cast<size_t>((K + 127) / 128) * 512u;
+}
+
+coda_status coda_quantize_mx_e4m3(const void* X, int64_t R, int64_t K, void* Q, void* scales, void* stream) {
+  coda_status s = check_dims(R, 32, K);
+  if (s != CODA_OK) return s;
+  if ((K % 32) != 0) return CODA_ERR_INVALID_ARG;
+  if (R == 0 || K == 0) return CODA_OK;
+  if (!X || !Q || !scales) return CODA_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q) || !aligned16(scales)) return CODA_ERR_ALIGNMENT;
+  DevInfo dev;
+  s = device_info(dev);
+  if (s != CODA_OK) return s;
+  const cudaError_t e = launch_quantize_mx_e4m3(X, R, K, Q, scales, coda_mx_scale_bytes(R, K), dev.sms,
+                                                static_cast<cudaStream_t>(stream));
   if (e == cudaSuccess) g_launches.fetch_add(1);
   return from_cuda(e);
 }

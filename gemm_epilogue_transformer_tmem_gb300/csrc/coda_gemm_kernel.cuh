@@ -200,6 +200,18 @@ struct WorkIter {
   }
 };
 
+// Tensor-memory accumulator of a CTA's local-th tile and the parity of its
+// barrier phases: two accumulators used in turn, or (MX kernels, whose scales
+// take the other half of tensor memory) one accumulator used by every tile.
+template <bool kMX>
+__device__ __forceinline__ int acc_index(int local) {
+  return kMX ? 0 : (local & 1);
+}
+template <bool kMX>
+__device__ __forceinline__ uint32_t acc_parity(int local) {
+  return kMX ? static_cast<uint32_t>(local & 1) : static_cast<uint32_t>((local >> 1) & 1);
+}
+
 // The CTA whose run holds unit u: the largest c with floor(c U / G) <= u.
 __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int64_t G) {
   return static_cast<int>(((u + 1) * G + U - 1) / U) - 1;
@@ -237,19 +249,28 @@ struct SmemAux {
 // reads the stored activations X [tokens, features] directly).
 // kFP8: A and B are FP8 E4M3, both K-major; a stage then holds 128 elements of
 // K (the same 128-byte rows), four MMAs of K = 32 (kind::f8f6f4).
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN, bool kFP8>
+// kMX (with kFP8): MX block-scaled E4M3 (kind::mxf8f6f4, one E8M0 scale per 32
+// elements of K).  Each stage also brings the scale tiles of its rows (512 bytes
+// per 128 rows, tmSA / tmSB); the MMA warp copies them into tensor memory
+// (tcgen05.cp) ahead of the stage's four MMAs.  The scales need tensor-memory
+// columns, so the MX kernel keeps one accumulator (256 columns) instead of two.
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN, bool kFP8, bool kMX = false>
 __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
                               const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
+                              const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                               const __grid_constant__ GemmParams p) {
+  static_assert(!kMX || kFP8, "MX operands are 8-bit");
   // Per-CTA tile geometry.  A CTA pair shares one 256-row tile: rank r of the
   // pair owns rows r*128 .. r*128+127 of it and stages half of B.
   constexpr int kTileM = kPair ? 2 * BM : BM;
   constexpr int kCsize = kPair ? 2 : 1;   // CTAs per cluster
   constexpr int kStageB = kPair ? kPairStageBBytes : kStageBBytes;
+  // MX scale tiles per stage and CTA: A's 128 rows, and both 128-row halves of B
+  constexpr int kStageSF = kMX ? kMxStageSFBytes : 0;
   // bytes the leader's full barrier expects per stage (both CTAs' loads for a pair)
-  constexpr uint32_t kExpectTx = kPair ? 2u * kPairStageBytes : static_cast<uint32_t>(kStageBytes);
+  constexpr uint32_t kExpectTx = kPair ? 2u * (kPairStageBytes + kStageSF) : static_cast<uint32_t>(kStageBytes + kStageSF);
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -257,6 +278,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + p.smem_ctl_off);
   uint8_t* sA = smem;
   uint8_t* sB = smem + p.stages * kStageABytes;
+  uint8_t* sSF = sB + p.stages * kStageB;   // MX scale tiles (kMX only)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
@@ -294,6 +316,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     if (p.num_kb > 0) {
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
+      if (kMX) {
+        tma_prefetch_desc(&tmSA);
+        tma_prefetch_desc(&tmSB);
+      }
     }
     tma_prefetch_desc(&tmD);
   }
@@ -353,6 +379,32 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           const int k0 = kb * (kFP8 ? 2 * BK : BK);   // elements of K
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * kStageB;
+          if constexpr (kMX) {
+            // scale tiles of this k-block: A's 128 rows (this CTA's), B's two
+            // 128-row halves of the tile (both in each CTA of a pair)
+            uint8_t* sf_dst = sSF + stage * kStageSF;
+            const int ca = (m0 / BM) * p.num_kb + kb;
+            int b0, b1;
+            if constexpr (kPair) {
+              b0 = kGLU ? n_tile * (BN / 2) : n_tile * BN;
+              b1 = kGLU ? p.half + n_tile * (BN / 2) : b0 + BN / 2;
+            } else {
+              b0 = nb0;
+              b1 = nb1;
+            }
+            const int cb0 = (b0 / BM) * p.num_kb + kb;
+            const int cb1 = (b1 / BM) * p.num_kb + kb;
+            if constexpr (kPair) {
+              const uint32_t fbc = mapa_shared(smem_u32(fb), 0u);
+              tma_load_2d_pair(sf_dst, &tmSA, fbc, 0, ca);
+              tma_load_2d_pair(sf_dst + 512, &tmSB, fbc, 0, cb0);
+              tma_load_2d_pair(sf_dst + 1024, &tmSB, fbc, 0, cb1);
+            } else {
+              tma_load_2d(sf_dst, &tmSA, fb, 0, ca);
+              tma_load_2d(sf_dst + 512, &tmSB, fb, 0, cb0);
+              tma_load_2d(sf_dst + 1024, &tmSB, fb, 0, cb1);
+            }
+          }
           if constexpr (kPair) {
             const uint32_t fbc = mapa_shared(smem_u32(fb), 0u);   // the leader's barrier
             if (kAMN) {
@@ -405,7 +457,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
-      constexpr uint32_t idesc = kFP8 ? make_idesc_e4m3(kTileM, BN) : make_idesc_bf16(kTileM, BN, kBMN, kAMN);
+      constexpr uint32_t idesc = kMX ? make_idesc_mx_e4m3(kTileM, BN)
+                                     : (kFP8 ? make_idesc_e4m3(kTileM, BN) : make_idesc_bf16(kTileM, BN, kBMN, kAMN));
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -414,8 +467,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       Item w;
       for (; ok && wi.next(p, w, ctl, W, rank, kCsize, false, lane, ok); ++local) {
         const int tile = w.tile;
-        const int acc = local & 1;
-        const uint32_t acc_phase = (local >> 1) & 1;
+        const int acc = acc_index<kMX>(local);
+        const uint32_t acc_phase = acc_parity<kMX>(local);
         if (!W(&ctl->tempty[acc], acc_phase ^ 1u, tile)) {
           ok = false;
           break;
@@ -430,6 +483,28 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
           const uint32_t b_addr = smem_u32(sB + stage * kStageB);
+          if constexpr (kMX) {
+            // the stage's scale tiles into tensor memory: A's at columns sf+0..3,
+            // B's halves at sf+4..7 and sf+8..11 (one 32-bit word per row and
+            // 32-row group, its four bytes the stage's four 32-element blocks);
+            // the MMAs below are issued after these copies by the same thread
+            const uint32_t sf = tmem_base + kMxSFCol0 + stage * kMxSFColsPerStage;
+            const uint32_t ss = smem_u32(sSF + stage * kStageSF);
+            tmem_cp_32x128b_x4<kPair>(sf, make_smem_desc_rows16(ss));
+            tmem_cp_32x128b_x4<kPair>(sf + 4, make_smem_desc_rows16(ss + 512));
+            tmem_cp_32x128b_x4<kPair>(sf + 8, make_smem_desc_rows16(ss + 1024));
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, 1024);
+              const uint64_t bd = make_smem_desc(b_addr + k * 32, 16, 1024);
+              const uint32_t acc_in = (kb != w.kb0 || k != 0) ? 1u : 0u;
+              const uint32_t id = idesc_sf_ids(idesc, static_cast<uint32_t>(k), static_cast<uint32_t>(k));
+              if constexpr (kPair)
+                mma_mxf8_ss_pair(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+              else
+                mma_mxf8_ss(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+            }
+          } else {
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             // MN-major operands: 64-element groups 8 KB apart, 16 k-rows of 128 B per UMMA_K
@@ -449,6 +524,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
               else
                 mma_bf16_ss(d_tmem, ad, bd, idesc, acc_in);
             }
+          }
           }
           if constexpr (kPair)
             mma_commit_pair_mc(&ctl->empty[stage], 0x3);
@@ -565,8 +641,8 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       const int col_base = n_tile * kOutCols;
       int nch = (p.N_out - col_base + kChunk - 1) / kChunk;
       if (nch > kOutCols / kChunk) nch = kOutCols / kChunk;
-      const int acc = local & 1;
-      const uint32_t acc_phase = (local >> 1) & 1;
+      const int acc = acc_index<kMX>(local);
+      const uint32_t acc_phase = acc_parity<kMX>(local);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       const bool partial = split && !(w.kb0 == 0 && w.kb1 == p.num_kb);
       if (n_aux > 0 && !partial) issue_aux(abuf, col_base, m0 + q * 32);
@@ -892,7 +968,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         const int col_base = n_tile * kOutCols;
         int nch = (p.N_out - col_base + kChunk - 1) / kChunk;
         if (nch > kOutCols / kChunk) nch = kOutCols / kChunk;
-        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (local & 1) * kAccCols;
+        const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc_index<kMX>(local) * kAccCols;
         // every MMA of the CTA has completed (used once: no phase ambiguity)
         if (warp_wait(W, &ctl->drain, 0u, static_cast<uint32_t>(tile), lane)) {
           tc_fence_after_sync();
@@ -969,9 +1045,10 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   }
 }
 
-template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN = false, bool kFP8 = false>
+template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN = false, bool kFP8 = false,
+          bool kMX = false>
 cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem, cudaStream_t st) {
-  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN, kFP8>;
+  auto kern = &coda_gemm_epilogue_kernel<kGLU, kBMN, kRowStats, kPair, Epi, kAMN, kFP8, kMX>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // Programmatic launch only behind the row-scale pre-pass, whose one output
@@ -981,7 +1058,8 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
   const bool after_prepass = p.rms_vec != nullptr && !p.rms_from_sumsq;
   if constexpr (!kPair) {
     if (!after_prepass) {
-      kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+      kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+                                                       maps[7], p);
       return cudaGetLastError();
     }
     // after the row-scale pre-pass (split-K grids): start the mainloop early,
@@ -996,7 +1074,8 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
+                              p);
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -1013,7 +1092,8 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = after_prepass ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], p);
+    return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], maps[7],
+                              p);
   }
 }
 
@@ -1083,6 +1163,14 @@ cudaError_t launch_variant_fp8(bool pair, const CUtensorMap* maps, const GemmPar
                                cudaStream_t st) {
   return pair ? launch_gemm_t<kGLU, false, false, true, Epi, false, true>(maps, p, grid, smem, st)
               : launch_gemm_t<kGLU, false, false, false, Epi, false, true>(maps, p, grid, smem, st);
+}
+
+// MX block-scaled E4M3 operands (scales in maps[6], maps[7])
+template <class Epi, bool kGLU>
+cudaError_t launch_variant_mx(bool pair, const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem,
+                              cudaStream_t st) {
+  return pair ? launch_gemm_t<kGLU, false, false, true, Epi, false, true, true>(maps, p, grid, smem, st)
+              : launch_gemm_t<kGLU, false, false, false, Epi, false, true, true>(maps, p, grid, smem, st);
 }
 
 }  // namespace coda

@@ -29,6 +29,13 @@ constexpr int kPairStageBBytes = (BN / 2) * BK * 2;  // 16 KB
 constexpr int kPairStageBytes = kStageABytes + kPairStageBBytes;
 constexpr int kBoxBytes = 32 * kChunk * 2;         // 32 rows x 32 bf16 = 2 KB
 constexpr int kMaxStages = 8;
+// MX operands: per stage and CTA, the scale tiles of A's 128 rows and of B's two
+// 128-row halves (512 bytes each); in tensor memory, after the one 256-column
+// accumulator, 16 columns per stage (A's tile at +0..3, B's at +4..7, +8..11)
+constexpr int kMxStageSFBytes = 3 * 512;
+constexpr int kMxSFCol0 = kAccCols;
+constexpr int kMxSFColsPerStage = 16;
+static_assert(kMxSFCol0 + kMaxStages * kMxSFColsPerStage <= kTmemCols, "MX scales must fit in tensor memory");
 // Split over K (stream-K): a tile's k-blocks may be shared by up to kSplitSegs
 // CTAs, each publishing a BM x BN fp32 partial accumulator as float4 vectors,
 // vector (row r, columns 4q..4q+3) at index q * BM + r (a warp's 32 rows of one

@@ -248,6 +248,64 @@ cudaError_t launch_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void*
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------ MX E4M3 quantiser
+// OCP Microscaling Formats (MX) v1.0: each block of 32 elements along K shares
+// an E8M0 scale X = 2^(e - 127).  The shared exponent is floor(log2 amax) - 8
+// (E4M3's largest normal is 1.75 * 2^8), clamped to the scale's range: with E
+// the biased fp32 exponent field of the block maximum, e = max(E - 8, 0) (0 for
+// a zero or subnormal-range maximum).  Codes e4m3(x * 2^(127 - e)), rounded to
+// nearest even and saturated at 448; the product is exact wherever the code is
+// not zero.  One thread per block of 32 (64 bytes in, 32 code bytes and one
+// scale byte out); scales go to the tiled storage of coda.h, whose padding the
+// caller set to 127 first.
+__global__ void quantize_mx_e4m3_kernel(const uint16_t* __restrict__ X, int64_t R, int64_t K,
+                                        uint8_t* __restrict__ Q, uint8_t* __restrict__ S) {
+  const int64_t nb = K >> 5;
+  const int64_t kbt = (nb + 3) >> 2;
+  const int64_t total = R * nb;
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = t / nb;
+    const int64_t j = t - r * nb;
+    const uint4* src = reinterpret_cast<const uint4*>(X + r * K + j * 32);
+    float x[32];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) unpack8(__ldg(src + q), x + 8 * q);
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 8;
+    if (e < 0) e = 0;
+    const float mul = __uint_as_float(static_cast<uint32_t>(254 - e) << 23);   // 2^(127 - e), e <= 247
+    uint32_t w[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t lo = cvt_e4m3x2(__fmul_rn(x[4 * q], mul), __fmul_rn(x[4 * q + 1], mul));
+      const uint32_t hi = cvt_e4m3x2(__fmul_rn(x[4 * q + 2], mul), __fmul_rn(x[4 * q + 3], mul));
+      w[q] = lo | (hi << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(Q + r * K + j * 32);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    S[((r >> 7) * kbt + (j >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (j & 3)] = static_cast<uint8_t>(e);
+  }
+}
+
+cudaError_t launch_quantize_mx_e4m3(const void* X, int64_t R, int64_t K, void* Q, void* S, size_t s_bytes, int num_sms,
+                                    cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(S, 127, s_bytes, st);   // padding: scale 1
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const int64_t total = R * (K >> 5);
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  quantize_mx_e4m3_kernel<<<static_cast<unsigned>(blocks), threads, 0, st>>>(
+      static_cast<const uint16_t*>(X), R, K, static_cast<uint8_t*>(Q), static_cast<uint8_t*>(S));
+  return cudaGetLastError();
+}
+
 // --------------------------------------------------------- norm backward
 // dX = r (g - sum_g / K - x_hat S / K), x_hat = (x - mu) r, S = r (sum_gx - mu sum_g);
 // RMSNorm: mu = sum_g = null.  Eight elements per thread, grid-stride over the

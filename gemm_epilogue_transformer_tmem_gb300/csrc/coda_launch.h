@@ -36,6 +36,10 @@ cudaError_t launch_gemm_gpt(int seq, bool a_mn_major, bool b_mn_major, bool row_
 // FP8 E4M3 operands: the interpreter and the FP8 fixed sequences
 cudaError_t launch_gemm_fp8(int seq, bool glu, bool pair, const CUtensorMap* maps, const GemmParams& p, int grid,
                             size_t smem, cudaStream_t st);
+// MX block-scaled E4M3 operands (maps[6], maps[7]: the scale tiles): the
+// interpreter, the plain GEMM and SwiGLU
+cudaError_t launch_gemm_mx(int seq, bool glu, bool pair, const CUtensorMap* maps, const GemmParams& p, int grid,
+                           size_t smem, cudaStream_t st);
 // how many CTA pairs of the pair kernel fit on the device at once
 cudaError_t max_pairs(bool glu, bool b_mn_major, size_t smem, int* pairs);
 
@@ -52,6 +56,9 @@ cudaError_t launch_ln_colsum(const void* W_folded, const void* W, const void* be
 cudaError_t launch_norm_backward(const void* g, const void* X, const float* r, const float* mu, const float* sum_g,
                                  const float* sum_gx, int64_t M, int64_t K, void* dX, int num_sms, cudaStream_t st);
 cudaError_t launch_quantize_e4m3_rows(const void* X, int64_t M, int64_t K, void* Q, float* scale, cudaStream_t st);
+// MX E4M3: codes [R, K] and E8M0 scales in the tiled storage (s_bytes, padding set to 127 first)
+cudaError_t launch_quantize_mx_e4m3(const void* X, int64_t R, int64_t K, void* Q, void* S, size_t s_bytes, int num_sms,
+                                    cudaStream_t st);
 cudaError_t launch_layernorm(const void* X, const void* gamma, const void* beta, int64_t M, int64_t K, float eps,
                              void* Xn, cudaStream_t st);
 cudaError_t launch_fold_gamma(const void* W, const void* gamma, void* W_out, int64_t K, int64_t N, bool kn,

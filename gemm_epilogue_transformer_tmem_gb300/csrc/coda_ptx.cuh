@@ -285,6 +285,66 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(int m, int n) {
          (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// ------------------------------------------------- MX block-scaled FP8 MMA
+// kind::mxf8f6f4 with E4M3 A and B (type code 0), fp32 D, both K-major, E8M0
+// scales (bit 23), one scale per 32 elements of K (scale_vec::1X); the scale
+// bytes used are selected by the A and B scale-factor ids (bits 29-30 and 4-5):
+// byte id of each 32-bit tensor-memory word holding the scales.
+__host__ __device__ constexpr uint32_t make_idesc_mx_e4m3(int m, int n) {
+  return (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t idesc, uint32_t a_id, uint32_t b_id) {
+  return idesc | (b_id << 4) | (a_id << 29);
+}
+
+// D[tmem] (+)= (A * sa) (B * sb)^T for 8-bit operands with block scales read
+// from tensor memory at sfa / sfb
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of a plain (unswizzled) block of 16-byte rows, rows
+// contiguous: the source of tcgen05.cp (leading and stride offsets both 128 B,
+// i.e. 8-row groups back to back)
+__device__ __forceinline__ uint64_t make_smem_desc_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(128 >> 4) << 16;
+  d |= static_cast<uint64_t>(128 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copy 32 rows x 16 bytes of shared memory into tensor-memory columns
+// taddr .. taddr+3 of all four lane quarters (row l -> lane l of each quarter);
+// for a CTA pair, issued by the even CTA, each CTA copies its own shared memory
+// into its own tensor memory
+template <bool kPair>
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  if constexpr (kPair)
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+  else
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // two fp32 values to two E4M3 bytes, round to nearest even, finite overflow
 // saturated to +-448: lo in bits 0-7, hi in bits 8-15
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {

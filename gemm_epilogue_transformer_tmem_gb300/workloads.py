@@ -223,6 +223,42 @@ def build_fp8swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> 
                 peak_scale=2.0, kernels_per_fused=2, kernels_per_unfused=3, prep=prep, outputs=dict(D=D, D_unfused=Du))
 
 
+def build_mxfp8swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
+    """The swiglu up-projection with MXFP8 operands (OCP MX: E4M3 codes, one
+    E8M0 scale per 32 elements of K, applied by the tensor cores): X quantised
+    in the step, W ([N, K]) once; out = SiLU(G) * U."""
+    t = t or inputs.make_swiglu(seed, M, K, N_out)
+    X = t["X"].to(dev)
+    W = t["W"].to(dev).t().contiguous()          # [2*N_out, K]
+    N = 2 * N_out
+    w8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((coda.mx_scale_bytes(N, K),), dtype=torch.uint8, device=dev)
+    prep = lambda: coda.quantize_mx_e4m3(W, out=w8, scales=sw)   # noqa: E731
+    prep()
+    x8 = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((coda.mx_scale_bytes(M, K),), dtype=torch.uint8, device=dev)
+    ops = [("SWIGLU",)]
+    D = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    Du = torch.empty_like(D)
+
+    def fused():
+        coda.quantize_mx_e4m3(X, out=x8, scales=sx)
+        coda.gemm_epilogue_mx(x8, sx, w8, sw, ops, out=D)
+
+    def unfused():
+        coda.quantize_mx_e4m3(X, out=x8, scales=sx)
+        coda.gemm_epilogue_mx(x8, sx, w8, sw, [], out=C)
+        coda.epilogue_apply(C, ops, out=Du)
+
+    sbytes = coda.mx_scale_bytes(M, K) + coda.mx_scale_bytes(N, K)
+    q = M * K * BF16 + M * K + coda.mx_scale_bytes(M, K)
+    fb = q + (M * K + N * K) + sbytes + M * N_out * BF16
+    ub = q + (M * K + N * K) + sbytes + M * N * BF16 + (M * N * BF16 + M * N_out * BF16)
+    return Step("mxfp8swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
+                peak_scale=2.0, kernels_per_fused=2, kernels_per_unfused=3, prep=prep, outputs=dict(D=D, D_unfused=Du))
+
+
 def build_wgrad(dev="cuda", seed=0, T=16384, d=4096, ffn=11008, t=None) -> Step:
     """dW = s * up^T @ dY + dW (in place), per-row sums of squares of the new dW:
     the down-projection's weight gradient, A read as [K, M] (the stored
@@ -421,4 +457,5 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,
-                llama=build_llama, skinny=build_skinny, wgrad=build_wgrad, fp8swiglu=build_fp8swiglu)
+                llama=build_llama, skinny=build_skinny, wgrad=build_wgrad, fp8swiglu=build_fp8swiglu,
+                mxfp8swiglu=build_mxfp8swiglu)

@@ -356,6 +356,62 @@ CODA_API coda_status coda_quantize_e4m3_rows(const void* X, int64_t M, int64_t K
                                              void* stream);
 
 /*
+ * MX (microscaling) FP8 operands.  The agentlenshq.com summary ("仕組み",
+ * Scaling) makes scaling by a vector one of the epilogue's primitives; with
+ * block-scaled FP8 the scaling moves inside the contraction: each block of 32
+ * elements along K carries its own power-of-two scale, applied by the tensor
+ * cores (tcgen05.mma kind::mxf8f6f4 block_scale) to every product before it is
+ * accumulated.  Format: OCP Microscaling Formats (MX) v1.0, MXFP8 E4M3 -- E4M3
+ * element codes, one E8M0 scale byte e per 32 elements (value 2^(e-127); 255 is
+ * NaN and must not occur).
+ *
+ * Scale storage ("tiled"): for an operand of R rows and K columns, rows are
+ * taken in groups of 128 and 32-element blocks in groups of 4, each group pair
+ * forming a 512-byte tile, tiles ordered by row group then block group; the
+ * scale of row r, block j (columns 32j .. 32j+31) is the byte at
+ *     ((r / 128) * ceil(K / 128) + j / 4) * 512
+ *       + (r % 32) * 16 + ((r % 128) / 32) * 4 + (j % 4).
+ * One tile is exactly what the tensor cores read for 128 rows and 128
+ * elements of K.  Positions beyond R rows or ceil(K/32) blocks are padding and
+ * must hold a finite scale (the quantiser writes 127 there).
+ */
+
+/* Bytes of the tiled scale storage of an [R, K] MX operand (0 if R or K <= 0). */
+CODA_API size_t coda_mx_scale_bytes(int64_t R, int64_t K);
+
+/*
+ * coda_quantize_mx_e4m3 -- MXFP8 quantisation of the rows of X (OCP MX v1.0
+ * conversion): for each block of 32 elements along K, the shared exponent is
+ * floor(log2(max |x|)) - 8 (E4M3's largest normal is 1.75 * 2^8), clamped to
+ * [-127, 127]; codes are e4m3(x / 2^shared), rounded to nearest even and
+ * saturated at +-448.  A block of zeros gets scale byte 0 and zero codes.
+ *   X       bf16 [R, K], K % 32 == 0, 16-byte aligned
+ *   Q       uint8 [R, K] E4M3 codes (output)
+ *   scales  coda_mx_scale_bytes(R, K) bytes, tiled storage (output; padding 127)
+ */
+CODA_API coda_status coda_quantize_mx_e4m3(const void* X, int64_t R, int64_t K, void* Q, void* scales,
+                                           void* stream);
+
+/*
+ * coda_gemm_epilogue_mx -- coda_gemm_epilogue with MXFP8 operands:
+ *     C[i, j] = sum_k 2^(ea(i, k/32) - 127) A[i, k] * 2^(eb(j, k/32) - 127) B[j, k]
+ * accumulated in fp32 by the tensor cores, then the op list as in
+ * coda_gemm_epilogue.  A is E4M3 [M, K] and B is E4M3 [N, K] (both K-major: B in
+ * the nn.Linear [out, in] layout); scale_A and scale_B are their tiled scales
+ * (coda_mx_scale_bytes(M, K) and coda_mx_scale_bytes(N, K) bytes).  K must be a
+ * multiple of 32; with SWIGLU, N/2 must be a multiple of 128 (the U half then
+ * starts on a scale tile); RMS_ROWSCALE, RMS_SUMSQ_ROWSCALE and LN_ROWSCALE are
+ * not available (they read bf16 A).  Other arguments, workspace and errors as
+ * coda_gemm_epilogue; coda_workspace_size gives the workspace (the split over
+ * K is not used with MX operands).
+ */
+CODA_API coda_status coda_gemm_epilogue_mx(const void* A, const void* scale_A, const void* B, const void* scale_B,
+                                           int64_t M, int64_t N, int64_t K, const coda_epilogue* epi,
+                                           const coda_aux* aux, void* D, float* row_stats,
+                                           uint32_t* row_keep_count, void* workspace, size_t workspace_bytes,
+                                           void* stream);
+
+/*
  * coda_epilogue_apply -- the same op list applied by a separate memory-bound
  * kernel to a bf16 tensor C [M, N] already in global memory (the unfused form:
  * one read of C, one write of D).  RMS_ROWSCALE and LN_ROWSCALE are not

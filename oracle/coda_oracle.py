@@ -569,27 +569,23 @@ def quantize_mx_e4m3(X):
     """MX E4M3 quantisation of each row of X [R, K] in blocks of 32 along K (the
     last block of a row may be shorter).  Returns (codes uint8 [R, K], scale
     bytes uint8 [R, ceil(K/32)]).  A block of zeros gets scale byte 0 and zero
-    codes.  Written element by element from the definition: the shared exponent
-    from the exact binary exponent of the block maximum (math.frexp), the
-    division by a power of two exact in fp64, then round-to-nearest-even onto
-    the E4M3 grid with saturation (e4m3_encode)."""
+    codes.  Per block, from the definition: the shared exponent from the exact
+    binary exponent of the block maximum (frexp: amax = m 2^e with 0.5 <= m < 1,
+    so floor(log2 amax) = e - 1), clamped; the division by that power of two,
+    exact in fp64; then round-to-nearest-even onto the E4M3 grid with saturation
+    (e4m3_encode).  The blocks are processed as one array."""
     X = np.asarray(X, dtype=np.float64)
     R, K = X.shape
     nb = (K + MX_BLOCK - 1) // MX_BLOCK
-    codes = np.zeros((R, K), dtype=np.uint8)
-    sexp = np.zeros((R, nb), dtype=np.uint8)
-    for i in range(R):
-        for b in range(nb):
-            blk = X[i, b * MX_BLOCK:(b + 1) * MX_BLOCK]
-            amax = float(np.max(np.abs(blk)))
-            if amax == 0.0:
-                shared = -127
-            else:
-                _, e = math.frexp(amax)            # amax = m 2^e, 0.5 <= m < 1: floor(log2 amax) = e - 1
-                shared = min(max((e - 1) - E4M3_EMAX, -127), 127)
-            sexp[i, b] = shared + 127
-            codes[i, b * MX_BLOCK:(b + 1) * MX_BLOCK] = e4m3_encode(blk / math.ldexp(1.0, shared))
-    return codes, sexp
+    padded = np.zeros((R, nb * MX_BLOCK))
+    padded[:, :K] = X
+    blocks = padded.reshape(R, nb, MX_BLOCK)
+    amax = np.max(np.abs(blocks), axis=2)
+    _, e = np.frexp(amax)
+    shared = np.clip((e - 1) - E4M3_EMAX, -127, 127)
+    shared = np.where(amax == 0.0, -127, shared)
+    codes = e4m3_encode(blocks / np.ldexp(1.0, shared)[:, :, None]).reshape(R, nb * MX_BLOCK)[:, :K]
+    return np.ascontiguousarray(codes), (shared + 127).astype(np.uint8)
 
 
 def dequantize_mx(codes, sexp) -> np.ndarray:

@@ -717,6 +717,131 @@ def test_e4m3_pipeline_approximates_bf16_gemm():
     assert err < 0.05, err
 
 
+# --------------------------------------------------------------- MX FP8
+def mx_tiled(sexp, R, K):
+    """Scale bytes [R, ceil(K/32)] placed in the library's tiled storage (the
+    layout coda.h defines), padding 127."""
+    buf = np.full((O.mx_scale_bytes(R, K),), 127, dtype=np.uint8)
+    for r in range(R):
+        for j in range(sexp.shape[1]):
+            buf[O.mx_scale_offset(r, j, K)] = sexp[r, j]
+    return torch.from_numpy(buf)
+
+
+def test_quantize_mx_e4m3_bit_exact():
+    # rows of very different magnitudes, zero rows and blocks, a constant row,
+    # and a K that is not a multiple of 128 (the scale storage has padding)
+    R, K = 300, 160
+    X = rand((R, K), 771).float()
+    X[1] = 0.0
+    X[2] = 3.0
+    X[3] *= 1e-30
+    X[4] *= 1e30
+    X[5, :32] = 0.0
+    X[6, 40] = 500.0                      # saturates to 448 after scaling
+    X = X.to(torch.bfloat16)
+    q, sc = coda.quantize_mx_e4m3(cu(X))
+    sync_ok()
+    q_ref, s_ref = O.quantize_mx_e4m3(f64(X))
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    buf = sc.cpu().numpy()
+    np.testing.assert_array_equal(O.mx_scales_from_tiled(buf, R, K), s_ref)
+    used = np.zeros(len(buf), dtype=bool)
+    for r in range(R):
+        for j in range(s_ref.shape[1]):
+            used[O.mx_scale_offset(r, j, K)] = True
+    assert (buf[~used] == 127).all(), "padding of the scale storage"
+
+
+MX_EXACT_CASES = [(300, 256, 264), (200, 160, 512), (129, 384, 256), (1, 32, 16)]
+
+
+@pytest.mark.parametrize("M,K,N", MX_EXACT_CASES)
+def test_mx_gemm_exact(M, K, N, mode):
+    # codes 1 .. 3.75 (multiples of 1/8) and block scales 1 or 2: every product
+    # is a multiple of 1/64 below 56.25, so every partial sum (below 384 * 56.25
+    # < 2^15) is exact in fp32 and D is the bf16 rounding of the exact product;
+    # a scale applied to the wrong block, row or column changes D
+    A8 = inputs.random_e4m3_codes((M, K), 781, 7, 8)
+    B8 = inputs.random_e4m3_codes((N, K), 782, 7, 8)
+    g = torch.Generator().manual_seed(783)
+    nb = (K + 31) // 32
+    sa = (127 + torch.randint(0, 2, (M, nb), generator=g)).to(torch.uint8).numpy()
+    sb = (127 + torch.randint(0, 2, (N, nb), generator=g)).to(torch.uint8).numpy()
+    r = coda.gemm_epilogue_mx(cu(A8), cu(mx_tiled(sa, M, K)), cu(B8), cu(mx_tiled(sb, N, K)), [])
+    sync_ok()
+    ref = O.round_bf16(O.gemm(O.dequantize_mx(A8.numpy(), sa), O.dequantize_mx(B8.numpy(), sb), "nk"))
+    np.testing.assert_array_equal(f64(r.D), ref)
+
+
+MX_OPS = {"swiglu": [("SWIGLU",)], "bias_gelu_rowsum": [("BIAS", 0), ("GELU_TANH",), ("ROW_SUM", 0)],
+          "plain": []}
+
+
+@pytest.mark.parametrize("case", sorted(MX_OPS))
+def test_mx_gemm_epilogue(case, mode):
+    # bf16 X and W quantised by the library (MXFP8), multiplied with the block
+    # scales applied by the tensor cores, the op list in the epilogue; against
+    # the oracle run on the dequantised codes the GPU produced
+    ops = MX_OPS[case]
+    M, K, n_out = 300, 384, 256
+    N = 2 * n_out if case == "swiglu" else n_out
+    X = rand((M, K), 791)
+    W = rand((N, K), 792, 1.0 / math.sqrt(K))
+    b = rand((n_out,), 793)
+    xq, xs = coda.quantize_mx_e4m3(cu(X))
+    wq, ws_ = coda.quantize_mx_e4m3(cu(W))
+    r = coda.gemm_epilogue_mx(xq, xs, wq, ws_, ops, col_vecs={0: cu(b)})
+    plan = coda.last_plan()
+    sync_ok()
+    assert plan["split"] == 0, plan
+    A = O.dequantize_mx(xq.cpu().numpy(), O.mx_scales_from_tiled(xs.cpu().numpy(), M, K))
+    B = O.dequantize_mx(wq.cpu().numpy(), O.mx_scales_from_tiled(ws_.cpu().numpy(), N, K))
+    ref = O.run_chain(A, B, ops, b_layout="nk", col_vecs={0: f64(b)})
+    assert_close(f64(r.D), ref["D"], f"mx {case}")
+    check_stats(r, ref, f"mx {case}", chain_tau(ops), K)
+    # and the whole pipeline stays within MXFP8's rounding of the bf16 product
+    exact = O.run_chain(f64(X), f64(W), ops, b_layout="nk", col_vecs={0: f64(b)})["D"]
+    assert np.linalg.norm(f64(r.D) - exact) / np.linalg.norm(exact) < 0.05
+
+
+def test_mx_rejections():
+    A = cu(torch.zeros((64, 96), dtype=torch.uint8))
+    B = cu(torch.zeros((288, 96), dtype=torch.uint8))
+    s_a = cu(torch.full((coda.mx_scale_bytes(64, 96),), 127, dtype=torch.uint8))
+    s_b = cu(torch.full((coda.mx_scale_bytes(288, 96),), 127, dtype=torch.uint8))
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):     # U half (144 rows in) not on a 128-row scale tile
+        coda.gemm_epilogue_mx(A, s_a, B, s_b, [("SWIGLU",)])
+    with pytest.raises(RuntimeError, match="UNSUPPORTED"):     # the norms read bf16 A
+        coda.gemm_epilogue_mx(A, s_a, B, s_b, [("RMS_ROWSCALE", None, 1e-6)])
+    with pytest.raises(RuntimeError, match="INVALID_ARG"):     # K not a multiple of 32
+        coda.gemm_epilogue_mx(A[:, :80].contiguous(), s_a, B[:, :80].contiguous(), s_b, [])
+
+
+def test_full_mxfp8swiglu_sampled():
+    # the SwiGLU up-projection with MXFP8 operands: X [8192, 4096] and W
+    # [22016, 4096] quantised by the library, SiLU(G) * U in the epilogue
+    t = inputs.make_swiglu()
+    X = cu(t["X"])
+    W = cu(t["W"].t().contiguous())          # [N, K]
+    M, K = X.shape
+    N = W.shape[0]
+    xq, xs = coda.quantize_mx_e4m3(X)
+    wq, ws_ = coda.quantize_mx_e4m3(W)
+    r = coda.gemm_epilogue_mx(xq, xs, wq, ws_, [("SWIGLU",)])
+    plan = coda.last_plan()
+    sync_ok()
+    assert plan["pair"] == 1 and plan["sequence"] > 0, plan
+    rows = _sampled(M, 6)
+    xq_ref, xs_ref = O.quantize_mx_e4m3(f64(t["X"][rows]))
+    np.testing.assert_array_equal(xq.cpu().numpy()[rows], xq_ref)
+    np.testing.assert_array_equal(O.mx_scales_from_tiled(xs.cpu().numpy(), M, K)[rows], xs_ref)
+    A = O.dequantize_mx(xq_ref, xs_ref)
+    B = O.dequantize_mx(wq.cpu().numpy(), O.mx_scales_from_tiled(ws_.cpu().numpy(), N, K))
+    ref = O.run_chain(A, B, [("SWIGLU",)], b_layout="nk")
+    assert_close(f64(r.D[rows]), ref["D"], "mxfp8 swiglu")
+
+
 # ------------------------------------------------------------------ dropout
 @pytest.mark.parametrize("seed", [0, 12345])
 @pytest.mark.parametrize("glu", [False, True])
@@ -1212,10 +1337,14 @@ def test_full_dgrad_sampled():
 
 
 def test_full_llama_block_chain_sampled():
-    # one layer of the stack: the input arrives with its row sums of squares
+    # One layer of the stack: the input arrives with its row sums of squares
     # (here from the library's unfused ROW_SUMSQ pass), the out-projection's
     # residual epilogue emits those of h for the MLP norm, the down-projection
-    # those of y; no call runs a pre-pass over its A operand
+    # those of y; no call runs a pre-pass over its A operand.
+    # Each call is checked elementwise against the oracle of that call on the
+    # bf16 tensors it actually read (the previous calls' GPU outputs); the
+    # block as a whole against the oracle's own chain (every call's output
+    # rounded to bf16 by the oracle) within the Frobenius bound.
     from gemm_epilogue_transformer_tmem_gb300 import workloads
     t = inputs.make_llama_block()
     td = {k: cu(v) for k, v in t.items()}
@@ -1228,53 +1357,53 @@ def test_full_llama_block_chain_sampled():
     sync_ok()
     assert launched == 6, f"{launched} launches: four GEMMs and two row-sum finishing kernels expected"
     rows = _sampled(inputs.LLAMA_BLOCK["tokens"], 4)
+    d, ffn = inputs.LLAMA_BLOCK["d"], inputs.LLAMA_BLOCK["ffn"]
+    eps = inputs.EPS_RMS
     ref = workloads_oracle_llama(t, rows, prepared=True)
-    for name in ("qkv", "h", "up"):
-        assert_close(f64(out[name][rows]), ref[name], f"llama {name}")
-    d = inputs.LLAMA_BLOCK["d"]
     X = f64(t["X"][rows])
-    assert_stat_close(f64(td["X_sumsq"][rows]), O.row_sumsq(X), 2.0 * np.sqrt(O.row_sumsq(X * X)), d, TAU_LIN, 0,
-                      "llama X sum of squares")
-    # the row sums of squares of each residual call, against the oracle of that
-    # call on the bf16 tensors it read (h's inputs are the block's own inputs;
-    # y's are the GPU's up and h)
-    assert_stat_close(f64(out["h_sumsq"][rows]), ref["h_sumsq"], ref["h_sumsq_scale"], d, TAU_LIN, d,
-                      "llama h sum of squares")
-    ffn = inputs.LLAMA_BLOCK["ffn"]
-    yo = O.run_chain(f64(out["up"][rows]), f64(t["W_down"]), [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
-                     residual_t=f64(out["h"][rows]))
-    assert_stat_close(f64(out["y_sumsq"][rows]), yo["stats"][0], yo["stat_scale"][0], d, TAU_LIN, ffn,
-                      "llama y sum of squares")
+    h_gpu, up_gpu = f64(out["h"][rows]), f64(out["up"][rows])
+    # qkv and h read the block's own inputs
+    assert_close(f64(out["qkv"][rows]), ref["qkv"], "llama qkv")
+    assert_close(h_gpu, ref["h"], "llama h")
     # h is a bf16 output that later calls read.  It is computed from exact
     # inputs, and the GPU (fp32) and oracle (fp64) values agree to ~1e-6
     # relative, so their bf16 roundings are equal except where the two straddle
     # a rounding boundary: there they are neighbours, one bf16 ulp apart.  (Near
     # zero the bf16 spacing falls below fp32's absolute accumulation error over
     # K = 4096, about 4e-6, so the ulp is taken at no less than |h| = 2^-6.)
-    g = f64(out["h"][rows])
     r = O.round_bf16(ref["h"])
-    diff = g != r
+    diff = h_gpu != r
     assert diff.mean() < 1e-2, f"h: {diff.mean():.2e} of elements differ from the rounded oracle"
     ulp = bf16_ulp(np.maximum(np.abs(r), 2.0 ** -6))
-    assert (np.abs(g - r)[diff] <= ulp[diff] * (1 + 1e-12)).all(), "h: a difference above 1 ulp"
-    # y adds h as its residual: one ulp of h on top of the bound
+    assert (np.abs(h_gpu - r)[diff] <= ulp[diff] * (1 + 1e-12)).all(), "h: a difference above 1 ulp"
+    # up reads the GPU's h (norm statistics from h as stored; weights prepared as the block does)
+    g_mlp, W_up = f64(t["gamma_mlp"]), f64(t["W_up"])
+    up_call = O.run_chain(h_gpu, O.round_bf16(g_mlp[:, None] * W_up), [("RMS_ROWSCALE", None, eps), ("SWIGLU",)],
+                          norm_gamma=np.ones_like(g_mlp))["D"]
+    assert_close(up_gpu, up_call, "llama up (on the GPU's h)")
+    # y reads the GPU's up and h
+    yo = O.run_chain(up_gpu, f64(t["W_down"]), [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual_t=h_gpu)
     y = f64(out["y"][rows])
-    bound = ATOL + RTOL * np.abs(ref["y"]) + bf16_ulp(O.round_bf16(ref["h"]))
-    bad = np.abs(y - ref["y"]) > bound
-    assert not bad.any(), (f"llama y: {bad.sum()} elements out of tolerance, worst excess "
-                           f"{(np.abs(y - ref['y']) - bound).max():.3e}, rms error "
-                           f"{np.sqrt(np.mean((y - ref['y']) ** 2)):.3e}")
-    assert np.linalg.norm(y - ref["y"]) / np.linalg.norm(ref["y"]) <= FRO
-    # against the unprepared block (gamma applied in fp64, no bf16 weight
-    # preparation): the whole-block deviation stays within the Frobenius bound
+    assert_close(y, yo["D"], "llama y (on the GPU's up and h)")
+    # the row sums of squares: the input's, and each residual call's on what it read
+    assert_stat_close(f64(td["X_sumsq"][rows]), O.row_sumsq(X), 2.0 * np.sqrt(O.row_sumsq(X * X)), d, TAU_LIN, 0,
+                      "llama X sum of squares")
+    assert_stat_close(f64(out["h_sumsq"][rows]), ref["h_sumsq"], ref["h_sumsq_scale"], d, TAU_LIN, d,
+                      "llama h sum of squares")
+    assert_stat_close(f64(out["y_sumsq"][rows]), yo["stats"][0], yo["stat_scale"][0], d, TAU_LIN, ffn,
+                      "llama y sum of squares")
+    # the whole block against the oracle's own chain, prepared weights and
+    # unprepared (gamma applied in fp64 to the activations, no bf16 weight
+    # preparation): within the Frobenius bound; elementwise excess reported
     ref0 = workloads_oracle_llama(t, rows, prepared=False)
-    for name in ("qkv", "up", "y"):
-        got = f64(out[name][rows])
-        fro0 = np.linalg.norm(got - ref0[name]) / np.linalg.norm(ref0[name])
-        over = np.abs(got - ref0[name]) > ATOL + RTOL * np.abs(ref0[name])
-        print(f"llama {name} against the unprepared oracle: {int(over.sum())} of {over.size} sampled elements over "
-              f"the elementwise bound, relative Frobenius {fro0:.3e}")
-        assert fro0 <= FRO, name
+    for tag, rr in (("prepared", ref), ("unprepared", ref0)):
+        for name in ("qkv", "up", "y"):
+            got = f64(out[name][rows])
+            fro = np.linalg.norm(got - rr[name]) / np.linalg.norm(rr[name])
+            over = np.abs(got - rr[name]) > ATOL + RTOL * np.abs(rr[name])
+            print(f"llama {name} against the {tag} oracle chain: {int(over.sum())} of {over.size} sampled elements "
+                  f"over the elementwise bound, relative Frobenius {fro:.3e}")
+            assert fro <= FRO, (tag, name)
 
 
 def bf16_ulp(v):

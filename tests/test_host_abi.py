@@ -265,3 +265,32 @@ def test_tuning_knobs_round_trip(L):
         coda.set_raster("diagonal", 1)
     with pytest.raises(ValueError):
         coda.set_tile_scheduler("round-robin")
+
+
+def test_mx_scale_bytes_and_validation(L):
+    # tiled scale storage: 512 bytes per 128 rows and 128 elements of K
+    assert coda.mx_scale_bytes(128, 128) == 512
+    assert coda.mx_scale_bytes(129, 160) == 2 * 2 * 512
+    assert coda.mx_scale_bytes(0, 128) == 0
+    e = coda.make_epilogue([("SWIGLU",)])
+    a = coda.CodaAux()
+    # SwiGLU whose U half does not start on a 128-row scale tile (N/2 = 144)
+    st = L.coda_gemm_epilogue_mx(0x1000, 0x2000, 0x3000, 0x4000, 64, 288, 128, ctypes.byref(e), ctypes.byref(a),
+                                 0x5000, None, None, None, 0, None)
+    assert coda.STATUS[st] == "CODA_ERR_UNSUPPORTED"
+    # K not a multiple of 32
+    e0 = coda.make_epilogue([])
+    st = L.coda_gemm_epilogue_mx(0x1000, 0x2000, 0x3000, 0x4000, 64, 256, 80, ctypes.byref(e0), ctypes.byref(a),
+                                 0x5000, None, None, None, 0, None)
+    assert coda.STATUS[st] == "CODA_ERR_INVALID_ARG"
+    # the commuted norms read bf16 A
+    en = coda.make_epilogue([("RMS_ROWSCALE", None, 1e-6)])
+    st = L.coda_gemm_epilogue_mx(0x1000, 0x2000, 0x3000, 0x4000, 64, 256, 128, ctypes.byref(en), ctypes.byref(a),
+                                 0x5000, None, None, None, 0, None)
+    assert coda.STATUS[st] == "CODA_ERR_UNSUPPORTED"
+    # missing scales
+    st = L.coda_gemm_epilogue_mx(0x1000, None, 0x3000, 0x4000, 64, 256, 128, ctypes.byref(e0), ctypes.byref(a),
+                                 0x5000, None, None, None, 0, None)
+    assert coda.STATUS[st] == "CODA_ERR_INVALID_ARG"
+    # the quantiser wants K % 32 == 0
+    assert coda.STATUS[L.coda_quantize_mx_e4m3(0x1000, 4, 48, 0x2000, 0x3000, None)] == "CODA_ERR_INVALID_ARG"
