@@ -647,7 +647,8 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   }
   c.prog.num_rb = static_cast<int32_t>((M + 31) / 32);
   p.epi_warp_bytes = static_cast<uint32_t>(2 * kBoxBytes + c.n_aux * 2 * kBoxBytes);
-  const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * p.epi_warp_bytes;
+  // MX kernels run two epilogue warp groups (even and odd chunks), each warp with its own staging
+  const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * (mx ? kMaxEpiGroups : 1) * p.epi_warp_bytes;
   const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
   const size_t fixed = 1024 + epi_bytes + ctl_bytes;
   const size_t stage_bytes = (pair ? kPairStageBytes : kStageBytes) + (mx ? kMxStageSFBytes : 0);
@@ -736,7 +737,7 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   // cluster) to +3% (skinny, 1 tile; lnproj) and -0.4% on grids of ~36 tiles per
   // cluster (swiglu), where the last tile's epilogue is a small share of the run
   const int64_t tiles_per_cluster = (g.num_tiles + grid / csize - 1) / (grid / csize);
-  p.helpers = (g_tail_helpers.load() != 0 && !split && p.clc == 0 && c.n_aux == 0 && !rowstat_warps &&
+  p.helpers = (g_tail_helpers.load() != 0 && !mx && !split && p.clc == 0 && c.n_aux == 0 && !rowstat_warps &&
                g.num_kb > 0 && tiles_per_cluster <= 16) ? 1 : 0;
   int seq = match_sequence(epi, c.glu);
   auto launch = [&](int sq) {

@@ -255,13 +255,19 @@ struct SmemAux {
 // (tcgen05.cp) ahead of the stage's four MMAs.  The scales need tensor-memory
 // columns, so the MX kernel keeps one accumulator (256 columns) instead of two.
 template <bool kGLU, bool kBMN, bool kRowStats, bool kPair, class Epi, bool kAMN, bool kFP8, bool kMX = false>
-__global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
+__global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
     coda_gemm_epilogue_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                               const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmX0,
                               const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
                               const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                               const __grid_constant__ GemmParams p) {
   static_assert(!kMX || kFP8, "MX operands are 8-bit");
+  static_assert(!(kMX && kRowStats), "MX kernels have no row-statistics warps");
+  // epilogue warp groups: MX kernels, whose one accumulator holds the next
+  // tile's MMAs back until it is drained, run two groups of four warps (warps
+  // 4-7 take the even chunks, 8-11 the odd ones); the others one group
+  constexpr int kEpiGroups = kMX ? 2 : 1;
+  constexpr int kEpiW = kEpiWarps * kEpiGroups;
   // Per-CTA tile geometry.  A CTA pair shares one 256-row tile: rank r of the
   // pair owns rows r*128 .. r*128+127 of it and stages half of B.
   constexpr int kTileM = kPair ? 2 * BM : BM;
@@ -283,8 +289,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0u;
-  // split-K grids run the single-CTA kernel without row-statistics warps
-  const bool split = !kPair && !kRowStats && p.split != 0;
+  // split-K grids run the single-CTA kernel without row-statistics warps (and
+  // never with MX operands)
+  const bool split = !kPair && !kRowStats && !kMX && p.split != 0;
   const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
@@ -296,12 +303,14 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&ctl->tfull[a], 1);
-      mbar_init(&ctl->tempty[a], kPair ? 256 : 128);
+      mbar_init(&ctl->tempty[a], (kPair ? 256 : 128) * kEpiGroups);
       mbar_init(&ctl->rsfull[a], 128);
       mbar_init(&ctl->rsempty[a], 128);
     }
-    for (int q = 0; q < kEpiWarps; ++q)
+    for (int q = 0; q < kEpiW; ++q)
       for (int b = 0; b < 2; ++b) mbar_init(&ctl->auxfull[q][b], 1);
+    for (int b = 0; b < 2; ++b)
+      for (int q = 0; q < kEpiWarps; ++q) mbar_init(&ctl->gfull[b][q], 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->esync, kEpiWarps);
     for (int q = 0; q < kEpiWarps; ++q) mbar_init(&ctl->helpdone[q], 1);
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       mbar_init(&ctl->sched_full[s], 1);
       // tile-walking roles: the producers, the MMA issuer and the epilogue warps
       // of the cluster (the row-statistics variant runs in static order)
-      mbar_init(&ctl->sched_empty[s], kPair ? 2 + 1 + 2 * kEpiWarps : 1 + 1 + kEpiWarps);
+      mbar_init(&ctl->sched_empty[s], kPair ? 2 + 1 + 2 * kEpiW : 1 + 1 + kEpiW);
     }
     ctl->abort_flag = 0u;
     fence_mbar_init();
@@ -584,12 +593,14 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         }
       }
     }
-  } else if (warp >= 4 && warp < 4 + kEpiWarps) {
+  } else if (warp >= 4 && warp < 4 + kEpiW) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp - 4;
+    const int ew = warp - 4;             // epilogue warp index (staging, aux barriers)
+    const int q = ew & (kEpiWarps - 1);  // tensor-memory lane quarter
+    const int grp = ew / kEpiWarps;      // chunk group: chunks c with c % kEpiGroups == grp
     const Waiter W{ctl, p.timeout_ns, p.err, ROLE_EPILOGUE};
     constexpr int kOutCols = kGLU ? BN / 2 : BN;
-    uint8_t* wbase = smem + p.smem_epi_off + q * p.epi_warp_bytes;
+    uint8_t* wbase = smem + p.smem_epi_off + ew * p.epi_warp_bytes;
     uint8_t* out_stage = wbase;
     uint8_t* aux_stage = wbase + 2 * kBoxBytes;
     const int n_aux = p.n_aux;
@@ -607,7 +618,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
     auto issue_aux = [&](int b, int col, int row0) {
       __syncwarp();
       if (lane == 0) {
-        uint64_t* bar = &ctl->auxfull[q][b];
+        uint64_t* bar = &ctl->auxfull[ew][b];
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_aux * kBoxBytes));
         tma_load_2d_hint(aux_stage + (0 * 2 + b) * kBoxBytes, &tmX0, bar, col, row0, stream_policy);
         if (n_aux > 1) tma_load_2d_hint(aux_stage + (1 * 2 + b) * kBoxBytes, &tmX1, bar, col, row0, stream_policy);
@@ -645,7 +656,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       const uint32_t acc_phase = acc_parity<kMX>(local);
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       const bool partial = split && !(w.kb0 == 0 && w.kb1 == p.num_kb);
-      if (n_aux > 0 && !partial) issue_aux(abuf, col_base, m0 + q * 32);
+      if (n_aux > 0 && !partial && grp < nch) issue_aux(abuf, col_base + grp * kChunk, m0 + q * 32);
 
       bool okw = warp_wait(W, &ctl->tfull[acc], acc_phase, tile, lane);
       if (!okw) {
@@ -747,12 +758,12 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       float red0[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       float red1[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t keep = 0;
-      for (int c = 0; c < nch; ++c) {
+      for (int c = grp; c < nch; c += kEpiGroups) {
         if (helped && (c & 1)) continue;
         const int col = col_base + c * kChunk;
         if (n_aux > 0) {
-          if (c + 1 < nch) issue_aux(abuf ^ 1, col + kChunk, m0 + q * 32);
-          okw = warp_wait(W, &ctl->auxfull[q][abuf], (aux_phase >> abuf) & 1u, tile, lane);
+          if (c + kEpiGroups < nch) issue_aux(abuf ^ 1, col + kEpiGroups * kChunk, m0 + q * 32);
+          okw = warp_wait(W, &ctl->auxfull[ew][abuf], (aux_phase >> abuf) & 1u, tile, lane);
           if (!okw) {
             ok = false;
             break;
@@ -796,8 +807,9 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
             }
           }
         }
-        if (c == nch - 1 && src_tmem) {
-          // accumulator drained: release it to the MMA warp (the leader's barrier)
+        if (c + kEpiGroups >= nch && src_tmem) {
+          // this group's last chunk of the accumulator is in registers: release
+          // it to the MMA warp (the leader's barrier)
           tc_fence_before_sync();
           if constexpr (kPair)
             mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0u));
@@ -843,6 +855,40 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
         if (n_aux > 0) abuf ^= 1;
       }
       if (!ok) break;
+      if (kEpiGroups > 1 && grp >= nch && src_tmem) {
+        // a group with no chunk in this tile releases the accumulator all the same
+        tc_fence_before_sync();
+        if constexpr (kPair)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0u));
+        else
+          mbar_arrive(&ctl->tempty[acc]);
+      }
+      if (kEpiGroups > 1 && (p.prog.n_red > 0 || p.ws_keep != nullptr)) {
+        // the odd-chunk group hands its row partials and keep counts to the
+        // even-chunk group of its lane quarter, in the slot of the tile's
+        // parity: the group can be at most one tile ahead (the accumulator
+        // of the tile after next needs the even group's release, which comes
+        // after the even group read this slot)
+        const int slot = local & 1;
+        if (grp == 1) {
+#pragma unroll
+          for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->gred[slot][q][r][lane] = red1[r];
+          ctl->gkeep[slot][q][lane] = keep;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->gfull[slot][q]);
+          continue;
+        }
+        if (!warp_wait(W, &ctl->gfull[slot][q], static_cast<uint32_t>((local >> 1) & 1), tile, lane)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
+          if (r < p.prog.n_red) red1[r] = ctl->gred[slot][q][r][lane];
+        keep += ctl->gkeep[slot][q][lane];
+      } else if (kEpiGroups > 1 && grp == 1) {
+        continue;
+      }
       if (helped && (p.prog.n_red > 0 || p.ws_keep != nullptr)) {
         if (!warp_wait(W, &ctl->helpdone[q], 0u, tile, lane)) {
           ok = false;
@@ -870,7 +916,7 @@ __global__ void __launch_bounds__(kRowStats ? 384 : 256, 1)
       bulk_wait_group<0>();
       if (!ok) {
         for (int b = 0; b < 2; ++b)
-          if (aux_armed & (1u << b)) wait_drain(&ctl->auxfull[q][b], (aux_phase >> b) & 1u, 2000000ull);
+          if (aux_armed & (1u << b)) wait_drain(&ctl->auxfull[ew][b], (aux_phase >> b) & 1u, 2000000ull);
       }
     }
     __syncwarp();
@@ -1058,7 +1104,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
   const bool after_prepass = p.rms_vec != nullptr && !p.rms_from_sumsq;
   if constexpr (!kPair) {
     if (!after_prepass) {
-      kern<<<grid, kRowStats ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
+      kern<<<grid, (kRowStats || kMX) ? 384 : 256, smem, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6],
                                                        maps[7], p);
       return cudaGetLastError();
     }
@@ -1066,7 +1112,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
     // the epilogue waits
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kRowStats ? 384 : 256, 1, 1);
+    cfg.blockDim = dim3((kRowStats || kMX) ? 384 : 256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -1079,7 +1125,7 @@ cudaError_t launch_gemm_t(const CUtensorMap* maps, const GemmParams& p, int grid
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(kRowStats ? 384 : 256, 1, 1);
+    cfg.blockDim = dim3((kRowStats || kMX) ? 384 : 256, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];

@@ -18,7 +18,8 @@ constexpr int BK = 64;
 constexpr int UMMA_K = 16;
 constexpr int kAccCols = 256;      // TMEM columns per accumulator buffer
 constexpr int kTmemCols = 512;     // two accumulator buffers
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 4;        // epilogue warps per group (one per tensor-memory lane quarter)
+constexpr int kMaxEpiGroups = 2;    // MX kernels: two groups, even and odd chunks
 constexpr int kChunk = 32;         // epilogue columns per TMEM load / TMA store box
 constexpr int kStageABytes = BM * BK * 2;          // 16 KB
 constexpr int kStageBBytes = BN * BK * 2;          // 32 KB
@@ -130,7 +131,7 @@ struct Ctl {
   uint64_t tempty[2];
   uint64_t rsfull[2];
   uint64_t rsempty[2];
-  uint64_t auxfull[kEpiWarps][2];
+  uint64_t auxfull[kMaxEpiGroups * kEpiWarps][2];
   uint64_t drain;
   uint64_t esync;          // the four epilogue warps meet here on split tiles (one arrival each)
   uint32_t eflag[2];       // flag broadcast through esync, by phase parity
@@ -140,6 +141,11 @@ struct Ctl {
   uint64_t helpdone[kEpiWarps];                           // a helper warp's row partials are in place
   float hred[kEpiWarps][CODA_MAX_REDUCTIONS][32];         // helper row-reduction partials (last tile)
   uint32_t hkeep[kEpiWarps][32];                          // helper dropout keep counts (last tile)
+  // two epilogue groups (MX kernels): the odd-chunk group's row partials and
+  // keep counts of a tile, handed to the even-chunk group, by tile parity
+  uint64_t gfull[2][kEpiWarps];
+  float gred[2][kEpiWarps][CODA_MAX_REDUCTIONS][32];
+  uint32_t gkeep[2][kEpiWarps][32];
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];

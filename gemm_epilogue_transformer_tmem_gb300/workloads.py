@@ -45,6 +45,11 @@ class Step:
     # roofline of the dominant call is measured on that call alone
     parts: Optional[list] = None
     parts_bytes: dict = field(default_factory=dict)    # name -> algorithmic DRAM bytes of that call
+    # end to end with host buffers: (h_in, h_out) -> None runs one step copying
+    # h_in[name] into host_inputs[name] first and host_outputs[name] into
+    # h_out[name] last; a step may overlap those copies with its own calls
+    # (side streams, ordered by events).  None: copy in, step, copy out.
+    e2e: Optional[Callable[[dict, dict], None]] = None
 
 
 def _ws(M, N, K, ops, dev):
@@ -155,14 +160,18 @@ def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Ste
 def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step:
     """up = silu(r G) * (r U), [G|U] = X @ (gamma (.) W): commuted RMSNorm into the
     SwiGLU up-projection at a decode-sized batch.  The 180 MB weight stream
-    bounds it, so its roofline is HBM bandwidth."""
+    bounds it, so its roofline is HBM bandwidth.  As in the LLaMA block, X is
+    the hidden state the out-projection's residual epilogue wrote, and it
+    arrives with its row sums of squares (that epilogue's ROW_SUMSQ), so the
+    norm needs no pass over X."""
     t = t or inputs.make_skinny(seed, M, K, N_out)
     X, g, W = (t[k].to(dev) for k in ("X", "gamma", "W"))
+    x_ss = row_sumsq(X)
     N = 2 * N_out
     Wf = torch.empty_like(W)
     prep = lambda: coda.fold_gamma(W, g, "kn", out=Wf)   # noqa: E731
     prep()
-    ops = [("RMS_ROWSCALE", None, inputs.EPS_RMS), ("SWIGLU",)]
+    ops = [("RMS_SUMSQ_ROWSCALE", 0, inputs.EPS_RMS), ("SWIGLU",)]
     D = torch.empty((M, N_out), dtype=torch.bfloat16, device=dev)
     ws, _ = _ws(M, N, K, ops, dev)
     Xn = torch.empty_like(X)
@@ -170,7 +179,7 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
     Du = torch.empty_like(D)
 
     def fused():
-        coda.gemm_epilogue(X, Wf, ops, out=D, workspace=ws)
+        coda.gemm_epilogue(X, Wf, ops, row_vecs={0: x_ss}, out=D, workspace=ws)
 
     def unfused():
         coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn)
@@ -179,9 +188,10 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
 
     library = lambda: torch.matmul(X, Wf, out=C)   # noqa: E731
 
-    fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16
+    fb = M * K * BF16 + M * F32 + K * N * BF16 + M * N_out * BF16
     ub = (2 * M * K * BF16 + K * BF16) + (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16
-    return Step("skinny", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
+    return Step("skinny", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X, X_sumsq=x_ss),
+                host_outputs=dict(D=D),
                 bound="hbm", kernels_per_fused=1, kernels_per_unfused=3, prep=prep,
                 outputs=dict(D=D, D_unfused=Du), library=library)
 
@@ -435,6 +445,41 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
     act = T * d * BF16
     rowvec = T * F32
 
+    # end to end: the inputs' host-to-device copies and the outputs' read-back
+    # on two side streams, overlapped with the block's calls: attn_out arrives
+    # while the qkv projection runs, qkv is read back while the other three run
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e(h_in, h_out):
+        main = torch.cuda.current_stream(dev)
+        s_in.wait_stream(main)
+        with torch.cuda.stream(s_in):
+            t["X"].copy_(h_in["X"], non_blocking=True)
+            t["X_sumsq"].copy_(h_in["X_sumsq"], non_blocking=True)
+            x_in = torch.cuda.Event()
+            x_in.record(s_in)
+            t["attn_out"].copy_(h_in["attn_out"], non_blocking=True)
+            a_in = torch.cuda.Event()
+            a_in.record(s_in)
+        main.wait_event(x_in)
+        calls[0][1]()                  # qkv
+        q_done = torch.cuda.Event()
+        q_done.record(main)
+        main.wait_event(a_in)
+        for _, call in calls[1:]:      # out-projection, up, down
+            call()
+        y_done = torch.cuda.Event()
+        y_done.record(main)
+        s_out.wait_event(q_done)
+        with torch.cuda.stream(s_out):
+            h_out["qkv"].copy_(out["qkv"], non_blocking=True)
+            s_out.wait_event(y_done)
+            h_out["y"].copy_(out["y"], non_blocking=True)
+            h_out["y_sumsq"].copy_(out["y_sumsq"], non_blocking=True)
+        main.wait_stream(s_out)
+        # the next step may overwrite the inputs only after this one read them
+        main.wait_stream(s_in)
+
     def library():
         torch.matmul(t["X"], prepared["W_qkv"], out=un["qkv"])
         torch.matmul(t["attn_out"], t["W_o"], out=un["c_o"])
@@ -453,7 +498,7 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
                 host_inputs=dict(X=t["X"], X_sumsq=t["X_sumsq"], attn_out=t["attn_out"]),
                 host_outputs=dict(y=out["y"], y_sumsq=out["y_sumsq"], qkv=out["qkv"]), kernels_per_fused=6,
                 kernels_per_unfused=9, prep=prep, outputs=out, library=library,
-                parts=[(name, call, part_flops[name]) for name, call in calls], parts_bytes=part_bytes)
+                parts=[(name, call, part_flops[name]) for name, call in calls], parts_bytes=part_bytes, e2e=e2e)
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,

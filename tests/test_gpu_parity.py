@@ -800,9 +800,13 @@ def test_mx_gemm_epilogue(case, mode):
     ref = O.run_chain(A, B, ops, b_layout="nk", col_vecs={0: f64(b)})
     assert_close(f64(r.D), ref["D"], f"mx {case}")
     check_stats(r, ref, f"mx {case}", chain_tau(ops), K)
-    # and the whole pipeline stays within MXFP8's rounding of the bf16 product
+    # and the whole pipeline stays within MXFP8's rounding of the bf16 product:
+    # E4M3 rounds each operand element by up to 2^-4 relative (rms 2^-4/sqrt 3,
+    # 3.6%), so a dot product of two quantised operands carries about 5% rms
+    # relative error; the SwiGLU gate multiplies two such products (about 7%)
     exact = O.run_chain(f64(X), f64(W), ops, b_layout="nk", col_vecs={0: f64(b)})["D"]
-    assert np.linalg.norm(f64(r.D) - exact) / np.linalg.norm(exact) < 0.05
+    lim = 0.09 if case == "swiglu" else 0.065
+    assert np.linalg.norm(f64(r.D) - exact) / np.linalg.norm(exact) < lim
 
 
 def test_mx_rejections():
@@ -1250,22 +1254,31 @@ def test_split_k_plan_and_segments():
         coda.set_cta_pair("auto")
 
 
-@pytest.mark.parametrize("split", ["auto", "force"])
+@pytest.mark.parametrize("split", ["auto", "force", "sumsq"])
 def test_full_skinny_sampled(split):
-    # the decode-sized up-projection: 86 tiles on one CTA each (automatic), and
-    # split over K across all SMs (forced)
+    # the decode-sized up-projection: 86 tiles on one CTA each (automatic), split
+    # over K across all SMs (forced), and with the input's row sums of squares
+    # supplied (as the benchmark runs it: no pre-pass)
     w = inputs.WORKLOADS["skinny"]
     t = inputs.make_skinny()
     Wf = coda.fold_gamma(cu(t["W"]), cu(t["gamma"]), "kn")
     ops = [("RMS_ROWSCALE", 0, inputs.EPS_RMS), ("SWIGLU",)]
-    coda.set_split_k(split)
+    coda.set_split_k("auto" if split == "sumsq" else split)
     try:
-        r = coda.gemm_epilogue(cu(t["X"]), Wf, ops)
+        if split == "sumsq":
+            from gemm_epilogue_transformer_tmem_gb300 import workloads
+            X = cu(t["X"])
+            rs = torch.empty((1, w.M), dtype=torch.float32, device="cuda")
+            r = coda.gemm_epilogue(X, Wf, [("RMS_SUMSQ_ROWSCALE", 0, inputs.EPS_RMS), ("SWIGLU",)],
+                                   row_vecs={0: workloads.row_sumsq(X)}, row_stats=rs)
+        else:
+            r = coda.gemm_epilogue(cu(t["X"]), Wf, ops)
         plan = coda.last_plan()
         sync_ok()
     finally:
         coda.set_split_k("auto")
-    assert plan["prepass"] == 1 and plan["split"] == (1 if split == "force" else 0), plan
+    assert plan["prepass"] == (0 if split == "sumsq" else 1), plan
+    assert plan["split"] == (1 if split == "force" else 0), plan
     if split == "force":
         assert plan["grid"] > plan["tiles"], plan
     assert r.D.shape == (w.M, w.N // 2)
@@ -1278,7 +1291,8 @@ def test_full_skinny_sampled(split):
     g, W = f64(t["gamma"]), f64(t["W"])
     ref = O.run_chain(f64(t["X"]), O.round_bf16(g[:, None] * W), ops, norm_gamma=np.ones_like(g))
     assert_close(f64(r.D), ref["D"], "skinny")
-    assert_close(f64(r.row_stats[0]), ref["stats"][0], "skinny r")
+    if split != "sumsq":     # with supplied sums r is not written out
+        assert_close(f64(r.row_stats[0]), ref["stats"][0], "skinny r")
     ref0 = O.run_chain(f64(t["X"]), W, ops, norm_gamma=g)
     got = f64(r.D)
     fro0 = np.linalg.norm(got - ref0["D"]) / np.linalg.norm(ref0["D"])
