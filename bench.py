@@ -321,6 +321,9 @@ def main():
     ap.add_argument("--raster", default="auto", choices=["auto", "rows", "cols"],
                     help="tile order of the persistent grid (library knob; default auto)")
     ap.add_argument("--raster-group", type=int, default=0, help="blocks per raster group (0: the library's)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="llama only: tokens per step (default 16384); smaller values make the small cases an "
+                         "ncu capture needs")
     ap.add_argument("--profile-steps", action="store_true",
                     help="one fused and one unfused step between L2 flushes, for an ncu capture; no JSON line")
     args = ap.parse_args()
@@ -350,7 +353,10 @@ def main():
     coda.set_raster(args.raster, args.raster_group)
 
     dev = torch.device("cuda", local)
-    step = workloads.BUILDERS[args.workload](dev=dev)
+    if args.tokens is not None and args.workload != "llama":
+        raise SystemExit("--tokens applies to the llama workload only")
+    step = (workloads.BUILDERS[args.workload](dev=dev) if args.tokens is None
+            else workloads.build_llama(dev=dev, tokens=args.tokens))
     stream = torch.cuda.current_stream()
     # L2 flush between steps: write a buffer larger than L2, then read another
     # one, so the timed step starts with a cold L2 that holds no dirty lines
@@ -501,7 +507,9 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}", "flops_per_step": step.flops,
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}" +
+                               (f" (run at {args.tokens} tokens, not 16384)" if args.tokens else ""),
+                   "flops_per_step": step.flops,
                    "l2": "flushed between steps outside the timed events: a 256 MiB device write, then a "
                          "256 MiB read, so no dirty lines are written back inside the timed region",
                    "parallelism": "replicas" if world > 1 else "single GPU",

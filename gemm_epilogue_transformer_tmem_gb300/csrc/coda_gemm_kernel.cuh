@@ -758,23 +758,103 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       float red0[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       float red1[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t keep = 0;
-      for (int c = grp; c < nch; c += kEpiGroups) {
-        if (helped && (c & 1)) continue;
+      // Aux tiles of chunk c: prefetch the group's next chunk, wait for this one.
+      auto aux_step = [&](int c) -> bool {
+        if (n_aux == 0) return true;
         const int col = col_base + c * kChunk;
-        if (n_aux > 0) {
-          if (c + kEpiGroups < nch) issue_aux(abuf ^ 1, col + kEpiGroups * kChunk, m0 + q * 32);
-          okw = warp_wait(W, &ctl->auxfull[ew][abuf], (aux_phase >> abuf) & 1u, tile, lane);
-          if (!okw) {
+        if (c + kEpiGroups < nch) issue_aux(abuf ^ 1, col + kEpiGroups * kChunk, m0 + q * 32);
+        if (!warp_wait(W, &ctl->auxfull[ew][abuf], (aux_phase >> abuf) & 1u, tile, lane)) return false;
+        aux_phase ^= 1u << abuf;
+        aux_armed &= ~(1u << abuf);
+        return true;
+      };
+      // The op list on chunk c's accumulator values, the row reductions kept by
+      // chunk parity, and the bf16 store of the chunk.
+      auto epi_chunk = [&](int c, float(&v)[32], float(&u)[32]) {
+        const int col = col_base + c * kChunk;
+        int nvalid = p.N_out - col;
+        if (nvalid > kChunk) nvalid = kChunk;
+        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
+        const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
+        if constexpr (kRowStats) {   // never helped: one running sum
+          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red0, keep);
+        } else {
+          float cred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
+          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, cred, keep);
+          if (c & 1) {
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red1[r] += cred[r];
+          } else {
+#pragma unroll
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red0[r] += cred[r];
+          }
+        }
+
+        // stage bf16 row chunk (64-byte swizzle) and TMA-store the 32x32 box
+        uint8_t* ob = out_stage + sbuf * kBoxBytes;
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        {
+          uint8_t* rowp = ob + lane * 64;
+          const int sw = (lane >> 1) & 3;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = pack8(v + 8 * cc);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d_hint(&tmD, ob, col, m0 + q * 32, stream_policy);
+          bulk_commit_group();
+        }
+        sbuf ^= 1;
+        if (n_aux > 0) abuf ^= 1;
+      };
+
+      if constexpr (kMX) {
+        // One accumulator: the next tile's MMAs wait for its release.  Load all
+        // of this group's chunks (two of SwiGLU's G/U pairs, or four plain
+        // chunks; columns past the matrix edge hold zero products and are not
+        // stored) in one round trip, release, then work from registers.
+        float pv[4][32];
+        if constexpr (kGLU)
+          tmem_ld32x4(t_row + grp * kChunk, t_row + BN / 2 + grp * kChunk, t_row + (grp + 2) * kChunk,
+                      t_row + BN / 2 + (grp + 2) * kChunk, pv);
+        else
+          tmem_ld32x4(t_row + grp * kChunk, t_row + (grp + 2) * kChunk, t_row + (grp + 4) * kChunk,
+                      t_row + (grp + 6) * kChunk, pv);
+        tc_fence_before_sync();
+        if constexpr (kPair)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0u));
+        else
+          mbar_arrive(&ctl->tempty[acc]);
+        constexpr int kPer = kGLU ? 2 : 4;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+          const int c = grp + i * kEpiGroups;
+          if (c >= nch) break;
+          if (!aux_step(c)) {
             ok = false;
             break;
           }
-          aux_phase ^= 1u << abuf;
-          aux_armed &= ~(1u << abuf);
+          if constexpr (kGLU)
+            epi_chunk(c, pv[2 * i], pv[2 * i + 1]);
+          else
+            epi_chunk(c, pv[i], pv[i]);
+        }
+      } else {
+      for (int c = grp; c < nch; c += kEpiGroups) {
+        if (helped && (c & 1)) continue;
+        if (!aux_step(c)) {
+          ok = false;
+          break;
         }
         float v[32], u[32];
         if (p.num_kb > 0 && src_tmem) {
-          tmem_ld32(t_row + c * kChunk, v);
-          if (kGLU) tmem_ld32(t_row + BN / 2 + c * kChunk, u);
+          if constexpr (kGLU)
+            tmem_ld32x2(t_row + c * kChunk, v, t_row + BN / 2 + c * kChunk, u);
+          else
+            tmem_ld32(t_row + c * kChunk, v);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -816,46 +896,11 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
           else
             mbar_arrive(&ctl->tempty[acc]);
         }
-        int nvalid = p.N_out - col;
-        if (nvalid > kChunk) nvalid = kChunk;
-        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
-        const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
-        if constexpr (kRowStats) {   // never helped: one running sum
-          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red0, keep);
-        } else {
-          float cred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
-          Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, cred, keep);
-          if (c & 1) {
-#pragma unroll
-            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red1[r] += cred[r];
-          } else {
-#pragma unroll
-            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) red0[r] += cred[r];
-          }
-        }
-
-        // stage bf16 row chunk (64-byte swizzle) and TMA-store the 32x32 box
-        uint8_t* ob = out_stage + sbuf * kBoxBytes;
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-        {
-          uint8_t* rowp = ob + lane * 64;
-          const int sw = (lane >> 1) & 3;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(rowp + ((cc ^ sw) << 4)) = pack8(v + 8 * cc);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d_hint(&tmD, ob, col, m0 + q * 32, stream_policy);
-          bulk_commit_group();
-        }
-        sbuf ^= 1;
-        if (n_aux > 0) abuf ^= 1;
+        epi_chunk(c, v, u);
+      }
       }
       if (!ok) break;
-      if (kEpiGroups > 1 && grp >= nch && src_tmem) {
+      if (kEpiGroups > 1 && !kMX && grp >= nch && src_tmem) {
         // a group with no chunk in this tile releases the accumulator all the same
         tc_fence_before_sync();
         if constexpr (kPair)
@@ -1034,8 +1079,10 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
           for (int c = 1; c < nch; c += 2) {
             const int col = col_base + c * kChunk;
             float v[32], u[32];
-            tmem_ld32(t_row + c * kChunk, v);
-            if (kGLU) tmem_ld32(t_row + BN / 2 + c * kChunk, u);
+            if constexpr (kGLU)
+              tmem_ld32x2(t_row + c * kChunk, v, t_row + BN / 2 + c * kChunk, u);
+            else
+              tmem_ld32(t_row + c * kChunk, v);
             int nvalid = p.N_out - col;
             if (nvalid > kChunk) nvalid = kChunk;
             const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
