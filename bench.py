@@ -419,6 +419,20 @@ def main():
                    "unit": UNIT, "kernels_per_step": u_launched / u_steps,
                    "speedup_fused": round(u_ms / ms, 3)}
 
+    # ---- the same unfused chain with cuBLAS's GEMM (torch.matmul) in place of the library's own
+    unfused_lib = None
+    if not args.no_unfused and not args.no_library and step.unfused_library is not None and rank == 0:
+        try:
+            ul_steps = max(steps // 2, 3)
+            _, ul_total, _ = timed_loop([step.unfused_library], ul_steps, warmup, flush, stream)
+            ul_ms = ul_total / ul_steps
+            unfused_lib = {"what": "the unfused chain with torch.matmul (cuBLAS) for its GEMMs, the library's "
+                                   "separate kernels for the other steps",
+                           "ms_per_step": round(ul_ms, 5), "value": round(step.flops / (ul_ms * 1e-3) / 1e12, 2),
+                           "unit": UNIT, "speedup_fused": round(ul_ms / ms, 3)}
+        except RuntimeError as exc:
+            unfused_lib = {"unavailable": str(exc).splitlines()[0][:200]}
+
     # ---- the step's GEMMs alone through torch.matmul (cuBLAS): a reference point
     library = None
     if not args.no_library and step.library is not None and rank == 0:
@@ -521,6 +535,7 @@ def main():
                        "unfused_measured": traffic.get("unfused_step_bytes") if traffic else None,
                        "measured_by": traffic.get("source") if traffic else None},
         "unfused": unfused,
+        "unfused_cublas": unfused_lib,
         "library_gemm": library,
         "e2e": e2e,
         "gpu_launches": int(launches),

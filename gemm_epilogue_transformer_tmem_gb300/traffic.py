@@ -21,6 +21,10 @@ kernels' reads and writes plus that pass's writes.
 
     python -m gemm_epilogue_transformer_tmem_gb300.traffic W traffic.csv \\
         [--json profiles/traffic.json] [--md profiles/dram_traffic_W.md] [--command "..."]
+
+With --launches the CSV is a plain launch list (gpu__time_duration.sum of every
+launch of a bench run) and the output is each kernel's launches, total time and
+share of the total.
 """
 from __future__ import annotations
 
@@ -158,6 +162,26 @@ def summarize(workload: str, launches: list[dict], command: str = "") -> tuple[d
     return entry, "\n".join(out) + "\n"
 
 
+def launch_shares(launches: list[dict], command: str = "") -> str:
+    """Per kernel (name without its argument list): launches, total time, share."""
+    agg: dict[str, list] = {}
+    for k in launches:
+        nm = k["name"].split("(")[0]
+        a = agg.setdefault(nm, [0, 0.0])
+        a[0] += 1
+        a[1] += k["us"]
+    total = sum(v[1] for v in agg.values()) or 1.0
+    out = ["# Launch list (ncu gpu__time_duration.sum; cold-cache, serialised: compare shares)", ""]
+    if command:
+        out += ["Command (one GB300; the same command exited 0 without ncu just before):", "", "```", command, "```", ""]
+    out += ["| kernel | launches | total us | share |", "|---|---|---|---|"]
+    for nm, (n, us) in sorted(agg.items(), key=lambda kv: -kv[1][1]):
+        short = nm if len(nm) < 100 else nm[:97] + "..."
+        out.append(f"| `{short}` | {n} | {us:.1f} | {100.0 * us / total:.1f}% |")
+    out.append(f"| **all** | {sum(v[0] for v in agg.values())} | {total:.1f} | 100% |")
+    return "\n".join(out) + "\n"
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("workload")
@@ -165,9 +189,18 @@ def main(argv=None) -> int:
     ap.add_argument("--json", help="traffic.json to update with this workload's entry")
     ap.add_argument("--md", help="markdown summary to write")
     ap.add_argument("--command", default="", help="the ncu command line, recorded in the summary")
+    ap.add_argument("--launches", action="store_true", help="summarise a plain launch list instead")
     a = ap.parse_args(argv)
     with open(a.csv, encoding="utf-8", errors="replace") as f:
         launches = read_launches(f.read())
+    if a.launches:
+        md = launch_shares(launches, a.command)
+        if a.md:
+            with open(a.md, "w") as f:
+                f.write(md)
+        else:
+            sys.stdout.write(md)
+        return 0
     entry, md = summarize(a.workload, launches, a.command)
     if a.json:
         d = {}

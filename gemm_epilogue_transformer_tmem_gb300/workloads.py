@@ -45,6 +45,9 @@ class Step:
     # roofline of the dominant call is measured on that call alone
     parts: Optional[list] = None
     parts_bytes: dict = field(default_factory=dict)    # name -> algorithmic DRAM bytes of that call
+    # the unfused chain with the vendor library's GEMM (torch.matmul, cuBLAS) in
+    # place of the library's own, the other steps the same separate kernels
+    unfused_library: Optional[Callable[[], None]] = None
     # end to end with host buffers: (h_in, h_out) -> None runs one step copying
     # h_in[name] into host_inputs[name] first and host_outputs[name] into
     # h_out[name] last; a step may overlap those copies with its own calls
@@ -82,11 +85,15 @@ def build_rmsproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
     Cl = torch.empty_like(D)
     library = lambda: torch.matmul(X, Wf, out=Cl)   # noqa: E731
 
+    def unfused_library():
+        coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn, rstd=rstd)
+        torch.matmul(Xn, W, out=Du)
+
     fb = M * K * BF16 + K * N * BF16 + M * N * BF16 + M * F32
     ub = (M * K * BF16 + K * BF16 + M * K * BF16 + M * F32) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
     return Step("rmsproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
                 host_outputs=dict(D=D, r=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
-                outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn), library=library)
+                outputs=dict(D=D, r=rs, D_unfused=Du, Xn=Xn), library=library, unfused_library=unfused_library)
 
 
 def build_lnproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
@@ -119,11 +126,16 @@ def build_lnproj(dev="cuda", seed=0, M=4096, K=2048, N=8192, t=None) -> Step:
     Cl = torch.empty_like(D)
     library = lambda: torch.matmul(X, prepared["Wf"], out=Cl)   # noqa: E731
 
+    def unfused_library():
+        coda.layernorm(X, g, beta, inputs.EPS_LN, out=Xn)
+        torch.matmul(Xn, W, out=Du)
+
     fb = M * K * BF16 + K * N * BF16 + 2 * N * F32 + M * N * BF16 + 2 * M * F32
     ub = (M * K * BF16 + 2 * K * BF16 + M * K * BF16) + (M * K * BF16 + K * N * BF16 + M * N * BF16)
     return Step("lnproj", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X),
                 host_outputs=dict(D=D, stats=rs), kernels_per_fused=1, kernels_per_unfused=2, prep=prep,
-                outputs=dict(D=D, stats=rs, D_unfused=Du, Xn=Xn), library=library)
+                outputs=dict(D=D, stats=rs, D_unfused=Du, Xn=Xn), library=library,
+                unfused_library=unfused_library)
 
 
 def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
@@ -150,11 +162,16 @@ def build_swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Ste
 
     library = lambda: torch.matmul(X, W, out=C)   # noqa: E731
 
+    def unfused_library():
+        torch.matmul(X, W, out=C)
+        coda.epilogue_apply(C, [("SWIGLU",)], out=H)
+        coda.epilogue_apply(H, [("DROPOUT", 0, inputs.DROPOUT_P)], seed=inputs.DROPOUT_SEED, out=Du, keep_count=kcu)
+
     fb = M * K * BF16 + K * N * BF16 + M * N_out * BF16 + M * 4
     ub = (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16 + (2 * M * N_out * BF16 + M * 4)
     return Step("swiglu", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X), host_outputs=dict(D=D),
                 kernels_per_fused=2, kernels_per_unfused=3, outputs=dict(D=D, keep=kc, D_unfused=Du),
-                library=library)
+                library=library, unfused_library=unfused_library)
 
 
 def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step:
@@ -188,12 +205,17 @@ def build_skinny(dev="cuda", seed=0, M=128, K=4096, N_out=11008, t=None) -> Step
 
     library = lambda: torch.matmul(X, Wf, out=C)   # noqa: E731
 
+    def unfused_library():
+        coda.rmsnorm(X, g, inputs.EPS_RMS, out=Xn)
+        torch.matmul(Xn, W, out=C)
+        coda.epilogue_apply(C, [("SWIGLU",)], out=Du)
+
     fb = M * K * BF16 + M * F32 + K * N * BF16 + M * N_out * BF16
     ub = (2 * M * K * BF16 + K * BF16) + (M * K + K * N + M * N) * BF16 + (M * N + M * N_out) * BF16
     return Step("skinny", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(X=X, X_sumsq=x_ss),
                 host_outputs=dict(D=D),
                 bound="hbm", kernels_per_fused=1, kernels_per_unfused=3, prep=prep,
-                outputs=dict(D=D, D_unfused=Du), library=library)
+                outputs=dict(D=D, D_unfused=Du), library=library, unfused_library=unfused_library)
 
 
 def build_fp8swiglu(dev="cuda", seed=0, M=8192, K=4096, N_out=11008, t=None) -> Step:
@@ -292,11 +314,15 @@ def build_wgrad(dev="cuda", seed=0, T=16384, d=4096, ffn=11008, t=None) -> Step:
 
     library = lambda: torch.matmul(up.t(), dY, out=C)   # noqa: E731
 
+    def unfused_library():
+        torch.matmul(up.t(), dY, out=C)
+        coda.epilogue_apply(C, ops, residual=dWu, out=dWu, row_stats=rsu)
+
     fb = (T * ffn + T * d + 2 * ffn * d) * BF16 + ffn * F32
     ub = (T * ffn + T * d + ffn * d) * BF16 + (3 * ffn * d * BF16 + ffn * F32)
     return Step("wgrad", 2 * ffn * d * T, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
                 host_outputs=dict(norms=rs), kernels_per_fused=2, kernels_per_unfused=3,
-                outputs=dict(dW=dW, norms=rs), library=library)
+                outputs=dict(dW=dW, norms=rs), library=library, unfused_library=unfused_library)
 
 
 def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
@@ -322,11 +348,17 @@ def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
 
     library = lambda: torch.matmul(dY, W.t(), out=C)   # noqa: E731
 
+    def unfused_library():
+        torch.matmul(dY, W.t(), out=C)
+        coda.epilogue_apply(C, [("GELU_TANH_GRAD",)], z=Z, out=Du)
+        coda.epilogue_apply(Du, [("ROW_DOT_AUX", 0), ("ROW_SUM", 1)], xhat=Xh, out=Dz, row_stats=rsu)
+
     fb = (M * K + N * K + 3 * M * N) * BF16 + 2 * M * F32
     ub = (M * K + N * K + M * N) * BF16 + 3 * M * N * BF16 + (2 * M * N * BF16 + 2 * M * F32)
     return Step("dgrad", 2 * M * N * K, fb, ub, fused, unfused, host_inputs=dict(dY=dY),
                 host_outputs=dict(D=D, stats=rs), kernels_per_fused=2, kernels_per_unfused=3,
-                outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu), library=library)
+                outputs=dict(D=D, stats=rs, D_unfused=Du, stats_unfused=rsu), library=library,
+                unfused_library=unfused_library)
 
 
 def llama_block_calls(t: dict, prepared: dict, out: dict) -> list:
@@ -480,6 +512,18 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
         # the next step may overwrite the inputs only after this one read them
         main.wait_stream(s_in)
 
+    def unfused_library():
+        eps = inputs.EPS_RMS
+        coda.rmsnorm(t["X"], t["gamma_attn"], eps, out=un["xn"])
+        torch.matmul(un["xn"], t["W_qkv"], out=un["qkv"])
+        torch.matmul(t["attn_out"], t["W_o"], out=un["c_o"])
+        coda.epilogue_apply(un["c_o"], [("RESIDUAL", 0, 1.0)], residual=t["X"], out=un["h"])
+        coda.rmsnorm(un["h"], t["gamma_mlp"], eps, out=un["hn"])
+        torch.matmul(un["hn"], t["W_up"], out=un["c_up"])
+        coda.epilogue_apply(un["c_up"], [("SWIGLU",)], out=un["up"])
+        torch.matmul(un["up"], t["W_down"], out=un["c_down"])
+        coda.epilogue_apply(un["c_down"], [("RESIDUAL", 0, 1.0)], residual=un["h"], out=un["y"])
+
     def library():
         torch.matmul(t["X"], prepared["W_qkv"], out=un["qkv"])
         torch.matmul(t["attn_out"], t["W_o"], out=un["c_o"])
@@ -498,7 +542,8 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
                 host_inputs=dict(X=t["X"], X_sumsq=t["X_sumsq"], attn_out=t["attn_out"]),
                 host_outputs=dict(y=out["y"], y_sumsq=out["y_sumsq"], qkv=out["qkv"]), kernels_per_fused=6,
                 kernels_per_unfused=9, prep=prep, outputs=out, library=library,
-                parts=[(name, call, part_flops[name]) for name, call in calls], parts_bytes=part_bytes, e2e=e2e)
+                parts=[(name, call, part_flops[name]) for name, call in calls], parts_bytes=part_bytes, e2e=e2e,
+                unfused_library=unfused_library)
 
 
 BUILDERS = dict(rmsproj=build_rmsproj, lnproj=build_lnproj, swiglu=build_swiglu, dgrad=build_dgrad,

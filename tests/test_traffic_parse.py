@@ -64,3 +64,10 @@ def test_units_and_dominant_call_of_a_chain():
 def test_kernel_hash_is_stable():
     assert traffic.kernel_hash() == traffic.kernel_hash()
     assert len(traffic.kernel_hash()) == 16
+
+
+def test_launch_shares():
+    seq = [("coda::a_kernel(int)", 0, 0, 30.0), ("coda::b_kernel(int)", 0, 0, 10.0), ("coda::a_kernel(int)", 0, 0, 60.0)]
+    md = traffic.launch_shares(traffic.read_launches(_csv(seq)), "ncu ...")
+    assert "| `coda::a_kernel` | 2 | 90.0 | 90.0% |" in md
+    assert "| `coda::b_kernel` | 1 | 10.0 | 10.0% |" in md
