@@ -229,6 +229,19 @@ __device__ __forceinline__ bool warp_wait(const Waiter& W, uint64_t* bar, uint32
   return ok != 0;
 }
 
+// Warp-wide wait of the producer and MMA warps, whose loops run on every lane:
+// every lane polls the barrier (the try_wait may suspend the warp until the
+// phase completes) and a vote keeps the warp converged; past a bounded number
+// of polls, lane 0 takes the bounded slow path and broadcasts the outcome.
+// (Polling by lane 0 alone, with the other lanes parked at a shuffle, cost the
+// CTA-pair workloads 4-9%: the warp reconverges late after each wait.)
+__device__ __forceinline__ bool warp_wait_poll(const Waiter& W, uint64_t* bar, uint32_t parity, uint32_t tile,
+                                               int lane) {
+  for (int i = 0; i < 64; ++i)
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity) ? 1 : 0)) return true;
+  return warp_wait(W, bar, parity, tile, lane);
+}
+
 // Aux values of one 32-row x 32-column box staged with the 64-byte swizzle:
 // 16-byte chunk c of row r sits at r*64 + ((c ^ ((r >> 1) & 3)) * 16).
 struct SmemAux {
@@ -350,7 +363,9 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && p.num_kb > 0) {
+    // The whole warp walks the tiles and stages (warp-uniform coordinates);
+    // one elected lane arms the stage's barrier and issues its copies.
+    if (p.num_kb > 0) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_PRODUCER};
       int stage = 0;
       uint32_t phase = 0;
@@ -358,7 +373,7 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       bool ok = true;
       WorkIter wi(p, split, tile0, tile_step);
       Item w;
-      while (ok && wi.next(p, w, ctl, W, rank, kCsize, false, lane, ok)) {
+      while (ok && wi.next(p, w, ctl, W, rank, kCsize, true, lane, ok)) {
         const int tile = w.tile;
         int m_tile, n_tile;
         tile_coords(tile, p, m_tile, n_tile);
@@ -375,19 +390,21 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
           nb1 = kGLU ? p.half + n_tile * (BN / 2) : nb0 + BN / 2;
         }
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!W(&ctl->empty[stage], phase ^ 1u, tile)) {
+          if (!warp_wait_poll(W, &ctl->empty[stage], phase ^ 1u, tile, lane)) {
             ok = false;
             break;
           }
           uint64_t* fb = &ctl->full[stage];
           if (leader) {
-            mbar_arrive_expect_tx(fb, kExpectTx);
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           }
+          const bool issuer = elect_one();
+          if (issuer && leader) mbar_arrive_expect_tx(fb, kExpectTx);
           const int k0 = kb * (kFP8 ? 2 * BK : BK);   // elements of K
           uint8_t* a_dst = sA + stage * kStageABytes;
           uint8_t* b_dst = sB + stage * kStageB;
+          if (issuer) {
           if constexpr (kMX) {
             // scale tiles of this k-block: A's 128 rows (this CTA's), B's two
             // 128-row halves of the tile (both in each CTA of a pair)
@@ -445,13 +462,15 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
               tma_load_2d(b_dst + 16384, &tmB, fb, k0, nb1);
             }
           }
+          }
+          __syncwarp();
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         // give copies already issued a bounded time to land before the CTA exits
         for (int s = 0; s < p.stages; ++s)
           if (armed & (1u << s)) wait_drain(&ctl->full[s], (armed_phase >> s) & 1u, 2000000ull);
@@ -461,105 +480,133 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
           }
         }
       }
+      __syncwarp();
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && leader) {
+    // The whole warp walks the tiles and stages, so that stage addresses and
+    // operand descriptors are warp-uniform values; one elected lane issues the
+    // tensor-memory copies, the MMAs and the commits.
+    if (leader) {
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_MMA};
       constexpr uint32_t idesc = kMX ? make_idesc_mx_e4m3(kTileM, BN)
                                      : (kFP8 ? make_idesc_e4m3(kTileM, BN) : make_idesc_bf16(kTileM, BN, kBMN, kAMN));
+      // per UMMA_K step the operand start address advances 32 bytes along a
+      // K-major row, or 16 k-rows of 128 bytes (2 KB) in an MN-major tile; in
+      // 16-byte units, the descriptor's start-address field
+      constexpr uint64_t kStepA = kAMN ? (2048 >> 4) : (32 >> 4);
+      constexpr uint64_t kStepB = kBMN ? (2048 >> 4) : (32 >> 4);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       WorkIter wi(p, split, tile0, tile_step);
       Item w;
-      for (; ok && wi.next(p, w, ctl, W, rank, kCsize, false, lane, ok); ++local) {
+      for (; ok && wi.next(p, w, ctl, W, rank, kCsize, true, lane, ok); ++local) {
         const int tile = w.tile;
         const int acc = acc_index<kMX>(local);
         const uint32_t acc_phase = acc_parity<kMX>(local);
-        if (!W(&ctl->tempty[acc], acc_phase ^ 1u, tile)) {
+        if (!warp_wait_poll(W, &ctl->tempty[acc], acc_phase ^ 1u, tile, lane)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!W(&ctl->full[stage], phase, tile)) {
+          if (!warp_wait_poll(W, &ctl->full[stage], phase, tile, lane)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
           const uint32_t a_addr = smem_u32(sA + stage * kStageABytes);
           const uint32_t b_addr = smem_u32(sB + stage * kStageB);
+          // MN-major operands: 64-element groups 8 KB apart
+          const uint64_t ad0 = make_smem_desc(a_addr, kAMN ? 8192 : 16, 1024);
+          const uint64_t bd0 = make_smem_desc(b_addr, kBMN ? 8192 : 16, 1024);
+          const bool first = kb == w.kb0;
           if constexpr (kMX) {
             // the stage's scale tiles into tensor memory: A's at columns sf+0..3,
             // B's halves at sf+4..7 and sf+8..11 (one 32-bit word per row and
             // 32-row group, its four bytes the stage's four 32-element blocks);
-            // the MMAs below are issued after these copies by the same thread.
+            // the MMAs below are issued after these copies by the same lane.
             // (Issuing the next stage's copies ahead of this stage's MMAs, once
             // its tiles had landed, measured 13% slower: the copies hold up the
             // MMAs queued behind them instead of overlapping them.)
             const uint32_t sf = tmem_base + kMxSFCol0 + stage * kMxSFColsPerStage;
             const uint32_t ss = smem_u32(sSF + stage * kStageSF);
-            tmem_cp_32x128b_x4<kPair>(sf, make_smem_desc_rows16(ss));
-            tmem_cp_32x128b_x4<kPair>(sf + 4, make_smem_desc_rows16(ss + 512));
-            tmem_cp_32x128b_x4<kPair>(sf + 8, make_smem_desc_rows16(ss + 1024));
+            const uint64_t sd0 = make_smem_desc_rows16(ss);
+            const uint64_t sd1 = make_smem_desc_rows16(ss + 512);
+            const uint64_t sd2 = make_smem_desc_rows16(ss + 1024);
+            if (elect_one()) {
+              tmem_cp_32x128b_x4<kPair>(sf, sd0);
+              tmem_cp_32x128b_x4<kPair>(sf + 4, sd1);
+              tmem_cp_32x128b_x4<kPair>(sf + 8, sd2);
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint64_t ad = make_smem_desc(a_addr + k * 32, 16, 1024);
-              const uint64_t bd = make_smem_desc(b_addr + k * 32, 16, 1024);
-              const uint32_t acc_in = (kb != w.kb0 || k != 0) ? 1u : 0u;
-              const uint32_t id = idesc_sf_ids(idesc, static_cast<uint32_t>(k), static_cast<uint32_t>(k));
+              for (int k = 0; k < BK / UMMA_K; ++k) {
+                const uint64_t ad = ad0 + k * kStepA;
+                const uint64_t bd = bd0 + k * kStepB;
+                const uint32_t acc_in = (first && k == 0) ? 0u : 1u;
+                const uint32_t id = idesc_sf_ids(idesc, static_cast<uint32_t>(k), static_cast<uint32_t>(k));
+                if constexpr (kPair)
+                  mma_mxf8_ss_pair(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+                else
+                  mma_mxf8_ss(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+              }
               if constexpr (kPair)
-                mma_mxf8_ss_pair(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+                mma_commit_pair_mc(&ctl->empty[stage], 0x3);
               else
-                mma_mxf8_ss(d_tmem, ad, bd, id, sf, sf + 4, acc_in);
+                mma_commit(&ctl->empty[stage]);
             }
           } else {
+            if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < BK / UMMA_K; ++k) {
-            // MN-major operands: 64-element groups 8 KB apart, 16 k-rows of 128 B per UMMA_K
-            const uint64_t ad = kAMN ? make_smem_desc(a_addr + k * 2048, 8192, 1024)
-                                     : make_smem_desc(a_addr + k * 32, 16, 1024);
-            const uint64_t bd = kBMN ? make_smem_desc(b_addr + k * 2048, 8192, 1024)
-                                     : make_smem_desc(b_addr + k * 32, 16, 1024);
-            const uint32_t acc_in = (kb != w.kb0 || k != 0) ? 1u : 0u;
-            if constexpr (kFP8) {
+              for (int k = 0; k < BK / UMMA_K; ++k) {
+                const uint64_t ad = ad0 + k * kStepA;
+                const uint64_t bd = bd0 + k * kStepB;
+                const uint32_t acc_in = (first && k == 0) ? 0u : 1u;
+                if constexpr (kFP8) {
+                  if constexpr (kPair)
+                    mma_f8_ss_pair(d_tmem, ad, bd, idesc, acc_in);
+                  else
+                    mma_f8_ss(d_tmem, ad, bd, idesc, acc_in);
+                } else {
+                  if constexpr (kPair)
+                    mma_bf16_ss_pair(d_tmem, ad, bd, idesc, acc_in);
+                  else
+                    mma_bf16_ss(d_tmem, ad, bd, idesc, acc_in);
+                }
+              }
               if constexpr (kPair)
-                mma_f8_ss_pair(d_tmem, ad, bd, idesc, acc_in);
+                mma_commit_pair_mc(&ctl->empty[stage], 0x3);
               else
-                mma_f8_ss(d_tmem, ad, bd, idesc, acc_in);
-            } else {
-              if constexpr (kPair)
-                mma_bf16_ss_pair(d_tmem, ad, bd, idesc, acc_in);
-              else
-                mma_bf16_ss(d_tmem, ad, bd, idesc, acc_in);
+                mma_commit(&ctl->empty[stage]);
             }
           }
-          }
-          if constexpr (kPair)
-            mma_commit_pair_mc(&ctl->empty[stage], 0x3);
-          else
-            mma_commit(&ctl->empty[stage]);
+          __syncwarp();
           if (++stage == p.stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if constexpr (kPair)
-          mma_commit_pair_mc(&ctl->tfull[acc], 0x3);
-        else
-          mma_commit(&ctl->tfull[acc]);
+        if (elect_one()) {
+          if constexpr (kPair)
+            mma_commit_pair_mc(&ctl->tfull[acc], 0x3);
+          else
+            mma_commit(&ctl->tfull[acc]);
+        }
+        __syncwarp();
       }
       // no MMA may still write tensor memory when it is freed (in a pair both
       // CTAs learn it: their helper warps wait for it too)
-      if constexpr (kPair)
-        mma_commit_pair_mc(&ctl->drain, 0x3);
-      else
-        mma_commit(&ctl->drain);
-      wait_drain(&ctl->drain, 0u, 2000000ull);
+      if (lane == 0) {
+        if constexpr (kPair)
+          mma_commit_pair_mc(&ctl->drain, 0x3);
+        else
+          mma_commit(&ctl->drain);
+        wait_drain(&ctl->drain, 0u, 2000000ull);
+      }
+      __syncwarp();
     }
   } else if (warp == 3) {
     // ------------------------------------------------- tile scheduler (dynamic order)
@@ -1125,8 +1172,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
     }
   }
 
-  // Lanes 1-31 of the producer and MMA warps got here while lane 0 was still in
-  // its loop: reconverge every warp first, so that the CTA barrier (an aligned
+  // Lanes 1-31 of the scheduler warp got here while lane 0 was still in its
+  // loop: reconverge every warp first, so that the CTA barrier (an aligned
   // barrier, which counts whole warps) waits for every role to finish
   __syncwarp();
   tc_fence_before_sync();

@@ -44,6 +44,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // true once the phase with the given parity has completed
+// One lane of the (converged) warp is elected: the issuing lane of a
+// warp-uniform loop, whose addresses and descriptors stay warp-uniform values
+// (a loop run by lane 0 alone made each tcgen05.mma cost ~75 cycles to issue).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
