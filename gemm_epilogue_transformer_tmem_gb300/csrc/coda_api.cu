@@ -367,18 +367,27 @@ bool use_pair(int64_t M, int64_t K) {
   return K > 0 && (mode == 2 || (mode == 0 && M > BM));
 }
 
-// Whether a single-CTA problem may split its K range over several CTAs
-// (stream-K).  Automatic: at most 76 tiles of 128 rows (half of GB300's 152
-// SMs) and at least 16 k-blocks (K >= 1024) -- problems that leave most SMs
-// idle and have a long K to share; the decision to split also checks the
-// device's SM count.  Forced: any problem with two k-blocks or more.
-// Independent of the device, so that coda_workspace_size is too.
-bool split_eligible(const Geometry& g, bool pair) {
+// Whether a problem may split K ranges over CTAs (stream-K), and for how many
+// partial slots the workspace holds room.  Two uses: problems with few tiles
+// (single CTAs; at most 76 tiles of 128 rows, half of GB300's 152 SMs, and at
+// least 16 k-blocks, K >= 1024), whose idle SMs take part of every tile's K
+// range (slots per tile); and problems of many tiles (at least
+// kSplitWaveTiles), whose last, partly filled wave of tiles is shared out
+// evenly instead (slots per CTA, kMaxSplitCtas).  The decision to split also
+// checks the device's SM count and the grid; the slots alone size the
+// workspace, so it is independent of the device and so is
+// coda_workspace_size.  Forced: any problem with two k-blocks or more.
+constexpr int64_t kSplitWaveTiles = 128;
+int64_t split_slots(const Geometry& g, bool pair) {
   const int mode = g_split_mode.load();
-  if (pair || mode == 1 || g.num_kb < 2) return false;
-  if (mode == 2) return g.num_tiles <= 4096;
-  return g.num_kb >= 16 && g.num_tiles <= 76;
+  if (mode == 1 || g.num_kb < 2) return 0;
+  const bool few = !pair && (mode == 2 || (g.num_kb >= 16 && g.num_tiles <= 76));
+  const bool waves = mode == 2 || g.num_tiles >= kSplitWaveTiles;
+  int64_t n = few ? g.num_tiles : 0;
+  if (waves && n < kMaxSplitCtas) n = kMaxSplitCtas;
+  return n;
 }
+bool split_eligible(const Geometry& g, bool pair) { return split_slots(g, pair) > 0; }
 
 // Split-K part of the workspace, after the rest rounded up to 256 bytes:
 // partial accumulators [tiles][kSplitSegs][BN x BM] fp32, then a u32 arrival
@@ -460,9 +469,9 @@ void raster_plan(const Geometry& g, int tile_m, int64_t K, int elem_bytes, int32
 }
 
 size_t split_base(size_t b) { return (b + 255) & ~size_t(255); }
-size_t split_bytes(const Geometry& g) {
-  return static_cast<size_t>(g.num_tiles) * kSplitSegs * kPartFloats * sizeof(float) +
-         static_cast<size_t>(g.num_tiles) * sizeof(uint32_t);
+size_t split_bytes(const Geometry& g, bool pair) {
+  const size_t n = static_cast<size_t>(split_slots(g, pair));
+  return n * kSplitSegs * kPartFloats * sizeof(float) + n * sizeof(uint32_t);
 }
 
 coda_status check_dims(int64_t M, int64_t N, int64_t K) {
@@ -500,7 +509,7 @@ coda_status workspace_need(int64_t M, int64_t N, int64_t K, const coda_epilogue*
   const bool pair = use_pair(M, K);
   const Geometry g = geometry(M, N, K, c.glu, pair ? 2 * BM : BM);
   const size_t base = workspace_bytes_for(M, g, c);
-  *bytes = (with_split && split_eligible(g, pair)) ? split_base(base) + split_bytes(g) : base;
+  *bytes = (with_split && split_eligible(g, pair)) ? split_base(base) + split_bytes(g, pair) : base;
   return CODA_OK;
 }
 }  // namespace coda
@@ -557,7 +566,7 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   const size_t ws_need = workspace_bytes_for(M, g, c);
   if (ws_need > 0 && (workspace == nullptr || workspace_bytes < ws_need)) return CODA_ERR_WORKSPACE;
   const bool split_room = !mx && split_eligible(g, pair) && workspace != nullptr &&
-                          workspace_bytes >= split_base(ws_need) + split_bytes(g);
+                          workspace_bytes >= split_base(ws_need) + split_bytes(g, pair);
   if (workspace && !aligned16(workspace)) return CODA_ERR_ALIGNMENT;
 
   DevInfo dev;
@@ -668,26 +677,35 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   int grid = dev.sms;
   if (cap > 0 && cap < grid) grid = cap;
   cudaError_t e;
-  // Split over K when the tiles would leave SMs idle: the grid takes equal
-  // runs of (tile, k-block) units, each at least half a tile long so that a
-  // tile has at most kSplitSegs contributors.
+  // Split over K (stream-K): clusters take equal runs of (tile, k-block) units
+  // and CTAs that share a tile publish fp32 partials to the workspace.
   bool split = false;
-  if (split_room) {
+  auto arm_split = [&](int64_t sk_tiles) -> cudaError_t {
+    const size_t slots = sk_tiles == g.num_tiles ? static_cast<size_t>(g.num_tiles) : static_cast<size_t>(kMaxSplitCtas);
+    split = true;
+    p.split = 1;
+    p.sk_tiles = static_cast<int32_t>(sk_tiles);
+    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + split_base(ws_need));
+    p.ws_cnt = reinterpret_cast<uint32_t*>(p.ws_part + slots * kSplitSegs * kPartFloats);
+    return cudaMemsetAsync(p.ws_cnt, 0, slots * sizeof(uint32_t), st);
+  };
+  // slots the workspace holds (per tile, or per CTA for the last waves)
+  const int64_t slots_room = split_room ? split_slots(g, pair) : 0;
+  // Few tiles (single CTAs): the whole problem, in runs at least half a tile
+  // long so that a tile has at most kSplitSegs contributors.
+  if (!pair && slots_room >= g.num_tiles) {
     const int64_t units = g.num_tiles * g.num_kb;
     int64_t G = units / ((g.num_kb + 1) / 2);
     if (G > grid) G = grid;
+    if (G > kMaxSplitCtas) G = kMaxSplitCtas;
     // automatic: only when at most half the SMs would have a tile.  Above that
     // the tiles' own weight streams already come close to HBM bandwidth
     // (86 CTAs pull ~6 TB/s), and publishing and re-reading the fp32 partials
     // costs more than the shorter mainloop saves.
     const bool idle = g_split_mode.load() == 2 || g.num_tiles * 2 <= static_cast<int64_t>(grid);
     if (idle && G > g.num_tiles) {
-      split = true;
       grid = static_cast<int>(G);
-      p.split = 1;
-      p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + split_base(ws_need));
-      p.ws_cnt = reinterpret_cast<uint32_t*>(p.ws_part + static_cast<size_t>(g.num_tiles) * kSplitSegs * kPartFloats);
-      e = cudaMemsetAsync(p.ws_cnt, 0, static_cast<size_t>(g.num_tiles) * sizeof(uint32_t), st);
+      e = arm_split(g.num_tiles);
       if (e != cudaSuccess) return CODA_ERR_CUDA;
     }
   }
@@ -724,9 +742,33 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   } else if (!split && g.num_tiles < grid) {
     grid = static_cast<int>(g.num_tiles);
   }
+  const int csize = pair ? 2 : 1;
+  // Many tiles: the whole-tile waves take ceil(T / C) tile times on C
+  // clusters, the last wave partly idle.  Where that idle share is above 5% of
+  // the run's cluster time, the tiles of the last, partly filled wave and of
+  // the one before it (C to 2C - 1 tiles) are shared out as stream-K units
+  // instead, ahead of the whole tiles (each run at least a tile long, so a
+  // split tile has two contributors): every cluster then runs T / C tile
+  // times, the partials' publish and re-read overlapping later tiles'
+  // mainloops.  Measured, the idle share costs far less than its size: under
+  // the power cap a partly filled last wave runs at higher clocks, so the
+  // split gains little and its partials (publish ~10 us, re-read ~10 us per
+  // cluster) can cost more; wgrad (9.5% idle) gains 1-5%, the LLaMA out- and
+  // down-projections (3.8%) and rmsproj (3.7%) lose 1-15% when split.
+  if (!split && slots_room >= kMaxSplitCtas && !rowstat_warps && grid <= kMaxSplitCtas) {
+    const int64_t C = grid / csize;
+    const int64_t T = g.num_tiles;
+    if (C > 0 && T >= 2 * C) {
+      const int64_t waves = (T + C - 1) / C;
+      const int64_t idle = waves * C - T;   // cluster-tile slots left idle in the last wave
+      if (g_split_mode.load() == 2 || idle * 20 > waves * C) {
+        e = arm_split(T - (T / C - 1) * C);
+        if (e != cudaSuccess) return CODA_ERR_CUDA;
+      }
+    }
+  }
   // Dynamic tile order: one cluster per tile, where the tiles outnumber the
   // clusters that are resident at once (otherwise every cluster has one tile)
-  const int csize = pair ? 2 : 1;
   p.clc = 0;
   if (g_dynamic_tiles.load() != 0 && !split && !rowstat_warps && cap == 0 && g.num_kb > 0 &&
       g.num_tiles > static_cast<int64_t>(grid / csize) && g.num_tiles * csize <= 0x7FFFFFFF) {

@@ -115,17 +115,26 @@ __device__ __forceinline__ float row_rms_scale(const GemmParams& p, int row) {
   return p.rms_from_sumsq ? rsqrtf(fmaf(v, p.inv_K, p.rms_eps)) : v;
 }
 
-// Work of one CTA.  Normally whole tiles, tile0, tile0 + step, ...  With the
-// split over K (stream-K, for problems with fewer tiles than SMs), the
-// num_tiles x num_kb (tile, k-block) units are cut into gridDim.x equal runs;
-// CTA c takes units [c U / G, (c+1) U / G), i.e. the tail of one tile, maybe
-// whole tiles, and the head of another.  Every role walks the same sequence.
+// Work of one CTA (of one cluster, for CTA pairs).  Normally whole tiles,
+// tile0, tile0 + step, ... (tile0: the cluster's index, step: the number of
+// clusters).  With the split over K (stream-K), the first p.sk_tiles tiles are
+// shared out as (tile, k-block) units: their U = sk_tiles x num_kb units are
+// cut into `step` equal runs, and cluster c starts with units
+// [c U / step, (c+1) U / step) -- the tail of one tile, maybe whole tiles, and
+// the head of another.  The tiles after them follow in whole-tile waves
+// (sk_tiles = num_tiles: the whole problem is split, for problems with fewer
+// tiles than SMs; otherwise sk_tiles is what the last, partly filled wave and
+// the one before it held, so that no cluster idles at the end).  The split
+// tiles come first so that a tile's last contributor applies the epilogue --
+// adding the other contributor's published partial -- while its MMAs already
+// run the next tile.  Every role walks the same sequence.
 struct Item {
   int tile, kb0, kb1;
 };
 
 struct WorkIter {
-  int64_t u, u_end;
+  int t, t_end;           // whole tiles: t, t + step, ... below t_end
+  int64_t u, u_end;       // stream-K units of this cluster (unit u: tile u / num_kb)
   int step;
   bool split;
   // Dynamic order (cluster launch control, p.clc): the grid has one cluster per
@@ -137,16 +146,13 @@ struct WorkIter {
   int slot;
   uint32_t ph;
   __device__ __forceinline__ WorkIter(const GemmParams& p, bool split_, int tile0, int tile_step)
-      : split(split_), dyn(!split_ && p.clc != 0), started(false), slot(0), ph(0) {
+      : t(tile0), t_end(p.num_tiles), u(0), u_end(0), step(tile_step), split(split_),
+        dyn(!split_ && p.clc != 0), started(false), slot(0), ph(0) {
     if (split) {
-      const int64_t U = static_cast<int64_t>(p.num_tiles) * p.num_kb;
-      u = U * blockIdx.x / gridDim.x;
-      u_end = U * (blockIdx.x + 1) / gridDim.x;
-      step = 0;
-    } else {
-      u = tile0;
-      u_end = p.num_tiles;
-      step = tile_step;
+      t = p.sk_tiles + tile0;
+      const int64_t U = static_cast<int64_t>(p.sk_tiles) * p.num_kb;
+      u = U * tile0 / tile_step;
+      u_end = U * (tile0 + 1) / tile_step;
     }
   }
   // One thread (or, with warp_call, a whole warp whose lane 0 waits) takes the
@@ -154,10 +160,10 @@ struct WorkIter {
   __device__ __forceinline__ bool next(const GemmParams& p, Item& w, Ctl* ctl, const Waiter& W, uint32_t rank,
                                        int csize, bool warp_call, int lane, bool& sched_ok) {
     if (dyn) {
-      int tile = static_cast<int>(u);
+      int tile = t;
       if (started) {
         if (!warp_call || lane == 0) {
-          if (W(&ctl->sched_full[slot], ph, static_cast<uint32_t>(u))) {
+          if (W(&ctl->sched_full[slot], ph, static_cast<uint32_t>(t))) {
             tile = clc_response_ctaid_x(smem_u32(&ctl->sched_resp[slot][0]));
             if (tile >= 0) tile /= csize;
             if (rank == 0)
@@ -177,25 +183,25 @@ struct WorkIter {
       started = true;
       if (tile == -2) sched_ok = false;
       if (tile < 0) return false;
-      u = tile;
+      t = tile;
       w.tile = tile;
       w.kb0 = 0;
       w.kb1 = p.num_kb;
       return true;
     }
-    if (u >= u_end) return false;
-    if (!split) {
-      w.tile = static_cast<int>(u);
-      w.kb0 = 0;
-      w.kb1 = p.num_kb;
-      u += step;
+    if (u < u_end) {
+      w.tile = static_cast<int>(u / p.num_kb);
+      w.kb0 = static_cast<int>(u - static_cast<int64_t>(w.tile) * p.num_kb);
+      const int64_t end = static_cast<int64_t>(w.kb0) + (u_end - u);
+      w.kb1 = end < p.num_kb ? static_cast<int>(end) : p.num_kb;
+      u += w.kb1 - w.kb0;
       return true;
     }
-    w.tile = static_cast<int>(u / p.num_kb);
-    w.kb0 = static_cast<int>(u - static_cast<int64_t>(w.tile) * p.num_kb);
-    const int64_t end = static_cast<int64_t>(w.kb0) + (u_end - u);
-    w.kb1 = end < p.num_kb ? static_cast<int>(end) : p.num_kb;
-    u += w.kb1 - w.kb0;
+    if (t >= t_end) return false;
+    w.tile = t;
+    w.kb0 = 0;
+    w.kb1 = p.num_kb;
+    t += step;
     return true;
   }
 };
@@ -302,9 +308,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const bool leader = rank == 0u;
-  // split-K grids run the single-CTA kernel without row-statistics warps (and
-  // never with MX operands)
-  const bool split = !kPair && !kRowStats && !kMX && p.split != 0;
+  // split-K grids run without row-statistics warps (and never with MX operands)
+  const bool split = !kRowStats && !kMX && p.split != 0;
   const int tile0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int tile_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
@@ -725,13 +730,19 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       int skip_seg = -1;       // ... except this one (the CTA's own, still in tensor memory)
       const float* seg_base = nullptr;
       if (partial) {
-        const int64_t U = static_cast<int64_t>(p.num_tiles) * p.num_kb;
+        const int64_t U = static_cast<int64_t>(p.sk_tiles) * p.num_kb;
         const int64_t tile_u = static_cast<int64_t>(tile) * p.num_kb;
-        const int first = unit_owner(tile_u, U, gridDim.x);
-        const int nseg = unit_owner(tile_u + p.num_kb - 1, U, gridDim.x) - first + 1;
-        const int seg = static_cast<int>(blockIdx.x) - first;
-        float* slots = p.ws_part + static_cast<size_t>(tile) * kSplitSegs * kPartFloats;
-        uint32_t* cnt = p.ws_cnt + tile;
+        const int first = unit_owner(tile_u, U, tile_step);
+        const int nseg = unit_owner(tile_u + p.num_kb - 1, U, tile_step) - first + 1;
+        const int seg = tile0 - first;
+        // Partial slots (one per segment) and the arrival counter of a split
+        // tile: per tile where the whole problem is split (few tiles); in the
+        // split waves of a large problem per CTA of the tile's first
+        // contributor, which is the first contributor of no other split tile
+        // (only the last tile that starts inside its run can end beyond it).
+        const int owner = p.sk_tiles == p.num_tiles ? tile : first * kCsize + static_cast<int>(rank);
+        float* slots = p.ws_part + static_cast<size_t>(owner) * kSplitSegs * kPartFloats;
+        uint32_t* cnt = p.ws_cnt + owner;
         const bool leader_thread = q == 0 && lane == 0;
         // every other segment already published: finish from tensor memory
         if (leader_thread) ctl->eflag[es_par] = ld_acquire_gpu(cnt) == static_cast<uint32_t>(nseg - 1) ? 1u : 0u;
@@ -756,7 +767,10 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
               __stcg(mine + (c * 8 + j) * BM, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
           }
           tc_fence_before_sync();
-          mbar_arrive(&ctl->tempty[acc]);
+          if constexpr (kPair)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->tempty[acc]), 0u));
+          else
+            mbar_arrive(&ctl->tempty[acc]);
           __threadfence();
           if (!esync(tile)) {     // every partial store is fenced before the count
             ok = false;
@@ -1007,8 +1021,10 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
         }
       }
     }
+    // the stores' shared-memory reads must be done before the CTA exits; the
+    // grid's completion makes their global writes visible to later work
     if (lane == 0) {
-      bulk_wait_group<0>();
+      bulk_wait_group_read<0>();
       if (!ok) {
         for (int b = 0; b < 2; ++b)
           if (aux_armed & (1u << b)) wait_drain(&ctl->auxfull[ew][b], (aux_phase >> b) & 1u, 2000000ull);
@@ -1165,7 +1181,7 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->helpdone[q]);
           }
-          if (lane == 0) bulk_wait_group<0>();
+          if (lane == 0) bulk_wait_group_read<0>();
           __syncwarp();
         }
       }

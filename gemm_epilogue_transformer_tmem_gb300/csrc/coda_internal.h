@@ -38,11 +38,16 @@ constexpr int kMxSFCol0 = kAccCols;
 constexpr int kMxSFColsPerStage = 16;
 static_assert(kMxSFCol0 + kMaxStages * kMxSFColsPerStage <= kTmemCols, "MX scales must fit in tensor memory");
 // Split over K (stream-K): a tile's k-blocks may be shared by up to kSplitSegs
-// CTAs, each publishing a BM x BN fp32 partial accumulator as float4 vectors,
-// vector (row r, columns 4q..4q+3) at index q * BM + r (a warp's 32 rows of one
-// vector column are 512 contiguous bytes).
+// clusters, each CTA publishing a BM x BN fp32 partial accumulator as float4
+// vectors, vector (row r, columns 4q..4q+3) at index q * BM + r (a warp's 32
+// rows of one vector column are 512 contiguous bytes).  Slots and arrival
+// counters are indexed by tile where the whole problem is split, and by the
+// CTAs of a split tile's first contributor where only the last waves are: the
+// workspace then holds them for kMaxSplitCtas CTAs (a larger grid does not
+// split).
 constexpr int kSplitSegs = 3;
 constexpr int kPartFloats = BN * BM;
+constexpr int kMaxSplitCtas = 160;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
 // Dynamic tile order (cluster launch control): responses in flight at once
 constexpr int kSchedSlots = 2;
@@ -113,9 +118,11 @@ struct GemmParams {
   int32_t rms_from_sumsq;  // 1: rms_vec holds sum_k A[i,k]^2; r = rsqrt(s / K + eps)
   const float* mu_vec;     // commuted LayerNorm row means from the pre-pass kernel, or null
   int32_t norm_ln;         // the row statistics are LayerNorm's (mean and centred variance)
-  int32_t split;           // 1: CTAs take equal runs of (tile, k-block) units (stream-K)
-  float* ws_part;          // split: [num_tiles][kSplitSegs][kPartFloats] partial accumulators
-  uint32_t* ws_cnt;        // split: [num_tiles] arrival counters, zero at launch
+  int32_t split;           // 1: clusters take equal runs of (tile, k-block) units (stream-K) ...
+  int32_t sk_tiles;        // ... of the first sk_tiles tiles (the rest follow in whole-tile waves)
+  float* ws_part;          // split: [slots][kSplitSegs][kPartFloats] partial accumulators (slots:
+                           // num_tiles with sk_tiles == num_tiles, else kMaxSplitCtas)
+  uint32_t* ws_cnt;        // split: [slots] arrival counters, zero at launch
   int32_t clc;             // 1: one cluster launched per tile; running clusters take
                            // the tiles of clusters not yet started (cluster launch control)
   int32_t helpers;         // 1: warps 0-3 take the odd chunks of each CTA's last tile

@@ -273,10 +273,12 @@ CODA_API coda_status coda_gemm_epilogue_noalloc(const void* A, const void* B, in
 
 /* Scratch bytes coda_gemm_epilogue wants for these sizes and this op list:
  * row-reduction and keep-count partials (one per 128/256-column tile), the
- * commuted-norm row statistics, and -- for a problem of at most 76 tiles of
- * 128 rows with K >= 1024, which leaves most SMs idle -- the split-K partial
- * accumulators (3 x 128 KB per tile) and arrival counters.  A workspace that
- * holds everything but the split-K part is accepted and runs without the split.
+ * commuted-norm row statistics, and the split-K partial accumulators (3 x 128
+ * KB per slot) and arrival counters (4 bytes per slot): one slot per tile for a
+ * problem of at most 76 tiles of 128 rows with K >= 1024, which leaves most SMs
+ * idle; 160 slots (one per CTA of the grid) for a problem of at least 128
+ * tiles, whose last, partly filled wave may be split.  A workspace that holds
+ * everything but the split-K part is accepted and runs without the split.
  * The answer depends on coda_set_cta_pair / coda_set_split_k, not on the device. */
 CODA_API coda_status coda_workspace_size(int64_t M, int64_t N, int64_t K, const coda_epilogue* epi,
                                 size_t* bytes);
@@ -449,13 +451,19 @@ CODA_API void coda_set_max_ctas(int32_t n);
 /* 0 (default): CTA pairs (tcgen05 cta_group::2 on 256-row tiles, two SMs per
  * tile) when M > 128; 1: single-CTA 128-row tiles only; 2: CTA pairs whenever K > 0. */
 CODA_API void coda_set_cta_pair(int32_t mode);
-/* Split over K (stream-K) for single-CTA problems with fewer tiles than SMs:
- * the grid takes equal runs of (tile, 64-wide k-block) units, CTAs that share a
- * tile publish fp32 partial accumulators to the workspace, and the last to
- * finish applies the epilogue to their sum; no CTA waits for another.
- * 0 (default): when at most half of the SMs would have a tile and the problem
- * is eligible (see coda_workspace_size) and the workspace holds the partials;
- * 1: never; 2: whenever a single-CTA problem has two k-blocks or more. */
+/* Split over K (stream-K): clusters take equal runs of (tile, 64-wide k-block)
+ * units, CTAs that share a tile publish fp32 partial accumulators to the
+ * workspace, and the last to finish applies the epilogue to their sum; no CTA
+ * waits for another.  Two uses: a single-CTA problem with fewer tiles than SMs
+ * splits all of its tiles; a problem of several waves of tiles runs whole
+ * tiles up to its last two waves and splits the tiles of those, so that the
+ * last, partly filled wave leaves no cluster idle.  0 (default): the first
+ * when at most half of the SMs would have a tile, the second when the last
+ * wave would leave more than 5% of the run's cluster time idle -- each where
+ * the problem is eligible (see coda_workspace_size) and the workspace holds the
+ * partials; 1: never; 2: whenever a problem has two k-blocks or more (the
+ * second use needs at least two waves of tiles).  Results agree within
+ * rounding: the sum over a split tile's K range is taken in another order. */
 CODA_API void coda_set_split_k(int32_t mode);
 /* Tile order of grids with more tiles than resident CTAs (clusters).
  * 0 (default): static -- a persistent grid walks tile0, tile0 + grid, ...;

@@ -1254,6 +1254,71 @@ def test_split_k_plan_and_segments():
         coda.set_cta_pair("auto")
 
 
+WAVE_SPLIT_CASES = {
+    "plain": [],
+    "gelu_rowsum": [("GELU_TANH",), ("ROW_SUM", 0)],
+    "residual_sumsq": [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
+    "swiglu": [("SWIGLU",)],
+    "dgrad_dbias": [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1), ("COL_SUM", 0)],
+}
+
+
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+@pytest.mark.parametrize("case", sorted(WAVE_SPLIT_CASES))
+def test_last_waves_split(kernel, case):
+    # Enough tiles for three waves on the device's clusters (160 CTA-pair tiles,
+    # 320 single-CTA tiles; ragged in M, N and K): forced, the tiles of the last
+    # two waves are shared out as (tile, k-block) runs over every cluster, the
+    # earlier ones run whole.  Split and unsplit runs both match the oracle.
+    ops = WAVE_SPLIT_CASES[case]
+    glu = any(o[0] == "SWIGLU" for o in ops)
+    M, K = 4000, 456
+    N = 2528 if glu else 2520
+    n_out = N // 2 if glu else N
+    A = rand((M, K), 1301)
+    B = rand((K, N), 1302, 1.0 / math.sqrt(K))
+    aux = dict(residual=rand((M, n_out), 1303), z=rand((M, n_out), 1304), xhat=rand((M, n_out), 1305))
+    ref = O.run_chain(f64(A), f64(B), ops, residual_t=f64(aux["residual"]), z=f64(aux["z"]), xhat=f64(aux["xhat"]))
+    coda.set_cta_pair(kernel)
+    try:
+        for mode in ("force", "off"):
+            coda.set_split_k(mode)
+            r = coda.gemm_epilogue(cu(A), cu(B), ops, residual=cu(aux["residual"]), z=cu(aux["z"]),
+                                   xhat=cu(aux["xhat"]))
+            plan = coda.last_plan()
+            sync_ok()
+            assert plan["pair"] == (1 if kernel == "pair" else 0), plan
+            clusters = plan["grid"] // (2 if kernel == "pair" else 1)
+            assert plan["tiles"] >= 2 * clusters, plan
+            assert plan["split"] == (1 if mode == "force" else 0), plan
+            what = f"{case} {kernel} split={mode}"
+            assert_close(f64(r.D), ref["D"], what)
+            check_stats(r, ref, what, chain_tau(ops), K)
+            for slot, v in ref.get("col_stats", {}).items():
+                assert_col_close(f64(r.col_stats[slot]), v, ref["col_stat_scale"][slot], M, chain_tau(ops), K,
+                                 f"{what} col stat {slot}")
+    finally:
+        coda.set_split_k("auto")
+        coda.set_cta_pair("auto")
+
+
+def test_last_waves_split_auto_plan():
+    # automatic: 160 CTA-pair tiles (4096 x 2560) on 76 clusters leave 68 of 228
+    # cluster-tile slots of the third wave idle (30%), so the last waves split;
+    # 152 tiles (4864 x 2048) fill two waves exactly and 1024 tiles (16384 x
+    # 4096) leave 40 of 1064 slots (3.8%) idle, and neither splits
+    for M, N, want in ((4096, 2560, 1), (4864, 2048, 0), (16384, 4096, 0)):
+        A = rand((M, 512), 1311)
+        B = rand((512, N), 1312, 1.0 / math.sqrt(512))
+        coda.gemm_epilogue(cu(A), cu(B), [])
+        plan = coda.last_plan()
+        sync_ok()
+        clusters = plan["grid"] // 2
+        if clusters != 76:
+            pytest.skip(f"plan for 76 clusters of CTA pairs; this device gives {clusters}")
+        assert plan["split"] == want, (N, plan)
+
+
 @pytest.mark.parametrize("split", ["auto", "force", "sumsq"])
 def test_full_skinny_sampled(split):
     # the decode-sized up-projection: 86 tiles on one CTA each (automatic), split

@@ -170,27 +170,33 @@ def test_plan_struct_layout():
 
 
 def test_workspace_size_split_k_closed_form(L):
-    # split-K part: 3 partial accumulators of 256 x 128 fp32 per tile and a u32
-    # counter per tile, after the rest rounded up to 256 bytes
-    part = lambda tiles: tiles * (3 * 256 * 128 * 4 + 4)   # noqa: E731
+    # split-K part: per slot 3 partial accumulators of 256 x 128 fp32 and a u32
+    # counter, after the rest rounded up to 256 bytes; one slot per tile for
+    # few-tile problems, 160 (one per CTA) for problems of at least 128 tiles
+    part = lambda slots: slots * (3 * 256 * 128 * 4 + 4)   # noqa: E731
     up = lambda b: (b + 255) // 256 * 256                  # noqa: E731
     # SwiGLU up-projection, 64 tiles of 128 output columns, K = 4096
     assert coda.workspace_size(128, 16384, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == up(128 * 4) + part(64)
     # plain GEMM, 16 tiles, K = 1024 (16 k-blocks): eligible with no other scratch
     assert coda.workspace_size(100, 4096, 1024, []) == part(16)
-    # K = 960 (15 k-blocks) or more than 76 tiles (the decode-sized 86): not split automatically
+    # K = 960 (15 k-blocks) or between 77 and 127 tiles (the decode-sized 86): not split automatically
     assert coda.workspace_size(100, 4096, 960, []) == 0
     assert coda.workspace_size(128, 77 * 256, 4096, []) == 0
     assert coda.workspace_size(128, 22016, 4096, [("RMS_ROWSCALE", -1, 1e-6), ("SWIGLU",)]) == 128 * 4
-    # M > 128 runs on CTA pairs, which never split
+    # 32 CTA-pair tiles: too few for the last-wave split, too many CTAs for the other
     assert coda.workspace_size(300, 4096, 4096, [("ROW_SUM", 0)]) == 16 * 300 * 4
+    # 512 CTA-pair tiles (4096 x 8192): the last waves may split
+    assert coda.workspace_size(4096, 8192, 2048, []) == part(160)
+    assert coda.workspace_size(4096, 8192, 2048, [("ROW_SUM", 0)]) == up(32 * 4096 * 4) + part(160)
     try:
         coda.set_split_k("off")
         assert coda.workspace_size(100, 4096, 1024, []) == 0
+        assert coda.workspace_size(4096, 8192, 2048, []) == 0
         coda.set_split_k("force")
         coda.set_cta_pair("single")
-        # forced: any single-CTA problem with two k-blocks or more (3 x 2 tiles here)
-        assert coda.workspace_size(300, 264, 192, [("ROW_SUM", 0)]) == up(2 * 300 * 4) + part(6)
+        # forced: any problem with two k-blocks or more (3 x 2 tiles here; room
+        # for both uses, the larger being the per-CTA slots)
+        assert coda.workspace_size(300, 264, 192, [("ROW_SUM", 0)]) == up(2 * 300 * 4) + part(160)
         assert coda.workspace_size(300, 264, 64, [("ROW_SUM", 0)]) == 2 * 300 * 4
     finally:
         coda.set_split_k("auto")
