@@ -223,10 +223,11 @@ __device__ __forceinline__ int unit_owner(int64_t u, int64_t U, int64_t G) {
   return static_cast<int>(((u + 1) * G + U - 1) / U) - 1;
 }
 
-// Warp-wide wait: lane 0 alone polls the barrier (32 lanes spinning on one
-// mbarrier serialise in shared memory and steal bandwidth from the MMA's
-// operand reads), then the outcome is broadcast and __syncwarp orders the other
-// lanes' subsequent reads after lane 0's acquire.
+// Warp-wide wait of the roles that wait once per tile or chunk (epilogue,
+// helpers, row statistics): lane 0 polls the barrier, then the outcome is
+// broadcast and __syncwarp orders the other lanes' subsequent reads after
+// lane 0's acquire.  (Polls by every lane measured the same there; the
+// producer and MMA warps, which wait once per stage, use warp_wait_poll.)
 __device__ __forceinline__ bool warp_wait(const Waiter& W, uint64_t* bar, uint32_t parity, uint32_t tile, int lane) {
   int ok = 1;
   if (lane == 0) ok = W(bar, parity, tile) ? 1 : 0;
