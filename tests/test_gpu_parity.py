@@ -1302,6 +1302,28 @@ def test_last_waves_split(kernel, case):
         coda.set_cta_pair("auto")
 
 
+@pytest.mark.parametrize("kernel", ["pair", "single"])
+def test_last_waves_split_e4m3_exact(kernel):
+    # FP8 codes that are multiples of 1/8 below 16 and K = 512: every partial
+    # sum is exact in fp32, so the split tiles (partials published, added by
+    # the last contributor) give D bit for bit
+    M, K, N = 4000, 512, 2560
+    A8 = inputs.random_e4m3_codes((M, K), 1321)
+    B8 = inputs.random_e4m3_codes((N, K), 1322)
+    ref = O.round_bf16(O.gemm(O.e4m3_decode(A8.numpy()), O.e4m3_decode(B8.numpy()), "nk"))
+    coda.set_cta_pair(kernel)
+    coda.set_split_k("force")
+    try:
+        r = coda.gemm_epilogue(cu(A8), cu(B8), [], b_layout="nk", e4m3=True)
+        plan = coda.last_plan()
+        sync_ok()
+    finally:
+        coda.set_split_k("auto")
+        coda.set_cta_pair("auto")
+    assert plan["split"] == 1 and plan["pair"] == (1 if kernel == "pair" else 0), plan
+    np.testing.assert_array_equal(f64(r.D), ref)
+
+
 def test_last_waves_split_auto_plan():
     # automatic: 160 CTA-pair tiles (4096 x 2560) on 76 clusters leave 68 of 228
     # cluster-tile slots of the third wave idle (30%), so the last waves split;
