@@ -468,7 +468,8 @@ def main():
         e_ms = e_total / e2e_steps
         e2e = {"value": round(step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e_ms, 5),
-               "copies": ("overlapped with the step's calls on two side streams (events order them)"
+               "copies": ("overlapped with the step's calls on two side streams (events order them), in "
+                          "blocks of tokens where the step is the LLaMA block"
                           if step.e2e is not None else "host-to-device, step, device-to-host on the launching stream"),
                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hin.values())),
                "d2h_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hout.values()))}

@@ -361,7 +361,10 @@ def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
                 unfused_library=unfused_library)
 
 
-def llama_block_calls(t: dict, prepared: dict, out: dict) -> list:
+E2E_CHUNKS = 4   # token blocks of the LLaMA block's end-to-end step (copies overlapped with calls)
+
+
+def llama_block_calls(t: dict, prepared: dict, out: dict, rows: Optional[slice] = None) -> list:
     """The LLaMA-like non-attention block's four fused calls, in order, as
     closures over `out` (preallocated outputs, filled in when missing), as one
     layer of a stack whose hidden states carry their row sums of squares:
@@ -372,33 +375,51 @@ def llama_block_calls(t: dict, prepared: dict, out: dict) -> list:
     t["X_sumsq"] (fp32 [tokens]) holds sum_k X^2 as the previous layer's
     down-projection emits it; without it the qkv call gathers r itself (a
     pre-pass over X).  attn_out stands in for the attention output (attention
-    is not part of this path).  prepared: W_qkv and W_up with gamma folded in."""
+    is not part of this path).  prepared: W_qkv and W_up with gamma folded in.
+    rows: the calls on these token rows only (every step is row-wise, so a block
+    of rows is a block of the same computation); `out` must then be allocated."""
     eps = inputs.EPS_RMS
     ws = out.get("ws", {})
+    sl = rows if rows is not None else slice(None)
+
+    def rs(key):      # [1, tokens] row statistics, restricted to the rows
+        v = out.get(key)
+        return None if v is None else v[:, sl]
 
     def qkv():
         x_ss = t.get("X_sumsq")
+        q_out = out.get("qkv")
+        q_out = None if q_out is None else q_out[sl]
         if x_ss is None:
-            r = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_ROWSCALE", None, eps)], out=out.get("qkv"))
+            r = coda.gemm_epilogue(t["X"][sl], prepared["W_qkv"], [("RMS_ROWSCALE", None, eps)], out=q_out)
         else:
-            r = coda.gemm_epilogue(t["X"], prepared["W_qkv"], [("RMS_SUMSQ_ROWSCALE", 0, eps)],
-                                   row_vecs={0: x_ss}, out=out.get("qkv"))
-        out["qkv"] = r.D
+            r = coda.gemm_epilogue(t["X"][sl], prepared["W_qkv"], [("RMS_SUMSQ_ROWSCALE", 0, eps)],
+                                   row_vecs={0: x_ss[sl]}, out=q_out)
+        if rows is None:
+            out["qkv"] = r.D
 
     def oproj():
-        r = coda.gemm_epilogue(t["attn_out"], t["W_o"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual=t["X"],
-                               out=out.get("h"), row_stats=out.get("h_sumsq"), workspace=ws.get("h"))
-        out["h"], out["h_sumsq"] = r.D, r.row_stats
+        h = out.get("h")
+        r = coda.gemm_epilogue(t["attn_out"][sl], t["W_o"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
+                               residual=t["X"][sl], out=None if h is None else h[sl], row_stats=rs("h_sumsq"),
+                               workspace=ws.get("h"))
+        if rows is None:
+            out["h"], out["h_sumsq"] = r.D, r.row_stats
 
     def up():
-        r = coda.gemm_epilogue(out["h"], prepared["W_up"], [("RMS_SUMSQ_ROWSCALE", 0, eps), ("SWIGLU",)],
-                               row_vecs={0: out["h_sumsq"][0]}, out=out.get("up"))
-        out["up"] = r.D
+        u = out.get("up")
+        r = coda.gemm_epilogue(out["h"][sl], prepared["W_up"], [("RMS_SUMSQ_ROWSCALE", 0, eps), ("SWIGLU",)],
+                               row_vecs={0: out["h_sumsq"][0][sl]}, out=None if u is None else u[sl])
+        if rows is None:
+            out["up"] = r.D
 
     def down():
-        r = coda.gemm_epilogue(out["up"], t["W_down"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)], residual=out["h"],
-                               out=out.get("y"), row_stats=out.get("y_sumsq"), workspace=ws.get("y"))
-        out["y"], out["y_sumsq"] = r.D, r.row_stats
+        y = out.get("y")
+        r = coda.gemm_epilogue(out["up"][sl], t["W_down"], [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
+                               residual=out["h"][sl], out=None if y is None else y[sl], row_stats=rs("y_sumsq"),
+                               workspace=ws.get("y"))
+        if rows is None:
+            out["y"], out["y_sumsq"] = r.D, r.row_stats
 
     return [("qkv", qkv), ("out", oproj), ("up", up), ("down", down)]
 
@@ -478,38 +499,41 @@ def build_llama(dev="cuda", seed=0, tokens=16384, d=4096, ffn=11008, t=None) -> 
     rowvec = T * F32
 
     # end to end: the inputs' host-to-device copies and the outputs' read-back
-    # on two side streams, overlapped with the block's calls: attn_out arrives
-    # while the qkv projection runs, qkv is read back while the other three run
+    # overlapped with the block's calls.  Every step of the block is row-wise,
+    # so the tokens go through in E2E_CHUNKS blocks of rows: block i's inputs
+    # are copied in on one side stream while block i-1 runs, and its outputs
+    # read back on another while block i+1 runs; events order them, so only the
+    # first block's copy-in and the last block's read-back are exposed.
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    nchunk = E2E_CHUNKS if T % E2E_CHUNKS == 0 else 1
+    blocks = [slice(i * (T // nchunk), (i + 1) * (T // nchunk)) for i in range(nchunk)]
+    block_calls = [llama_block_calls(t, prepared, out, rows=b) for b in blocks]
 
     def e2e(h_in, h_out):
         main = torch.cuda.current_stream(dev)
-        s_in.wait_stream(main)
+        s_in.wait_stream(main)          # the previous step has read its inputs
+        s_out.wait_stream(main)
+        arrived = []
         with torch.cuda.stream(s_in):
-            t["X"].copy_(h_in["X"], non_blocking=True)
-            t["X_sumsq"].copy_(h_in["X_sumsq"], non_blocking=True)
-            x_in = torch.cuda.Event()
-            x_in.record(s_in)
-            t["attn_out"].copy_(h_in["attn_out"], non_blocking=True)
-            a_in = torch.cuda.Event()
-            a_in.record(s_in)
-        main.wait_event(x_in)
-        calls[0][1]()                  # qkv
-        q_done = torch.cuda.Event()
-        q_done.record(main)
-        main.wait_event(a_in)
-        for _, call in calls[1:]:      # out-projection, up, down
-            call()
-        y_done = torch.cuda.Event()
-        y_done.record(main)
-        s_out.wait_event(q_done)
-        with torch.cuda.stream(s_out):
-            h_out["qkv"].copy_(out["qkv"], non_blocking=True)
-            s_out.wait_event(y_done)
-            h_out["y"].copy_(out["y"], non_blocking=True)
-            h_out["y_sumsq"].copy_(out["y_sumsq"], non_blocking=True)
+            for b in blocks:
+                t["X"][b].copy_(h_in["X"][b], non_blocking=True)
+                t["X_sumsq"][b].copy_(h_in["X_sumsq"][b], non_blocking=True)
+                t["attn_out"][b].copy_(h_in["attn_out"][b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_in)
+                arrived.append(ev)
+        for b, calls_b, ev in zip(blocks, block_calls, arrived):
+            main.wait_event(ev)
+            for _, call in calls_b:
+                call()
+            done = torch.cuda.Event()
+            done.record(main)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                h_out["qkv"][b].copy_(out["qkv"][b], non_blocking=True)
+                h_out["y"][b].copy_(out["y"][b], non_blocking=True)
+                h_out["y_sumsq"][:, b].copy_(out["y_sumsq"][:, b], non_blocking=True)
         main.wait_stream(s_out)
-        # the next step may overwrite the inputs only after this one read them
         main.wait_stream(s_in)
 
     def unfused_library():

@@ -1437,6 +1437,30 @@ def test_full_dgrad_sampled():
                           chain_tau(ops), w.K, f"dgrad stat {slot}")
 
 
+def test_llama_e2e_token_blocks_match_the_step():
+    # The end-to-end step copies the block's inputs in, runs its calls and
+    # reads its outputs back in token blocks on three streams (events order
+    # them).  Every call is row-wise, so with the split over K off the outputs
+    # read back equal the device-resident step's bit for bit.
+    from gemm_epilogue_transformer_tmem_gb300 import workloads
+    coda.set_split_k("off")
+    try:
+        step = workloads.build_llama(dev="cuda", tokens=2048)
+        step.fused()
+        torch.cuda.synchronize()
+        ref = {k: v.detach().cpu().clone() for k, v in step.host_outputs.items()}
+        hin = {k: v.detach().cpu().clone().pin_memory() for k, v in step.host_inputs.items()}
+        hout = {k: torch.full(v.shape, float("nan"), dtype=v.dtype).pin_memory() for k, v in step.host_outputs.items()}
+        for v in step.host_outputs.values():
+            v.zero_()      # the e2e step must write every output again
+        step.e2e(hin, hout)
+        sync_ok()
+    finally:
+        coda.set_split_k("auto")
+    for k in ref:
+        assert torch.equal(hout[k], ref[k]), k
+
+
 def test_full_llama_block_chain_sampled():
     # One layer of the stack: the input arrives with its row sums of squares
     # (here from the library's unfused ROW_SUMSQ pass), the out-projection's
