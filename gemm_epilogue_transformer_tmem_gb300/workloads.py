@@ -361,7 +361,7 @@ def build_dgrad(dev="cuda", seed=0, M=8192, K=4096, N=16384, t=None) -> Step:
                 unfused_library=unfused_library)
 
 
-E2E_CHUNKS = 4   # token blocks of the LLaMA block's end-to-end step (copies overlapped with calls)
+E2E_CHUNKS = 8   # token blocks of the LLaMA block's end-to-end step (copies overlapped with calls)
 
 
 def llama_block_calls(t: dict, prepared: dict, out: dict, rows: Optional[slice] = None) -> list:
