@@ -274,6 +274,61 @@ def test_op(case, layout, mode):
         assert_close(f64(preact), ref["preact"], f"{case} preact")
 
 
+def _random_op_list(rng, glu):
+    """A valid op list drawn at random: ops before SWIGLU act on the N-wide
+    accumulator, ops after it on the N/2-wide output; reductions last."""
+    pre_pool = [("SCALE", 0, 1.25), ("BIAS", 0), ("COL_SCALE", 1), ("ROW_SCALE", 0), ("GELU_TANH",), ("SILU",),
+                ("GELU_ERF",)]
+    post_pool = [("BIAS", 2), ("RESIDUAL", 0, 0.5), ("GELU_TANH",), ("SCALE", 0, 0.75), ("GELU_TANH_GRAD",)]
+    red_pool = [("ROW_SUM", 0), ("ROW_SUMSQ", 1), ("ROW_DOT_AUX", 2)]
+    pick = lambda pool, n: [pool[i] for i in sorted(rng.choice(len(pool), size=n, replace=False))]  # noqa: E731
+    ops = pick(pre_pool, int(rng.integers(0, 4)))
+    if glu:
+        ops.append(("SWIGLU",))
+    ops += pick(post_pool, int(rng.integers(0, 3)))
+    ops += pick(red_pool, int(rng.integers(0, 3)))
+    return ops
+
+
+@pytest.mark.parametrize("seed", range(96))
+def test_random_op_lists(seed):
+    # Random sizes (ragged in every dimension, 1 to 700 rows), layouts, kernels
+    # (single CTA, CTA pair, split over K) and op lists, against the oracle.
+    rng = np.random.default_rng(5000 + seed)
+    M = int(rng.integers(1, 701))
+    K = 8 * int(rng.integers(1, 151))
+    n_out = 8 * int(rng.integers(1, 101))
+    glu = bool(rng.random() < 0.3)
+    N = 2 * n_out if glu else n_out
+    layout = str(rng.choice(["kn", "nk"]))
+    kernel = str(rng.choice(["single", "pair", "split"]))
+    ops = _random_op_list(rng, glu)
+    sd = 7000 + 100 * seed
+    A = rand((M, K), sd)
+    B = rand((K, N) if layout == "kn" else (N, K), sd + 1, 1.0 / math.sqrt(K))
+    col = {0: rand((N,), sd + 2), 1: rand((N,), sd + 3), 2: rand((n_out,), sd + 4)}
+    row = {0: torch.rand((M,), generator=torch.Generator().manual_seed(sd + 5)) + 0.5}
+    aux = dict(residual=rand((M, n_out), sd + 6), z=rand((M, n_out), sd + 7), xhat=rand((M, n_out), sd + 8))
+    coda.set_cta_pair("pair" if kernel == "pair" else "single")
+    coda.set_split_k("force" if kernel == "split" else "off")
+    try:
+        r = coda.gemm_epilogue(cu(A), cu(B), ops, b_layout=layout, col_vecs={k: cu(v) for k, v in col.items()},
+                               row_vecs={0: cu(row[0])}, residual=cu(aux["residual"]), z=cu(aux["z"]),
+                               xhat=cu(aux["xhat"]))
+        sync_ok()
+    finally:
+        coda.set_split_k("auto")
+        coda.set_cta_pair("auto")
+    ref = O.run_chain(f64(A), f64(B), ops, b_layout=layout, col_vecs={k: f64(v) for k, v in col.items()},
+                      row_vecs={0: f64(row[0])}, residual_t=f64(aux["residual"]), z=f64(aux["z"]),
+                      xhat=f64(aux["xhat"]))
+    what = f"seed {seed}: {M}x{K}x{N} {layout} {kernel} {ops}"
+    assert_close(f64(r.D), ref["D"], what)
+    # each approximate activation on the way adds up to TAU_ACT of relative error
+    n_act = sum(1 for o in ops if o[0] in ACTIVATIONS)
+    check_stats(r, ref, what, TAU_ACT * n_act if n_act else TAU_LIN, K)
+
+
 @pytest.mark.parametrize("layout", ["kn", "nk"])
 @pytest.mark.parametrize("case", FIXED_SEQUENCE_CASES)
 def test_fixed_sequence_matches_interpreter(case, layout, mode):
