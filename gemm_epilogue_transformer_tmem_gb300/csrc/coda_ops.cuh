@@ -59,12 +59,15 @@ __device__ __forceinline__ float gelu_tanh_f(float x) {
 // with s = sigmoid(2u): (1 + t) / 2 = s and 1 - t^2 = 4 s (1 - s), so the
 // derivative is s + 2 z s (1 - s) u'(z), free of the cancellation in 1 - t^2
 __device__ __forceinline__ float gelu_tanh_grad_f(float z) {
+  // constants folded: u = z (c + c k z^2), 2 u'(z) = 2 c + 6 c k z^2 (c = sqrt(2/pi), k = 0.044715)
+  constexpr float kC1 = kSqrt2OverPi * kGeluC;
   const float z2 = z * z;
-  const float u = kSqrt2OverPi * fmaf(kGeluC * z2, z, z);
-  const float du = kSqrt2OverPi * fmaf(3.0f * kGeluC, z2, 1.0f);
-  float om;
-  const float s = sigmoid_f(2.0f * u, om);
-  return fmaf(2.0f * z * du, s * om, s);
+  const float u = z * fmaf(kC1, z2, kSqrt2OverPi);
+  const float du2 = fmaf(6.0f * kC1, z2, 2.0f * kSqrt2OverPi);
+  const float t = tanh_hw(u);                    // sigmoid(2u) = (1 + tanh(u)) / 2
+  const float s = fmaf(0.5f, t, 0.5f);
+  const float om = fmaf(-0.5f, t, 0.5f);
+  return fmaf(z * du2, s * om, s);
 }
 
 // exact GELU: x * Phi(x), Phi the standard normal distribution function
@@ -363,15 +366,25 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
     case CODA_OP_ROW_SUM:
     case CODA_OP_ROW_MEAN: {
       float s = 0.0f;
+      if (c.nvalid >= NE) {   // a whole chunk: no per-element masks
 #pragma unroll
-      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] : 0.0f;
+        for (int j = 0; j < NE; ++j) s += v[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] : 0.0f;
+      }
       add_red(red, op.red, s);
       break;
     }
     case CODA_OP_ROW_SUMSQ: {
       float s = 0.0f;
+      if (c.nvalid >= NE) {
 #pragma unroll
-      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * v[j] : 0.0f;
+        for (int j = 0; j < NE; ++j) s += v[j] * v[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * v[j] : 0.0f;
+      }
       add_red(red, op.red, s);
       break;
     }
@@ -379,8 +392,13 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
       float x[NE];
       aux.load(op.aux, x);
       float s = 0.0f;
+      if (c.nvalid >= NE) {
 #pragma unroll
-      for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * x[j] : 0.0f;
+        for (int j = 0; j < NE; ++j) s += v[j] * x[j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < NE; ++j) s += (j < c.nvalid) ? v[j] * x[j] : 0.0f;
+      }
       add_red(red, op.red, s);
       break;
     }
