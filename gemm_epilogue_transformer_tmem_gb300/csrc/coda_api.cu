@@ -392,6 +392,45 @@ bool split_eligible(const Geometry& g, bool pair) { return split_slots(g, pair) 
 // Split-K part of the workspace, after the rest rounded up to 256 bytes:
 // partial accumulators [tiles][kSplitSegs][BN x BM] fp32, then a u32 arrival
 // counter per tile.
+// The column vectors the op list reads, for the epilogue's per-tile L1
+// prefetch: each once, the entries of SwiGLU's up half (read by the ops
+// before SWIGLU) as a vector of their own.  Past kMaxColPrefetch the rest are
+// left to the loads themselves.
+void plan_colvec_prefetch(const EpiProgram& prog, int32_t half, GemmParams& p) {
+  p.n_colpf = 0;
+  auto add = [&](const void* v, int shift) {
+    if (v == nullptr || p.n_colpf == kMaxColPrefetch) return;
+    for (int i = 0; i < p.n_colpf; ++i)
+      if (p.colpf[i] == v) return;
+    p.colpf[p.n_colpf] = v;
+    p.colpf_shift[p.n_colpf] = shift;
+    ++p.n_colpf;
+  };
+  for (int o = 0; o < prog.n_ops; ++o) {
+    const bool pre = half > 0 && o < prog.glu_pos;
+    auto both = [&](const void* v, int shift) {
+      add(v, shift);
+      if (pre && v != nullptr) add(static_cast<const char*>(v) + (static_cast<size_t>(half) << shift), shift);
+    };
+    const DevOp& op = prog.ops[o];
+    switch (op.code) {
+      case CODA_OP_BIAS:
+      case CODA_OP_COL_SCALE:
+        if (op.slot < CODA_MAX_COL_VECS) both(prog.col_vec[op.slot], 1);
+        break;
+      case CODA_OP_COL_SCALE_F32:
+        both(prog.col_scale_f32, 2);
+        break;
+      case CODA_OP_LN_ROWSCALE:
+        both(prog.ln_colsum, 2);
+        both(prog.ln_bias, 2);
+        break;
+      default:
+        break;
+    }
+  }
+}
+
 // The fixed op sequence whose opcodes are exactly this list's, or SEQ_INTERP.
 // RMS_SUMSQ_ROWSCALE runs as RMS_ROWSCALE (only the source of r differs).
 int match_sequence(const coda_epilogue* epi, bool glu) {
@@ -427,6 +466,7 @@ cudaError_t launch_gemm_seq(int seq, bool glu, bool a_mn_major, bool b_mn_major,
     case SEQ_SWIGLU_DROPOUT:
       return launch_gemm_fwd_glu(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_DGRAD:
+    case SEQ_WGRAD:
       return launch_gemm_bwd(seq, a_mn_major, b_mn_major, row_stats, pair, maps, p, grid, smem, st);
     case SEQ_BIAS:
     case SEQ_BIAS_GELU:
@@ -669,6 +709,7 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   p.smem_ctl_off = static_cast<uint32_t>(stages * stage_bytes + epi_bytes);
   p.err = dev.err;
   p.prog = c.prog;
+  plan_colvec_prefetch(c.prog, p.half, p);
   const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -713,6 +713,22 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
       const bool partial = split && !(w.kb0 == 0 && w.kb1 == p.num_kb);
       if (n_aux > 0 && !partial && grp < nch) issue_aux(abuf, col_base + grp * kChunk, m0 + q * 32);
+      // Each chunk reads its 32 entries of every column vector of the op list
+      // with warp-uniform loads, which from L2 would each stall the chunk:
+      // bring the tile's slices into L1 while its accumulator is computed.
+      // Lane l takes the l-th 128-byte line of a slice; every line it touches
+      // holds at least one entry of the slice.
+      if (p.n_colpf > 0) {
+        const int col_end = min(col_base + kOutCols, p.N_out);
+        for (int e = 0; e < p.n_colpf && col_end > col_base; ++e) {
+          const int sh = p.colpf_shift[e];
+          const uint64_t v = reinterpret_cast<uint64_t>(p.colpf[e]);
+          const uint64_t first = v + (static_cast<uint64_t>(col_base) << sh);
+          const uint64_t last = v + (static_cast<uint64_t>(col_end) << sh) - 1;
+          const uint64_t line = (first & ~uint64_t(127)) + static_cast<uint64_t>(lane) * 128;
+          if (line <= last) prefetch_l1(line);
+        }
+      }
 
       bool okw = warp_wait(W, &ctl->tfull[acc], acc_phase, tile, lane);
       if (!okw) {

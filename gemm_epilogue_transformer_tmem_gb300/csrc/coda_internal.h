@@ -48,6 +48,8 @@ static_assert(kMxSFCol0 + kMaxStages * kMxSFColsPerStage <= kTmemCols, "MX scale
 constexpr int kSplitSegs = 3;
 constexpr int kPartFloats = BN * BM;
 constexpr int kMaxSplitCtas = 160;
+// column vectors whose slices the epilogue prefetches into L1 per tile
+constexpr int kMaxColPrefetch = 8;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
 // Dynamic tile order (cluster launch control): responses in flight at once
 constexpr int kSchedSlots = 2;
@@ -126,6 +128,10 @@ struct GemmParams {
   int32_t clc;             // 1: one cluster launched per tile; running clusters take
                            // the tiles of clusters not yet started (cluster launch control)
   int32_t helpers;         // 1: warps 0-3 take the odd chunks of each CTA's last tile
+  int32_t n_colpf;         // column vectors the op list reads (bias, column scales, LayerNorm's
+                           // c and b; the SwiGLU up half of one as an entry of its own) ...
+  int32_t colpf_shift[kMaxColPrefetch];     // ... log2 of their element bytes (1: bf16, 2: fp32)
+  const void* colpf[kMaxColPrefetch];       // ... and their first elements
   EpiProgram prog;
 };
 

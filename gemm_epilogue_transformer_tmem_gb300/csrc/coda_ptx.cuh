@@ -120,6 +120,12 @@ __device__ __forceinline__ int clc_response_ctaid_x(uint32_t resp) {
   return taken ? static_cast<int>(x) : -1;
 }
 
+// the 128-byte line holding `ptr`, from global memory into L1 (a hint: no
+// register waits for it)
+__device__ __forceinline__ void prefetch_l1(uint64_t ptr) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr) : "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -33,6 +33,7 @@ enum SeqId : int {
   SEQ_BIAS_RESIDUAL,      // bias -> + residual: attention out / MLP down-projection
   SEQ_GELU,               // GELU(tanh) without bias
   SEQ_RESIDUAL_SUMSQ,     // + residual, row sums of squares (the next norm's statistics)
+  SEQ_WGRAD,              // s * X^T dY + dW (in place), row sums of squares of the new dW
   SEQ_COUNT_
 };
 
@@ -61,6 +62,7 @@ constexpr SeqDef kSeqDefs[] = {
     {SEQ_BIAS_RESIDUAL, false, 2, {CODA_OP_BIAS, CODA_OP_RESIDUAL, 0, 0}},
     {SEQ_GELU, false, 1, {CODA_OP_GELU_TANH, 0, 0, 0}},
     {SEQ_RESIDUAL_SUMSQ, false, 2, {CODA_OP_RESIDUAL, CODA_OP_ROW_SUMSQ, 0, 0}},
+    {SEQ_WGRAD, false, 3, {CODA_OP_SCALE, CODA_OP_RESIDUAL, CODA_OP_ROW_SUMSQ, 0}},
 };
 
 }  // namespace coda

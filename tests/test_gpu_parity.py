@@ -223,12 +223,13 @@ OP_CASES = {
     "bias_gelu": [("BIAS", 0), ("GELU_TANH",)],
     "bias_gelu_erf": [("BIAS", 0), ("GELU_ERF",)],
     "bias_residual": [("BIAS", 0), ("RESIDUAL", 0, 1.0)],
+    "wgrad": [("SCALE", 0, 0.5), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
 }
 
 # op lists the library runs as fixed op sequences (straight-line epilogues);
 # every other list runs the interpreter
 FIXED_SEQUENCE_CASES = ["none", "residual", "bias_gelu_residual", "dgrad", "swiglu", "bias", "bias_gelu",
-                        "bias_gelu_erf", "bias_residual", "gelu"]
+                        "bias_gelu_erf", "bias_residual", "gelu", "wgrad"]
 
 
 def _op_case_tensors(ops, layout, seed):
@@ -612,23 +613,51 @@ def test_a_km_small_integer_bit_exact(layout, mode):
     np.testing.assert_array_equal(f64(r.D), ref)
 
 
+@pytest.mark.parametrize("cols", [True, False])
 @pytest.mark.parametrize("layout", ["kn", "nk"])
-def test_wgrad_scale_accumulate_in_place(layout, mode):
+def test_wgrad_scale_accumulate_in_place(layout, cols, mode):
     # dW = s * X^T dH + dW_old, written over dW_old (output and residual alias),
-    # with the per-row sums of squares (gradient-norm partials) and column sums
+    # with the per-row sums of squares (gradient-norm partials), and column
+    # sums (the interpreter) or not (the fixed sequence of the weight gradient)
     T, K_in, N = 384, 264, 520          # tokens (the reduction), features, outputs
     X = rand((T, K_in), 541)
     dH = rand((T, N) if layout == "kn" else (N, T), 542, 1.0 / math.sqrt(T))
     dW_old = rand((K_in, N), 543)
-    ops = [("SCALE", 0, 0.5), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0), ("COL_SUM", 0)]
+    ops = [("SCALE", 0, 0.5), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)] + ([("COL_SUM", 0)] if cols else [])
     dW = cu(dW_old.clone())
     r = coda.gemm_epilogue(cu(X), cu(dH), ops, b_layout=layout, a_layout="km", residual=dW, out=dW)
+    assert (coda.last_plan()["sequence"] == 0) == cols
     sync_ok()
     ref = O.run_chain(f64(X).T, f64(dH), ops, b_layout=layout, residual_t=f64(dW_old))
     assert_close(f64(dW), ref["D"], "wgrad")
     check_stats(r, ref, "wgrad", TAU_LIN, T)
-    assert_col_close(f64(r.col_stats[0]), ref["col_stats"][0], ref["col_stat_scale"][0], K_in, TAU_LIN, T,
-                     "wgrad colsum")
+    if cols:
+        assert_col_close(f64(r.col_stats[0]), ref["col_stats"][0], ref["col_stat_scale"][0], K_in, TAU_LIN, T,
+                         "wgrad colsum")
+
+
+@pytest.mark.parametrize("layout", ["kn", "nk"])
+def test_wgrad_sequence_bit_identical_to_interpreter(layout, mode):
+    # A as [K, M], in place: the weight gradient's fixed sequence and the
+    # interpreter apply the same operations in the same order, so D and the
+    # row sums of squares agree bit for bit
+    T, K_in, N = 640, 392, 776
+    X, dH = rand((T, K_in), 551), rand((T, N) if layout == "kn" else (N, T), 552, 1.0 / math.sqrt(T))
+    dW_old = cu(rand((K_in, N), 553))
+    ops = [("SCALE", 0, 0.125), ("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)]
+    out = {}
+    try:
+        for fixed in (True, False):
+            coda.set_fixed_sequences(fixed)
+            dW = dW_old.clone()
+            r = coda.gemm_epilogue(cu(X), cu(dH), ops, b_layout=layout, a_layout="km", residual=dW, out=dW)
+            assert (coda.last_plan()["sequence"] > 0) == fixed
+            sync_ok()
+            out[fixed] = (dW.clone(), r.row_stats[0].clone())
+    finally:
+        coda.set_fixed_sequences(True)
+    assert torch.equal(out[True][0], out[False][0])
+    assert torch.equal(out[True][1], out[False][1])
 
 
 # ------------------------------------------------------------ norm backward
