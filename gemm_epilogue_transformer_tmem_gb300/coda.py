@@ -55,7 +55,7 @@ class CodaAux(ctypes.Structure):
 class CodaPlan(ctypes.Structure):
     _fields_ = [("pair", ctypes.c_int32), ("split", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("tiles", ctypes.c_int64), ("prepass", ctypes.c_int32),
-                ("sequence", ctypes.c_int32), ("dynamic", ctypes.c_int32)]
+                ("sequence", ctypes.c_int32), ("dynamic", ctypes.c_int32), ("colvecs", ctypes.c_int32)]
 
 
 class CodaError(RuntimeError):

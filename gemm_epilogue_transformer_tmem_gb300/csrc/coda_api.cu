@@ -173,6 +173,7 @@ coda_status compile_epilogue(const coda_epilogue* epi, const coda_aux* aux, int6
     d.u = 0;
     d.red = -1;
     d.aux = -1;
+    d.cv = -1;
     if (op.f1 != 0.0f || !std::isfinite(op.f0)) return CODA_ERR_INVALID_ARG;
     const bool after_glu = !c.glu || static_cast<int32_t>(o) > c.prog.glu_pos;
     switch (op.opcode) {
@@ -392,43 +393,60 @@ bool split_eligible(const Geometry& g, bool pair) { return split_slots(g, pair) 
 // Split-K part of the workspace, after the rest rounded up to 256 bytes:
 // partial accumulators [tiles][kSplitSegs][BN x BM] fp32, then a u32 arrival
 // counter per tile.
-// The column vectors the op list reads, for the epilogue's per-tile L1
-// prefetch: each once, the entries of SwiGLU's up half (read by the ops
-// before SWIGLU) as a vector of their own.  Past kMaxColPrefetch the rest are
-// left to the loads themselves.
-void plan_colvec_prefetch(const EpiProgram& prog, int32_t half, GemmParams& p) {
+// The column vectors the op list reads, for the epilogue's per-tile staging
+// (or L1 prefetch): each op's slices consecutive from its `cv` index, in the
+// order the ops read them (a vector, then its SwiGLU up half where the op runs
+// before SWIGLU; LayerNorm's c before b).  An op list that needs more than
+// kMaxColPrefetch slices stages none (its ops read global memory) and
+// prefetches the first kMaxColPrefetch.  Returns whether the slices can be staged.
+bool plan_colvecs(EpiProgram& prog, int32_t half, GemmParams& p) {
   p.n_colpf = 0;
+  bool fits = true;
   auto add = [&](const void* v, int shift) {
-    if (v == nullptr || p.n_colpf == kMaxColPrefetch) return;
-    for (int i = 0; i < p.n_colpf; ++i)
-      if (p.colpf[i] == v) return;
+    if (p.n_colpf == kMaxColPrefetch) {
+      fits = false;
+      return;
+    }
     p.colpf[p.n_colpf] = v;
     p.colpf_shift[p.n_colpf] = shift;
     ++p.n_colpf;
   };
   for (int o = 0; o < prog.n_ops; ++o) {
+    DevOp& op = prog.ops[o];
+    op.cv = -1;
     const bool pre = half > 0 && o < prog.glu_pos;
     auto both = [&](const void* v, int shift) {
       add(v, shift);
-      if (pre && v != nullptr) add(static_cast<const char*>(v) + (static_cast<size_t>(half) << shift), shift);
+      if (pre) add(static_cast<const char*>(v) + (static_cast<size_t>(half) << shift), shift);
     };
-    const DevOp& op = prog.ops[o];
     switch (op.code) {
       case CODA_OP_BIAS:
       case CODA_OP_COL_SCALE:
-        if (op.slot < CODA_MAX_COL_VECS) both(prog.col_vec[op.slot], 1);
+        if (op.slot < CODA_MAX_COL_VECS && prog.col_vec[op.slot] != nullptr) {
+          op.cv = p.n_colpf;
+          both(prog.col_vec[op.slot], 1);
+        }
         break;
       case CODA_OP_COL_SCALE_F32:
-        both(prog.col_scale_f32, 2);
+        if (prog.col_scale_f32 != nullptr) {
+          op.cv = p.n_colpf;
+          both(prog.col_scale_f32, 2);
+        }
         break;
       case CODA_OP_LN_ROWSCALE:
-        both(prog.ln_colsum, 2);
-        both(prog.ln_bias, 2);
+        if (prog.ln_colsum != nullptr) {
+          op.cv = p.n_colpf;
+          both(prog.ln_colsum, 2);
+          if (prog.ln_bias != nullptr) both(prog.ln_bias, 2);
+        }
         break;
       default:
         break;
     }
   }
+  if (!fits)
+    for (int o = 0; o < prog.n_ops; ++o) prog.ops[o].cv = -1;
+  return fits && p.n_colpf > 0;
 }
 
 // The fixed op sequence whose opcodes are exactly this list's, or SEQ_INTERP.
@@ -697,10 +715,28 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   c.prog.num_rb = static_cast<int32_t>((M + 31) / 32);
   p.epi_warp_bytes = static_cast<uint32_t>(2 * kBoxBytes + c.n_aux * 2 * kBoxBytes);
   // MX kernels run two epilogue warp groups (even and odd chunks), each warp with its own staging
-  const size_t epi_bytes = static_cast<size_t>(kEpiWarps) * (mx ? kMaxEpiGroups : 1) * p.epi_warp_bytes;
+  const size_t n_epi_warps = static_cast<size_t>(kEpiWarps) * (mx ? kMaxEpiGroups : 1);
   const size_t ctl_bytes = (sizeof(Ctl) + 127) & ~size_t(127);
-  const size_t fixed = 1024 + epi_bytes + ctl_bytes;
   const size_t stage_bytes = (pair ? kPairStageBytes : kStageBytes) + (mx ? kMxStageSFBytes : 0);
+  auto stages_for = [&](size_t warp_bytes) -> int {
+    const size_t fixed_b = 1024 + n_epi_warps * warp_bytes + ctl_bytes;
+    if (static_cast<size_t>(dev.max_smem) < fixed_b + 2 * stage_bytes) return 0;
+    const int s = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed_b) / stage_bytes);
+    return s > kMaxStages ? kMaxStages : s;
+  };
+  // Column vectors: staged per tile in each epilogue warp's shared memory
+  // where that costs no pipeline stage (a stage is worth more), else
+  // prefetched into L1.
+  const bool cv_fit = plan_colvecs(c.prog, p.half, p);
+  const size_t cv_bytes = static_cast<size_t>(p.n_colpf) * (c.glu ? BN / 2 : BN) * sizeof(float);
+  if (cv_fit && stages_for(p.epi_warp_bytes + cv_bytes) == stages_for(p.epi_warp_bytes)) {
+    p.cv_smem = 1;
+    p.epi_warp_bytes += static_cast<uint32_t>(cv_bytes);
+  } else {
+    for (int o = 0; o < c.prog.n_ops; ++o) c.prog.ops[o].cv = -1;
+  }
+  const size_t epi_bytes = n_epi_warps * p.epi_warp_bytes;
+  const size_t fixed = 1024 + epi_bytes + ctl_bytes;
   if (static_cast<size_t>(dev.max_smem) < fixed + 2 * stage_bytes) return CODA_ERR_UNSUPPORTED;
   int stages = static_cast<int>((static_cast<size_t>(dev.max_smem) - fixed) / stage_bytes);
   if (stages > kMaxStages) stages = kMaxStages;
@@ -709,7 +745,6 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   p.smem_ctl_off = static_cast<uint32_t>(stages * stage_bytes + epi_bytes);
   p.err = dev.err;
   p.prog = c.prog;
-  plan_colvec_prefetch(c.prog, p.half, p);
   const size_t smem = fixed + static_cast<size_t>(stages) * stage_bytes;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -837,7 +872,8 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   if (e != cudaSuccess) return CODA_ERR_CUDA;
   g_launches.fetch_add(1);
   g_last_plan = coda_plan{pair ? 1 : 0, split ? 1 : 0, grid, stages, g.num_tiles,
-                          (p.rms_vec != nullptr && !p.rms_from_sumsq) ? 1 : 0, seq, p.clc};
+                          (p.rms_vec != nullptr && !p.rms_from_sumsq) ? 1 : 0, seq, p.clc,
+                          p.cv_smem ? p.n_colpf : -p.n_colpf};
   if (c.prog.n_colred > 0) {
     e = launch_finalize_cols(c.prog.ws_col, c.prog.n_colred, c.prog.num_rb, g.n_out, c.prog.colred_slot,
                              c.col_stats, st);

@@ -659,6 +659,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
     uint8_t* wbase = smem + p.smem_epi_off + ew * p.epi_warp_bytes;
     uint8_t* out_stage = wbase;
     uint8_t* aux_stage = wbase + 2 * kBoxBytes;
+    // the tile's slices of the op list's column vectors (cv_smem), fp32 [n_colpf][kOutCols]
+    float* cv_stage = reinterpret_cast<float*>(wbase + 2 * kBoxBytes + p.n_aux * 2 * kBoxBytes);
     const int n_aux = p.n_aux;
     const int r_in_tile = q * 32 + lane;
     uint32_t aux_phase = 0;   // bit b: parity of the next completion of buffer b
@@ -714,11 +716,36 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       const bool partial = split && !(w.kb0 == 0 && w.kb1 == p.num_kb);
       if (n_aux > 0 && !partial && grp < nch) issue_aux(abuf, col_base + grp * kChunk, m0 + q * 32);
       // Each chunk reads its 32 entries of every column vector of the op list
-      // with warp-uniform loads, which from L2 would each stall the chunk:
-      // bring the tile's slices into L1 while its accumulator is computed.
-      // Lane l takes the l-th 128-byte line of a slice; every line it touches
-      // holds at least one entry of the slice.
-      if (p.n_colpf > 0) {
+      // with warp-uniform loads, which from L2 would each stall the chunk.
+      // While the tile's accumulator is computed, copy the tile's slices to
+      // this warp's shared memory (fp32, 0 past N_out; lane l takes columns
+      // l, l + 32, ...), or, where there is no room, prefetch them into L1
+      // (lane l the l-th 128-byte line of a slice; every line it touches holds
+      // at least one entry of the slice).
+      if (p.cv_smem) {
+        __syncwarp();   // every lane is done with the previous tile's slices
+        for (int e = 0; e < p.n_colpf; ++e) {
+          float x[kOutCols / 32];
+          if (p.colpf_shift[e] == 1) {
+            const uint16_t* src = static_cast<const uint16_t*>(p.colpf[e]);
+#pragma unroll
+            for (int i = 0; i < kOutCols / 32; ++i) {
+              const int col = col_base + i * 32 + lane;
+              x[i] = col < p.N_out ? __uint_as_float(static_cast<uint32_t>(__ldg(src + col)) << 16) : 0.0f;
+            }
+          } else {
+            const float* src = static_cast<const float*>(p.colpf[e]);
+#pragma unroll
+            for (int i = 0; i < kOutCols / 32; ++i) {
+              const int col = col_base + i * 32 + lane;
+              x[i] = col < p.N_out ? __ldg(src + col) : 0.0f;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < kOutCols / 32; ++i) cv_stage[e * kOutCols + i * 32 + lane] = x[i];
+        }
+        __syncwarp();
+      } else if (p.n_colpf > 0) {
         const int col_end = min(col_base + kOutCols, p.N_out);
         for (int e = 0; e < p.n_colpf && col_end > col_base; ++e) {
           const int sh = p.colpf_shift[e];
@@ -835,7 +862,7 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       // The CTA's last tile (static order): the helper warp of this lane quarter
       // takes its odd chunks.  Row reductions keep even and odd chunks apart in
       // every tile, so that the sum does not depend on who took which chunk.
-      const bool helped = !kRowStats && p.helpers != 0 && !split && tile + tile_step >= p.num_tiles;
+      const bool helped = !kRowStats && !kMX && p.helpers != 0 && !split && tile + tile_step >= p.num_tiles;
       float red0[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       float red1[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
       uint32_t keep = 0;
@@ -855,7 +882,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
         const int col = col_base + c * kChunk;
         int nvalid = p.N_out - col;
         if (nvalid > kChunk) nvalid = kChunk;
-        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu};
+        const RowCtx rc{row, row_ok, col, nvalid, p.half, p.N_out, p.M, r_rms, mu,
+                        p.cv_smem ? cv_stage + c * kChunk : nullptr, kOutCols};
         const SmemAux ax{aux_stage + abuf * kBoxBytes, lane};
         if constexpr (kRowStats) {   // never helped: one running sum
           Epi::template run<32, kGLU>(p.prog, v, u, rc, ax, red0, keep);
@@ -998,8 +1026,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
         const int slot = local & 1;
         if (grp == 1) {
 #pragma unroll
-          for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->gred[slot][q][r][lane] = red1[r];
-          ctl->gkeep[slot][q][lane] = keep;
+          for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->g.gred[slot][q][r][lane] = red1[r];
+          ctl->g.gkeep[slot][q][lane] = keep;
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctl->gfull[slot][q]);
           continue;
@@ -1010,8 +1038,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
         }
 #pragma unroll
         for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
-          if (r < p.prog.n_red) red1[r] = ctl->gred[slot][q][r][lane];
-        keep += ctl->gkeep[slot][q][lane];
+          if (r < p.prog.n_red) red1[r] = ctl->g.gred[slot][q][r][lane];
+        keep += ctl->g.gkeep[slot][q][lane];
       } else if (kEpiGroups > 1 && grp == 1) {
         continue;
       }
@@ -1022,8 +1050,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
         }
 #pragma unroll
         for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r)
-          if (r < p.prog.n_red) red1[r] = ctl->hred[q][r][lane];
-        keep += ctl->hkeep[q][lane];
+          if (r < p.prog.n_red) red1[r] = ctl->h.hred[q][r][lane];
+        keep += ctl->h.hkeep[q][lane];
       }
       if (row_ok) {
         const size_t Ms = static_cast<size_t>(p.M);
@@ -1125,7 +1153,7 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
     // the producer, MMA, allocator and scheduler warps (lane quarters 0-3) take
     // the odd chunks of the CTA's last tile, halving the epilogue that nothing
     // overlaps.  Only in the static order, without aux tensors or a split.
-    if (p.helpers != 0 && !split && warp < kEpiWarps) {
+    if (!kMX && p.helpers != 0 && !split && warp < kEpiWarps) {
       __syncwarp();
       const int q = warp;
       const Waiter W{ctl, p.timeout_ns, p.err, ROLE_EPILOGUE};
@@ -1193,8 +1221,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
           }
           if (p.prog.n_red > 0 || p.ws_keep != nullptr) {
 #pragma unroll
-            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->hred[q][r][lane] = hred[r];
-            ctl->hkeep[q][lane] = keep;
+            for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->h.hred[q][r][lane] = hred[r];
+            ctl->h.hkeep[q][lane] = keep;
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->helpdone[q]);
           }

@@ -48,7 +48,7 @@ static_assert(kMxSFCol0 + kMaxStages * kMxSFColsPerStage <= kTmemCols, "MX scale
 constexpr int kSplitSegs = 3;
 constexpr int kPartFloats = BN * BM;
 constexpr int kMaxSplitCtas = 160;
-// column vectors whose slices the epilogue prefetches into L1 per tile
+// column vectors whose slices the epilogue stages (or prefetches) per tile
 constexpr int kMaxColPrefetch = 8;
 constexpr int kMaxAux = 3;                         // residual, z, xhat
 // Dynamic tile order (cluster launch control): responses in flight at once
@@ -67,6 +67,8 @@ struct DevOp {
   uint64_t u;
   int32_t red;
   int32_t aux;      // staging index of the aux tensor this op reads, or -1
+  int32_t cv;       // its first column-vector slice staged in shared memory, or -1
+                    // (GemmParams::cv_smem; an op's slices are consecutive)
 };
 
 struct RedInfo {
@@ -132,6 +134,9 @@ struct GemmParams {
                            // c and b; the SwiGLU up half of one as an entry of its own) ...
   int32_t colpf_shift[kMaxColPrefetch];     // ... log2 of their element bytes (1: bf16, 2: fp32)
   const void* colpf[kMaxColPrefetch];       // ... and their first elements
+  int32_t cv_smem;         // 1: each epilogue warp copies the tile's slices of them to its shared
+                           // memory (fp32 [n_colpf][output columns of a tile]) before the tile's
+                           // accumulator is ready; 0: they are prefetched into L1 instead
   EpiProgram prog;
 };
 
@@ -152,13 +157,20 @@ struct Ctl {
   uint64_t sched_empty[kSchedSlots];   // every tile-walking role read it (leader CTA's barrier)
   alignas(16) uint32_t sched_resp[kSchedSlots][4];
   uint64_t helpdone[kEpiWarps];                           // a helper warp's row partials are in place
-  float hred[kEpiWarps][CODA_MAX_REDUCTIONS][32];         // helper row-reduction partials (last tile)
-  uint32_t hkeep[kEpiWarps][32];                          // helper dropout keep counts (last tile)
   // two epilogue groups (MX kernels): the odd-chunk group's row partials and
   // keep counts of a tile, handed to the even-chunk group, by tile parity
   uint64_t gfull[2][kEpiWarps];
-  float gred[2][kEpiWarps][CODA_MAX_REDUCTIONS][32];
-  uint32_t gkeep[2][kEpiWarps][32];
+  // tail helpers run in the other kernels only: their partials share the space
+  union {
+    struct {
+      float hred[kEpiWarps][CODA_MAX_REDUCTIONS][32];     // helper row-reduction partials (last tile)
+      uint32_t hkeep[kEpiWarps][32];                      // helper dropout keep counts (last tile)
+    } h;
+    struct {
+      float gred[2][kEpiWarps][CODA_MAX_REDUCTIONS][32];
+      uint32_t gkeep[2][kEpiWarps][32];
+    } g;
+  };
   uint32_t tmem_base;
   uint32_t abort_flag;
   float rs[2][BM];

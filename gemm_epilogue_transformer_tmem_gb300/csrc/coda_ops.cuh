@@ -199,7 +199,24 @@ struct RowCtx {
   int M;
   float r_rms;      // commuted-norm row scale of this row
   float mu;         // commuted-LayerNorm row mean of this row
+  const float* cvs; // this run's first column in the warp's staged column-vector slices
+                    // (slice k at cvs + k * cv_stride), or null: read them from global memory
+  int cv_stride;
 };
+
+// NE staged fp32 values (shared memory, 16-byte aligned; the same address in
+// every lane, so each load is a broadcast)
+template <int NE>
+__device__ __forceinline__ void load_staged(const float* s, float (&out)[NE]) {
+#pragma unroll
+  for (int i = 0; i < NE / 4; ++i) {
+    const float4 q = reinterpret_cast<const float4*>(s)[i];
+    out[4 * i] = q.x;
+    out[4 * i + 1] = q.y;
+    out[4 * i + 2] = q.z;
+    out[4 * i + 3] = q.w;
+  }
+}
 
 // One op of the list applied to v (and, before SWIGLU, to u: `pre`), with the
 // opcode fixed at compile time.  Both the op-list interpreter below and the
@@ -222,8 +239,12 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
     case CODA_OP_COL_SCALE:
     case CODA_OP_BIAS: {
       const uint16_t* vec = P.col_vec[op.slot];
+      const bool staged = c.cvs != nullptr && op.cv >= 0;
       float cv[NE];
-      load_colvec<NE>(vec, c.col, c.n_out, cv);
+      if (staged)
+        load_staged<NE>(c.cvs + op.cv * c.cv_stride, cv);
+      else
+        load_colvec<NE>(vec, c.col, c.n_out, cv);
       constexpr bool is_bias = CODE == CODA_OP_BIAS;
       if constexpr (is_bias) {
 #pragma unroll
@@ -233,7 +254,10 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
         for (int j = 0; j < NE; ++j) v[j] *= cv[j];
       }
       if (pre) {
-        load_colvec<NE>(vec + c.half, c.col, c.n_out, cv);
+        if (staged)
+          load_staged<NE>(c.cvs + (op.cv + 1) * c.cv_stride, cv);
+        else
+          load_colvec<NE>(vec + c.half, c.col, c.n_out, cv);
         if constexpr (is_bias) {
 #pragma unroll
           for (int j = 0; j < NE; ++j) u[j] += cv[j];
@@ -245,12 +269,19 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
       break;
     }
     case CODA_OP_COL_SCALE_F32: {
+      const bool staged = c.cvs != nullptr && op.cv >= 0;
       float cv[NE];
-      load_colvec_f32<NE>(P.col_scale_f32, c.col, c.n_out, cv);
+      if (staged)
+        load_staged<NE>(c.cvs + op.cv * c.cv_stride, cv);
+      else
+        load_colvec_f32<NE>(P.col_scale_f32, c.col, c.n_out, cv);
 #pragma unroll
       for (int j = 0; j < NE; ++j) v[j] *= cv[j];
       if (pre) {
-        load_colvec_f32<NE>(P.col_scale_f32 + c.half, c.col, c.n_out, cv);
+        if (staged)
+          load_staged<NE>(c.cvs + (op.cv + 1) * c.cv_stride, cv);
+        else
+          load_colvec_f32<NE>(P.col_scale_f32 + c.half, c.col, c.n_out, cv);
 #pragma unroll
         for (int j = 0; j < NE; ++j) u[j] *= cv[j];
       }
@@ -269,15 +300,33 @@ __device__ __forceinline__ void op_apply(const EpiProgram& P, const DevOp& op, b
       break;
     }
     case CODA_OP_LN_ROWSCALE: {
-      // r (x - mu c_j) + b_j
+      // r (x - mu c_j) + b_j; staged slices: c (and its up half before
+      // SWIGLU), then b (likewise) where the op has one
+      const bool staged = c.cvs != nullptr && op.cv >= 0;
+      const int nc = pre ? 2 : 1;
       float cv[NE], bv[NE];
-      load_colvec_f32<NE>(P.ln_colsum, c.col, c.n_out, cv);
-      load_colvec_f32<NE>(P.ln_bias, c.col, c.n_out, bv);
+      if (staged) {
+        load_staged<NE>(c.cvs + op.cv * c.cv_stride, cv);
+        if (P.ln_bias != nullptr) {
+          load_staged<NE>(c.cvs + (op.cv + nc) * c.cv_stride, bv);
+        } else {
+#pragma unroll
+          for (int j = 0; j < NE; ++j) bv[j] = 0.0f;
+        }
+      } else {
+        load_colvec_f32<NE>(P.ln_colsum, c.col, c.n_out, cv);
+        load_colvec_f32<NE>(P.ln_bias, c.col, c.n_out, bv);
+      }
 #pragma unroll
       for (int j = 0; j < NE; ++j) v[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], v[j]), bv[j]);
       if (pre) {
-        load_colvec_f32<NE>(P.ln_colsum ? P.ln_colsum + c.half : nullptr, c.col, c.n_out, cv);
-        load_colvec_f32<NE>(P.ln_bias ? P.ln_bias + c.half : nullptr, c.col, c.n_out, bv);
+        if (staged) {
+          load_staged<NE>(c.cvs + (op.cv + 1) * c.cv_stride, cv);
+          if (P.ln_bias != nullptr) load_staged<NE>(c.cvs + (op.cv + 3) * c.cv_stride, bv);
+        } else {
+          load_colvec_f32<NE>(P.ln_colsum ? P.ln_colsum + c.half : nullptr, c.col, c.n_out, cv);
+          load_colvec_f32<NE>(P.ln_bias ? P.ln_bias + c.half : nullptr, c.col, c.n_out, bv);
+        }
 #pragma unroll
         for (int j = 0; j < NE; ++j) u[j] = fmaf(c.r_rms, fmaf(-c.mu, cv[j], u[j]), bv[j]);
       }

@@ -501,6 +501,9 @@ typedef struct {
   int32_t prepass;   /* 1: a row-statistics pre-pass kernel ran first         */
   int32_t sequence;  /* 0: op-list interpreter; > 0: a fixed op sequence      */
   int32_t dynamic;   /* 1: dynamic tile order (cluster launch control)        */
+  int32_t colvecs;   /* column-vector slices the epilogue reads per tile (bias,
+                        column scales, LayerNorm's c and b): n > 0 copied to
+                        shared memory per tile, -n prefetched into L1, 0 none */
 } coda_plan;
 CODA_API void coda_last_plan(coda_plan* out);
 

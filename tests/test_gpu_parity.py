@@ -1198,12 +1198,29 @@ def test_commuted_layernorm_then_swiglu(mode):
     Wf, c, b = coda.fold_layernorm(cu(W), cu(g), cu(beta), "kn")
     ops = [("LN_ROWSCALE", 0, 1e-5), ("SWIGLU",), ("ROW_SUM", 2)]
     r = coda.gemm_epilogue(cu(X), Wf, ops, ln_colsum=c, ln_bias=b)
+    assert abs(coda.last_plan()["colvecs"]) == 4     # c, b and their up halves
     sync_ok()
     ref = O.run_chain(f64(X), f64(W), ops, norm_gamma=f64(g), norm_beta=f64(beta))
     assert_close(f64(r.D), ref["D"], "ln -> swiglu")
     assert_close(f64(r.row_stats[0]), ref["stats"][0], "ln r")
     check_stats(r, {"D": ref["D"], "stats": {2: ref["stats"][2]}, "stat_scale": ref["stat_scale"]}, "ln -> swiglu",
                 chain_tau(ops, fold=True), K)
+
+
+def test_column_vector_slices_staged_or_prefetched(mode):
+    # Column vectors reach the epilogue as per-tile slices copied to shared
+    # memory (up to 8: here 5, the SwiGLU up halves included) or, past 8, as
+    # global loads prefetched into L1 (here 10 slices): both against the oracle,
+    # ragged in every dimension, several tiles per CTA in persist4
+    cases = {5: [("BIAS", 0), ("COL_SCALE", 1), ("SWIGLU",), ("BIAS", 2)],
+             -8: [("BIAS", 0), ("COL_SCALE", 1), ("BIAS", 2), ("COL_SCALE", 3), ("BIAS", 0), ("SWIGLU",)]}
+    for want, ops in cases.items():
+        A, B, N, n_out, col, row, aux = _op_case_tensors(ops, "kn", 700 + want)
+        r = coda.gemm_epilogue(cu(A), cu(B), ops, col_vecs={k: cu(v) for k, v in col.items()})
+        assert coda.last_plan()["colvecs"] == want, coda.last_plan()
+        sync_ok()
+        ref = O.run_chain(f64(A), f64(B), ops, col_vecs={k: f64(v) for k, v in col.items()})
+        assert_close(f64(r.D), ref["D"], f"{len(ops)} ops, colvecs {want}")
 
 
 def test_layernorm_rowscale_rejected_unfused_and_without_colsum():
