@@ -20,7 +20,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcoda.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["coda_api.cu", "coda_kernels.cu", "coda_noalloc.cu", "coda_gemm_interp.cu", "coda_gemm_norm.cu", "coda_gemm_mx.cu",
+SOURCES = ["coda_api.cu", "coda_kernels.cu", "coda_noalloc.cu", "coda_gemm_interp.cu", "coda_gemm_interp_glu.cu",
+           "coda_gemm_interp_glu_amn.cu", "coda_gemm_norm.cu", "coda_gemm_mx.cu",
            "coda_gemm_norm_glu.cu", "coda_gemm_fwd.cu", "coda_gemm_fwd_glu.cu", "coda_gemm_bwd.cu",
            "coda_gemm_fp8.cu", "coda_gemm_gpt.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

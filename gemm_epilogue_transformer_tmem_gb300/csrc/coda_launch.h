@@ -10,10 +10,15 @@ namespace coda {
 
 // fused GEMM + epilogue; maps = {A, B, D, aux0, aux1, aux2}
 // pair: cta_group::2 on clusters of two CTAs (grid counts CTAs and is even)
-// the op-list interpreter (any op list)
+// the op-list interpreter (any op list); SwiGLU-paired outputs in their own unit
 cudaError_t launch_gemm_interp(bool glu, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
                              const CUtensorMap* maps,
                                const GemmParams& p, int grid, size_t smem, cudaStream_t st);
+cudaError_t launch_gemm_interp_glu(bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
+                                   const CUtensorMap* maps, const GemmParams& p, int grid, size_t smem,
+                                   cudaStream_t st);
+cudaError_t launch_gemm_interp_glu_amn(bool b_mn_major, bool row_stats, bool pair, const CUtensorMap* maps,
+                                       const GemmParams& p, int grid, size_t smem, cudaStream_t st);
 // fixed op sequences (coda_sequences.h); cudaErrorNotSupported for a sequence
 // or variant a translation unit does not hold
 cudaError_t launch_gemm_norm(int seq, bool a_mn_major, bool b_mn_major, bool row_stats, bool pair,
@@ -42,6 +47,7 @@ cudaError_t launch_gemm_mx(int seq, bool glu, bool pair, const CUtensorMap* maps
                            size_t smem, cudaStream_t st);
 // how many CTA pairs of the pair kernel fit on the device at once
 cudaError_t max_pairs(bool glu, bool b_mn_major, size_t smem, int* pairs);
+cudaError_t max_pairs_glu(bool b_mn_major, size_t smem, int* pairs);
 
 cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M, int num_n_tiles, int n_red,
                             const RedInfo& info, float inv_width, float* row_stats, uint32_t* keep_count,
