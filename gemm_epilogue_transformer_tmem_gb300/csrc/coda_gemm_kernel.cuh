@@ -366,6 +366,9 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
   if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before any remote use
   tc_fence_after_sync();
   const uint32_t tmem_base = ctl->tmem_base;
+  // The row-statistics finish launched behind this grid may be scheduled now:
+  // it waits (griddepcontrol.wait) for this grid to complete before reading.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer

@@ -12,12 +12,33 @@
 
 namespace coda {
 
+// Launch a kernel as the programmatic dependent of the previous kernel on the
+// stream: it may be scheduled once that grid has signalled
+// (griddepcontrol.launch_dependents) and begins with griddepcontrol.wait,
+// which holds it until that grid has completed and its writes are visible.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), unsigned blocks, unsigned threads, cudaStream_t st,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- finalize
 // row_stats[slot][i] = sum over column tiles of the partials, in tile order
 // (deterministic), divided by the row width for ROW_MEAN; keep counts likewise.
 __global__ void finalize_rows_kernel(const float* __restrict__ ws_red, const uint32_t* __restrict__ ws_keep,
                                      int M, int num_n_tiles, int n_red, RedInfo info, float inv_width,
                                      float* __restrict__ row_stats, uint32_t* __restrict__ keep_count) {
+  griddep_wait();   // the fused kernel's partials (launched as its programmatic dependent)
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= M) return;
   const size_t Ms = static_cast<size_t>(M);
@@ -40,9 +61,8 @@ cudaError_t launch_finalize(const float* ws_red, const uint32_t* ws_keep, int M,
                             cudaStream_t st) {
   const int threads = 256;
   const int blocks = (M + threads - 1) / threads;
-  finalize_rows_kernel<<<blocks, threads, 0, st>>>(ws_red, ws_keep, M, num_n_tiles, n_red, info, inv_width,
-                                                   row_stats, keep_count);
-  return cudaGetLastError();
+  return launch_dependent(finalize_rows_kernel, blocks, threads, st, ws_red, ws_keep, M, num_n_tiles, n_red, info,
+                          inv_width, row_stats, keep_count);
 }
 
 // Column reductions: col_stats[slot][j] = sum over the 32-row blocks of the
@@ -53,6 +73,7 @@ struct ColSlots {
 
 __global__ void finalize_cols_kernel(const float* __restrict__ ws_col, int n_colred, int num_rb, int64_t n_out,
                                      ColSlots slots, float* __restrict__ col_stats) {
+  griddep_wait();   // the fused kernel's partials (launched as its programmatic dependent)
   const int64_t j = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
   if (j >= n_out) return;
   for (int r = 0; r < n_colred; ++r) {
@@ -68,9 +89,8 @@ cudaError_t launch_finalize_cols(const float* ws_col, int n_colred, int num_rb, 
   ColSlots cs{};
   for (int r = 0; r < n_colred && r < CODA_MAX_COL_REDUCTIONS; ++r) cs.s[r] = slots[r];
   const int threads = 256;
-  finalize_cols_kernel<<<static_cast<unsigned>((n_out + threads - 1) / threads), threads, 0, st>>>(
-      ws_col, n_colred, num_rb, n_out, cs, col_stats);
-  return cudaGetLastError();
+  return launch_dependent(finalize_cols_kernel, static_cast<unsigned>((n_out + threads - 1) / threads), threads, st,
+                          ws_col, n_colred, num_rb, n_out, cs, col_stats);
 }
 
 // ------------------------------------------------- commuted-norm row scales
