@@ -855,7 +855,10 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   // cluster) to +3% (skinny, 1 tile; lnproj) and -0.4% on grids of ~36 tiles per
   // cluster (swiglu), where the last tile's epilogue is a small share of the run
   const int64_t tiles_per_cluster = (g.num_tiles + grid / csize - 1) / (grid / csize);
-  p.helpers = (g_tail_helpers.load() != 0 && !mx && !split && p.clc == 0 && c.n_aux == 0 && !rowstat_warps &&
+  // (their aux tiles are staged in the ring: four warps' output and aux buffers must fit in it)
+  const bool ring_room = static_cast<size_t>(kEpiWarps) * (2 + 2 * c.n_aux) * kBoxBytes <=
+                         static_cast<size_t>(stages) * stage_bytes;
+  p.helpers = (g_tail_helpers.load() != 0 && !mx && !split && p.clc == 0 && ring_room && !rowstat_warps &&
                g.num_kb > 0 && tiles_per_cluster <= 16) ? 1 : 0;
   int seq = match_sequence(epi, c.glu);
   auto launch = [&](int sq) {

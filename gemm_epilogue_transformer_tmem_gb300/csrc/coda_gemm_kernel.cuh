@@ -332,7 +332,11 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       for (int q = 0; q < kEpiWarps; ++q) mbar_init(&ctl->gfull[b][q], 1);
     mbar_init(&ctl->drain, 1);
     mbar_init(&ctl->esync, kEpiWarps);
-    for (int q = 0; q < kEpiWarps; ++q) mbar_init(&ctl->helpdone[q], 1);
+    for (int q = 0; q < kEpiWarps; ++q) {
+      mbar_init(&ctl->helpdone[q], 1);
+      mbar_init(&ctl->haux[q][0], 1);
+      mbar_init(&ctl->haux[q][1], 1);
+    }
     for (int s = 0; s < kSchedSlots; ++s) {
       mbar_init(&ctl->sched_full[s], 1);
       // tile-walking roles: the producers, the MMA issuer and the epilogue warps
@@ -873,7 +877,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
       auto aux_step = [&](int c) -> bool {
         if (n_aux == 0) return true;
         const int col = col_base + c * kChunk;
-        if (c + kEpiGroups < nch) issue_aux(abuf ^ 1, col + kEpiGroups * kChunk, m0 + q * 32);
+        const int next = helped ? 2 : kEpiGroups;   // the helpers take the odd chunks
+        if (c + next < nch) issue_aux(abuf ^ 1, col + next * kChunk, m0 + q * 32);
         if (!warp_wait(W, &ctl->auxfull[ew][abuf], (aux_phase >> abuf) & 1u, tile, lane)) return false;
         aux_phase ^= 1u << abuf;
         aux_armed &= ~(1u << abuf);
@@ -1155,7 +1160,8 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
     // Once the last accumulator is complete nothing is left to load or issue:
     // the producer, MMA, allocator and scheduler warps (lane quarters 0-3) take
     // the odd chunks of the CTA's last tile, halving the epilogue that nothing
-    // overlaps.  Only in the static order, without aux tensors or a split.
+    // overlaps; their aux tiles come by TMA into the idle ring, one chunk ahead.
+    // Only in the static order, without a split.
     if (!kMX && p.helpers != 0 && !split && warp < kEpiWarps) {
       __syncwarp();
       const int q = warp;
@@ -1184,14 +1190,42 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
             if (p.mu_vec != nullptr) mu = row_ok ? p.mu_vec[row] : 0.0f;
           }
           const uint64_t stream_policy = policy_evict_first();
-          // staging in the ring, whose copies have all landed and been consumed
-          uint8_t* hstage = smem + q * (2 * kBoxBytes);
-          const SmemAux ax{hstage, lane};   // unused: no aux tensors here
+          // staging in the ring, whose copies have all landed and been consumed:
+          // two output boxes, then two aux buffers of n_aux boxes (aux k of
+          // buffer b at (2k + b) boxes, as in the epilogue warps' staging)
+          const int n_aux = p.n_aux;
+          uint8_t* hstage = smem + q * (2 + 2 * n_aux) * kBoxBytes;
+          uint8_t* haux = hstage + 2 * kBoxBytes;
+          uint32_t haux_phase = 0, haux_armed = 0;
+          int hb = 0;
+          auto h_issue = [&](int b, int col) {
+            __syncwarp();
+            if (lane == 0) {
+              uint64_t* bar = &ctl->haux[q][b];
+              mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n_aux * kBoxBytes));
+              tma_load_2d_hint(haux + (0 * 2 + b) * kBoxBytes, &tmX0, bar, col, m0 + q * 32, stream_policy);
+              if (n_aux > 1) tma_load_2d_hint(haux + (1 * 2 + b) * kBoxBytes, &tmX1, bar, col, m0 + q * 32, stream_policy);
+              if (n_aux > 2) tma_load_2d_hint(haux + (2 * 2 + b) * kBoxBytes, &tmX2, bar, col, m0 + q * 32, stream_policy);
+            }
+            haux_armed |= 1u << b;
+          };
+          bool hok = true;
+          if (n_aux > 0 && 1 < nch) h_issue(0, col_base + kChunk);
           float hred[CODA_MAX_REDUCTIONS] = {0.0f, 0.0f, 0.0f, 0.0f};
           uint32_t keep = 0;
           int sbuf = 0;
           for (int c = 1; c < nch; c += 2) {
             const int col = col_base + c * kChunk;
+            if (n_aux > 0) {
+              if (c + 2 < nch) h_issue(hb ^ 1, col + 2 * kChunk);
+              if (!warp_wait(W, &ctl->haux[q][hb], (haux_phase >> hb) & 1u, static_cast<uint32_t>(tile), lane)) {
+                hok = false;
+                break;
+              }
+              haux_phase ^= 1u << hb;
+              haux_armed &= ~(1u << hb);
+            }
+            const SmemAux ax{haux + hb * kBoxBytes, lane};
             float v[32], u[32];
             if constexpr (kGLU)
               tmem_ld32x2(t_row + c * kChunk, v, t_row + BN / 2 + c * kChunk, u);
@@ -1221,8 +1255,14 @@ __global__ void __launch_bounds__((kRowStats || kMX) ? 384 : 256, 1)
               bulk_commit_group();
             }
             sbuf ^= 1;
+            if (n_aux > 0) hb ^= 1;
           }
-          if (p.prog.n_red > 0 || p.ws_keep != nullptr) {
+          if (!hok && lane == 0) {
+            // aux copies still in flight land before the CTA exits
+            for (int b = 0; b < 2; ++b)
+              if (haux_armed & (1u << b)) wait_drain(&ctl->haux[q][b], (haux_phase >> b) & 1u, 2000000ull);
+          }
+          if (hok && (p.prog.n_red > 0 || p.ws_keep != nullptr)) {
 #pragma unroll
             for (int r = 0; r < CODA_MAX_REDUCTIONS; ++r) ctl->h.hred[q][r][lane] = hred[r];
             ctl->h.hkeep[q][lane] = keep;

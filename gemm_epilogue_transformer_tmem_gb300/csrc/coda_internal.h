@@ -157,6 +157,7 @@ struct Ctl {
   uint64_t sched_empty[kSchedSlots];   // every tile-walking role read it (leader CTA's barrier)
   alignas(16) uint32_t sched_resp[kSchedSlots][4];
   uint64_t helpdone[kEpiWarps];                           // a helper warp's row partials are in place
+  uint64_t haux[kEpiWarps][2];                            // a helper warp's aux tiles landed (two buffers)
   // two epilogue groups (MX kernels): the odd-chunk group's row partials and
   // keep counts of a tile, handed to the even-chunk group, by tile parity
   uint64_t gfull[2][kEpiWarps];

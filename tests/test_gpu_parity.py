@@ -547,34 +547,39 @@ HELPER_CASES = {
     "scale_preact_swiglu": [("SCALE", 0, 2.0), ("STORE_PREACT",), ("SWIGLU",), ("ROW_SUMSQ", 1)],
     "gelu_colsum_rowsum": [("GELU_TANH",), ("COL_SUM", 0), ("ROW_SUM", 0)],
     "rms_swiglu": [("RMS_ROWSCALE", 0, 1e-6), ("SWIGLU",)],
+    "residual_sumsq": [("RESIDUAL", 0, 1.0), ("ROW_SUMSQ", 0)],
+    "dgrad": [("GELU_TANH_GRAD",), ("ROW_DOT_AUX", 0), ("ROW_SUM", 1)],
+    "bias_gelu_residual": [("BIAS", 0), ("GELU_TANH",), ("RESIDUAL", 0, 1.0)],
 }
 
 
 @pytest.mark.parametrize("case", sorted(HELPER_CASES))
 def test_tail_helpers_bit_identical(case, mode):
     # the non-epilogue warps taking half of each CTA's last tile change nothing:
-    # outputs, row and column statistics and keep counts are bit-identical
+    # outputs, row and column statistics and keep counts are bit-identical; with
+    # aux tensors (residual, Z, Xhat) the helpers stage their aux tiles themselves
     ops = HELPER_CASES[case]
-    if case == "reductions":
-        ops = [o for o in ops if o[0] != "ROW_DOT_AUX"]    # an aux tensor disables the helpers
     A, B, N, n_out, col, row, aux = _op_case_tensors(ops, "kn", 700 + len(case))
     preact = None
     if any(o[0] == "STORE_PREACT" for o in ops):
         preact = torch.zeros((M_R, N), dtype=torch.bfloat16, device="cuda")
+    args = dict(col_vecs={k: cu(v) for k, v in col.items()}, residual=cu(aux["residual"]), z=cu(aux["z"]),
+                xhat=cu(aux["xhat"]))
     out = []
     try:
         for helpers in (True, False):
             coda.set_tail_helpers(helpers)
             if preact is not None:
                 preact.zero_()
-            r = coda.gemm_epilogue(cu(A), cu(B), ops, seed=9, preact_out=preact)
+            r = coda.gemm_epilogue(cu(A), cu(B), ops, seed=9, preact_out=preact, **args)
             sync_ok()
             out.append((r, None if preact is None else preact.clone()))
     finally:
         coda.set_tail_helpers(True)
     (a, pa), (b, pb) = out
     assert torch.equal(a.D, b.D), case
-    ref = O.run_chain(f64(A), f64(B), ops, seed=9)
+    ref = O.run_chain(f64(A), f64(B), ops, seed=9, col_vecs={k: f64(v) for k, v in col.items()},
+                      residual_t=f64(aux["residual"]), z=f64(aux["z"]), xhat=f64(aux["xhat"]))
     for slot in ref["stats"]:
         assert torch.equal(a.row_stats[slot], b.row_stats[slot]), (case, slot)
     for slot in ref.get("col_stats", {}):
