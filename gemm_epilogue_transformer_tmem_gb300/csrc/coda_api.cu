@@ -853,13 +853,14 @@ coda_status gemm_impl(const void* A, const void* B, int64_t M, int64_t N, int64_
   }
   // Helpers on each CTA's last tile: measured +1.5% (rmsproj, 7 tiles per
   // cluster) to +3% (skinny, 1 tile; lnproj) and -0.4% on grids of ~36 tiles per
-  // cluster (swiglu), where the last tile's epilogue is a small share of the run
+  // cluster (swiglu), where the last tile's epilogue is a small share of the run;
+  // an epilogue with aux tiles is long enough to gain up to 64 (dgrad, 27: +0.6%)
   const int64_t tiles_per_cluster = (g.num_tiles + grid / csize - 1) / (grid / csize);
   // (their aux tiles are staged in the ring: four warps' output and aux buffers must fit in it)
   const bool ring_room = static_cast<size_t>(kEpiWarps) * (2 + 2 * c.n_aux) * kBoxBytes <=
                          static_cast<size_t>(stages) * stage_bytes;
   p.helpers = (g_tail_helpers.load() != 0 && !mx && !split && p.clc == 0 && ring_room && !rowstat_warps &&
-               g.num_kb > 0 && tiles_per_cluster <= 16) ? 1 : 0;
+               g.num_kb > 0 && (tiles_per_cluster <= 16 || (c.n_aux > 0 && tiles_per_cluster <= 64))) ? 1 : 0;
   int seq = match_sequence(epi, c.glu);
   auto launch = [&](int sq) {
     return mx ? launch_gemm_mx(sq, c.glu, pair, maps, p, grid, smem, st)

@@ -486,9 +486,10 @@ CODA_API void coda_set_tile_scheduler(int32_t dynamic);
  * in every order. */
 CODA_API void coda_set_raster(int32_t mode, int32_t group);
 /* 1 (default): once a CTA's last accumulator is complete, its producer, MMA and
- * other non-epilogue warps take half of that tile's epilogue chunks (static tile
- * order, op lists without aux tensors, no split over K, at most 16 tiles per
- * cluster); 0: the epilogue warps alone.  Results are bit-identical either way. */
+ * other non-epilogue warps take half of that tile's epilogue chunks, loading
+ * their own aux tiles (static tile order, no split over K, at most 16 tiles per
+ * cluster, or 64 for op lists with aux tensors); 0: the epilogue warps alone.
+ * Results are bit-identical either way. */
 CODA_API void coda_set_tail_helpers(int32_t enable);
 
 /* How the calling thread's last successful coda_gemm_epilogue call ran. */
