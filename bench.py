@@ -156,10 +156,12 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ timing
-def timed_loop(calls, steps, warmup, flush, stream, counter=None):
+def timed_loop(calls, steps, warmup, flush, stream, counter=None, sync_each=False):
     """Run `steps` steps; returns (per-call total ms list, total ms, kernels the
     library launched during the timed steps per `counter`, or None).  Every
-    call is bracketed by events on `stream`; the L2 flush runs outside them."""
+    call is bracketed by events on `stream`; the L2 flush runs outside them.
+    sync_each: the host waits for each step before queueing the next (as a
+    caller that reads the step's result back does)."""
     for _ in range(warmup):
         flush()
         for c in calls:
@@ -174,6 +176,8 @@ def timed_loop(calls, steps, warmup, flush, stream, counter=None):
             evs[i][j][0].record(stream)
             c()
             evs[i][j][1].record(stream)
+        if sync_each:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     launched = (counter() - count0) if counter else None
     per_call = [0.0] * len(calls)
@@ -464,13 +468,15 @@ def main():
             for k, v in hout.items():
                 v.copy_(step.host_outputs[k], non_blocking=True)
 
-        _, e_total, _ = timed_loop([e2e_call], e2e_steps, 3, flush, stream)
+        # the host reads each step's result back before it queues the next
+        _, e_total, _ = timed_loop([e2e_call], e2e_steps, 3, flush, stream, sync_each=True)
         e_ms = e_total / e2e_steps
         e2e = {"value": round(step.flops / (e_ms * 1e-3) / 1e12, 2), "unit": UNIT,
                "ms_per_step": round(e_ms, 5),
                "copies": ("overlapped with the step's calls on two side streams (events order them), in "
                           "blocks of tokens where the step is the LLaMA block"
-                          if step.e2e is not None else "host-to-device, step, device-to-host on the launching stream"),
+                          if step.e2e is not None else "host-to-device, step, device-to-host on the launching stream")
+                         + "; the host waits for each step's read-back before the next step",
                "h2d_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hin.values())),
                "d2h_bytes_per_step": int(sum(v.numel() * v.element_size() for v in hout.values()))}
 
