@@ -189,12 +189,26 @@ def make_aux(col_vecs=None, row_vecs=None, residual=None, z=None, xhat=None, pre
 
 
 def output_width(N: int, ops: Sequence) -> int:
-    return N // 2 if any(o[0] == "SWIGLU" for o in _norm_ops(ops)) else N
+    return _out_width(N, _norm_ops(ops))
 
 
 def stat_slots(ops: Sequence) -> int:
+    return _stat_slots(_norm_ops(ops))
+
+
+def col_slots(ops: Sequence) -> int:
+    return _col_slots(_norm_ops(ops))
+
+
+# the same on an op list already normalised by _norm_ops (each call below
+# normalises its list once)
+def _out_width(N: int, nops: list) -> int:
+    return N // 2 if any(name == "SWIGLU" for name, _, _ in nops) else N
+
+
+def _stat_slots(nops: list) -> int:
     n = 0
-    for name, slot, _ in _norm_ops(ops):
+    for name, slot, _ in nops:
         if (name in REDUCTIONS or name == "RMS_ROWSCALE") and slot != NO_SLOT:
             n = max(n, slot + 1)
         if name == "LN_ROWSCALE" and slot != NO_SLOT:
@@ -202,19 +216,22 @@ def stat_slots(ops: Sequence) -> int:
     return n
 
 
-def col_slots(ops: Sequence) -> int:
+def _col_slots(nops: list) -> int:
     n = 0
-    for name, slot, _ in _norm_ops(ops):
+    for name, slot, _ in nops:
         if name in COL_REDUCTIONS and slot != NO_SLOT:
             n = max(n, slot + 1)
     return n
 
 
-def workspace_size(M: int, N: int, K: int, ops: Sequence = ()) -> int:
+def _workspace_bytes(M: int, N: int, K: int, e: CodaEpilogue) -> int:
     n = ctypes.c_size_t(0)
-    e = make_epilogue(ops)
     _check(lib().coda_workspace_size(M, N, K, ctypes.byref(e), ctypes.byref(n)), "coda_workspace_size")
     return n.value
+
+
+def workspace_size(M: int, N: int, K: int, ops: Sequence = ()) -> int:
+    return _workspace_bytes(M, N, K, make_epilogue(ops))
 
 
 @dataclass
@@ -240,23 +257,25 @@ def gemm_epilogue(A: torch.Tensor, B: torch.Tensor, ops: Sequence = (), *, b_lay
         raise ValueError(a_layout)
     M, K = A.shape if a_layout == "mk" else (A.shape[1], A.shape[0])
     N = B.shape[1] if b_layout == "kn" else B.shape[0]
-    n_out = output_width(N, ops)
+    nops = _norm_ops(ops)
+    n_out = _out_width(N, nops)
     dev = A.device
     if out is None:
         out = torch.empty((M, n_out), dtype=torch.bfloat16, device=dev)
-    ns = stat_slots(ops)
+    ns = _stat_slots(nops)
     if row_stats is None and ns > 0:
         row_stats = torch.empty((ns, M), dtype=torch.float32, device=dev)
-    has_dropout = any(o[0] == "DROPOUT" for o in _norm_ops(ops))
+    has_dropout = any(name == "DROPOUT" for name, _, _ in nops)
     if keep_count is None and has_dropout and want_keep_count:
         keep_count = torch.empty((M,), dtype=torch.int32, device=dev)
-    nc = col_slots(ops)
+    nc = _col_slots(nops)
     if col_stats is None and nc > 0:
         col_stats = torch.empty((nc, n_out), dtype=torch.float32, device=dev)
-    wbytes = workspace_size(M, N, K, ops)
-    if workspace is None and wbytes > 0:
-        workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
-    e = make_epilogue(ops, seed)
+    e = make_epilogue(nops, seed)
+    if workspace is None:
+        wbytes = _workspace_bytes(M, N, K, e)
+        if wbytes > 0:
+            workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
     a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, ln_colsum, ln_bias, col_stats, col_scale_f32)
     layout = B_LAYOUTS[b_layout] | (A_KM if a_layout == "km" else 0) | (AB_E4M3 if e4m3 else 0)
     st = lib().coda_gemm_epilogue(_ptr(A), _ptr(B), M, N, K, layout, ctypes.byref(e), ctypes.byref(a),
@@ -295,22 +314,24 @@ def gemm_epilogue_mx(A: torch.Tensor, scale_A: torch.Tensor, B: torch.Tensor, sc
     scale_A / scale_B their tiled E8M0 scales (coda_gemm_epilogue_mx)."""
     M, K = A.shape
     N = B.shape[0]
-    n_out = output_width(N, ops)
+    nops = _norm_ops(ops)
+    n_out = _out_width(N, nops)
     dev = A.device
     if out is None:
         out = torch.empty((M, n_out), dtype=torch.bfloat16, device=dev)
-    ns = stat_slots(ops)
+    ns = _stat_slots(nops)
     if row_stats is None and ns > 0:
         row_stats = torch.empty((ns, M), dtype=torch.float32, device=dev)
-    if keep_count is None and any(o[0] == "DROPOUT" for o in _norm_ops(ops)):
+    if keep_count is None and any(name == "DROPOUT" for name, _, _ in nops):
         keep_count = torch.empty((M,), dtype=torch.int32, device=dev)
-    nc = col_slots(ops)
+    nc = _col_slots(nops)
     if col_stats is None and nc > 0:
         col_stats = torch.empty((nc, n_out), dtype=torch.float32, device=dev)
-    wbytes = workspace_size(M, N, K, ops)
-    if workspace is None and wbytes > 0:
-        workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
-    e = make_epilogue(ops, seed)
+    e = make_epilogue(nops, seed)
+    if workspace is None:
+        wbytes = _workspace_bytes(M, N, K, e)
+        if wbytes > 0:
+            workspace = torch.empty((wbytes,), dtype=torch.uint8, device=dev)
     a = make_aux(col_vecs, row_vecs, residual, z, xhat, preact_out, None, None, col_stats, col_scale_f32)
     st = lib().coda_gemm_epilogue_mx(_ptr(A), _ptr(scale_A), _ptr(B), _ptr(scale_B), M, N, K, ctypes.byref(e),
                                      ctypes.byref(a), _ptr(out), _ptr(row_stats), _ptr(keep_count), _ptr(workspace),
